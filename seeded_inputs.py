@@ -1,0 +1,105 @@
+"""Seeded synthetic inputs for the groupwise int4/int5 small-batch projection.
+
+This module only draws random numbers and stores them in the library's canonical
+input types (uint32 code words, fp16 and bf16 bit patterns). Conversions to fp16 and
+bf16 are done by NumPy / PyTorch library casts. It holds none of the method's
+arithmetic: no unpacking, no dequantisation, no contraction. The CPU oracle and the
+CUDA path are both fed from here and from nowhere else.
+
+Canonical layouts (the library's format definition, also stated in include/nq.h):
+  X     bf16   [T][K]      row-major activations
+  Wq    uint32 [N][K/8]    Q4 codes, nibble i (bits 4i..4i+3) of word j = q[n, 8j+i]
+  Wn    uint32 [N][K/8]    Q5 low nibbles, same rule
+  Wh    uint32 [N][K/32]   Q5 high bits, bit i of word j = bit 4 of q[n, 32j+i]
+  S     fp16   [N][K/64]   one scale per (output row n, 64-wide K group)
+
+Value distributions (the workloads of the pages' T=8 verify / decode projections):
+  codes  uniform on [0, 15] (Q4) or [0, 31] (Q5). Eight independent uniform 4-bit
+         fields are exactly a uniform 32-bit word, so whole words are drawn.
+  scales fp16(0.01 * exp(z)), z ~ N(0, 0.25) read as variance 0.25 (sigma = 0.5)
+  X      bf16(x), x ~ N(0, 1)
+Draw order inside one generator: code words (nibble plane, then high plane for Q5),
+then scale normals, then activation normals.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+SCALE_BASE = 0.01
+SCALE_SIGMA = 0.5
+GROUP = 64
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 (round to nearest even, PyTorch cast) as uint16 bit patterns."""
+    x32 = np.ascontiguousarray(x, dtype=np.float32)
+    return torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def fp16_bits(x: np.ndarray) -> np.ndarray:
+    """fp64/fp32 -> fp16 (round to nearest even, NumPy cast) as uint16 bit patterns."""
+    return np.asarray(x).astype(np.float16).view(np.uint16).copy()
+
+
+def code_words(g: np.random.Generator, rows: int, words: int) -> np.ndarray:
+    return g.integers(0, 2**32, size=(rows, words), dtype=np.uint32)
+
+
+def scales(g: np.random.Generator, N: int, K: int) -> np.ndarray:
+    z = g.standard_normal((N, K // GROUP))
+    return fp16_bits(SCALE_BASE * np.exp(SCALE_SIGMA * z))
+
+
+def activations(g: np.random.Generator, T: int, K: int) -> np.ndarray:
+    return bf16_bits(g.standard_normal((T, K)).astype(np.float32))
+
+
+def q4_problem(T: int, K: int, N: int, seed: int) -> dict:
+    """One seeded Q4 projection: codes, then scales, then X, from one generator."""
+    g = rng(seed)
+    wq = code_words(g, N, K // 8)
+    s = scales(g, N, K)
+    x = activations(g, T, K)
+    return {"bits": 4, "T": T, "K": K, "N": N, "x": x, "wq": wq, "s": s}
+
+
+def q5_problem(T: int, K: int, N: int, seed: int) -> dict:
+    """One seeded Q5 projection: nibble plane, high plane, scales, then X."""
+    g = rng(seed)
+    wn = code_words(g, N, K // 8)
+    wh = code_words(g, N, K // 32)
+    s = scales(g, N, K)
+    x = activations(g, T, K)
+    return {"bits": 5, "T": T, "K": K, "N": N, "x": x, "wn": wn, "wh": wh, "s": s}
+
+
+def swiglu_problem(T: int, K: int, N: int, seed: int) -> dict:
+    """Gate and up Q4 weights (each [N][K]) and X, from one generator."""
+    g = rng(seed)
+    wg = code_words(g, N, K // 8)
+    wu = code_words(g, N, K // 8)
+    sg = scales(g, N, K)
+    su = scales(g, N, K)
+    x = activations(g, T, K)
+    return {"T": T, "K": K, "N": N, "x": x, "wg": wg, "sg": sg, "wu": wu, "su": su}
+
+
+# The five workloads. Shapes are those of a 27B-class dense decoder layer.
+TINY_Q4 = dict(T=1, K=256, N=128, seed=0)                  # tiny Q4 correctness case
+DECODE_Q4 = dict(T=1, K=5120, N=17408, seed=1)             # decode GEMV, FFN up-projection
+VERIFY_Q5 = dict(T=8, K=5120, N=6144, seed=2)              # T=8 verify, attention gate/value
+SWIGLU_Q4 = dict(T=8, K=5120, N=17408, seed=3)             # gate+up, then down K=17408,N=5120
+SWIGLU_DOWN = dict(K=17408, N=5120)
+LAYER_Q4 = [("gate", 5120, 17408), ("up", 5120, 17408), ("down", 17408, 5120)]
+LAYER_Q5 = [("qgate", 5120, 6144), ("kv", 5120, 1024), ("out", 6144, 5120)]
+N_LAYERS = 64
+
+
+def layer_seed(layer: int, proj: int) -> int:
+    """Per-layer, per-projection seed of the layer-stack sweep."""
+    return 1000 * layer + proj
