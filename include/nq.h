@@ -1,0 +1,187 @@
+/*
+ * nq.h -- C ABI of the GB300 (sm_103a) groupwise int4/int5 small-batch projection library.
+ *
+ * The operation (what the pages tune for single-GPU decode and speculative verify rounds):
+ *
+ *     Y[t,n] = sum_k X[t,k] * W[k,n],   W[k,n] = s[n, k/64] * (q[n,k] - z),
+ *     z = 8 for 4-bit codes (Q4), z = 16 for 5-bit codes (Q5),  t < T <= 8.
+ *
+ * Sources: "NInfer-4090" release post (lcz.me), section "V3 做了什么" -- small-batch Q4/Q5
+ * projections with T=8 routing, used by the GDN projections, the attention Q5 projections
+ * and the SwiGLU path; same post, section "实测数据" -- per-op timings of a T=8 attention Q5
+ * gate/value projection and a GDN QK Q4 projection; "ninfer-ext" README, section
+ * "与原版 NInfer 的对比" -- the Q5 K-split MMA path for small-batch verify rounds.
+ * The pages give neither an API nor a storage format: both are this library's definition.
+ *
+ * Canonical layouts (host or device arrays; all little-endian):
+ *   X    bf16   [T][K]     row-major activations
+ *   Y, H bf16   [T][N]     row-major outputs (round to nearest even from fp32)
+ *   Wq   uint32 [N][K/8]   Q4 codes: nibble i (bits 4i..4i+3) of word j is q[n, 8j+i]
+ *   Wn   uint32 [N][K/8]   Q5 low nibbles, same rule
+ *   Wh   uint32 [N][K/32]  Q5 high bits: bit i of word j is bit 4 of q[n, 32j+i]
+ *   S    fp16   [N][K/64]  one scale per (output row n, 64-wide group of K)
+ *
+ * Packed layout: nq_pack_* rewrites the canonical codes and scales into an opaque,
+ * kernel-friendly tile order (16 output rows x one 64-wide K group per tile). Its size
+ * depends only on (bits, K, N) and is given by nq_packed_*_bytes. The projection calls take
+ * the packed form only.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers on the current CUDA device, owned by the caller; the
+ *     library never frees or retains them. `stream` is a cudaStream_t (NULL = the legacy
+ *     default stream). Calls are asynchronous on `stream`; none synchronises or prints.
+ *   - Shapes: K % 64 == 0, N % 16 == 0, 0 <= T <= 8. T == 0 or N == 0 is an empty problem
+ *     (NQ_OK, nothing launched). K == 0 makes Y an empty sum: zeros are written.
+ *   - Alignment: every pointer 16-byte aligned.
+ *   - All argument checks run on the host before anything is launched; a call that returns
+ *     an error has launched nothing and left every output untouched.
+ *   - Outputs must not overlap inputs (NQ_ERR_ALIAS).
+ *   - The projection calls use a per-device workspace owned by the library (a few MB at
+ *     most). It is allocated, or grown, on the first call that needs it: that call
+ *     synchronises the device and must not be made during stream capture. nq_reserve
+ *     allocates it ahead of time. Projection calls that overlap in time on one device
+ *     (different streams, no ordering) share it and race: order them on one stream.
+ *   - Device-side waits are bounded; a wait that runs out sets a device error flag that
+ *     nq_device_error reads.
+ */
+#ifndef NQ_H
+#define NQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int nq_status;
+
+enum {
+    NQ_OK = 0,
+    NQ_ERR_NULL = -1,     /* a required pointer is NULL                                   */
+    NQ_ERR_SHAPE = -2,    /* K % 64, N % 16, T outside [0, 8], negative size, too large   */
+    NQ_ERR_ALIGN = -3,    /* a pointer is not 16-byte aligned                             */
+    NQ_ERR_ALIAS = -4,    /* an output range overlaps an input range                      */
+    NQ_ERR_CUDA = -5,     /* a CUDA runtime call or kernel launch failed                  */
+    NQ_ERR_DEVICE = -6,   /* current device is not compute capability 10.3 (sm_103)      */
+    NQ_ERR_TIMEOUT = -7   /* a bounded device-side wait ran out (reported by nq_device_error) */
+};
+
+/* Human-readable name of a status code. Never NULL; static storage. */
+const char* nq_status_string(nq_status status);
+
+/* Library version, (major << 16) | minor. */
+int nq_version(void);
+
+/* ---------------------------------------------------------------- packed sizes */
+
+/* Bytes of the packed Q4 codes for a K x N weight: K*N/2. Returns 0 on a bad shape. */
+size_t nq_packed_bytes_q4(int K, int N);
+/* Bytes of the packed Q5 codes (nibble and high planes together): 5*K*N/8. */
+size_t nq_packed_bytes_q5(int K, int N);
+/* Bytes of the packed fp16 scales (either width): 2*N*(K/64). */
+size_t nq_packed_scale_bytes(int K, int N);
+
+/* ---------------------------------------------------------------- offline repack */
+
+/*
+ * nq_pack_q4: canonical Q4 codes and scales -> packed form (one-off, "offline repack").
+ *   wq_canon  device uint32 [N][K/8]     canonical codes
+ *   s_canon   device fp16   [N][K/64]    canonical scales (bit patterns)
+ *   wq_packed device, nq_packed_bytes_q4(K, N) bytes, written
+ *   s_packed  device, nq_packed_scale_bytes(K, N) bytes, written
+ * Pure bit permutation: nq_dequant_q4_debug(packed) reproduces the canonical weights.
+ */
+nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N,
+                     void* wq_packed, void* s_packed, void* stream);
+
+/* nq_pack_q5: as nq_pack_q4 for 5-bit codes given as nibble plane wn_canon [N][K/8] and
+ * high plane wh_canon [N][K/32]; wq_packed holds nq_packed_bytes_q5(K, N) bytes. */
+nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon,
+                     int K, int N, void* wq_packed, void* s_packed, void* stream);
+
+/* ---------------------------------------------------------------- projections */
+
+/*
+ * nq_gemm_q4: Y = X * dequant(Wq, S) for 4-bit codes, 1 <= T <= 8 tokens.
+ *   X  device bf16 [T][K];  Wq, S packed by nq_pack_q4;  Y device bf16 [T][N], written.
+ * Accumulation is fp32; Y is rounded once to bf16. Results are deterministic for a given
+ * device (the split of K across thread blocks depends only on shape and SM count).
+ */
+nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                     void* stream);
+
+/* nq_gemm_q5: as nq_gemm_q4 for 5-bit codes packed by nq_pack_q5 (z = 16). */
+nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                     void* stream);
+
+/*
+ * nq_swiglu_q4: fused gate/up projection of the SwiGLU MLP ("NInfer-4090" release post,
+ * section "V3 做了什么", SwiGLU path at T=8):
+ *   g = X * dequant(Wg, Sg),  u = X * dequant(Wu, Su)   (each [T][N], fp32 accumulation)
+ *   H = bf16(silu(g) * u),    silu(g) = g / (1 + exp(-g)) in fp32
+ *   X device bf16 [T][K]; Wg/Sg and Wu/Su packed by nq_pack_q4 (K x N each);
+ *   H device bf16 [T][N], written. The down projection is nq_gemm_q4 on H.
+ */
+nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu,
+                       const void* Su, void* H, int T, int K, int N, void* stream);
+
+/* ---------------------------------------------------------------- debug dumps */
+
+/*
+ * nq_dequant_q4_debug: decodes the PACKED form with the projection kernels' own decode
+ * and writes W[n][k] = (float)s * (float)(q - 8) in fp32, canonical order [N][K].
+ * The value is exact, so it must equal the CPU definition bit for bit.
+ */
+nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream);
+
+/* nq_dequant_q5_debug: as above for the Q5 packed form (z = 16). */
+nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream);
+
+/* ---------------------------------------------------------------- runtime */
+
+/*
+ * nq_reserve: allocate the current device's workspace for projections of up to
+ * (T_max, K_max, N_max) now, so that later calls of at most that size allocate nothing
+ * (e.g. before capturing a CUDA graph). Synchronises the device.
+ */
+nq_status nq_reserve(int T_max, int K_max, int N_max);
+
+/*
+ * nq_device_error: synchronise the current device, then report and clear the device-side
+ * error flag of its workspace: NQ_OK, or NQ_ERR_TIMEOUT if a bounded wait inside a kernel
+ * ran out since the last check (that call's outputs are then undefined). Clears the
+ * split-K tickets as well, so later calls start clean.
+ */
+nq_status nq_device_error(void);
+
+/* nq_shutdown: free every device workspace of this process (synchronises each device). */
+void nq_shutdown(void);
+
+/*
+ * nq_plan_info: the work split a projection of this shape would use, for inspection and
+ * host-side tests (no GPU needed). mode 0 = gemm, 1 = swiglu. num_sms = SMs to plan for.
+ *   out[0] ctas      thread blocks launched (persistent, at most one per SM)
+ *   out[1] units     work units (one unit = two 16-row tiles x one 64-wide K group)
+ *   out[2] slabs     K slabs (K is cut when T*K activations exceed the on-chip X buffer)
+ *   out[3] slab_groups  64-wide groups per slab (the last slab may be shorter)
+ *   out[4] pairs     row pairs (gemm: pairs of 16-row tiles; swiglu: gate/up tile pairs)
+ *   out[5] ws_slots  fp32 partial-sum slots of the workspace used by this shape
+ *   out[6] stages    shared-memory pipeline stages
+ *   out[7] chunk_groups  K groups per pipeline stage
+ */
+nq_status nq_plan_info(int bits, int mode, int T, int K, int N, int num_sms, int64_t out[8]);
+
+/*
+ * nq_plan_segments: the (slab, pair, first group, end group) runs that thread block `cta`
+ * processes, in order, for the same plan as nq_plan_info. Writes up to `cap` rows of 4
+ * int64 into `seg`; returns the number of runs (which may exceed cap), or a negative status.
+ */
+int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, int cta,
+                         int64_t* seg, int64_t cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NQ_H */

@@ -103,3 +103,22 @@ N_LAYERS = 64
 def layer_seed(layer: int, proj: int) -> int:
     """Per-layer, per-projection seed of the layer-stack sweep."""
     return 1000 * layer + proj
+
+
+# ---------------------------------------------------------------- device-side generators
+# Same recipe, drawn on the GPU with a seeded torch generator: used where the volume makes
+# host generation slow (the benchmark's rotated weight copies and the 64-layer stack).
+# Parity tests use the host generators above.
+
+def device_code_words(rows: int, words: int, gen: "torch.Generator", device) -> "torch.Tensor":
+    return torch.randint(-2**31, 2**31, (rows, words), dtype=torch.int64, generator=gen,
+                         device=device).to(torch.int32)
+
+
+def device_scales(N: int, K: int, gen, device) -> "torch.Tensor":
+    z = torch.randn((N, K // GROUP), generator=gen, device=device, dtype=torch.float32)
+    return (SCALE_BASE * torch.exp(SCALE_SIGMA * z)).to(torch.float16).view(torch.int16)
+
+
+def device_activations(T: int, K: int, gen, device) -> "torch.Tensor":
+    return torch.randn((T, K), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)

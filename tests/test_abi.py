@@ -1,0 +1,101 @@
+"""The C ABI library loads and exports every function include/nq.h declares, and its
+host-only calls (sizes, status strings, argument checks that fail before any CUDA call,
+plan inspection) behave as documented. No GPU compute here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    return nq.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "nq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(nq_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_swiglu_q4",
+                 "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_status_string",
+                 "nq_packed_bytes_q4", "nq_packed_bytes_q5", "nq_packed_scale_bytes"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_sizes_and_strings(L):
+    from weight_only_groupwise_gb300 import nq
+    assert nq.packed_bytes_q4(5120, 17408) == 5120 * 17408 // 2
+    assert nq.packed_bytes_q5(5120, 6144) == 5120 * 6144 * 5 // 8
+    assert nq.packed_scale_bytes(5120, 6144) == 6144 * 80 * 2
+    assert nq.packed_bytes_q4(100, 16) == 0          # K % 64 != 0
+    assert nq.packed_bytes_q4(64, 8) == 0            # N % 16 != 0
+    for s in range(-7, 1):
+        assert nq.status_string(s).startswith("NQ_")
+    assert nq.status_string(-99) == "NQ_ERR_UNKNOWN"
+    assert L.nq_version() >> 16 == 1
+
+
+def test_shape_errors_are_reported_before_any_cuda_call(L):
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(64)
+    p16 = P((ctypes.addressof(buf) + 15) & ~15)
+    assert L.nq_gemm_q4(p16, p16, p16, p16, 9, 64, 16, None) == -2     # T > 8
+    assert L.nq_gemm_q4(p16, p16, p16, p16, -1, 64, 16, None) == -2
+    assert L.nq_gemm_q5(p16, p16, p16, p16, 1, 96, 16, None) == -2     # K % 64
+    assert L.nq_gemm_q4(p16, p16, p16, p16, 1, 64, 24, None) == -2     # N % 16
+    assert L.nq_swiglu_q4(p16, p16, p16, p16, p16, p16, 1, 65, 16, None) == -2
+    assert L.nq_pack_q4(p16, p16, 63, 16, p16, p16, None) == -2
+    assert L.nq_dequant_q5_debug(p16, p16, p16, 64, 17, None) == -2
+
+
+def test_empty_problems_launch_nothing(L):
+    # T == 0 or N == 0: NQ_OK without touching any pointer (NULLs are fine)
+    assert L.nq_gemm_q4(None, None, None, None, 0, 64, 16, None) == 0
+    assert L.nq_gemm_q5(None, None, None, None, 4, 64, 0, None) == 0
+    assert L.nq_swiglu_q4(None, None, None, None, None, None, 0, 64, 16, None) == 0
+
+
+def test_null_alignment_alias_errors(L):
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(4096)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    x, w, s, y = P(base), P(base + 1024), P(base + 2048), P(base + 3072)
+    assert L.nq_gemm_q4(None, w, s, y, 1, 64, 16, None) == -1
+    assert L.nq_gemm_q4(x, w, None, y, 1, 64, 16, None) == -1
+    assert L.nq_swiglu_q4(x, w, s, None, s, y, 1, 64, 16, None) == -1
+    assert L.nq_gemm_q4(P(base + 2), w, s, y, 1, 64, 16, None) == -3    # X misaligned
+    assert L.nq_gemm_q4(x, w, s, P(base + 3080), 1, 64, 16, None) == -3
+    # Y overlapping X / W / S
+    assert L.nq_gemm_q4(x, w, s, x, 1, 64, 16, None) == -4
+    assert L.nq_gemm_q4(x, w, s, P(base + 1024 + 256), 1, 64, 16, None) == -4
+    assert L.nq_gemm_q5(x, w, s, P(base + 2048), 2, 64, 16, None) == -4
+    assert L.nq_pack_q4(x, s, 64, 16, x, y, None) == -4
+
+
+def test_plan_info_matches_workloads(L):
+    from weight_only_groupwise_gb300 import nq
+    p = nq.plan_info(4, 0, 1, 5120, 17408, 152)
+    assert p["ctas"] == 152 and p["pairs"] == 544 and p["units"] == 544 * 80 and p["slabs"] == 1
+    p = nq.plan_info(4, 0, 8, 17408, 5120, 152)   # T=8 down projection needs K slabs
+    assert p["slabs"] == 3 and p["slab_groups"] * 3 >= 272
+    p = nq.plan_info(4, 1, 8, 5120, 17408, 152)   # swiglu pairs gate/up tiles
+    assert p["pairs"] == 1088
+    with pytest.raises(Exception):
+        nq.plan_info(5, 1, 8, 5120, 17408, 152)   # no Q5 swiglu

@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64 CPU oracle on the
+same seeded inputs. Dequantised weights must match bit for bit; outputs within
+max|y - y_ref| / max|y_ref| <= 5e-3 (the bf16 output rounding alone is up to 2^-9 relative)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    return nq
+
+
+# ---------------------------------------------------------------- dequant: bit-exact
+
+DEQ_SHAPES = [(256, 128, 0), (192, 48, 1), (64, 16, 2), (640, 272, 3), (5120, 6144, 4)]
+
+
+@pytest.mark.parametrize("K,N,seed", DEQ_SHAPES)
+def test_dequant_q4_bit_exact(nq, K, N, seed):
+    p = si.q4_problem(1, K, N, seed)
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    w_gpu = nq.dequant_q4_debug(wq, sp, K, N).cpu().numpy()
+    w_ref = oracle.dequant_q4(p["wq"], p["s"], K, N)
+    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("K,N,seed", DEQ_SHAPES)
+def test_dequant_q5_bit_exact(nq, K, N, seed):
+    p = si.q5_problem(1, K, N, seed)
+    wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+    w_gpu = nq.dequant_q5_debug(wq, sp, K, N).cpu().numpy()
+    w_ref = oracle.dequant_q5(p["wn"], p["wh"], p["s"], K, N)
+    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+
+
+def test_dequant_full_size_decode_q4(nq):
+    c = si.DECODE_Q4
+    p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
+    w_gpu = nq.dequant_q4_debug(wq, sp, c["K"], c["N"]).cpu().numpy()
+    w_ref = oracle.dequant_q4(p["wq"], p["s"], c["K"], c["N"])
+    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------- projections, small/ragged
+
+GEMM_SHAPES = [
+    # T, K, N, seed: tiny case, ragged row tiles (odd tile count), one group, several
+    # chunks, every T, K slabs at T=8 (K > 6144) with a ragged last slab
+    (1, 256, 128, 0), (3, 192, 48, 1), (5, 640, 80, 2), (7, 64, 16, 3), (8, 1024, 272, 4),
+    (2, 4096, 496, 5), (4, 2048, 1040, 6), (6, 320, 4112, 7), (8, 6208, 48, 8), (8, 17408, 64, 9),
+    (1, 17408, 32, 10), (8, 12352, 112, 11),
+]
+
+
+@pytest.mark.parametrize("T,K,N,seed", GEMM_SHAPES)
+def test_gemm_q4_parity(nq, T, K, N, seed):
+    p = si.q4_problem(T, K, N, seed)
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, N))
+    y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+    assert gu.rel_err(y, y_ref) <= gu.TOL
+
+
+@pytest.mark.parametrize("T,K,N,seed", GEMM_SHAPES)
+def test_gemm_q5_parity(nq, T, K, N, seed):
+    p = si.q5_problem(T, K, N, seed + 100)
+    wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, sp, N))
+    y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
+    assert gu.rel_err(y, y_ref) <= gu.TOL
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_gemm_every_T(nq, T):
+    K, N = 1536, 208
+    p = si.q4_problem(T, K, N, 50 + T)
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, N))
+    assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)) <= gu.TOL
+    q = si.q5_problem(T, K, N, 60 + T)
+    wq5, sp5 = gu.pack_q5(nq, q["wn"], q["wh"], q["s"], K, N)
+    y5 = gu.host_f64(nq.gemm_q5(gu.dev_bf16(q["x"]), wq5, sp5, N))
+    assert gu.rel_err(y5, oracle.gemm_q5(q["x"], q["wn"], q["wh"], q["s"], T, K, N)) <= gu.TOL
+
+
+SWIGLU_SHAPES = [(8, 256, 48, 0), (1, 640, 16, 1), (5, 1024, 272, 2), (8, 6208, 32, 3), (3, 17408, 48, 4)]
+
+
+@pytest.mark.parametrize("T,K,N,seed", SWIGLU_SHAPES)
+def test_swiglu_q4_parity(nq, T, K, N, seed):
+    p = si.swiglu_problem(T, K, N, seed)
+    wg, sg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu, su = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, sg, wu, su, N))
+    g, u, h_ref_bits = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
+    h_exact = g / (1.0 + np.exp(-g)) * u
+    assert gu.rel_err(h, h_exact) <= gu.TOL
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_workload_tiny_q4(nq):
+    c = si.TINY_Q4
+    p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, c["N"]))
+    assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], c["T"], c["K"], c["N"])) <= gu.TOL
+
+
+def test_workload_decode_q4_full(nq):
+    c = si.DECODE_Q4
+    p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, c["N"]))
+    assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], c["T"], c["K"], c["N"])) <= gu.TOL
+
+
+@pytest.mark.parametrize("T", [8, 1, 2, 4])
+def test_workload_verify_q5_full(nq, T):
+    c = si.VERIFY_Q5
+    p = si.q5_problem(T, c["K"], c["N"], c["seed"])
+    wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], c["K"], c["N"])
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, sp, c["N"]))
+    y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, c["K"], c["N"])
+    assert gu.rel_err(y, y_ref) <= gu.TOL
+
+
+def test_workload_swiglu_block_full(nq):
+    """Gate/up fused with the silu epilogue, then the down projection on the GPU's own H."""
+    c = si.SWIGLU_Q4
+    T, K, N = c["T"], c["K"], c["N"]
+    p = si.swiglu_problem(T, K, N, c["seed"])
+    wg, sg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu, su = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    h_dev = nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, sg, wu, su, N)
+    rows = gu.sample_rows(N, 384, 1)
+    g, u, _ = oracle.swiglu_q4_rows(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, rows)
+    h_exact = (g / (1.0 + np.exp(-g)) * u).T           # [T][rows]
+    h = gu.host_f64(h_dev)
+    assert gu.rel_err(h[:, rows], h_exact) <= gu.TOL
+    # down projection K=17408 -> N=5120 on the GPU's H (decoupled from H's rounding)
+    d = si.SWIGLU_DOWN
+    pd = si.q4_problem(T, d["K"], d["N"], c["seed"] + 1000)
+    wd, sd = gu.pack_q4(nq, pd["wq"], pd["s"], d["K"], d["N"])
+    y = gu.host_f64(nq.gemm_q4(h_dev, wd, sd, d["N"]))
+    h_bits = h_dev.view(torch.int16).cpu().numpy().view(np.uint16)
+    y_ref = oracle.gemm_q4(h_bits, pd["wq"], pd["s"], T, d["K"], d["N"])
+    assert gu.rel_err(y, y_ref) <= gu.TOL
+
+
+@pytest.mark.parametrize("layer", [0, 63])
+@pytest.mark.parametrize("T", [1, 8])
+def test_workload_layer_stack_sampled(nq, layer, T):
+    """One layer of the 64-layer sweep: all six projections, sampled output rows."""
+    x_full = si.activations(si.rng(si.layer_seed(layer, 99)), T, 17408)
+    for j, (name, K, N) in enumerate(si.LAYER_Q4 + si.LAYER_Q5):
+        bits = 4 if j < 3 else 5
+        rows = gu.sample_rows(N, 128, j)
+        x = np.ascontiguousarray(x_full[:, :K])
+        if bits == 4:
+            p = si.q4_problem(T, K, N, si.layer_seed(layer, j))
+            wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, sp, N))
+            y_ref = oracle.gemm_q4_rows(x, p["wq"], p["s"], T, K, rows).T
+        else:
+            p = si.q5_problem(T, K, N, si.layer_seed(layer, j))
+            wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(x), wq, sp, N))
+            y_ref = oracle.gemm_q5_rows(x, p["wn"], p["wh"], p["s"], T, K, rows).T
+        assert gu.rel_err(y[:, rows], y_ref) <= gu.TOL, name
+
+
+# ---------------------------------------------------------------- properties and edges
+
+def test_deterministic_and_zero_point_exact(nq):
+    T, K, N = 8, 6208, 272       # two K slabs, split-K fix-up
+    p = si.q4_problem(T, K, N, 77)
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    x = gu.dev_bf16(p["x"])
+    y1 = nq.gemm_q4(x, wq, sp, N)
+    y2 = nq.gemm_q4(x, wq, sp, N)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    # all codes at the zero point: exactly zero output, however K is split
+    z4, zs = gu.pack_q4(nq, np.full((N, K // 8), 0x88888888, np.uint32), p["s"], K, N)
+    assert torch.count_nonzero(nq.gemm_q4(x, z4, zs, N).float()) == 0
+    z5, zs5 = gu.pack_q5(nq, np.zeros((N, K // 8), np.uint32), np.full((N, K // 32), 0xFFFFFFFF, np.uint32),
+                         p["s"], K, N)
+    assert torch.count_nonzero(nq.gemm_q5(x, z5, zs5, N).float()) == 0
+
+
+def test_one_hot_x_selects_codes(nq):
+    """Unit scales and a one-hot X give Y = q - z exactly (small integers are exact in bf16)."""
+    K, N = 640, 48
+    p = si.q4_problem(1, K, N, 78)
+    s1 = np.full((N, K // 64), 0x3C00, np.uint16)
+    wq, sp = gu.pack_q4(nq, p["wq"], s1, K, N)
+    codes = oracle.dequant_q4(p["wq"], s1, K, N)     # = q - 8 with unit scales
+    x = np.zeros((8, K), np.uint16)
+    ks = [0, 1, 63, 64, 300, 500, 638, 639]
+    for t, k in enumerate(ks):
+        x[t, k] = 0x3F80
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, sp, N))
+    for t, k in enumerate(ks):
+        assert np.array_equal(y[t], codes[:, k].astype(np.float64))
+
+
+def test_empty_and_k0(nq):
+    N = 32
+    x = torch.zeros((2, 0), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((2, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    # K == 0: Y is an empty sum -> zeros
+    from weight_only_groupwise_gb300.nq import _ptr, _stream, lib
+    x16 = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    rc = lib().nq_gemm_q4(_ptr(x16), _ptr(dummy), _ptr(dummy), _ptr(y), 2, 0, N, _stream(None))
+    assert rc == 0
+    assert torch.count_nonzero(y.float()) == 0
+    # T == 0: nothing written
+    y.fill_(3.0)
+    rc = lib().nq_gemm_q5(_ptr(x16), _ptr(dummy), _ptr(dummy), _ptr(y), 0, 64, N, _stream(None))
+    assert rc == 0 and bool((y.float() == 3.0).all())
+
+
+def test_errors_leave_output_untouched(nq):
+    T, K, N = 2, 128, 32
+    p = si.q4_problem(T, K, N, 79)
+    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    x = gu.dev_bf16(p["x"])
+    y = torch.full((T, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    from weight_only_groupwise_gb300.nq import NqError
+    with pytest.raises(NqError) as e:
+        nq.gemm_q4(x, wq, sp, N + 1, out=y)        # N % 16 != 0
+    assert e.value.status == -2
+    xo = torch.empty(T * K + 8, dtype=torch.bfloat16, device="cuda")[1:1 + T * K].view(T, K)
+    with pytest.raises(NqError) as e:
+        nq.gemm_q4(xo, wq, sp, N, out=y)           # misaligned X
+    assert e.value.status == -3
+    with pytest.raises(NqError) as e:
+        nq.gemm_q4(x, wq, sp, N, out=x.view(-1)[:T * N].view(T, N))  # Y aliases X
+    assert e.value.status == -4
+    torch.cuda.synchronize()
+    assert bool((y.float() == 5.0).all())
+    nq.device_error()                               # no device-side wait ran out

@@ -1,0 +1,55 @@
+"""Host logic of the stream-K work split (CPU only): every (slab, pair, group) unit is
+processed by exactly one block, blocks get equal shares, and the split-K partial slots are
+unique and inside the workspace the plan reserves."""
+import pytest
+
+SHAPES = [
+    # bits, mode, T, K, N
+    (4, 0, 1, 256, 128), (4, 0, 1, 5120, 17408), (5, 0, 8, 5120, 6144), (4, 1, 8, 5120, 17408),
+    (4, 0, 8, 17408, 5120), (5, 0, 8, 5120, 1024), (5, 0, 3, 6144, 5120), (4, 0, 8, 6208, 48),
+    (4, 0, 5, 64, 16), (4, 0, 2, 1024, 272), (4, 1, 7, 17408, 48), (5, 0, 1, 64, 16),
+]
+
+
+@pytest.fixture(scope="module")
+def nq():
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    return nq
+
+
+@pytest.mark.parametrize("bits,mode,T,K,N", SHAPES)
+@pytest.mark.parametrize("sms", [152, 148, 7, 1])
+def test_partition_covers_every_unit_once(nq, bits, mode, T, K, N, sms):
+    info = nq.plan_info(bits, mode, T, K, N, sms)
+    G, RP, S, GS = K // 64, info["pairs"], info["slabs"], info["slab_groups"]
+    assert info["ctas"] <= sms and info["units"] == RP * G
+    seen = set()
+    slots = set()
+    per_cta = []
+    fan_in = {}
+    prev_end = None
+    for c in range(info["ctas"]):
+        segs = nq.plan_segments(bits, mode, T, K, N, sms, c)
+        n_units = 0
+        for (s, rp, ga, gb) in segs:
+            assert 0 <= s < S and 0 <= rp < RP and s * GS <= ga < gb <= min(G, (s + 1) * GS)
+            for g in range(ga, gb):
+                assert (rp, g) not in seen
+                seen.add((rp, g))
+            # slot index s*RP + rp + c must be unique and inside the reserved slots
+            slot = s * RP + rp + c
+            assert slot not in slots and slot < info["ws_slots"]
+            slots.add(slot)
+            fan_in[rp] = fan_in.get(rp, 0) + 1
+            # units advance monotonically in slab-major order
+            key = (s, rp, ga)
+            assert prev_end is None or key > prev_end
+            prev_end = key
+            n_units += gb - ga
+        per_cta.append(n_units)
+    assert len(seen) == RP * G
+    assert max(per_cta) - min(per_cta) <= 1          # equal shares
+    # every pair is covered by at least one run per slab
+    assert all(fan_in[rp] >= S for rp in range(RP))

@@ -1,0 +1,487 @@
+// nq_api.cu -- the C ABI of include/nq.h: argument checks, the per-device workspace, the
+// offline repack kernels, the debug dequantisation kernels and the projection launches.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nq.h"
+#include "nq_launch.h"
+
+using namespace nq;
+
+namespace {
+
+// ---------------------------------------------------------------- repack kernels
+
+// Canonical -> packed codes. One thread per (tile, lane): gathers the lane's 32 codes of the
+// tile from the canonical [N][K/8] nibble words (and [N][K/32] high words for Q5) and writes
+// its four fragment words (+ one high word). Nibble i of fragment word j of lane l is the
+// code at row l/4 + 8*((i&3)&1), column 16j + 2(l%4) + 8*((i&3)>>1) + (i>>2) of the tile,
+// which is the m16n8k16 A-fragment order once decode_q4 widens the nibbles.
+template <int BITS>
+__global__ void pack_codes_kernel(const uint32_t* __restrict__ wn, const uint32_t* __restrict__ wh,
+                                  int K, int N, uint32_t* __restrict__ out) {
+    const int G = K / kGroup;
+    const long long total = (long long)(N / kTileRows) * G * 32;
+    constexpr int TW = (BITS == 4 ? kQ4TileBytes : kQ5TileBytes) / 4;  // words per tile
+    const int kw8 = K / 8, kw32 = K / 32;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx & 31);
+        const long long tile = idx >> 5;
+        const int rt = (int)(tile / G), g = (int)(tile % G);
+        const int gid = lane >> 2, c = lane & 3;
+        uint32_t words[4];
+        uint32_t hw = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t wv = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int m = i & 3, hi = i >> 2;
+                const int row = gid + 8 * (m & 1);
+                const int k = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1) + hi;
+                const int n = rt * kTileRows + row;
+                const uint32_t nib = (wn[(size_t)n * kw8 + (k >> 3)] >> (4 * (k & 7))) & 0xFu;
+                wv |= nib << (4 * i);
+                if (BITS == 5) {
+                    const uint32_t bit = (wh[(size_t)n * kw32 + (k >> 5)] >> (k & 31)) & 1u;
+                    const int pos = i < 4 ? 4 * j + i : 16 + 4 * j + (i - 4);
+                    hw |= bit << pos;
+                }
+            }
+            words[j] = wv;
+        }
+        uint32_t* base = out + tile * TW;
+        reinterpret_cast<uint4*>(base)[lane] = make_uint4(words[0], words[1], words[2], words[3]);
+        if (BITS == 5) base[128 + lane] = hw;
+    }
+}
+
+// Canonical [N][K/64] fp16 scales -> per tile 16 halves ordered (r, r+8) for r = 0..7.
+__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N, uint16_t* __restrict__ out) {
+    const int G = K / kGroup;
+    const long long total = (long long)(N / kTileRows) * G * 16;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int e = (int)(idx & 15);
+        const long long tile = idx >> 4;
+        const int rt = (int)(tile / G), g = (int)(tile % G);
+        const int row = (e >> 1) + 8 * (e & 1);
+        out[idx] = s[(size_t)(rt * kTileRows + row) * G + g];
+    }
+}
+
+// Packed -> fp32 W[n][k], decoding with the projection kernels' own decode_q4/decode_q5:
+// w = (float)s * ((128 + q as bf16) - (128 + z)), both steps exact in fp32.
+template <int BITS>
+__global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ sp, int K,
+                               int N, float* __restrict__ w) {
+    const int G = K / kGroup;
+    const long long total = (long long)(N / kTileRows) * G * 32;
+    constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
+    constexpr float off = BITS == 4 ? 136.0f : 144.0f;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx & 31);
+        const long long tile = idx >> 5;
+        const int rt = (int)(tile / G), g = (int)(tile % G);
+        const int gid = lane >> 2, c = lane & 3;
+        const uint8_t* tb = wq + tile * TB;
+        const uint4 wv = reinterpret_cast<const uint4*>(tb)[lane];
+        const uint32_t hb = BITS == 5 ? reinterpret_cast<const uint32_t*>(tb + 512)[lane] : 0u;
+        const uint16_t* st = sp + tile * 16;
+        const float s_lo = __half2float(__ushort_as_half(st[2 * gid]));
+        const float s_hi = __half2float(__ushort_as_half(st[2 * gid + 1]));
+        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t a[4];
+            if (BITS == 4) {
+                decode_q4(ws[j], a);
+            } else {
+                if (j == 0) decode_q5<0>(ws[j], hb, a);
+                if (j == 1) decode_q5<1>(ws[j], hb, a);
+                if (j == 2) decode_q5<2>(ws[j], hb, a);
+                if (j == 3) decode_q5<3>(ws[j], hb, a);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int row = gid + 8 * (m & 1);
+                const int k = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1);
+                const float s = (m & 1) ? s_hi : s_lo;
+                const float lo = __uint_as_float(a[m] << 16) - off;
+                const float hi = __uint_as_float(a[m] & 0xFFFF0000u) - off;
+                float* dst = w + (size_t)(rt * kTileRows + row) * K + k;
+                dst[0] = s * lo;
+                dst[1] = s * hi;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- per-device state
+
+struct DevState {
+    bool init = false;
+    int major = 0, minor = 0, sms = 0;
+    uint8_t* ws = nullptr;     // [err: 256 B][tickets][partials]
+    long long slots_cap = 0;
+    long long tickets_cap = 0;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+bool g_pdl = true;
+bool g_fold = false;
+bool g_env_read = false;
+
+size_t ws_tickets_off() { return 256; }
+size_t ws_partials_off(long long tickets_cap) {
+    return 256 + (((size_t)tickets_cap * 4 + 255) / 256) * 256;
+}
+
+// Device state of the current device (initialised on first use). Returns a status.
+nq_status current_device(DevState** out, int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return NQ_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_env_read) {
+        const char* e = std::getenv("NQ_PDL");
+        if (e && e[0] == '0') g_pdl = false;
+        const char* f = std::getenv("NQ_DECODE");
+        if (f && std::strcmp(f, "fold") == 0) g_fold = true;
+        g_env_read = true;
+    }
+    DevState& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return NQ_ERR_CUDA;
+        d.init = true;
+    }
+    if (d.major != 10 || d.minor != 3) return NQ_ERR_DEVICE;
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return NQ_OK;
+}
+
+// Make the workspace of d hold `slots` partial slots and `tickets` tickets. Growing it
+// synchronises the device (old buffer may be in use) and zero-fills the new one.
+nq_status ensure_workspace(DevState& d, long long slots, long long tickets) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d.ws && slots <= d.slots_cap && tickets <= d.tickets_cap) return NQ_OK;
+    long long sc = d.slots_cap > slots ? d.slots_cap : slots;
+    long long tc = d.tickets_cap > tickets ? d.tickets_cap : tickets;
+    if (sc < 1024) sc = 1024;
+    if (tc < 4096) tc = 4096;
+    const size_t bytes = ws_partials_off(tc) + (size_t)sc * kPartialFloats * sizeof(float);
+    if (d.ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return NQ_ERR_CUDA;
+        cudaFree(d.ws);
+        d.ws = nullptr;
+        d.slots_cap = d.tickets_cap = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return NQ_ERR_CUDA;
+    if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(p);
+        return NQ_ERR_CUDA;
+    }
+    d.ws = static_cast<uint8_t*>(p);
+    d.slots_cap = sc;
+    d.tickets_cap = tc;
+    return NQ_OK;
+}
+
+// ---------------------------------------------------------------- argument checks
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+constexpr long long kMaxDim = 1 << 20;  // K, N bound: keeps every index well inside 64 bits
+
+nq_status check_shape(int K, int N) {
+    if (K < 0 || N < 0 || K > kMaxDim || N > kMaxDim) return NQ_ERR_SHAPE;
+    if (K % kGroup != 0 || N % kTileRows != 0) return NQ_ERR_SHAPE;
+    return NQ_OK;
+}
+
+size_t packed_codes(int bits, int K, int N) {
+    return (size_t)K * N / 8 * (bits == 4 ? 4 : 5);
+}
+size_t packed_scales(int K, int N) { return (size_t)N * (K / kGroup) * 2; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int grid_for(long long work, int per_block) {
+    long long b = (work + per_block - 1) / per_block;
+    if (b > 65535LL * 16) b = 65535LL * 16;
+    return (int)(b < 1 ? 1 : b);
+}
+
+// Shared body of the three projection entry points.
+nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0,
+                  const void* W1, const void* S1, void* Y, int T, int K, int N, void* stream) {
+    if (T < 0 || T > 8) return NQ_ERR_SHAPE;
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    if (T == 0 || N == 0) return NQ_OK;  // empty output
+    if (!X || !W0 || !S0 || !Y || (swiglu && (!W1 || !S1))) return NQ_ERR_NULL;
+    if (misaligned(X) || misaligned(W0) || misaligned(S0) || misaligned(Y) ||
+        (swiglu && (misaligned(W1) || misaligned(S1))))
+        return NQ_ERR_ALIGN;
+    const size_t xb = (size_t)T * K * 2, yb = (size_t)T * N * 2;
+    const size_t cb = packed_codes(bits, K, N), sb = packed_scales(K, N);
+    if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, cb) || overlap(Y, yb, S0, sb) ||
+        (swiglu && (overlap(Y, yb, W1, cb) || overlap(Y, yb, S1, sb))))
+        return NQ_ERR_ALIAS;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    if (K == 0) {  // empty sum
+        return cudaMemsetAsync(Y, 0, yb, as_stream(stream)) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+    }
+    ProjArgs a;
+    if (!make_plan(bits, swiglu ? 1 : 0, T, K, N, d->sms, a.p)) return NQ_ERR_SHAPE;
+    st = ensure_workspace(*d, a.p.slots, a.p.RP);
+    if (st != NQ_OK) return st;
+    a.X = static_cast<const uint16_t*>(X);
+    a.W0 = static_cast<const uint8_t*>(W0);
+    a.S0 = static_cast<const uint8_t*>(S0);
+    a.W1 = static_cast<const uint8_t*>(swiglu ? W1 : W0);
+    a.S1 = static_cast<const uint8_t*>(swiglu ? S1 : S0);
+    a.Y = static_cast<uint16_t*>(Y);
+    a.dev_err = reinterpret_cast<int*>(d->ws);
+    a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
+    a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
+    cudaError_t e;
+    if (swiglu)
+        e = launch_proj_swiglu_q4(a, as_stream(stream), g_pdl, g_fold);
+    else if (bits == 4)
+        e = launch_proj_q4(a, as_stream(stream), g_pdl, g_fold);
+    else
+        e = launch_proj_q5(a, as_stream(stream), g_pdl, g_fold);
+    return e == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N,
+               void* wq_packed, void* s_packed, void* stream) {
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    if (K == 0 || N == 0) return NQ_OK;
+    if (!wn || !s || !wq_packed || !s_packed || (bits == 5 && !wh)) return NQ_ERR_NULL;
+    if (misaligned(wn) || misaligned(s) || misaligned(wq_packed) || misaligned(s_packed) ||
+        (bits == 5 && misaligned(wh)))
+        return NQ_ERR_ALIGN;
+    const size_t cb = packed_codes(bits, K, N), sb = packed_scales(K, N);
+    const size_t in_n = (size_t)N * K / 2, in_h = (size_t)N * K / 8, in_s = sb;
+    for (const void* o : {wq_packed, s_packed}) {
+        const size_t ob = o == wq_packed ? cb : sb;
+        if (overlap(o, ob, wn, in_n) || overlap(o, ob, s, in_s) || (bits == 5 && overlap(o, ob, wh, in_h)))
+            return NQ_ERR_ALIAS;
+    }
+    if (overlap(wq_packed, cb, s_packed, sb)) return NQ_ERR_ALIAS;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
+    if (bits == 4)
+        pack_codes_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
+            wn, nullptr, K, N, static_cast<uint32_t*>(wq_packed));
+    else
+        pack_codes_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
+            wn, wh, K, N, static_cast<uint32_t*>(wq_packed));
+    if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
+    pack_scales_kernel<<<grid_for(lanes / 2, 256), 256, 0, as_stream(stream)>>>(
+        s, K, N, static_cast<uint16_t*>(s_packed));
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+nq_status dequant(int bits, const void* wq, const void* s, float* w, int K, int N, void* stream) {
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    if (K == 0 || N == 0) return NQ_OK;
+    if (!wq || !s || !w) return NQ_ERR_NULL;
+    if (misaligned(wq) || misaligned(s) || misaligned(w)) return NQ_ERR_ALIGN;
+    const size_t wb = (size_t)N * K * 4;
+    if (overlap(w, wb, wq, packed_codes(bits, K, N)) || overlap(w, wb, s, packed_scales(K, N)))
+        return NQ_ERR_ALIAS;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
+    if (bits == 4)
+        dequant_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
+            static_cast<const uint8_t*>(wq), static_cast<const uint16_t*>(s), K, N, w);
+    else
+        dequant_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
+            static_cast<const uint8_t*>(wq), static_cast<const uint16_t*>(s), K, N, w);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+const char* nq_status_string(nq_status s) {
+    switch (s) {
+        case NQ_OK: return "NQ_OK";
+        case NQ_ERR_NULL: return "NQ_ERR_NULL: a required pointer is NULL";
+        case NQ_ERR_SHAPE: return "NQ_ERR_SHAPE: need K % 64 == 0, N % 16 == 0, 0 <= T <= 8";
+        case NQ_ERR_ALIGN: return "NQ_ERR_ALIGN: pointers must be 16-byte aligned";
+        case NQ_ERR_ALIAS: return "NQ_ERR_ALIAS: an output overlaps an input";
+        case NQ_ERR_CUDA: return "NQ_ERR_CUDA: a CUDA call or launch failed";
+        case NQ_ERR_DEVICE: return "NQ_ERR_DEVICE: current device is not sm_103 (GB300)";
+        case NQ_ERR_TIMEOUT: return "NQ_ERR_TIMEOUT: a bounded device-side wait ran out";
+        default: return "NQ_ERR_UNKNOWN";
+    }
+}
+
+int nq_version(void) { return (1 << 16) | 0; }
+
+size_t nq_packed_bytes_q4(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_codes(4, K, N) : 0; }
+size_t nq_packed_bytes_q5(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_codes(5, K, N) : 0; }
+size_t nq_packed_scale_bytes(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_scales(K, N) : 0; }
+
+nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* wq_packed,
+                     void* s_packed, void* stream) {
+    return pack(4, wq_canon, nullptr, s_canon, K, N, wq_packed, s_packed, stream);
+}
+
+nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon, int K,
+                     int N, void* wq_packed, void* s_packed, void* stream) {
+    return pack(5, wn_canon, wh_canon, s_canon, K, N, wq_packed, s_packed, stream);
+}
+
+nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                     void* stream) {
+    return project(4, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
+}
+
+nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                     void* stream) {
+    return project(5, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
+}
+
+nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su,
+                       void* H, int T, int K, int N, void* stream) {
+    return project(4, true, X, Wg, Sg, Wu, Su, H, T, K, N, stream);
+}
+
+nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
+    return dequant(4, Wq, S, W, K, N, stream);
+}
+
+nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
+    return dequant(5, Wq, S, W, K, N, stream);
+}
+
+nq_status nq_reserve(int T_max, int K_max, int N_max) {
+    if (T_max < 1 || T_max > 8) return NQ_ERR_SHAPE;
+    nq_status st = check_shape(K_max, N_max);
+    if (st != NQ_OK) return st;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    long long slots = 0, tickets = 0;
+    // The largest plan over T <= T_max and both modes bounds every smaller call.
+    for (int T = 1; T <= T_max; ++T)
+        for (int mode = 0; mode < 2; ++mode) {
+            Plan p;
+            make_plan(4, mode, T, K_max > 0 ? K_max : 64, N_max > 0 ? N_max : 16, d->sms, p);
+            if (p.slots > slots) slots = p.slots;
+            if (p.RP > tickets) tickets = p.RP;
+        }
+    return ensure_workspace(*d, slots, tickets);
+}
+
+nq_status nq_device_error(void) {
+    DevState* d = nullptr;
+    nq_status st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return NQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!d->ws) return NQ_OK;
+    int err = 0;
+    if (cudaMemcpy(&err, d->ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NQ_ERR_CUDA;
+    if (err == 0) return NQ_OK;
+    if (cudaMemset(d->ws, 0, ws_partials_off(d->tickets_cap)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return NQ_ERR_CUDA;
+    return NQ_ERR_TIMEOUT;
+}
+
+void nq_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (int i = 0; i < kMaxDevices; ++i) {
+        if (!g_dev[i].ws) continue;
+        cudaSetDevice(i);
+        cudaDeviceSynchronize();
+        cudaFree(g_dev[i].ws);
+        g_dev[i].ws = nullptr;
+        g_dev[i].slots_cap = g_dev[i].tickets_cap = 0;
+    }
+    cudaSetDevice(cur);
+}
+
+nq_status nq_plan_info(int bits, int mode, int T, int K, int N, int num_sms, int64_t out[8]) {
+    if (!out) return NQ_ERR_NULL;
+    if ((bits != 4 && bits != 5) || (mode != 0 && mode != 1) || (mode == 1 && bits != 4)) return NQ_ERR_SHAPE;
+    if (T < 1 || T > 8 || K < kGroup || N < kTileRows || num_sms < 1) return NQ_ERR_SHAPE;
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    Plan p;
+    if (!make_plan(bits, mode, T, K, N, num_sms, p)) return NQ_ERR_SHAPE;
+    out[0] = p.P;
+    out[1] = p.U;
+    out[2] = p.S;
+    out[3] = p.GS;
+    out[4] = p.RP;
+    out[5] = p.slots;
+    out[6] = p.stages;
+    out[7] = p.CG;
+    return NQ_OK;
+}
+
+int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, int cta, int64_t* seg,
+                         int64_t cap) {
+    int64_t info[8];
+    nq_status st = nq_plan_info(bits, mode, T, K, N, num_sms, info);
+    if (st != NQ_OK) return st;
+    Plan p;
+    make_plan(bits, mode, T, K, N, num_sms, p);
+    if (cta < 0 || cta >= p.P) return NQ_ERR_SHAPE;
+    if (cap > 0 && !seg) return NQ_ERR_NULL;
+    int64_t n = 0;
+    const long long u1 = cta_begin(p, cta + 1);
+    for (long long u = cta_begin(p, cta); u < u1;) {
+        const Segment sg = segment_at(p, u, u1);
+        if (n < cap) {
+            seg[4 * n + 0] = sg.s;
+            seg[4 * n + 1] = sg.rp;
+            seg[4 * n + 2] = sg.ga;
+            seg[4 * n + 3] = sg.gb;
+        }
+        ++n;
+        u = sg.u_next;
+    }
+    return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,291 @@
+// nq_common.cuh -- layout constants, the work plan and PTX helpers shared by the kernels
+// of the groupwise int4/int5 small-batch projection (sm_103a).
+//
+// Packed layout (this library's definition; the pages give none):
+//   The K x N weight is cut into tiles of 16 output rows x one 64-wide K group.
+//   Tile (rt, g) -- rt = n / 16, g = k / 64 -- sits at index rt * G + g (G = K / 64), so the
+//   groups of one row tile are contiguous. Inside a tile, lane l (0..31) of a warp owns 16
+//   bytes = four uint32 code words, one per 16-wide K step j: the word is exactly the lane's
+//   bf16 A-operand fragment of an m16n8k16 tensor-core MMA for that step once each nibble is
+//   widened to a 16-bit half (see decode_q4). Q5 tiles append one uint32 of high bits per
+//   lane (128 bytes per tile). Scales: 16 fp16 per tile, ordered (row r, row r+8) for
+//   r = 0..7, so lane l reads one uint32 holding the scales of its rows l/4 and l/4+8.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define NQ_HD __host__ __device__ __forceinline__
+#else
+#define NQ_HD inline
+#endif
+
+namespace nq {
+
+constexpr int kGroup = 64;           // K elements per scale group
+constexpr int kTileRows = 16;        // output rows per tile (MMA M)
+constexpr int kQ4TileBytes = 512;    // 16 x 64 nibbles
+constexpr int kQ5TileBytes = 640;    // + 16 x 64 high bits
+constexpr int kScaleTileBytes = 32;  // 16 fp16
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kChunkGroups = 16;     // K groups per pipeline stage
+constexpr int kMaxStages = 12;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kXBudget = 96 * 1024;  // on-chip activation slab
+constexpr int kMinUnitsPerCta = 16;
+constexpr int kPartialFloats = 256;  // 2 M tiles x 16 rows x 8 tokens
+constexpr long long kWaitTimeoutNs = 2000000000LL;  // 2 s per bounded wait
+
+// Errors a kernel can raise through the workspace flag word.
+constexpr int kDevErrTimeout = 1;
+
+NQ_HD int tpad(int T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
+
+// The work split of one projection call. One "unit" is one 64-wide K group of one row pair
+// (two 16-row tiles; for SwiGLU the gate tile and the up tile of the same rows). Units are
+// ordered slab-major: for each K slab, for each pair, the slab's groups. The persistent
+// grid of P blocks takes equal contiguous ranges of units ("stream-K"), so every block
+// streams the same number of weight bytes whatever the shape.
+struct Plan {
+    int bits, mode, T, TP, K, N, G, RT, RP;
+    int GS, S;             // groups per slab (last slab may be shorter), slab count
+    long long U;           // units
+    int P;                 // blocks
+    int CG, stages;
+    long long slots;       // partial-sum slots: S * RP + P
+    int tile_bytes, stage_bytes, x_bytes, corr_bytes, red_bytes, bar_bytes, smem_bytes;
+};
+
+NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan& p) {
+    p.bits = bits;
+    p.mode = mode;
+    p.T = T;
+    p.TP = tpad(T);
+    p.K = K;
+    p.N = N;
+    p.G = K / kGroup;
+    p.RT = N / kTileRows;
+    p.RP = mode ? p.RT : (p.RT + 1) / 2;
+    // Largest slab whose T padded activation rows plus one zero row fit the X budget.
+    const int Tr = T > 0 ? T : 1;
+    int gs_max = ((kXBudget - 16) / Tr - 16) / 128;
+    if (gs_max < 1) gs_max = 1;
+    p.S = (p.G + gs_max - 1) / gs_max;
+    if (p.S < 1) p.S = 1;
+    p.GS = (p.G + p.S - 1) / p.S;
+    p.U = (long long)p.RP * p.G;
+    long long P = p.U / kMinUnitsPerCta;
+    if (P > num_sms) P = num_sms;
+    if (P < 1) P = 1;
+    p.P = (int)P;
+    p.CG = kChunkGroups;
+    p.tile_bytes = bits == 4 ? kQ4TileBytes : kQ5TileBytes;
+    p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
+    p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
+    p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;
+    p.red_bytes = kConsumerWarps * 2 * 512;
+    p.bar_bytes = 256;  // full/empty per stage, x_full, x_empty, flags
+    const int fixed = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes;
+    int st = (kSmemLimit - fixed) / p.stage_bytes;
+    if (st > kMaxStages) st = kMaxStages;
+    p.stages = st;
+    p.smem_bytes = fixed + st * p.stage_bytes;
+    p.slots = (long long)p.S * p.RP + p.P;
+    return st >= 2;
+}
+
+NQ_HD int slab_groups(const Plan& p, int s) { return s < p.S - 1 ? p.GS : p.G - (p.S - 1) * p.GS; }
+NQ_HD long long slab_base(const Plan& p, int s) { return (long long)s * p.RP * p.GS; }
+NQ_HD long long cta_begin(const Plan& p, int c) { return (long long)c * p.U / p.P; }
+// Block that owns unit u: the largest c with cta_begin(c) <= u.
+NQ_HD int cta_of(const Plan& p, long long u) { return (int)(((u + 1) * p.P - 1) / p.U); }
+
+// One run of consecutive units of one block inside one (slab, pair).
+struct Segment {
+    int s, rp, ga, gb;     // slab, pair, groups [ga, gb) in K-group numbering
+    long long u_next;      // first unit after the segment
+};
+
+NQ_HD Segment segment_at(const Plan& p, long long u, long long u_end) {
+    Segment sg;
+    long long s = u / ((long long)p.RP * p.GS);
+    if (s > p.S - 1) s = p.S - 1;
+    sg.s = (int)s;
+    const int gs = slab_groups(p, sg.s);
+    const long long off = u - slab_base(p, sg.s);
+    sg.rp = (int)(off / gs);
+    const int gl = (int)(off % gs);
+    const long long run_end = slab_base(p, sg.s) + (long long)(sg.rp + 1) * gs;
+    const long long e = run_end < u_end ? run_end : u_end;
+    sg.ga = sg.s * p.GS + gl;
+    sg.gb = sg.ga + (int)(e - u);
+    sg.u_next = e;
+    return sg;
+}
+
+// Number of (block, slab) runs that contribute to pair rp: the split-K fan-in.
+NQ_HD int contributions(const Plan& p, int rp) {
+    int c = 0;
+    for (int s = 0; s < p.S; ++s) {
+        const int gs = slab_groups(p, s);
+        const long long a = slab_base(p, s) + (long long)rp * gs;
+        c += cta_of(p, a + gs - 1) - cta_of(p, a) + 1;
+    }
+    return c;
+}
+
+// Partial-sum slot of the segment (s, rp) of block c. Unique because segments advance
+// monotonically in both the run index s*RP+rp and the block index.
+NQ_HD long long slot_of(const Plan& p, int s, int rp, int c) { return (long long)s * p.RP + rp + c; }
+
+}  // namespace nq
+
+#if defined(__CUDACC__)
+namespace nq {
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase. Returns false (and raises the block's abort flag and
+// the device error word) if the phase does not complete within kWaitTimeoutNs, or at once if
+// the block has already aborted. Never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* dev_err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (*abort_flag) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > (uint64_t)kWaitTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(dev_err, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies in flight before exit).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// One-dimensional bulk async copy global -> shared (TMA engine), completing on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Same copy without an L2 eviction hint (activations: re-read by every block).
+__device__ __forceinline__ void bulk_g2s_keep(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- code decode
+//
+// bf16 0x4300 is 128.0 with a unit step in its 7 fraction bits, so OR-ing a code q < 128
+// into the low bits gives exactly the bf16 value 128 + q. The projection kernels feed
+// 128 + q to the tensor cores and fold the constant -(128 + z) * sum(x) into the MMA's
+// starting accumulator, so no per-weight subtraction is needed.
+constexpr uint32_t kBf16Magic = 0x43004300u;
+
+// Four bf16x2 A-fragment registers (values 128 + q) from one packed Q4 word: register m
+// holds nibble m in its low half and nibble m + 4 in its high half.
+__device__ __forceinline__ void decode_q4(uint32_t w, uint32_t a[4]) {
+    a[0] = (w & 0x000F000Fu) | kBf16Magic;
+    a[1] = ((w >> 4) & 0x000F000Fu) | kBf16Magic;
+    a[2] = ((w >> 8) & 0x000F000Fu) | kBf16Magic;
+    a[3] = ((w >> 12) & 0x000F000Fu) | kBf16Magic;
+}
+
+// Q5: as decode_q4, plus bit 4 of each code from the lane's high word h. For K step J the
+// high bit of nibble m (m < 4) sits at bit 4J + m and that of nibble m + 4 at bit 16 + 4J + m,
+// so one shift moves both onto bits 4 and 20.
+template <int J>
+__device__ __forceinline__ void decode_q5(uint32_t w, uint32_t h, uint32_t a[4]) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int sh = 4 * J + m - 4;
+        const uint32_t hb = sh >= 0 ? (h >> sh) : (h << (-sh));
+        a[m] = ((w >> (4 * m)) & 0x000F000Fu) | (hb & 0x00100010u) | kBf16Magic;
+    }
+}
+
+}  // namespace nq
+#endif

@@ -1,0 +1,43 @@
+// nq_launch.h -- internal launchers of the projection kernel instantiations.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "nq_proj.cuh"
+
+namespace nq {
+
+// Launch proj_kernel<BITS, SWIGLU> with a.p's grid and shared memory on `stream`.
+// pdl: allow programmatic dependent launch behind the preceding kernel of the stream.
+// fold: use the 128+q encoding with the offset folded into the accumulator (else exact q - z).
+cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl, bool fold);
+cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl, bool fold);
+cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl, bool fold);
+
+template <int BITS, bool SWIGLU, bool FOLD>
+cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
+    auto kern = proj_kernel<BITS, SWIGLU, FOLD>;
+    // The shared-memory opt-in is per device; set it on every launch of a new size class
+    // (cheap: the driver caches it) rather than tracking devices here.
+    static thread_local int set_for_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (set_for_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        set_for_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.p.P);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = a.p.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace nq
