@@ -203,8 +203,7 @@ def build_step(nq, w: dict, dev, T_override=None):
         fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
 
         def step(i):
-            wq, sp = copies[i % R]
-            fn(x, wq, sp, N, out=y)
+            fn(x, copies[i % R], N, out=y)
         return step, b, R, f"rotate {R} packed weight copies ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     if w["kind"] == "swiglu":
         T, K, N, Kd, Nd = T_override or w["T"], w["K"], w["N"], w["Kd"], w["Nd"]
@@ -219,8 +218,8 @@ def build_step(nq, w: dict, dev, T_override=None):
 
         def step(i):
             j = i % R
-            nq.swiglu_q4(x, gate[j][0], gate[j][1], up[j][0], up[j][1], N, out=h)
-            nq.gemm_q4(h, down[j][0], down[j][1], Nd, out=y)
+            nq.swiglu_q4(x, gate[j], up[j], N, out=h)
+            nq.gemm_q4(h, down[j], Nd, out=y)
         return step, b, R, f"rotate {R} weight sets ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     # layer stack: 64 independent layers, ~12 GB of packed weights (no reuse within a pass)
     T, L = T_override or w["T"], w["layers"]
@@ -236,15 +235,19 @@ def build_step(nq, w: dict, dev, T_override=None):
     x = si.device_activations(T, 5120, gen, dev)
     x6 = si.device_activations(T, 6144, gen, dev)
     h = torch.empty((T, 17408), dtype=torch.bfloat16, device=dev)
-    y = torch.empty((T, 6144), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty((T, 5120), dtype=torch.bfloat16, device=dev)
+    yq = torch.empty((T, 6144), dtype=torch.bfloat16, device=dev)
+    ykv = torch.empty((T, 1024), dtype=torch.bfloat16, device=dev)
+    yo = torch.empty((T, 5120), dtype=torch.bfloat16, device=dev)
+    y = (yd, yq, ykv, yo)
 
     def step(i):
         for ly in layers:
-            nq.swiglu_q4(x, ly["gate"][0], ly["gate"][1], ly["up"][0], ly["up"][1], 17408, out=h)
-            nq.gemm_q4(h, ly["down"][0], ly["down"][1], 5120, out=y[:, :5120])
-            nq.gemm_q5(x, ly["qg"][0], ly["qg"][1], 6144, out=y)
-            nq.gemm_q5(x, ly["kv"][0], ly["kv"][1], 1024, out=y[:, :1024])
-            nq.gemm_q5(x6, ly["out"][0], ly["out"][1], 5120, out=y[:, :5120])
+            nq.swiglu_q4(x, ly["gate"], ly["up"], 17408, out=h)
+            nq.gemm_q4(h, ly["down"], 5120, out=yd)
+            nq.gemm_q5(x, ly["qg"], 6144, out=yq)
+            nq.gemm_q5(x, ly["kv"], 1024, out=ykv)
+            nq.gemm_q5(x6, ly["out"], 5120, out=yo)
     w2 = dict(w, T=T)
     return step, workload_bytes(w2), 1, "64 distinct layers (~12 GB) per pass, no reuse", (x, y)
 
@@ -295,8 +298,7 @@ def time_e2e(nq, w: dict, steps: int, warmup: int, stream, dev):
 
     def step(i):
         xd.copy_(xs[i % 4], non_blocking=True)
-        wq, sp = copies[i % R]
-        fn(xd, wq, sp, N, out=yd)
+        fn(xd, copies[i % R], N, out=yd)
         ys[i % 4].copy_(yd, non_blocking=True)
 
     with torch.cuda.stream(stream):

@@ -21,10 +21,11 @@
  *   Wh   uint32 [N][K/32]  Q5 high bits: bit i of word j is bit 4 of q[n, 32j+i]
  *   S    fp16   [N][K/64]  one scale per (output row n, 64-wide group of K)
  *
- * Packed layout: nq_pack_* rewrites the canonical codes and scales into an opaque,
- * kernel-friendly tile order (16 output rows x one 64-wide K group per tile). Its size
- * depends only on (bits, K, N) and is given by nq_packed_*_bytes. The projection calls take
- * the packed form only.
+ * Packed layout: nq_pack_* rewrites the canonical codes and scales into ONE opaque,
+ * kernel-friendly buffer: tiles of 16 output rows x one 64-wide K group, in blocks of 16
+ * groups per row tile, each block holding its codes followed by its scales, so one bulk copy
+ * fetches both. Its size depends only on (bits, K, N), is exactly codes + scales (no padding,
+ * no header) and is given by nq_packed_bytes_*. The projection calls take the packed form.
  *
  * Conventions for every call:
  *   - Pointers are DEVICE pointers on the current CUDA device, owned by the caller; the
@@ -75,68 +76,64 @@ int nq_version(void);
 
 /* ---------------------------------------------------------------- packed sizes */
 
-/* Bytes of the packed Q4 codes for a K x N weight: K*N/2. Returns 0 on a bad shape. */
+/* Bytes of a packed Q4 weight (codes and scales): K*N/2 + 2*N*(K/64). 0 on a bad shape. */
 size_t nq_packed_bytes_q4(int K, int N);
-/* Bytes of the packed Q5 codes (nibble and high planes together): 5*K*N/8. */
+/* Bytes of a packed Q5 weight (nibble plane, high plane, scales): 5*K*N/8 + 2*N*(K/64). */
 size_t nq_packed_bytes_q5(int K, int N);
-/* Bytes of the packed fp16 scales (either width): 2*N*(K/64). */
-size_t nq_packed_scale_bytes(int K, int N);
 
 /* ---------------------------------------------------------------- offline repack */
 
 /*
- * nq_pack_q4: canonical Q4 codes and scales -> packed form (one-off, "offline repack").
+ * nq_pack_q4: canonical Q4 codes and scales -> packed weight (one-off, "offline repack").
  *   wq_canon  device uint32 [N][K/8]     canonical codes
  *   s_canon   device fp16   [N][K/64]    canonical scales (bit patterns)
- *   wq_packed device, nq_packed_bytes_q4(K, N) bytes, written
- *   s_packed  device, nq_packed_scale_bytes(K, N) bytes, written
+ *   packed    device, nq_packed_bytes_q4(K, N) bytes, written
  * Pure bit permutation: nq_dequant_q4_debug(packed) reproduces the canonical weights.
  */
-nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N,
-                     void* wq_packed, void* s_packed, void* stream);
+nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* packed,
+                     void* stream);
 
 /* nq_pack_q5: as nq_pack_q4 for 5-bit codes given as nibble plane wn_canon [N][K/8] and
- * high plane wh_canon [N][K/32]; wq_packed holds nq_packed_bytes_q5(K, N) bytes. */
+ * high plane wh_canon [N][K/32]; packed holds nq_packed_bytes_q5(K, N) bytes. */
 nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon,
-                     int K, int N, void* wq_packed, void* s_packed, void* stream);
+                     int K, int N, void* packed, void* stream);
 
 /* ---------------------------------------------------------------- projections */
 
 /*
- * nq_gemm_q4: Y = X * dequant(Wq, S) for 4-bit codes, 1 <= T <= 8 tokens.
- *   X  device bf16 [T][K];  Wq, S packed by nq_pack_q4;  Y device bf16 [T][N], written.
+ * nq_gemm_q4: Y = X * dequant(W) for 4-bit codes, 1 <= T <= 8 tokens.
+ *   X  device bf16 [T][K];  W packed by nq_pack_q4 (codes and scales);
+ *   Y  device bf16 [T][N], written.
  * Accumulation is fp32; Y is rounded once to bf16. Results are deterministic for a given
  * device (the split of K across thread blocks depends only on shape and SM count).
  */
-nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
-                     void* stream);
+nq_status nq_gemm_q4(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
 
 /* nq_gemm_q5: as nq_gemm_q4 for 5-bit codes packed by nq_pack_q5 (z = 16). */
-nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
-                     void* stream);
+nq_status nq_gemm_q5(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
 
 /*
  * nq_swiglu_q4: fused gate/up projection of the SwiGLU MLP ("NInfer-4090" release post,
  * section "V3 做了什么", SwiGLU path at T=8):
- *   g = X * dequant(Wg, Sg),  u = X * dequant(Wu, Su)   (each [T][N], fp32 accumulation)
+ *   g = X * dequant(Wg),  u = X * dequant(Wu)   (each [T][N], fp32 accumulation)
  *   H = bf16(silu(g) * u),    silu(g) = g / (1 + exp(-g)) in fp32
- *   X device bf16 [T][K]; Wg/Sg and Wu/Su packed by nq_pack_q4 (K x N each);
+ *   X device bf16 [T][K]; Wg and Wu packed by nq_pack_q4 (K x N each);
  *   H device bf16 [T][N], written. The down projection is nq_gemm_q4 on H.
  */
-nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu,
-                       const void* Su, void* H, int T, int K, int N, void* stream);
+nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N,
+                       void* stream);
 
 /* ---------------------------------------------------------------- debug dumps */
 
 /*
- * nq_dequant_q4_debug: decodes the PACKED form with the projection kernels' own decode
- * and writes W[n][k] = (float)s * (float)(q - 8) in fp32, canonical order [N][K].
+ * nq_dequant_q4_debug: decodes the PACKED weight with the projection kernels' own decode
+ * and writes out[n][k] = (float)s * (float)(q - 8) in fp32, canonical order [N][K].
  * The value is exact, so it must equal the CPU definition bit for bit.
  */
-nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream);
+nq_status nq_dequant_q4_debug(const void* W, float* out, int K, int N, void* stream);
 
-/* nq_dequant_q5_debug: as above for the Q5 packed form (z = 16). */
-nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream);
+/* nq_dequant_q5_debug: as above for a Q5 packed weight (z = 16). */
+nq_status nq_dequant_q5_debug(const void* W, float* out, int K, int N, void* stream);
 
 /* ---------------------------------------------------------------- runtime */
 

@@ -23,6 +23,7 @@ def host_f64(t: torch.Tensor) -> np.ndarray:
 
 
 def pack_q4(nq, wq: np.ndarray, s: np.ndarray, K: int, N: int):
+    """Packed weight (one uint8 device tensor)."""
     return nq.pack_q4(dev_u32(wq), dev_u16(s), K, N)
 
 

@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_swiglu_q4",
                  "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_status_string",
-                 "nq_packed_bytes_q4", "nq_packed_bytes_q5", "nq_packed_scale_bytes"):
+                 "nq_packed_bytes_q4", "nq_packed_bytes_q5"):
         assert must in names
 
 
@@ -41,9 +41,9 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_sizes_and_strings(L):
     from weight_only_groupwise_gb300 import nq
-    assert nq.packed_bytes_q4(5120, 17408) == 5120 * 17408 // 2
-    assert nq.packed_bytes_q5(5120, 6144) == 5120 * 6144 * 5 // 8
-    assert nq.packed_scale_bytes(5120, 6144) == 6144 * 80 * 2
+    # packed = codes + fp16 scales, nothing else
+    assert nq.packed_bytes_q4(5120, 17408) == 5120 * 17408 // 2 + 17408 * 80 * 2
+    assert nq.packed_bytes_q5(5120, 6144) == 5120 * 6144 * 5 // 8 + 6144 * 80 * 2
     assert nq.packed_bytes_q4(100, 16) == 0          # K % 64 != 0
     assert nq.packed_bytes_q4(64, 8) == 0            # N % 16 != 0
     for s in range(-7, 1):
@@ -56,20 +56,20 @@ def test_shape_errors_are_reported_before_any_cuda_call(L):
     P = ctypes.c_void_p
     buf = ctypes.create_string_buffer(64)
     p16 = P((ctypes.addressof(buf) + 15) & ~15)
-    assert L.nq_gemm_q4(p16, p16, p16, p16, 9, 64, 16, None) == -2     # T > 8
-    assert L.nq_gemm_q4(p16, p16, p16, p16, -1, 64, 16, None) == -2
-    assert L.nq_gemm_q5(p16, p16, p16, p16, 1, 96, 16, None) == -2     # K % 64
-    assert L.nq_gemm_q4(p16, p16, p16, p16, 1, 64, 24, None) == -2     # N % 16
-    assert L.nq_swiglu_q4(p16, p16, p16, p16, p16, p16, 1, 65, 16, None) == -2
-    assert L.nq_pack_q4(p16, p16, 63, 16, p16, p16, None) == -2
-    assert L.nq_dequant_q5_debug(p16, p16, p16, 64, 17, None) == -2
+    assert L.nq_gemm_q4(p16, p16, p16, 9, 64, 16, None) == -2     # T > 8
+    assert L.nq_gemm_q4(p16, p16, p16, -1, 64, 16, None) == -2
+    assert L.nq_gemm_q5(p16, p16, p16, 1, 96, 16, None) == -2     # K % 64
+    assert L.nq_gemm_q4(p16, p16, p16, 1, 64, 24, None) == -2     # N % 16
+    assert L.nq_swiglu_q4(p16, p16, p16, p16, 1, 65, 16, None) == -2
+    assert L.nq_pack_q4(p16, p16, 63, 16, p16, None) == -2
+    assert L.nq_dequant_q5_debug(p16, p16, 64, 17, None) == -2
 
 
 def test_empty_problems_launch_nothing(L):
     # T == 0 or N == 0: NQ_OK without touching any pointer (NULLs are fine)
-    assert L.nq_gemm_q4(None, None, None, None, 0, 64, 16, None) == 0
-    assert L.nq_gemm_q5(None, None, None, None, 4, 64, 0, None) == 0
-    assert L.nq_swiglu_q4(None, None, None, None, None, None, 0, 64, 16, None) == 0
+    assert L.nq_gemm_q4(None, None, None, 0, 64, 16, None) == 0
+    assert L.nq_gemm_q5(None, None, None, 4, 64, 0, None) == 0
+    assert L.nq_swiglu_q4(None, None, None, None, 0, 64, 16, None) == 0
 
 
 def test_null_alignment_alias_errors(L):
@@ -77,16 +77,17 @@ def test_null_alignment_alias_errors(L):
     buf = ctypes.create_string_buffer(4096)
     base = (ctypes.addressof(buf) + 15) & ~15
     x, w, s, y = P(base), P(base + 1024), P(base + 2048), P(base + 3072)
-    assert L.nq_gemm_q4(None, w, s, y, 1, 64, 16, None) == -1
-    assert L.nq_gemm_q4(x, w, None, y, 1, 64, 16, None) == -1
-    assert L.nq_swiglu_q4(x, w, s, None, s, y, 1, 64, 16, None) == -1
-    assert L.nq_gemm_q4(P(base + 2), w, s, y, 1, 64, 16, None) == -3    # X misaligned
-    assert L.nq_gemm_q4(x, w, s, P(base + 3080), 1, 64, 16, None) == -3
-    # Y overlapping X / W / S
-    assert L.nq_gemm_q4(x, w, s, x, 1, 64, 16, None) == -4
-    assert L.nq_gemm_q4(x, w, s, P(base + 1024 + 256), 1, 64, 16, None) == -4
-    assert L.nq_gemm_q5(x, w, s, P(base + 2048), 2, 64, 16, None) == -4
-    assert L.nq_pack_q4(x, s, 64, 16, x, y, None) == -4
+    assert L.nq_gemm_q4(None, w, y, 1, 64, 16, None) == -1
+    assert L.nq_gemm_q4(x, None, y, 1, 64, 16, None) == -1
+    assert L.nq_swiglu_q4(x, w, None, y, 1, 64, 16, None) == -1
+    assert L.nq_gemm_q4(P(base + 2), w, y, 1, 64, 16, None) == -3    # X misaligned
+    assert L.nq_gemm_q4(x, w, P(base + 3080), 1, 64, 16, None) == -3
+    # Y overlapping X / W (the packed Q4 64 x 16 weight is 576 bytes)
+    assert L.nq_gemm_q4(x, w, x, 1, 64, 16, None) == -4
+    assert L.nq_gemm_q4(x, w, P(base + 1024 + 256), 1, 64, 16, None) == -4
+    assert L.nq_gemm_q5(x, w, P(base + 1024 + 640), 2, 64, 16, None) == -4
+    assert L.nq_swiglu_q4(x, w, s, P(base + 2048 + 512), 1, 64, 16, None) == -4
+    assert L.nq_pack_q4(x, s, 64, 16, x, None) == -4
 
 
 def test_plan_info_matches_workloads(L):

@@ -29,8 +29,8 @@ DEQ_SHAPES = [(256, 128, 0), (192, 48, 1), (64, 16, 2), (640, 272, 3), (5120, 61
 @pytest.mark.parametrize("K,N,seed", DEQ_SHAPES)
 def test_dequant_q4_bit_exact(nq, K, N, seed):
     p = si.q4_problem(1, K, N, seed)
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-    w_gpu = nq.dequant_q4_debug(wq, sp, K, N).cpu().numpy()
+    w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    w_gpu = nq.dequant_q4_debug(w, K, N).cpu().numpy()
     w_ref = oracle.dequant_q4(p["wq"], p["s"], K, N)
     assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
 
@@ -38,8 +38,8 @@ def test_dequant_q4_bit_exact(nq, K, N, seed):
 @pytest.mark.parametrize("K,N,seed", DEQ_SHAPES)
 def test_dequant_q5_bit_exact(nq, K, N, seed):
     p = si.q5_problem(1, K, N, seed)
-    wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-    w_gpu = nq.dequant_q5_debug(wq, sp, K, N).cpu().numpy()
+    w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+    w_gpu = nq.dequant_q5_debug(w, K, N).cpu().numpy()
     w_ref = oracle.dequant_q5(p["wn"], p["wh"], p["s"], K, N)
     assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
 
@@ -47,8 +47,8 @@ def test_dequant_q5_bit_exact(nq, K, N, seed):
 def test_dequant_full_size_decode_q4(nq):
     c = si.DECODE_Q4
     p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
-    w_gpu = nq.dequant_q4_debug(wq, sp, c["K"], c["N"]).cpu().numpy()
+    w = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
+    w_gpu = nq.dequant_q4_debug(w, c["K"], c["N"]).cpu().numpy()
     w_ref = oracle.dequant_q4(p["wq"], p["s"], c["K"], c["N"])
     assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
 
@@ -67,8 +67,8 @@ GEMM_SHAPES = [
 @pytest.mark.parametrize("T,K,N,seed", GEMM_SHAPES)
 def test_gemm_q4_parity(nq, T, K, N, seed):
     p = si.q4_problem(T, K, N, seed)
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, N))
+    wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, N))
     y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
     assert gu.rel_err(y, y_ref) <= gu.TOL
 
@@ -76,8 +76,8 @@ def test_gemm_q4_parity(nq, T, K, N, seed):
 @pytest.mark.parametrize("T,K,N,seed", GEMM_SHAPES)
 def test_gemm_q5_parity(nq, T, K, N, seed):
     p = si.q5_problem(T, K, N, seed + 100)
-    wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, sp, N))
+    wq = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, N))
     y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
     assert gu.rel_err(y, y_ref) <= gu.TOL
 
@@ -86,12 +86,12 @@ def test_gemm_q5_parity(nq, T, K, N, seed):
 def test_gemm_every_T(nq, T):
     K, N = 1536, 208
     p = si.q4_problem(T, K, N, 50 + T)
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, N))
+    wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, N))
     assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)) <= gu.TOL
     q = si.q5_problem(T, K, N, 60 + T)
-    wq5, sp5 = gu.pack_q5(nq, q["wn"], q["wh"], q["s"], K, N)
-    y5 = gu.host_f64(nq.gemm_q5(gu.dev_bf16(q["x"]), wq5, sp5, N))
+    wq5 = gu.pack_q5(nq, q["wn"], q["wh"], q["s"], K, N)
+    y5 = gu.host_f64(nq.gemm_q5(gu.dev_bf16(q["x"]), wq5, N))
     assert gu.rel_err(y5, oracle.gemm_q5(q["x"], q["wn"], q["wh"], q["s"], T, K, N)) <= gu.TOL
 
 
@@ -101,9 +101,9 @@ SWIGLU_SHAPES = [(8, 256, 48, 0), (1, 640, 16, 1), (5, 1024, 272, 2), (8, 6208, 
 @pytest.mark.parametrize("T,K,N,seed", SWIGLU_SHAPES)
 def test_swiglu_q4_parity(nq, T, K, N, seed):
     p = si.swiglu_problem(T, K, N, seed)
-    wg, sg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
-    wu, su = gu.pack_q4(nq, p["wu"], p["su"], K, N)
-    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, sg, wu, su, N))
+    wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, wu, N))
     g, u, h_ref_bits = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
     h_exact = g / (1.0 + np.exp(-g)) * u
     assert gu.rel_err(h, h_exact) <= gu.TOL
@@ -114,16 +114,16 @@ def test_swiglu_q4_parity(nq, T, K, N, seed):
 def test_workload_tiny_q4(nq):
     c = si.TINY_Q4
     p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, c["N"]))
+    wq = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, c["N"]))
     assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], c["T"], c["K"], c["N"])) <= gu.TOL
 
 
 def test_workload_decode_q4_full(nq):
     c = si.DECODE_Q4
     p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, sp, c["N"]))
+    wq = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, c["N"]))
     assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], c["T"], c["K"], c["N"])) <= gu.TOL
 
 
@@ -131,8 +131,8 @@ def test_workload_decode_q4_full(nq):
 def test_workload_verify_q5_full(nq, T):
     c = si.VERIFY_Q5
     p = si.q5_problem(T, c["K"], c["N"], c["seed"])
-    wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], c["K"], c["N"])
-    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, sp, c["N"]))
+    wq = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], c["K"], c["N"])
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, c["N"]))
     y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, c["K"], c["N"])
     assert gu.rel_err(y, y_ref) <= gu.TOL
 
@@ -142,9 +142,9 @@ def test_workload_swiglu_block_full(nq):
     c = si.SWIGLU_Q4
     T, K, N = c["T"], c["K"], c["N"]
     p = si.swiglu_problem(T, K, N, c["seed"])
-    wg, sg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
-    wu, su = gu.pack_q4(nq, p["wu"], p["su"], K, N)
-    h_dev = nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, sg, wu, su, N)
+    wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    h_dev = nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, wu, N)
     rows = gu.sample_rows(N, 384, 1)
     g, u, _ = oracle.swiglu_q4_rows(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, rows)
     h_exact = (g / (1.0 + np.exp(-g)) * u).T           # [T][rows]
@@ -153,8 +153,8 @@ def test_workload_swiglu_block_full(nq):
     # down projection K=17408 -> N=5120 on the GPU's H (decoupled from H's rounding)
     d = si.SWIGLU_DOWN
     pd = si.q4_problem(T, d["K"], d["N"], c["seed"] + 1000)
-    wd, sd = gu.pack_q4(nq, pd["wq"], pd["s"], d["K"], d["N"])
-    y = gu.host_f64(nq.gemm_q4(h_dev, wd, sd, d["N"]))
+    wd = gu.pack_q4(nq, pd["wq"], pd["s"], d["K"], d["N"])
+    y = gu.host_f64(nq.gemm_q4(h_dev, wd, d["N"]))
     h_bits = h_dev.view(torch.int16).cpu().numpy().view(np.uint16)
     y_ref = oracle.gemm_q4(h_bits, pd["wq"], pd["s"], T, d["K"], d["N"])
     assert gu.rel_err(y, y_ref) <= gu.TOL
@@ -171,13 +171,13 @@ def test_workload_layer_stack_sampled(nq, layer, T):
         x = np.ascontiguousarray(x_full[:, :K])
         if bits == 4:
             p = si.q4_problem(T, K, N, si.layer_seed(layer, j))
-            wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, sp, N))
+            wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, N))
             y_ref = oracle.gemm_q4_rows(x, p["wq"], p["s"], T, K, rows).T
         else:
             p = si.q5_problem(T, K, N, si.layer_seed(layer, j))
-            wq, sp = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(x), wq, sp, N))
+            wq = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(x), wq, N))
             y_ref = oracle.gemm_q5_rows(x, p["wn"], p["wh"], p["s"], T, K, rows).T
         assert gu.rel_err(y[:, rows], y_ref) <= gu.TOL, name
 
@@ -187,17 +187,17 @@ def test_workload_layer_stack_sampled(nq, layer, T):
 def test_deterministic_and_zero_point_exact(nq):
     T, K, N = 8, 6208, 272       # two K slabs, split-K fix-up
     p = si.q4_problem(T, K, N, 77)
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
     x = gu.dev_bf16(p["x"])
-    y1 = nq.gemm_q4(x, wq, sp, N)
-    y2 = nq.gemm_q4(x, wq, sp, N)
+    y1 = nq.gemm_q4(x, wq, N)
+    y2 = nq.gemm_q4(x, wq, N)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     # all codes at the zero point: exactly zero output, however K is split
-    z4, zs = gu.pack_q4(nq, np.full((N, K // 8), 0x88888888, np.uint32), p["s"], K, N)
-    assert torch.count_nonzero(nq.gemm_q4(x, z4, zs, N).float()) == 0
-    z5, zs5 = gu.pack_q5(nq, np.zeros((N, K // 8), np.uint32), np.full((N, K // 32), 0xFFFFFFFF, np.uint32),
+    z4 = gu.pack_q4(nq, np.full((N, K // 8), 0x88888888, np.uint32), p["s"], K, N)
+    assert torch.count_nonzero(nq.gemm_q4(x, z4, N).float()) == 0
+    z5 = gu.pack_q5(nq, np.zeros((N, K // 8), np.uint32), np.full((N, K // 32), 0xFFFFFFFF, np.uint32),
                          p["s"], K, N)
-    assert torch.count_nonzero(nq.gemm_q5(x, z5, zs5, N).float()) == 0
+    assert torch.count_nonzero(nq.gemm_q5(x, z5, N).float()) == 0
 
 
 def test_one_hot_x_selects_codes(nq):
@@ -205,13 +205,13 @@ def test_one_hot_x_selects_codes(nq):
     K, N = 640, 48
     p = si.q4_problem(1, K, N, 78)
     s1 = np.full((N, K // 64), 0x3C00, np.uint16)
-    wq, sp = gu.pack_q4(nq, p["wq"], s1, K, N)
+    wq = gu.pack_q4(nq, p["wq"], s1, K, N)
     codes = oracle.dequant_q4(p["wq"], s1, K, N)     # = q - 8 with unit scales
     x = np.zeros((8, K), np.uint16)
     ks = [0, 1, 63, 64, 300, 500, 638, 639]
     for t, k in enumerate(ks):
         x[t, k] = 0x3F80
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, sp, N))
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, N))
     for t, k in enumerate(ks):
         assert np.array_equal(y[t], codes[:, k].astype(np.float64))
 
@@ -224,31 +224,31 @@ def test_empty_and_k0(nq):
     # K == 0: Y is an empty sum -> zeros
     from weight_only_groupwise_gb300.nq import _ptr, _stream, lib
     x16 = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    rc = lib().nq_gemm_q4(_ptr(x16), _ptr(dummy), _ptr(dummy), _ptr(y), 2, 0, N, _stream(None))
+    rc = lib().nq_gemm_q4(_ptr(x16), _ptr(dummy), _ptr(y), 2, 0, N, _stream(None))
     assert rc == 0
     assert torch.count_nonzero(y.float()) == 0
     # T == 0: nothing written
     y.fill_(3.0)
-    rc = lib().nq_gemm_q5(_ptr(x16), _ptr(dummy), _ptr(dummy), _ptr(y), 0, 64, N, _stream(None))
+    rc = lib().nq_gemm_q5(_ptr(x16), _ptr(dummy), _ptr(y), 0, 64, N, _stream(None))
     assert rc == 0 and bool((y.float() == 3.0).all())
 
 
 def test_errors_leave_output_untouched(nq):
     T, K, N = 2, 128, 32
     p = si.q4_problem(T, K, N, 79)
-    wq, sp = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
     x = gu.dev_bf16(p["x"])
     y = torch.full((T, N), 5.0, dtype=torch.bfloat16, device="cuda")
     from weight_only_groupwise_gb300.nq import NqError
     with pytest.raises(NqError) as e:
-        nq.gemm_q4(x, wq, sp, N + 1, out=y)        # N % 16 != 0
+        nq.gemm_q4(x, wq, N + 1, out=y)        # N % 16 != 0
     assert e.value.status == -2
     xo = torch.empty(T * K + 8, dtype=torch.bfloat16, device="cuda")[1:1 + T * K].view(T, K)
     with pytest.raises(NqError) as e:
-        nq.gemm_q4(xo, wq, sp, N, out=y)           # misaligned X
+        nq.gemm_q4(xo, wq, N, out=y)           # misaligned X
     assert e.value.status == -3
     with pytest.raises(NqError) as e:
-        nq.gemm_q4(x, wq, sp, N, out=x.view(-1)[:T * N].view(T, N))  # Y aliases X
+        nq.gemm_q4(x, wq, N, out=x.view(-1)[:T * N].view(T, N))  # Y aliases X
     assert e.value.status == -4
     torch.cuda.synchronize()
     assert bool((y.float() == 5.0).all())

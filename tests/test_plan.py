@@ -29,7 +29,6 @@ def test_partition_covers_every_unit_once(nq, bits, mode, T, K, N, sms):
     slots = set()
     per_cta = []
     fan_in = {}
-    prev_end = None
     for c in range(info["ctas"]):
         segs = nq.plan_segments(bits, mode, T, K, N, sms, c)
         n_units = 0
@@ -43,13 +42,23 @@ def test_partition_covers_every_unit_once(nq, bits, mode, T, K, N, sms):
             assert slot not in slots and slot < info["ws_slots"]
             slots.add(slot)
             fan_in[rp] = fan_in.get(rp, 0) + 1
-            # units advance monotonically in slab-major order
-            key = (s, rp, ga)
-            assert prev_end is None or key > prev_end
-            prev_end = key
             n_units += gb - ga
         per_cta.append(n_units)
     assert len(seen) == RP * G
     assert max(per_cta) - min(per_cta) <= 1          # equal shares
     # every pair is covered by at least one run per slab
     assert all(fan_in[rp] >= S for rp in range(RP))
+    # a run writes its output directly exactly when it is its pair's only contribution
+    for c in range(info["ctas"]):
+        segs = nq.plan_segments(bits, mode, T, K, N, sms, c)
+        for (s, rp, ga, gb) in segs:
+            complete = S == 1 and ga == 0 and gb == G
+            assert complete == (fan_in[rp] == 1)
+        # processing order: natural order with several slabs; with one slab the first and
+        # last natural runs come first and the block ends on a complete run (if it has one)
+        nat = sorted(segs, key=lambda x: (x[0], x[1], x[2]))
+        if S > 1 or len(segs) <= 2:
+            assert segs == nat
+        else:
+            assert segs[0] == nat[0] and segs[1] == nat[-1] and segs[2:] == nat[1:-1]
+            assert segs[-1][2] == 0 and segs[-1][3] == G

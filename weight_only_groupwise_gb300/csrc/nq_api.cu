@@ -23,10 +23,10 @@ namespace {
 // which is the m16n8k16 A-fragment order once decode_q4 widens the nibbles.
 template <int BITS>
 __global__ void pack_codes_kernel(const uint32_t* __restrict__ wn, const uint32_t* __restrict__ wh,
-                                  int K, int N, uint32_t* __restrict__ out) {
+                                  int K, int N, uint8_t* __restrict__ out) {
     const int G = K / kGroup;
     const long long total = (long long)(N / kTileRows) * G * 32;
-    constexpr int TW = (BITS == 4 ? kQ4TileBytes : kQ5TileBytes) / 4;  // words per tile
+    constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
     const int kw8 = K / 8, kw32 = K / 32;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -55,14 +55,15 @@ __global__ void pack_codes_kernel(const uint32_t* __restrict__ wn, const uint32_
             }
             words[j] = wv;
         }
-        uint32_t* base = out + tile * TW;
+        uint8_t* base = out + packed_code_off(rt, g, G, TB);
         reinterpret_cast<uint4*>(base)[lane] = make_uint4(words[0], words[1], words[2], words[3]);
-        if (BITS == 5) base[128 + lane] = hw;
+        if (BITS == 5) reinterpret_cast<uint32_t*>(base + 512)[lane] = hw;
     }
 }
 
-// Canonical [N][K/64] fp16 scales -> per tile 16 halves ordered (r, r+8) for r = 0..7.
-__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N, uint16_t* __restrict__ out) {
+// Canonical [N][K/64] fp16 scales -> per tile 16 halves ordered (r, r+8) for r = 0..7, stored
+// after the codes of the tile's block.
+__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N, int TB, uint8_t* __restrict__ out) {
     const int G = K / kGroup;
     const long long total = (long long)(N / kTileRows) * G * 16;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -71,15 +72,14 @@ __global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N,
         const long long tile = idx >> 4;
         const int rt = (int)(tile / G), g = (int)(tile % G);
         const int row = (e >> 1) + 8 * (e & 1);
-        out[idx] = s[(size_t)(rt * kTileRows + row) * G + g];
+        reinterpret_cast<uint16_t*>(out + packed_scale_off(rt, g, G, TB))[e] = s[(size_t)(rt * kTileRows + row) * G + g];
     }
 }
 
 // Packed -> fp32 W[n][k], decoding with the projection kernels' own decode_q4/decode_q5:
 // w = (float)s * ((128 + q as bf16) - (128 + z)), both steps exact in fp32.
 template <int BITS>
-__global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ sp, int K,
-                               int N, float* __restrict__ w) {
+__global__ void dequant_kernel(const uint8_t* __restrict__ wq, int K, int N, float* __restrict__ w) {
     const int G = K / kGroup;
     const long long total = (long long)(N / kTileRows) * G * 32;
     constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
@@ -90,10 +90,10 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint16_t* _
         const long long tile = idx >> 5;
         const int rt = (int)(tile / G), g = (int)(tile % G);
         const int gid = lane >> 2, c = lane & 3;
-        const uint8_t* tb = wq + tile * TB;
+        const uint8_t* tb = wq + packed_code_off(rt, g, G, TB);
         const uint4 wv = reinterpret_cast<const uint4*>(tb)[lane];
         const uint32_t hb = BITS == 5 ? reinterpret_cast<const uint32_t*>(tb + 512)[lane] : 0u;
-        const uint16_t* st = sp + tile * 16;
+        const uint16_t* st = reinterpret_cast<const uint16_t*>(wq + packed_scale_off(rt, g, G, TB));
         const float s_lo = __half2float(__ushort_as_half(st[2 * gid]));
         const float s_hi = __half2float(__ushort_as_half(st[2 * gid + 1]));
         const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -137,7 +137,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 bool g_pdl = true;
-bool g_fold = false;
 bool g_env_read = false;
 
 size_t ws_tickets_off() { return 256; }
@@ -154,8 +153,6 @@ nq_status current_device(DevState** out, int* dev_out) {
     if (!g_env_read) {
         const char* e = std::getenv("NQ_PDL");
         if (e && e[0] == '0') g_pdl = false;
-        const char* f = std::getenv("NQ_DECODE");
-        if (f && std::strcmp(f, "fold") == 0) g_fold = true;
         g_env_read = true;
     }
     DevState& d = g_dev[dev];
@@ -218,10 +215,10 @@ nq_status check_shape(int K, int N) {
     return NQ_OK;
 }
 
-size_t packed_codes(int bits, int K, int N) {
-    return (size_t)K * N / 8 * (bits == 4 ? 4 : 5);
+// Packed bytes: codes (K*N/2 or 5*K*N/8) plus fp16 scales (N*K/32), interleaved per block.
+size_t packed_bytes(int bits, int K, int N) {
+    return (size_t)K * N / 8 * (bits == 4 ? 4 : 5) + (size_t)N * (K / kGroup) * 2;
 }
-size_t packed_scales(int K, int N) { return (size_t)N * (K / kGroup) * 2; }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -232,20 +229,17 @@ int grid_for(long long work, int per_block) {
 }
 
 // Shared body of the three projection entry points.
-nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0,
-                  const void* W1, const void* S1, void* Y, int T, int K, int N, void* stream) {
+nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* W1, void* Y, int T, int K,
+                  int N, void* stream) {
     if (T < 0 || T > 8) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
     if (T == 0 || N == 0) return NQ_OK;  // empty output
-    if (!X || !W0 || !S0 || !Y || (swiglu && (!W1 || !S1))) return NQ_ERR_NULL;
-    if (misaligned(X) || misaligned(W0) || misaligned(S0) || misaligned(Y) ||
-        (swiglu && (misaligned(W1) || misaligned(S1))))
-        return NQ_ERR_ALIGN;
+    if (!X || !W0 || !Y || (swiglu && !W1)) return NQ_ERR_NULL;
+    if (misaligned(X) || misaligned(W0) || misaligned(Y) || (swiglu && misaligned(W1))) return NQ_ERR_ALIGN;
     const size_t xb = (size_t)T * K * 2, yb = (size_t)T * N * 2;
-    const size_t cb = packed_codes(bits, K, N), sb = packed_scales(K, N);
-    if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, cb) || overlap(Y, yb, S0, sb) ||
-        (swiglu && (overlap(Y, yb, W1, cb) || overlap(Y, yb, S1, sb))))
+    const size_t wb = packed_bytes(bits, K, N);
+    if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, wb) || (swiglu && overlap(Y, yb, W1, wb)))
         return NQ_ERR_ALIAS;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
@@ -259,75 +253,62 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     if (st != NQ_OK) return st;
     a.X = static_cast<const uint16_t*>(X);
     a.W0 = static_cast<const uint8_t*>(W0);
-    a.S0 = static_cast<const uint8_t*>(S0);
     a.W1 = static_cast<const uint8_t*>(swiglu ? W1 : W0);
-    a.S1 = static_cast<const uint8_t*>(swiglu ? S1 : S0);
     a.Y = static_cast<uint16_t*>(Y);
     a.dev_err = reinterpret_cast<int*>(d->ws);
     a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
     a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
     cudaError_t e;
     if (swiglu)
-        e = launch_proj_swiglu_q4(a, as_stream(stream), g_pdl, g_fold);
+        e = launch_proj_swiglu_q4(a, as_stream(stream), g_pdl);
     else if (bits == 4)
-        e = launch_proj_q4(a, as_stream(stream), g_pdl, g_fold);
+        e = launch_proj_q4(a, as_stream(stream), g_pdl);
     else
-        e = launch_proj_q5(a, as_stream(stream), g_pdl, g_fold);
+        e = launch_proj_q5(a, as_stream(stream), g_pdl);
     return e == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N,
-               void* wq_packed, void* s_packed, void* stream) {
+nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N, void* packed,
+               void* stream) {
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
     if (K == 0 || N == 0) return NQ_OK;
-    if (!wn || !s || !wq_packed || !s_packed || (bits == 5 && !wh)) return NQ_ERR_NULL;
-    if (misaligned(wn) || misaligned(s) || misaligned(wq_packed) || misaligned(s_packed) ||
-        (bits == 5 && misaligned(wh)))
-        return NQ_ERR_ALIGN;
-    const size_t cb = packed_codes(bits, K, N), sb = packed_scales(K, N);
-    const size_t in_n = (size_t)N * K / 2, in_h = (size_t)N * K / 8, in_s = sb;
-    for (const void* o : {wq_packed, s_packed}) {
-        const size_t ob = o == wq_packed ? cb : sb;
-        if (overlap(o, ob, wn, in_n) || overlap(o, ob, s, in_s) || (bits == 5 && overlap(o, ob, wh, in_h)))
-            return NQ_ERR_ALIAS;
-    }
-    if (overlap(wq_packed, cb, s_packed, sb)) return NQ_ERR_ALIAS;
-    DevState* d = nullptr;
-    st = current_device(&d, nullptr);
-    if (st != NQ_OK) return st;
-    const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
-    if (bits == 4)
-        pack_codes_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
-            wn, nullptr, K, N, static_cast<uint32_t*>(wq_packed));
-    else
-        pack_codes_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
-            wn, wh, K, N, static_cast<uint32_t*>(wq_packed));
-    if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
-    pack_scales_kernel<<<grid_for(lanes / 2, 256), 256, 0, as_stream(stream)>>>(
-        s, K, N, static_cast<uint16_t*>(s_packed));
-    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
-}
-
-nq_status dequant(int bits, const void* wq, const void* s, float* w, int K, int N, void* stream) {
-    nq_status st = check_shape(K, N);
-    if (st != NQ_OK) return st;
-    if (K == 0 || N == 0) return NQ_OK;
-    if (!wq || !s || !w) return NQ_ERR_NULL;
-    if (misaligned(wq) || misaligned(s) || misaligned(w)) return NQ_ERR_ALIGN;
-    const size_t wb = (size_t)N * K * 4;
-    if (overlap(w, wb, wq, packed_codes(bits, K, N)) || overlap(w, wb, s, packed_scales(K, N)))
+    if (!wn || !s || !packed || (bits == 5 && !wh)) return NQ_ERR_NULL;
+    if (misaligned(wn) || misaligned(s) || misaligned(packed) || (bits == 5 && misaligned(wh))) return NQ_ERR_ALIGN;
+    const size_t ob = packed_bytes(bits, K, N);
+    const size_t in_n = (size_t)N * K / 2, in_h = (size_t)N * K / 8, in_s = (size_t)N * (K / kGroup) * 2;
+    if (overlap(packed, ob, wn, in_n) || overlap(packed, ob, s, in_s) || (bits == 5 && overlap(packed, ob, wh, in_h)))
         return NQ_ERR_ALIAS;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
     const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
+    uint8_t* out = static_cast<uint8_t*>(packed);
     if (bits == 4)
-        dequant_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
-            static_cast<const uint8_t*>(wq), static_cast<const uint16_t*>(s), K, N, w);
+        pack_codes_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(wn, nullptr, K, N, out);
     else
-        dequant_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
-            static_cast<const uint8_t*>(wq), static_cast<const uint16_t*>(s), K, N, w);
+        pack_codes_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(wn, wh, K, N, out);
+    if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
+    pack_scales_kernel<<<grid_for(lanes / 2, 256), 256, 0, as_stream(stream)>>>(
+        s, K, N, bits == 4 ? kQ4TileBytes : kQ5TileBytes, out);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+nq_status dequant(int bits, const void* wq, float* w, int K, int N, void* stream) {
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    if (K == 0 || N == 0) return NQ_OK;
+    if (!wq || !w) return NQ_ERR_NULL;
+    if (misaligned(wq) || misaligned(w)) return NQ_ERR_ALIGN;
+    if (overlap(w, (size_t)N * K * 4, wq, packed_bytes(bits, K, N))) return NQ_ERR_ALIAS;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
+    if (bits == 4)
+        dequant_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(static_cast<const uint8_t*>(wq), K, N, w);
+    else
+        dequant_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(static_cast<const uint8_t*>(wq), K, N, w);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
@@ -353,41 +334,36 @@ const char* nq_status_string(nq_status s) {
 
 int nq_version(void) { return (1 << 16) | 0; }
 
-size_t nq_packed_bytes_q4(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_codes(4, K, N) : 0; }
-size_t nq_packed_bytes_q5(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_codes(5, K, N) : 0; }
-size_t nq_packed_scale_bytes(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_scales(K, N) : 0; }
+size_t nq_packed_bytes_q4(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_bytes(4, K, N) : 0; }
+size_t nq_packed_bytes_q5(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_bytes(5, K, N) : 0; }
 
-nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* wq_packed,
-                     void* s_packed, void* stream) {
-    return pack(4, wq_canon, nullptr, s_canon, K, N, wq_packed, s_packed, stream);
+nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* packed, void* stream) {
+    return pack(4, wq_canon, nullptr, s_canon, K, N, packed, stream);
 }
 
-nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon, int K,
-                     int N, void* wq_packed, void* s_packed, void* stream) {
-    return pack(5, wn_canon, wh_canon, s_canon, K, N, wq_packed, s_packed, stream);
+nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon, int K, int N,
+                     void* packed, void* stream) {
+    return pack(5, wn_canon, wh_canon, s_canon, K, N, packed, stream);
 }
 
-nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
-                     void* stream) {
-    return project(4, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
+nq_status nq_gemm_q4(const void* X, const void* W, void* Y, int T, int K, int N, void* stream) {
+    return project(4, false, X, W, nullptr, Y, T, K, N, stream);
 }
 
-nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
-                     void* stream) {
-    return project(5, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
+nq_status nq_gemm_q5(const void* X, const void* W, void* Y, int T, int K, int N, void* stream) {
+    return project(5, false, X, W, nullptr, Y, T, K, N, stream);
 }
 
-nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su,
-                       void* H, int T, int K, int N, void* stream) {
-    return project(4, true, X, Wg, Sg, Wu, Su, H, T, K, N, stream);
+nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N, void* stream) {
+    return project(4, true, X, Wg, Wu, H, T, K, N, stream);
 }
 
-nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
-    return dequant(4, Wq, S, W, K, N, stream);
+nq_status nq_dequant_q4_debug(const void* W, float* out, int K, int N, void* stream) {
+    return dequant(4, W, out, K, N, stream);
 }
 
-nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
-    return dequant(5, Wq, S, W, K, N, stream);
+nq_status nq_dequant_q5_debug(const void* W, float* out, int K, int N, void* stream) {
+    return dequant(5, W, out, K, N, stream);
 }
 
 nq_status nq_reserve(int T_max, int K_max, int N_max) {
@@ -468,10 +444,13 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
     make_plan(bits, mode, T, K, N, num_sms, p);
     if (cta < 0 || cta >= p.P) return NQ_ERR_SHAPE;
     if (cap > 0 && !seg) return NQ_ERR_NULL;
+    // Same walk as the kernels: the block's segments in processing order.
     int64_t n = 0;
-    const long long u1 = cta_begin(p, cta + 1);
-    for (long long u = cta_begin(p, cta); u < u1;) {
-        const Segment sg = segment_at(p, u, u1);
+    const long long u0 = cta_begin(p, cta), u1 = cta_begin(p, cta + 1);
+    const SegOrder order = seg_order(p, u0, u1);
+    Segment nat;
+    for (int si = 0; si < order.count; ++si) {
+        const Segment sg = seg_pick(p, order, si, nat, u1);
         if (n < cap) {
             seg[4 * n + 0] = sg.s;
             seg[4 * n + 1] = sg.rp;
@@ -479,7 +458,6 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
             seg[4 * n + 3] = sg.gb;
         }
         ++n;
-        u = sg.u_next;
     }
     return n;
 }

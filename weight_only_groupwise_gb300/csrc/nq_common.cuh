@@ -2,14 +2,16 @@
 // of the groupwise int4/int5 small-batch projection (sm_103a).
 //
 // Packed layout (this library's definition; the pages give none):
-//   The K x N weight is cut into tiles of 16 output rows x one 64-wide K group.
-//   Tile (rt, g) -- rt = n / 16, g = k / 64 -- sits at index rt * G + g (G = K / 64), so the
-//   groups of one row tile are contiguous. Inside a tile, lane l (0..31) of a warp owns 16
-//   bytes = four uint32 code words, one per 16-wide K step j: the word is exactly the lane's
-//   bf16 A-operand fragment of an m16n8k16 tensor-core MMA for that step once each nibble is
-//   widened to a 16-bit half (see decode_q4). Q5 tiles append one uint32 of high bits per
-//   lane (128 bytes per tile). Scales: 16 fp16 per tile, ordered (row r, row r+8) for
-//   r = 0..7, so lane l reads one uint32 holding the scales of its rows l/4 and l/4+8.
+//   The K x N weight is cut into tiles of 16 output rows x one 64-wide K group, tile (rt, g)
+//   with rt = n / 16 and g = k / 64. Each row tile is a contiguous stream of blocks of 16
+//   groups (the last block of a row tile may hold fewer, nb = min(16, G - 16b)); a block is
+//   [nb tiles of codes][nb x 32 B of fp16 scales], so one bulk copy fetches a block's codes
+//   and scales together. Inside a code tile, lane l (0..31) of a warp owns 16 bytes = four
+//   uint32 words, one per 16-wide K step j: the word is exactly the lane's bf16 A-operand
+//   fragment of an m16n8k16 tensor-core MMA for that step once each nibble is widened to a
+//   16-bit half (see decode_q4). Q5 code tiles append one uint32 of high bits per lane (128
+//   bytes per tile). A tile's 16 scales are ordered (row r, row r+8) for r = 0..7, so lane l
+//   reads one uint32 holding the scales of its rows l/4 and l/4+8.
 #pragma once
 
 #include <cstdint>
@@ -27,12 +29,20 @@ constexpr int kTileRows = 16;        // output rows per tile (MMA M)
 constexpr int kQ4TileBytes = 512;    // 16 x 64 nibbles
 constexpr int kQ5TileBytes = 640;    // + 16 x 64 high bits
 constexpr int kScaleTileBytes = 32;  // 16 fp16
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kChunkGroups = 16;     // K groups per pipeline stage
+constexpr int kBlockGroups = 16;     // groups per packed block (= groups per pipeline stage)
+#ifndef NQ_CONSUMER_WARPS
+#define NQ_CONSUMER_WARPS 8
+#endif
+constexpr int kConsumerWarps = NQ_CONSUMER_WARPS;
+constexpr int kProducerWarp = kConsumerWarps;         // issues the bulk copies
+constexpr int kEpilogueWarp = kConsumerWarps + 1;     // reduces runs, stores, settles split-K
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kChunkGroups = kBlockGroups;           // K groups per pipeline stage
+constexpr int kGroupsPerWarp = kChunkGroups / kConsumerWarps;
+static_assert(kGroupsPerWarp * kConsumerWarps == kChunkGroups, "stage groups split evenly over warps");
 constexpr int kMaxStages = 12;
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kXBudget = 96 * 1024;  // on-chip activation slab
+constexpr int kXBudget = 97 * 1024;  // on-chip activation slab (96 groups x 8 rows + padding)
 constexpr int kMinUnitsPerCta = 16;
 constexpr int kPartialFloats = 256;  // 2 M tiles x 16 rows x 8 tokens
 constexpr long long kWaitTimeoutNs = 2000000000LL;  // 2 s per bounded wait
@@ -42,6 +52,22 @@ constexpr int kDevErrTimeout = 1;
 
 NQ_HD int tpad(int T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
 
+// Byte offsets inside a packed matrix (TB = code bytes per tile, 512 or 640).
+NQ_HD long long packed_tile_stride(int TB) { return TB + kScaleTileBytes; }
+NQ_HD long long packed_row_tile_bytes(int G, int TB) { return (long long)G * packed_tile_stride(TB); }
+NQ_HD long long packed_block_off(int rt, int b, int G, int TB) {
+    return rt * packed_row_tile_bytes(G, TB) + (long long)b * kBlockGroups * packed_tile_stride(TB);
+}
+NQ_HD int block_groups(int b, int G) { return G - kBlockGroups * b < kBlockGroups ? G - kBlockGroups * b : kBlockGroups; }
+NQ_HD long long packed_code_off(int rt, int g, int G, int TB) {
+    return packed_block_off(rt, g / kBlockGroups, G, TB) + (long long)(g % kBlockGroups) * TB;
+}
+NQ_HD long long packed_scale_off(int rt, int g, int G, int TB) {
+    const int b = g / kBlockGroups;
+    return packed_block_off(rt, b, G, TB) + (long long)block_groups(b, G) * TB +
+           (long long)(g % kBlockGroups) * kScaleTileBytes;
+}
+
 // The work split of one projection call. One "unit" is one 64-wide K group of one row pair
 // (two 16-row tiles; for SwiGLU the gate tile and the up tile of the same rows). Units are
 // ordered slab-major: for each K slab, for each pair, the slab's groups. The persistent
@@ -50,8 +76,9 @@ NQ_HD int tpad(int T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
 struct Plan {
     int bits, mode, T, TP, K, N, G, RT, RP;
     int GS, S;             // groups per slab (last slab may be shorter), slab count
-    long long U;           // units
+    long long U;           // units (< 2^31 for every accepted shape)
     int P;                 // blocks
+    int Uq, Ur;            // U = Uq * P + Ur: block c owns Uq units, plus one if c < Ur
     int CG, stages;
     long long slots;       // partial-sum slots: S * RP + P
     int tile_bytes, stage_bytes, x_bytes, corr_bytes, red_bytes, bar_bytes, smem_bytes;
@@ -69,23 +96,26 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.RP = mode ? p.RT : (p.RT + 1) / 2;
     // Largest slab whose T padded activation rows plus one zero row fit the X budget.
     const int Tr = T > 0 ? T : 1;
-    int gs_max = ((kXBudget - 16) / Tr - 16) / 128;
-    if (gs_max < 1) gs_max = 1;
+    int gs_max = ((kXBudget - 16) / Tr - 16) / 128 / kBlockGroups * kBlockGroups;
+    if (gs_max < kBlockGroups) gs_max = kBlockGroups;
     p.S = (p.G + gs_max - 1) / gs_max;
     if (p.S < 1) p.S = 1;
     p.GS = (p.G + p.S - 1) / p.S;
+    if (p.S > 1) p.GS = (p.GS + kBlockGroups - 1) / kBlockGroups * kBlockGroups;  // slabs on block edges
     p.U = (long long)p.RP * p.G;
     long long P = p.U / kMinUnitsPerCta;
     if (P > num_sms) P = num_sms;
     if (P < 1) P = 1;
     p.P = (int)P;
+    p.Uq = (int)(p.U / p.P);
+    p.Ur = (int)(p.U % p.P);
     p.CG = kChunkGroups;
     p.tile_bytes = bits == 4 ? kQ4TileBytes : kQ5TileBytes;
     p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
     p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
-    p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;
-    p.red_bytes = kConsumerWarps * 2 * 512;
-    p.bar_bytes = 256;  // full/empty per stage, x_full, x_empty, flags
+    p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
+    p.red_bytes = 2 * kConsumerWarps * 2 * 512;  // double-buffered run reduction
+    p.bar_bytes = 256;                           // barriers and flags
     const int fixed = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes;
     int st = (kSmemLimit - fixed) / p.stage_bytes;
     if (st > kMaxStages) st = kMaxStages;
@@ -97,9 +127,15 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
 
 NQ_HD int slab_groups(const Plan& p, int s) { return s < p.S - 1 ? p.GS : p.G - (p.S - 1) * p.GS; }
 NQ_HD long long slab_base(const Plan& p, int s) { return (long long)s * p.RP * p.GS; }
-NQ_HD long long cta_begin(const Plan& p, int c) { return (long long)c * p.U / p.P; }
-// Block that owns unit u: the largest c with cta_begin(c) <= u.
-NQ_HD int cta_of(const Plan& p, long long u) { return (int)(((u + 1) * p.P - 1) / p.U); }
+// Balanced split: the first Ur blocks own Uq + 1 units, the others Uq (32-bit arithmetic).
+NQ_HD long long cta_begin(const Plan& p, int c) {
+    return (long long)((unsigned)c * (unsigned)p.Uq + (unsigned)(c < p.Ur ? c : p.Ur));
+}
+// Block that owns unit u.
+NQ_HD int cta_of(const Plan& p, long long u) {
+    const unsigned uu = (unsigned)u, big = (unsigned)p.Ur * (unsigned)(p.Uq + 1);
+    return uu < big ? (int)(uu / (unsigned)(p.Uq + 1)) : p.Ur + (int)((uu - big) / (unsigned)p.Uq);
+}
 
 // One run of consecutive units of one block inside one (slab, pair).
 struct Segment {
@@ -109,19 +145,81 @@ struct Segment {
 
 NQ_HD Segment segment_at(const Plan& p, long long u, long long u_end) {
     Segment sg;
-    long long s = u / ((long long)p.RP * p.GS);
-    if (s > p.S - 1) s = p.S - 1;
+    unsigned s = (unsigned)u / ((unsigned)p.RP * (unsigned)p.GS);
+    if (s > (unsigned)(p.S - 1)) s = p.S - 1;
     sg.s = (int)s;
     const int gs = slab_groups(p, sg.s);
-    const long long off = u - slab_base(p, sg.s);
-    sg.rp = (int)(off / gs);
-    const int gl = (int)(off % gs);
+    const unsigned off = (unsigned)(u - slab_base(p, sg.s));
+    sg.rp = (int)(off / (unsigned)gs);
+    const int gl = (int)(off % (unsigned)gs);
     const long long run_end = slab_base(p, sg.s) + (long long)(sg.rp + 1) * gs;
     const long long e = run_end < u_end ? run_end : u_end;
     sg.ga = sg.s * p.GS + gl;
     sg.gb = sg.ga + (int)(e - u);
     sg.u_next = e;
     return sg;
+}
+
+// The segment after sg in the same block (runs after the first start at a slab's first
+// group). Returns false when the block's range [.., u_end) is exhausted. No divisions.
+NQ_HD bool segment_next(const Plan& p, Segment& sg, long long u_end) {
+    const long long u = sg.u_next;
+    if (u >= u_end) return false;
+    if (sg.rp + 1 < p.RP) {
+        sg.rp += 1;
+    } else {
+        sg.s += 1;
+        sg.rp = 0;
+    }
+    const int gs = slab_groups(p, sg.s);
+    const long long left = u_end - u;
+    const int len = left < gs ? (int)left : gs;
+    sg.ga = sg.s * p.GS;
+    sg.gb = sg.ga + len;
+    sg.u_next = u + len;
+    return true;
+}
+
+// Processing order of a block's segments. With one slab, the (possibly partial) first and
+// last runs go first, so their split-K partials are settled early and the block ends on a
+// complete run; with several slabs every run is partial and the natural order keeps the
+// activation slab loaded once per slab.
+struct SegOrder {
+    Segment first, last;   // natural first and last segment of the block
+    int count;             // number of segments
+};
+
+NQ_HD SegOrder seg_order(const Plan& p, long long u0, long long u1) {
+    SegOrder o;
+    o.first = segment_at(p, u0, u1);
+    o.last = o.first;
+    o.count = 1;
+    Segment sg = o.first;
+    while (segment_next(p, sg, u1)) {
+        o.last = sg;
+        ++o.count;
+    }
+    return o;
+}
+
+// The i-th segment in processing order (i < count); `nat` is the natural-order iterator
+// state used to walk the middle runs (call with i increasing by one from 0).
+NQ_HD Segment seg_pick(const Plan& p, const SegOrder& o, int i, Segment& nat, long long u1) {
+    if (p.S > 1 || o.count <= 2) {
+        if (i == 0) nat = o.first; else segment_next(p, nat, u1);
+        return nat;
+    }
+    if (i == 0) return o.first;
+    if (i == 1) return o.last;
+    if (i == 2) nat = o.first;
+    segment_next(p, nat, u1);  // middle runs: natural segments 1 .. count-2
+    return nat;
+}
+
+// A segment that covers its whole pair (one slab, all K groups) is the pair's only
+// contribution: its block writes the output directly.
+NQ_HD bool segment_complete(const Plan& p, const Segment& sg) {
+    return p.S == 1 && sg.ga == 0 && sg.gb == p.G;
 }
 
 // Number of (block, slab) runs that contribute to pair rp: the split-K fan-in.
@@ -240,6 +338,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Ticket for the split-K fix-up: one thread adds 1 with acquire-release semantics at GPU
+// scope. Preceded by a block barrier, it publishes every thread's partial stores (release
+// is cumulative); the last taker's acquire, followed by a block barrier, makes every
+// earlier taker's partials visible to the whole block.
+__device__ __forceinline__ int ticket_add(int* p) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -261,29 +373,37 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], 
 //
 // bf16 0x4300 is 128.0 with a unit step in its 7 fraction bits, so OR-ing a code q < 128
 // into the low bits gives exactly the bf16 value 128 + q. The projection kernels feed
-// 128 + q to the tensor cores and fold the constant -(128 + z) * sum(x) into the MMA's
-// starting accumulator, so no per-weight subtraction is needed.
+// 128 + q to the tensor cores and subtract the same MMA chain run on the constant code z,
+// so no per-weight subtraction is needed.
 constexpr uint32_t kBf16Magic = 0x43004300u;
 
+// (a & MASK) | c in one LOP3 (c is kept in a register so it is not split in two ops).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+
 // Four bf16x2 A-fragment registers (values 128 + q) from one packed Q4 word: register m
-// holds nibble m in its low half and nibble m + 4 in its high half.
-__device__ __forceinline__ void decode_q4(uint32_t w, uint32_t a[4]) {
-    a[0] = (w & 0x000F000Fu) | kBf16Magic;
-    a[1] = ((w >> 4) & 0x000F000Fu) | kBf16Magic;
-    a[2] = ((w >> 8) & 0x000F000Fu) | kBf16Magic;
-    a[3] = ((w >> 12) & 0x000F000Fu) | kBf16Magic;
+// holds nibble m in its low half and nibble m + 4 in its high half. `magic` = kBf16Magic.
+__device__ __forceinline__ void decode_q4(uint32_t w, uint32_t a[4], uint32_t magic = kBf16Magic) {
+    a[0] = and_or<0x000F000Fu>(w, magic);
+    a[1] = and_or<0x000F000Fu>(w >> 4, magic);
+    a[2] = and_or<0x000F000Fu>(w >> 8, magic);
+    a[3] = and_or<0x000F000Fu>(w >> 12, magic);
 }
 
 // Q5: as decode_q4, plus bit 4 of each code from the lane's high word h. For K step J the
 // high bit of nibble m (m < 4) sits at bit 4J + m and that of nibble m + 4 at bit 16 + 4J + m,
 // so one shift moves both onto bits 4 and 20.
 template <int J>
-__device__ __forceinline__ void decode_q5(uint32_t w, uint32_t h, uint32_t a[4]) {
+__device__ __forceinline__ void decode_q5(uint32_t w, uint32_t h, uint32_t a[4], uint32_t magic = kBf16Magic) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const int sh = 4 * J + m - 4;
         const uint32_t hb = sh >= 0 ? (h >> sh) : (h << (-sh));
-        a[m] = ((w >> (4 * m)) & 0x000F000Fu) | (hb & 0x00100010u) | kBf16Magic;
+        a[m] = and_or<0x000F000Fu>(w >> (4 * m), and_or<0x00100010u>(hb, magic));
     }
 }
 

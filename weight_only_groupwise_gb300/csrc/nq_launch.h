@@ -9,14 +9,13 @@ namespace nq {
 
 // Launch proj_kernel<BITS, SWIGLU> with a.p's grid and shared memory on `stream`.
 // pdl: allow programmatic dependent launch behind the preceding kernel of the stream.
-// fold: use the 128+q encoding with the offset folded into the accumulator (else exact q - z).
-cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl, bool fold);
-cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl, bool fold);
-cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl, bool fold);
+cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
+cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
+cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
-template <int BITS, bool SWIGLU, bool FOLD>
+template <int BITS, bool SWIGLU>
 cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    auto kern = proj_kernel<BITS, SWIGLU, FOLD>;
+    auto kern = proj_kernel<BITS, SWIGLU>;
     // The shared-memory opt-in is per device; set it on every launch of a new size class
     // (cheap: the driver caches it) rather than tracking devices here.
     static thread_local int set_for_device = -1;

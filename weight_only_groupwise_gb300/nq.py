@@ -36,16 +36,16 @@ def lib() -> ctypes.CDLL:
         L.nq_status_string.argtypes = [I]
         L.nq_status_string.restype = ctypes.c_char_p
         L.nq_version.restype = I
-        for f in ("nq_packed_bytes_q4", "nq_packed_bytes_q5", "nq_packed_scale_bytes"):
+        for f in ("nq_packed_bytes_q4", "nq_packed_bytes_q5"):
             getattr(L, f).argtypes = [I, I]
             getattr(L, f).restype = S
-        L.nq_pack_q4.argtypes = [P, P, I, I, P, P, P]
-        L.nq_pack_q5.argtypes = [P, P, P, I, I, P, P, P]
-        L.nq_gemm_q4.argtypes = [P, P, P, P, I, I, I, P]
-        L.nq_gemm_q5.argtypes = [P, P, P, P, I, I, I, P]
-        L.nq_swiglu_q4.argtypes = [P, P, P, P, P, P, I, I, I, P]
-        L.nq_dequant_q4_debug.argtypes = [P, P, P, I, I, P]
-        L.nq_dequant_q5_debug.argtypes = [P, P, P, I, I, P]
+        L.nq_pack_q4.argtypes = [P, P, I, I, P, P]
+        L.nq_pack_q5.argtypes = [P, P, P, I, I, P, P]
+        L.nq_gemm_q4.argtypes = [P, P, P, I, I, I, P]
+        L.nq_gemm_q5.argtypes = [P, P, P, I, I, I, P]
+        L.nq_swiglu_q4.argtypes = [P, P, P, P, I, I, I, P]
+        L.nq_dequant_q4_debug.argtypes = [P, P, I, I, P]
+        L.nq_dequant_q5_debug.argtypes = [P, P, I, I, P]
         L.nq_reserve.argtypes = [I, I, I]
         L.nq_device_error.argtypes = []
         L.nq_shutdown.argtypes = []
@@ -96,32 +96,25 @@ def packed_bytes_q5(K: int, N: int) -> int:
     return int(lib().nq_packed_bytes_q5(K, N))
 
 
-def packed_scale_bytes(K: int, N: int) -> int:
-    return int(lib().nq_packed_scale_bytes(K, N))
-
-
 # ---------------------------------------------------------------- repack
 
-def pack_q4(wq_canon: torch.Tensor, s_canon: torch.Tensor, K: int, N: int, stream=None):
+def pack_q4(wq_canon: torch.Tensor, s_canon: torch.Tensor, K: int, N: int, stream=None) -> torch.Tensor:
     """Canonical Q4 codes (4-byte words [N][K/8]) and fp16 scales ([N][K/64]) on the GPU ->
-    (packed codes uint8, packed scales uint8)."""
+    packed weight (uint8 tensor holding codes and scales)."""
     dev = _cuda(wq_canon, "wq_canon").device
     _cuda(s_canon, "s_canon")
-    wq = torch.empty(max(packed_bytes_q4(K, N), 16), dtype=torch.uint8, device=dev)
-    sp = torch.empty(max(packed_scale_bytes(K, N), 16), dtype=torch.uint8, device=dev)
-    _check(lib().nq_pack_q4(_ptr(wq_canon), _ptr(s_canon), K, N, _ptr(wq), _ptr(sp), _stream(stream)))
-    return wq, sp
+    w = torch.empty(max(packed_bytes_q4(K, N), 16), dtype=torch.uint8, device=dev)
+    _check(lib().nq_pack_q4(_ptr(wq_canon), _ptr(s_canon), K, N, _ptr(w), _stream(stream)))
+    return w
 
 
-def pack_q5(wn_canon, wh_canon, s_canon, K: int, N: int, stream=None):
+def pack_q5(wn_canon, wh_canon, s_canon, K: int, N: int, stream=None) -> torch.Tensor:
     dev = _cuda(wn_canon, "wn_canon").device
     _cuda(wh_canon, "wh_canon")
     _cuda(s_canon, "s_canon")
-    wq = torch.empty(max(packed_bytes_q5(K, N), 16), dtype=torch.uint8, device=dev)
-    sp = torch.empty(max(packed_scale_bytes(K, N), 16), dtype=torch.uint8, device=dev)
-    _check(lib().nq_pack_q5(_ptr(wn_canon), _ptr(wh_canon), _ptr(s_canon), K, N, _ptr(wq), _ptr(sp),
-                            _stream(stream)))
-    return wq, sp
+    w = torch.empty(max(packed_bytes_q5(K, N), 16), dtype=torch.uint8, device=dev)
+    _check(lib().nq_pack_q5(_ptr(wn_canon), _ptr(wh_canon), _ptr(s_canon), K, N, _ptr(w), _stream(stream)))
+    return w
 
 
 # ---------------------------------------------------------------- projections
@@ -133,43 +126,42 @@ def _out(x: torch.Tensor, N: int, out):
     return _cuda(out, "out")
 
 
-def gemm_q4(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, N: int, out=None, stream=None):
-    """Y[T,N] (bf16) = X[T,K] (bf16) * dequant(packed Q4 codes, packed scales)."""
+def gemm_q4(x: torch.Tensor, w: torch.Tensor, N: int, out=None, stream=None):
+    """Y[T,N] (bf16) = X[T,K] (bf16) * dequant(packed Q4 weight)."""
     _cuda(x, "x")
     T, K = x.shape
     y = _out(x, N, out)
-    _check(lib().nq_gemm_q4(_ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N, _stream(stream)))
+    _check(lib().nq_gemm_q4(_ptr(x), _ptr(w), _ptr(y), T, K, N, _stream(stream)))
     return y
 
 
-def gemm_q5(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, N: int, out=None, stream=None):
+def gemm_q5(x: torch.Tensor, w: torch.Tensor, N: int, out=None, stream=None):
     _cuda(x, "x")
     T, K = x.shape
     y = _out(x, N, out)
-    _check(lib().nq_gemm_q5(_ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N, _stream(stream)))
+    _check(lib().nq_gemm_q5(_ptr(x), _ptr(w), _ptr(y), T, K, N, _stream(stream)))
     return y
 
 
-def swiglu_q4(x, wg, sg, wu, su, N: int, out=None, stream=None):
+def swiglu_q4(x, wg, wu, N: int, out=None, stream=None):
     """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with both weights packed Q4."""
     _cuda(x, "x")
     T, K = x.shape
     h = _out(x, N, out)
-    _check(lib().nq_swiglu_q4(_ptr(x), _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(h), T, K, N,
-                              _stream(stream)))
+    _check(lib().nq_swiglu_q4(_ptr(x), _ptr(wg), _ptr(wu), _ptr(h), T, K, N, _stream(stream)))
     return h
 
 
-def dequant_q4_debug(wq, s, K: int, N: int, stream=None) -> torch.Tensor:
-    w = torch.empty((N, K), dtype=torch.float32, device=wq.device)
-    _check(lib().nq_dequant_q4_debug(_ptr(wq), _ptr(s), _ptr(w), K, N, _stream(stream)))
-    return w
+def dequant_q4_debug(w, K: int, N: int, stream=None) -> torch.Tensor:
+    out = torch.empty((N, K), dtype=torch.float32, device=w.device)
+    _check(lib().nq_dequant_q4_debug(_ptr(w), _ptr(out), K, N, _stream(stream)))
+    return out
 
 
-def dequant_q5_debug(wq, s, K: int, N: int, stream=None) -> torch.Tensor:
-    w = torch.empty((N, K), dtype=torch.float32, device=wq.device)
-    _check(lib().nq_dequant_q5_debug(_ptr(wq), _ptr(s), _ptr(w), K, N, _stream(stream)))
-    return w
+def dequant_q5_debug(w, K: int, N: int, stream=None) -> torch.Tensor:
+    out = torch.empty((N, K), dtype=torch.float32, device=w.device)
+    _check(lib().nq_dequant_q5_debug(_ptr(w), _ptr(out), K, N, _stream(stream)))
+    return out
 
 
 # ---------------------------------------------------------------- runtime / plan
