@@ -65,7 +65,8 @@ enum {
     NQ_ERR_ALIAS = -4,    /* an output range overlaps an input range                      */
     NQ_ERR_CUDA = -5,     /* a CUDA runtime call or kernel launch failed                  */
     NQ_ERR_DEVICE = -6,   /* current device is not compute capability 10.3 (sm_103)      */
-    NQ_ERR_TIMEOUT = -7   /* a bounded device-side wait ran out (reported by nq_device_error) */
+    NQ_ERR_TIMEOUT = -7,  /* a bounded device-side wait ran out (reported by nq_device_error) */
+    NQ_ERR_SCRATCH = -8   /* the problem needs more scratch than nq_gemm_q4_noalloc's fixed array */
 };
 
 /* Human-readable name of a status code. Never NULL; static storage. */
@@ -108,6 +109,28 @@ nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const u
  * device (the split of K across thread blocks depends only on shape and SM count).
  */
 nq_status nq_gemm_q4(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
+
+/*
+ * nq_gemm_q4_noalloc: nq_gemm_q4 for callers that cannot allocate device memory. The pages
+ * have no counterpart; this is a library convenience.
+ *
+ * nq_gemm_q4 allocates its split-K scratch with cudaMalloc the first time a shape needs it.
+ * Code running during CUDA graph capture, plug-ins whose host framework owns all device
+ * memory, and processes on a fixed memory budget cannot allow that. This call computes the
+ * same Y with the same kernel but keeps its scratch in a fixed array of about 2.1 MB that
+ * the library holds in every device's memory until the process exits; it calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   Arguments, layouts, alignment and results: as nq_gemm_q4.
+ *   Limit: the split-K plan must fit 2048 partial slots and 4096 tickets (for T <= 4 and
+ *   K <= 24576 that is N up to about 60000); larger problems return NQ_ERR_SCRATCH before
+ *   anything is launched.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   Every call clears the part of the array that must start at zero (error word, tickets)
+ *   on its own stream, then launches. All calls share the one array: calls that overlap on
+ *   the GPU (unordered streams) race and give wrong results; order them on one stream.
+ */
+nq_status nq_gemm_q4_noalloc(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
 
 /* nq_gemm_q5: as nq_gemm_q4 for 5-bit codes packed by nq_pack_q5 (z = 16). */
 nq_status nq_gemm_q5(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);

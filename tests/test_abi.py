@@ -46,7 +46,7 @@ def test_sizes_and_strings(L):
     assert nq.packed_bytes_q5(5120, 6144) == 5120 * 6144 * 5 // 8 + 6144 * 80 * 2
     assert nq.packed_bytes_q4(100, 16) == 0          # K % 64 != 0
     assert nq.packed_bytes_q4(64, 8) == 0            # N % 16 != 0
-    for s in range(-7, 1):
+    for s in range(-8, 1):
         assert nq.status_string(s).startswith("NQ_")
     assert nq.status_string(-99) == "NQ_ERR_UNKNOWN"
     assert L.nq_version() >> 16 == 1

@@ -328,6 +328,7 @@ const char* nq_status_string(nq_status s) {
         case NQ_ERR_CUDA: return "NQ_ERR_CUDA: a CUDA call or launch failed";
         case NQ_ERR_DEVICE: return "NQ_ERR_DEVICE: current device is not sm_103 (GB300)";
         case NQ_ERR_TIMEOUT: return "NQ_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case NQ_ERR_SCRATCH: return "NQ_ERR_SCRATCH: problem exceeds the fixed scratch of nq_gemm_q4_noalloc";
         default: return "NQ_ERR_UNKNOWN";
     }
 }

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libnq.so")
 _lib = None
 
 STATUS = {0: "NQ_OK", -1: "NQ_ERR_NULL", -2: "NQ_ERR_SHAPE", -3: "NQ_ERR_ALIGN", -4: "NQ_ERR_ALIAS",
-          -5: "NQ_ERR_CUDA", -6: "NQ_ERR_DEVICE", -7: "NQ_ERR_TIMEOUT"}
+          -5: "NQ_ERR_CUDA", -6: "NQ_ERR_DEVICE", -7: "NQ_ERR_TIMEOUT", -8: "NQ_ERR_SCRATCH"}
 
 
 class NqError(RuntimeError):
@@ -43,6 +43,7 @@ def lib() -> ctypes.CDLL:
         L.nq_pack_q5.argtypes = [P, P, P, I, I, P, P]
         L.nq_gemm_q4.argtypes = [P, P, P, I, I, I, P]
         L.nq_gemm_q5.argtypes = [P, P, P, I, I, I, P]
+        L.nq_gemm_q4_noalloc.argtypes = [P, P, P, I, I, I, P]
         L.nq_swiglu_q4.argtypes = [P, P, P, P, I, I, I, P]
         L.nq_dequant_q4_debug.argtypes = [P, P, I, I, P]
         L.nq_dequant_q5_debug.argtypes = [P, P, I, I, P]
@@ -53,7 +54,7 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_info.argtypes = [I, I, I, I, I, I, P]
         L.nq_plan_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_segments.restype = ctypes.c_int64
-        for f in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_swiglu_q4",
+        for f in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_gemm_q4_noalloc", "nq_swiglu_q4",
                   "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_reserve", "nq_device_error",
                   "nq_plan_info"):
             getattr(L, f).restype = I
