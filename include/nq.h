@@ -22,7 +22,7 @@
  *   S    fp16   [N][K/64]  one scale per (output row n, 64-wide group of K)
  *
  * Packed layout: nq_pack_* rewrites the canonical codes and scales into ONE opaque,
- * kernel-friendly buffer: tiles of 16 output rows x one 64-wide K group, in blocks of 16
+ * kernel-friendly buffer: tiles of 16 output rows x one 64-wide K group, in blocks of 32
  * groups per row tile, each block holding its codes followed by its scales, so one bulk copy
  * fetches both. Its size depends only on (bits, K, N), is exactly codes + scales (no padding,
  * no header) and is given by nq_packed_bytes_*. The projection calls take the packed form.
@@ -44,6 +44,13 @@
  *     (different streams, no ordering) share it and race: order them on one stream.
  *   - Device-side waits are bounded; a wait that runs out sets a device error flag that
  *     nq_device_error reads.
+ *   - nq_gemm_q4, nq_gemm_q5 and nq_swiglu_q4 launch with programmatic dependent launch:
+ *     their kernel may start while the previous kernel on `stream` is finishing. It reads
+ *     X and writes Y, H and its workspace only after that kernel has completed, but starts
+ *     streaming the packed weights at once: the weights must not be written by a kernel
+ *     that lets its dependents start before its writes are done (one that calls
+ *     cudaTriggerProgrammaticLaunchCompletion early). The environment variable NQ_PDL=0,
+ *     read at the first call, turns this launch mode off.
  */
 #ifndef NQ_H
 #define NQ_H

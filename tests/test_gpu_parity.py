@@ -253,3 +253,30 @@ def test_errors_leave_output_untouched(nq):
     torch.cuda.synchronize()
     assert bool((y.float() == 5.0).all())
     nq.device_error()                               # no device-side wait ran out
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+def test_activation_range_outliers(nq, bits):
+    """Activations far outside fp16's range (outliers up to 3e38, values down to 1e-30) still
+    give results within tolerance: the kernels scale each token's slab by a power of two."""
+    T, K, N = 6, 1280, 96
+    p = si.q4_problem(T, K, N, 91) if bits == 4 else si.q5_problem(T, K, N, 91)
+    g = np.random.default_rng(92)
+    x = g.standard_normal((T, K)).astype(np.float32)
+    x[0, 5] = 3.0e38                      # near the bf16 maximum
+    x[1, :] *= 1.0e6                      # a whole token of large activations
+    x[2, 100:200] = 70000.0               # just past the fp16 maximum
+    x[3, :] *= 1.0e-30                    # tiny token
+    x[4, 7] = -4.0e4
+    xb = si.bf16_bits(x)
+    if bits == 4:
+        w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+        y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(xb), w, N))
+        y_ref = oracle.gemm_q4(xb, p["wq"], p["s"], T, K, N)
+    else:
+        w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+        y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), w, N))
+        y_ref = oracle.gemm_q5(xb, p["wn"], p["wh"], p["s"], T, K, N)
+    for t in range(T):   # per token: each row has its own magnitude
+        assert np.all(np.isfinite(y[t]))
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t

@@ -18,9 +18,10 @@ namespace {
 
 // Canonical -> packed codes. One thread per (tile, lane): gathers the lane's 32 codes of the
 // tile from the canonical [N][K/8] nibble words (and [N][K/32] high words for Q5) and writes
-// its four fragment words (+ one high word). Nibble i of fragment word j of lane l is the
-// code at row l/4 + 8*((i&3)&1), column 16j + 2(l%4) + 8*((i&3)>>1) + (i>>2) of the tile,
-// which is the m16n8k16 A-fragment order once decode_q4 widens the nibbles.
+// its four fragment words (+ one high word). Nibble slot i of fragment word j of lane l holds
+// the code at row l/4 + 8*((i&3)>>1), column 16j + 2(l%4) + 8*(i&1) + (i>>2) of the tile; its
+// high bit (Q5) goes to bit j + 4*(i&3) + 16*(i>>2) of the lane's high word. This is the
+// order decode_q4 / decode_q5 turn into m16n8k16 A fragments.
 template <int BITS>
 __global__ void pack_codes_kernel(const uint32_t* __restrict__ wn, const uint32_t* __restrict__ wh,
                                   int K, int N, uint8_t* __restrict__ out) {
@@ -41,16 +42,15 @@ __global__ void pack_codes_kernel(const uint32_t* __restrict__ wn, const uint32_
             uint32_t wv = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int m = i & 3, hi = i >> 2;
-                const int row = gid + 8 * (m & 1);
-                const int k = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1) + hi;
+                const int sm = i & 3, hi = i >> 2;
+                const int row = gid + 8 * (sm >> 1);
+                const int k = g * kGroup + 16 * j + 2 * c + 8 * (sm & 1) + hi;
                 const int n = rt * kTileRows + row;
                 const uint32_t nib = (wn[(size_t)n * kw8 + (k >> 3)] >> (4 * (k & 7))) & 0xFu;
                 wv |= nib << (4 * i);
                 if (BITS == 5) {
                     const uint32_t bit = (wh[(size_t)n * kw32 + (k >> 5)] >> (k & 31)) & 1u;
-                    const int pos = i < 4 ? 4 * j + i : 16 + 4 * j + (i - 4);
-                    hw |= bit << pos;
+                    hw |= bit << (j + 4 * sm + 16 * hi);
                 }
             }
             words[j] = wv;
@@ -77,13 +77,14 @@ __global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N,
 }
 
 // Packed -> fp32 W[n][k], decoding with the projection kernels' own decode_q4/decode_q5:
-// w = (float)s * ((128 + q as bf16) - (128 + z)), both steps exact in fp32.
+// a lower-K half holds 1024 + q, an upper-K half 1024 + 16 q (fp16); w = (float)s * (q - z),
+// every step exact in fp32.
 template <int BITS>
 __global__ void dequant_kernel(const uint8_t* __restrict__ wq, int K, int N, float* __restrict__ w) {
     const int G = K / kGroup;
     const long long total = (long long)(N / kTileRows) * G * 32;
     constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
-    constexpr float off = BITS == 4 ? 136.0f : 144.0f;
+    constexpr float z = BITS == 4 ? 8.0f : 16.0f;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const int lane = (int)(idx & 31);
@@ -110,14 +111,16 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, int K, int N, flo
             }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
+                // register m: rows r (m even) / r+8 (m odd), K pair k (m < 2) / k+8 (m >= 2)
                 const int row = gid + 8 * (m & 1);
                 const int k = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1);
                 const float s = (m & 1) ? s_hi : s_lo;
-                const float lo = __uint_as_float(a[m] << 16) - off;
-                const float hi = __uint_as_float(a[m] & 0xFFFF0000u) - off;
+                const float step = m < 2 ? 1.0f : 16.0f;
+                const float v0 = __half2float(__ushort_as_half((unsigned short)(a[m] & 0xFFFFu)));
+                const float v1 = __half2float(__ushort_as_half((unsigned short)(a[m] >> 16)));
                 float* dst = w + (size_t)(rt * kTileRows + row) * K + k;
-                dst[0] = s * lo;
-                dst[1] = s * hi;
+                dst[0] = s * ((v0 - 1024.0f) / step - z);
+                dst[1] = s * ((v1 - 1024.0f) / step - z);
             }
         }
     }
@@ -137,6 +140,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 bool g_pdl = true;
+int g_operands = -1;   // -1: by T (plan), 0: bf16, 1: fp16 (NQ_OPERANDS, for measurement)
 bool g_env_read = false;
 
 size_t ws_tickets_off() { return 256; }
@@ -153,6 +157,9 @@ nq_status current_device(DevState** out, int* dev_out) {
     if (!g_env_read) {
         const char* e = std::getenv("NQ_PDL");
         if (e && e[0] == '0') g_pdl = false;
+        const char* o = std::getenv("NQ_OPERANDS");
+        if (o && std::strcmp(o, "fp16") == 0) g_operands = 1;
+        if (o && std::strcmp(o, "bf16") == 0) g_operands = 0;
         g_env_read = true;
     }
     DevState& d = g_dev[dev];
@@ -249,6 +256,7 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     }
     ProjArgs a;
     if (!make_plan(bits, swiglu ? 1 : 0, T, K, N, d->sms, a.p)) return NQ_ERR_SHAPE;
+    if (g_operands >= 0) a.p.f16 = g_operands;
     st = ensure_workspace(*d, a.p.slots, a.p.RP);
     if (st != NQ_OK) return st;
     a.X = static_cast<const uint16_t*>(X);

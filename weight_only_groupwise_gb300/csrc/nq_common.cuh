@@ -29,7 +29,10 @@ constexpr int kTileRows = 16;        // output rows per tile (MMA M)
 constexpr int kQ4TileBytes = 512;    // 16 x 64 nibbles
 constexpr int kQ5TileBytes = 640;    // + 16 x 64 high bits
 constexpr int kScaleTileBytes = 32;  // 16 fp16
-constexpr int kBlockGroups = 16;     // groups per packed block (= groups per pipeline stage)
+#ifndef NQ_BLOCK_GROUPS
+#define NQ_BLOCK_GROUPS 32
+#endif
+constexpr int kBlockGroups = NQ_BLOCK_GROUPS;  // groups per packed block (= per pipeline stage)
 #ifndef NQ_CONSUMER_WARPS
 #define NQ_CONSUMER_WARPS 8
 #endif
@@ -82,7 +85,14 @@ struct Plan {
     int CG, stages;
     long long slots;       // partial-sum slots: S * RP + P
     int tile_bytes, stage_bytes, x_bytes, corr_bytes, red_bytes, bar_bytes, smem_bytes;
+    int f16;               // 1: fp16 MMA operands (X converted in shared memory), 0: bf16
 };
+
+// Largest T that uses fp16 operands: one shift per code word instead of three, paid for by
+// converting the activation slab to fp16 once per block, which grows with T.
+#ifndef NQ_F16_MAX_T
+#define NQ_F16_MAX_T 2
+#endif
 
 NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan& p) {
     p.bits = bits;
@@ -115,13 +125,14 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
     p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
     p.red_bytes = 2 * kConsumerWarps * 2 * 512;  // double-buffered run reduction
-    p.bar_bytes = 256;                           // barriers and flags
+    p.bar_bytes = 512;                           // barriers, flags, per-token range data
     const int fixed = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes;
     int st = (kSmemLimit - fixed) / p.stage_bytes;
     if (st > kMaxStages) st = kMaxStages;
     p.stages = st;
     p.smem_bytes = fixed + st * p.stage_bytes;
     p.slots = (long long)p.S * p.RP + p.P;
+    p.f16 = T <= NQ_F16_MAX_T ? 1 : 0;
     return st >= 2;
 }
 
@@ -326,14 +337,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// Same copy without an L2 eviction hint (activations: re-read by every block).
-__device__ __forceinline__ void bulk_g2s_keep(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -350,6 +353,16 @@ __device__ __forceinline__ int ticket_add(int* p) {
     int old;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
     return old;
+}
+
+// 16-byte asynchronous copy global -> shared through L2 (LSU path); both addresses 16-byte
+// aligned. cp_async_wait_all waits for all of the thread's outstanding copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ void grid_dependency_wait() {
@@ -369,13 +382,48 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A * B (zero accumulator), m16n8k16, fp16 or bf16 inputs, fp32 results.
+template <bool F16>
+__device__ __forceinline__ void mma_zero_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    const float z = 0.f;
+    if constexpr (F16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // ---------------------------------------------------------------- code decode
 //
-// bf16 0x4300 is 128.0 with a unit step in its 7 fraction bits, so OR-ing a code q < 128
-// into the low bits gives exactly the bf16 value 128 + q. The projection kernels feed
-// 128 + q to the tensor cores and subtract the same MMA chain run on the constant code z,
-// so no per-weight subtraction is needed.
-constexpr uint32_t kBf16Magic = 0x43004300u;
+// The MMAs run on fp16 operands. fp16 0x6400 is 1024.0 with a unit step in its 10 fraction
+// bits, so OR-ing a code q into bits 0..3 (or 0..4) of a half gives exactly 1024 + q, and
+// OR-ing it into bits 4..7 gives exactly 1024 + 16 q. A lane's code word is laid out so that
+// the codes of the fragment's lower-K pairs (registers 0, 1) sit at bits 0..3 and the codes
+// of its upper-K pairs (registers 2, 3) at bits 4..7 of each half, after at most one shift:
+//   word bits  0-3  a0 (row r,   k)       16-19 a1 (row r,   k+1)
+//              4-7  a4 (row r,   k+8)     20-23 a5 (row r,   k+9)
+//              8-11 a2 (row r+8, k)       24-27 a3 (row r+8, k+1)
+//             12-15 a6 (row r+8, k+8)     28-31 a7 (row r+8, k+9)
+// with r = lane/4 and k = 2*(lane%4) of the K step. The upper-K registers carry 16x their
+// weight; the kernels store X / 16 at the upper-K positions of every 16-wide K step, so every
+// product is (1024 + q) * x or (1024 + 16 q) * (x / 16) = (1024/16 ... ) exactly as wanted: the
+// sum over a K step is sum(q * x) + 1024 * sum(x_lo + x_hi / 16), and the second term is the
+// same MMA chain on the constant code 0 -- removed exactly by subtracting that chain.
+constexpr uint32_t kF16Magic = 0x64006400u;   // 1024.0 in both halves
 
 // (a & MASK) | c in one LOP3 (c is kept in a register so it is not split in two ops).
 template <uint32_t MASK>
@@ -385,26 +433,49 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
     return d;
 }
 
-// Four bf16x2 A-fragment registers (values 128 + q) from one packed Q4 word: register m
-// holds nibble m in its low half and nibble m + 4 in its high half. `magic` = kBf16Magic.
-__device__ __forceinline__ void decode_q4(uint32_t w, uint32_t a[4], uint32_t magic = kBf16Magic) {
+// Four fp16x2 A-fragment registers from one packed Q4 word: registers 0, 1 hold 1024 + q of
+// the lower-K pairs, registers 2, 3 hold 1024 + 16 q of the upper-K pairs. One shift, four LOP3.
+__device__ __forceinline__ void decode_q4(uint32_t w, uint32_t a[4], uint32_t magic = kF16Magic) {
+    const uint32_t w8 = w >> 8;
     a[0] = and_or<0x000F000Fu>(w, magic);
-    a[1] = and_or<0x000F000Fu>(w >> 4, magic);
-    a[2] = and_or<0x000F000Fu>(w >> 8, magic);
+    a[2] = and_or<0x00F000F0u>(w, magic);
+    a[1] = and_or<0x000F000Fu>(w8, magic);
+    a[3] = and_or<0x00F000F0u>(w8, magic);
+}
+
+// The same packed word decoded for bf16 operands (bf16 0x4300 = 128.0 with a unit step in its
+// 7 fraction bits): every register holds 128 + q, so each code must sit at bits 0..3 of its
+// half -- three shifts, four LOP3 -- and X is used as is (no division by 16).
+constexpr uint32_t kBf16Magic = 0x43004300u;
+__device__ __forceinline__ void decode_q4_bf16(uint32_t w, uint32_t a[4], uint32_t magic = kBf16Magic) {
+    a[0] = and_or<0x000F000Fu>(w, magic);
+    a[2] = and_or<0x000F000Fu>(w >> 4, magic);
+    a[1] = and_or<0x000F000Fu>(w >> 8, magic);
     a[3] = and_or<0x000F000Fu>(w >> 12, magic);
 }
 
-// Q5: as decode_q4, plus bit 4 of each code from the lane's high word h. For K step J the
-// high bit of nibble m (m < 4) sits at bit 4J + m and that of nibble m + 4 at bit 16 + 4J + m,
-// so one shift moves both onto bits 4 and 20.
+// Q5 for bf16 operands: the high bit of every code goes to bit 4 of its half (+16).
 template <int J>
-__device__ __forceinline__ void decode_q5(uint32_t w, uint32_t h, uint32_t a[4], uint32_t magic = kBf16Magic) {
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int sh = 4 * J + m - 4;
-        const uint32_t hb = sh >= 0 ? (h >> sh) : (h << (-sh));
-        a[m] = and_or<0x000F000Fu>(w >> (4 * m), and_or<0x00100010u>(hb, magic));
-    }
+__device__ __forceinline__ void decode_q5_bf16(uint32_t w, uint32_t h, uint32_t a[4], uint32_t magic = kBf16Magic) {
+    a[0] = and_or<0x000F000Fu>(w, and_or<0x00100010u>(h << (4 - J), magic));
+    a[2] = and_or<0x000F000Fu>(w >> 4, and_or<0x00100010u>(h >> J, magic));
+    a[1] = and_or<0x000F000Fu>(w >> 8, and_or<0x00100010u>(h >> (4 + J), magic));
+    a[3] = and_or<0x000F000Fu>(w >> 12, and_or<0x00100010u>(h >> (8 + J), magic));
+}
+
+// Q5: as decode_q4, plus bit 4 of each code from the lane's high word h, which lands on bit 4
+// of a lower-K half (+16) or bit 8 of an upper-K half (+256 = 16 * 16). For K step J the high
+// bits of registers 0 / 2 sit at bits {J, 16+J} / {4+J, 20+J} of h and those of registers
+// 1 / 3 at bits {8+J, 24+J} / {12+J, 28+J}: one left shift by 4-J aligns the first pair of
+// registers, one right shift by 4+J the second.
+template <int J>
+__device__ __forceinline__ void decode_q5(uint32_t w, uint32_t h, uint32_t a[4], uint32_t magic = kF16Magic) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t ha = h << (4 - J), hb = h >> (4 + J);
+    a[0] = and_or<0x000F000Fu>(w, and_or<0x00100010u>(ha, magic));
+    a[2] = and_or<0x00F000F0u>(w, and_or<0x01000100u>(ha, magic));
+    a[1] = and_or<0x000F000Fu>(w8, and_or<0x00100010u>(hb, magic));
+    a[3] = and_or<0x00F000F0u>(w8, and_or<0x01000100u>(hb, magic));
 }
 
 }  // namespace nq

@@ -13,9 +13,9 @@ cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
-template <int BITS, bool SWIGLU>
-cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    auto kern = proj_kernel<BITS, SWIGLU>;
+template <int BITS, bool SWIGLU, bool F16>
+cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
+    auto kern = proj_kernel<BITS, SWIGLU, F16>;
     // The shared-memory opt-in is per device; set it on every launch of a new size class
     // (cheap: the driver caches it) rather than tracking devices here.
     static thread_local int set_for_device = -1;
@@ -37,6 +37,13 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// The operand type is part of the plan (a.p.f16): fp16 operands for small T, bf16 otherwise.
+template <int BITS, bool SWIGLU>
+cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
+    return a.p.f16 ? launch_proj_t<BITS, SWIGLU, true>(a, stream, pdl)
+                   : launch_proj_t<BITS, SWIGLU, false>(a, stream, pdl);
 }
 
 }  // namespace nq

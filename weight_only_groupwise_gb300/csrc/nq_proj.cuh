@@ -11,13 +11,14 @@
 //     scales) of each of the two M tiles: one copy per tile, which keeps the copy engine at
 //     full rate. It also bulk-copies the activations of the current K slab (T rows, padded).
 //   * Consumer warps (kConsumerWarps): warp w takes K groups w and w + 8 of every stage, for
-//     both 16-row tiles of the row pair. A lane decodes its 16 code bytes into bf16 A
-//     fragments holding 128 + q (exact), loads the B fragment of X with ldmatrix and runs
-//     four m16n8k16 MMAs from a zero accumulator: P = sum((128 + q) * x). The MMAs of the
+//     both 16-row tiles of the row pair. A lane decodes its 16 code bytes into fp16 A
+//     fragments (1024 + q, or 1024 + 16 q against X / 16; exact), loads the B fragment of X
+//     with ldmatrix and runs four m16n8k16 MMAs from a zero accumulator: P. The MMAs of the
 //     warp's four tiles are issued K-step by K-step so the four accumulator chains overlap.
-//     The same four MMAs on the constant code z give O = sum((128 + z) * x) once per group
-//     and slab; P - O = sum((q - z) * x) up to fp32 rounding, and exactly 0 where every code
-//     equals z (identical MMA inputs). The fp16 scale is applied with one FMA per group.
+//     The same four MMAs on the constant code z give O once per group and slab;
+//     P - O = sum((q - z) * x) up to fp32 rounding, and exactly 0 where every code equals z
+//     (identical MMA inputs). The fp16 scale is applied with one FMA per group. X is turned
+//     into fp16 in shared memory once per slab (per-token power-of-two range guard).
 //   * Epilogue warp: at the end of each (slab, row pair) run the consumers drop their
 //     accumulators into one of two shared buffers and carry on. The epilogue warp reduces
 //     the warps' parts in a fixed order and writes Y directly when the run covers its whole
@@ -67,28 +68,39 @@ __device__ __forceinline__ uint32_t word_of(const uint4& w) {
     return J == 0 ? w.x : (J == 1 ? w.y : (J == 2 ? w.z : w.w));
 }
 
-// A fragment of K step J: 128 + q as bf16 pairs.
-template <int BITS, int J>
+// A fragment of K step J: fp16 pairs (1024 + q lower-K, 1024 + 16 q upper-K) or bf16 pairs
+// (128 + q everywhere).
+template <int BITS, bool F16, int J>
 __device__ __forceinline__ void decode_step(const uint4& w, uint32_t hb, uint32_t a[4], uint32_t magic) {
-    if constexpr (BITS == 4) decode_q4(word_of<J>(w), a, magic);
-    else decode_q5<J>(word_of<J>(w), hb, a, magic);
+    if constexpr (F16) {
+        if constexpr (BITS == 4) decode_q4(word_of<J>(w), a, magic);
+        else decode_q5<J>(word_of<J>(w), hb, a, magic);
+    } else {
+        if constexpr (BITS == 4) decode_q4_bf16(word_of<J>(w), a, magic);
+        else decode_q5_bf16<J>(word_of<J>(w), hb, a, magic);
+    }
 }
 
-// Which group (0/1: B fragments xb[h], O o[h]) and which M tile (acc[m]) tile t of a pass
-// uses. GROUPS groups x TILES M tiles, tile t = m * GROUPS + h.
+template <bool F16>
+__device__ __forceinline__ void mma_acc(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    if constexpr (F16) mma_f16_16816(d, a, b0, b1); else mma_bf16_16816(d, a, b0, b1);
+}
+
+// Which group (B fragments xb[h], O o[h]) and which M tile (acc[m]) tile t of a pass uses:
+// GROUPS groups x TILES M tiles, tile t = m * GROUPS + h.
 template <int GROUPS>
 __device__ __forceinline__ constexpr int group_of(int t) { return t % GROUPS; }
 template <int GROUPS>
 __device__ __forceinline__ constexpr int mtile_of(int t) { return t / GROUPS; }
 
 // GROUPS x TILES tiles in one pass, K-step-major so their accumulator chains overlap. Each
-// tile's chain is "zero, then K steps 0..3", exactly as for O. code[t] / scale[t]: this
-// lane's code bytes / scale pair of tile t.
-template <int BITS, int GROUPS, int TILES>
+// tile's chain is "K step 0 from a zero accumulator, then K steps 1..3", exactly as for O.
+// code[t] / scale[t]: this lane's code bytes / scale pair of tile t.
+template <int BITS, bool F16, int GROUPS, int TILES>
 __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * TILES],
                                           const uint8_t* const (&scale)[GROUPS * TILES],
-                                          const uint32_t (&xb)[2][8], const float2 (&o)[2], uint32_t magic,
-                                          float (&acc)[2][4]) {
+                                          const uint32_t (&xb)[GROUPS][8], const float2 (&o)[GROUPS],
+                                          uint32_t magic, float (&acc)[2][4]) {
     constexpr int NT = GROUPS * TILES;
     uint4 w[NT];
     uint32_t hb[NT], sw[NT];
@@ -100,25 +112,27 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * 
         sw[t] = *reinterpret_cast<const uint32_t*>(scale[t]);
     }
     float d[NT][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
     uint32_t a[NT][4];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) decode_step<BITS, 0>(w[t], hb[t], a[t], magic);
+    for (int t = 0; t < NT; ++t) {
+        decode_step<BITS, F16, 0>(w[t], hb[t], a[t], magic);
+        mma_zero_16816<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][0], xb[group_of<GROUPS>(t)][1]);
+    }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) mma_bf16_16816(d[t], a[t], xb[group_of<GROUPS>(t)][0], xb[group_of<GROUPS>(t)][1]);
+    for (int t = 0; t < NT; ++t) {
+        decode_step<BITS, F16, 1>(w[t], hb[t], a[t], magic);
+        mma_acc<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][2], xb[group_of<GROUPS>(t)][3]);
+    }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) decode_step<BITS, 1>(w[t], hb[t], a[t], magic);
+    for (int t = 0; t < NT; ++t) {
+        decode_step<BITS, F16, 2>(w[t], hb[t], a[t], magic);
+        mma_acc<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][4], xb[group_of<GROUPS>(t)][5]);
+    }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) mma_bf16_16816(d[t], a[t], xb[group_of<GROUPS>(t)][2], xb[group_of<GROUPS>(t)][3]);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) decode_step<BITS, 2>(w[t], hb[t], a[t], magic);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) mma_bf16_16816(d[t], a[t], xb[group_of<GROUPS>(t)][4], xb[group_of<GROUPS>(t)][5]);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) decode_step<BITS, 3>(w[t], hb[t], a[t], magic);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) mma_bf16_16816(d[t], a[t], xb[group_of<GROUPS>(t)][6], xb[group_of<GROUPS>(t)][7]);
+    for (int t = 0; t < NT; ++t) {
+        decode_step<BITS, F16, 3>(w[t], hb[t], a[t], magic);
+        mma_acc<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][6], xb[group_of<GROUPS>(t)][7]);
+    }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         __half2 sh;
@@ -138,6 +152,22 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// Power-of-two range exponent of one token's X slab from the bits of its max |x| (bf16):
+// x * 2^-e has its maximum in [2^14, 2^15), clear of fp16 overflow and far above its
+// subnormals; clamped so that 2^e and 2^-e stay normal fp32 numbers.
+__device__ __forceinline__ int token_exponent(int max_bits) {
+    const int e = ((max_bits >> 7) & 0xFF) - 127 - 14;
+    return e < -113 ? -113 : (e > 113 ? 113 : e);
+}
+
+// The bf16-operand path keeps fp32's range, but its chains P and O run on offset codes
+// (128 + q): with max |x| < 2^100 neither can overflow (|P| < 2^100 * 143 * 64 < 2^114).
+// A larger token is scaled by 2^-e, e = (exponent of max |x|) - 99 > 0; otherwise e = 0.
+__device__ __forceinline__ int token_exponent_bf16(int max_bits) {
+    const int e = ((max_bits >> 7) & 0xFF) - 127 - 99;
+    return e < 0 ? 0 : e;
+}
+
 // Output element (tile m, token, row) of a run -> its place in the consumers' accumulator
 // layout (m16n8 C fragment: lane l holds rows l/4 and l/4+8, tokens 2(l%4) and 2(l%4)+1).
 __device__ __forceinline__ int red_index(int w, int m, int tok, int row) {
@@ -145,7 +175,7 @@ __device__ __forceinline__ int red_index(int w, int m, int tok, int row) {
     return ((w * 2 + m) * 32 + l) * 4 + j;
 }
 
-template <int BITS, bool SWIGLU>
+template <int BITS, bool SWIGLU, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
@@ -155,9 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     constexpr int kStageBytes = 2 * kTileArea;
     constexpr int NW = kConsumerWarps;
     constexpr int kRedFloats = NW * 2 * 128;          // one run buffer
-    static_assert(kGroupsPerWarp == 2, "two groups per warp per stage");
-    // bf16 pair of the zero-point code in the 128 + q encoding: 136 (Q4) or 144 (Q5)
-    constexpr uint32_t kZeroCode = BITS == 4 ? 0x43084308u : 0x43104310u;
+    constexpr int GPW = kGroupsPerWarp;
+    static_assert(GPW >= 1 && GPW <= 4, "one to four groups per warp per stage");
+    // the zero-point code z in the decode encoding. fp16: 1024 + z for the lower-K registers,
+    // 1024 + 16 z for the upper-K registers; bf16: 128 + z everywhere (z = 8 Q4, 16 Q5)
+    constexpr uint32_t kZeroLo = F16 ? (BITS == 4 ? 0x64086408u : 0x64106410u) : (BITS == 4 ? 0x43084308u : 0x43104310u);
+    constexpr uint32_t kZeroHi = F16 ? (BITS == 4 ? 0x64806480u : 0x65006500u) : kZeroLo;
 
     // plan fields used in loops, in registers
     const Plan& p = a.p;
@@ -172,56 +205,46 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     float* osum = reinterpret_cast<float*>(xs + p.x_bytes);  // O[gl][8]
     float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(osum) + p.corr_bytes);  // [2][kRedFloats]
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + p.red_bytes);
-    // bars: full[kMaxStages], empty[kMaxStages]; then x_full, x_empty; then flags
-    volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 2);
+    // bars: full[kMaxStages], empty[kMaxStages]; then flags
+    volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages);
+    // per token: max |x| bits of the current slab, then its power-of-two range exponent
+    int* xmax = const_cast<int*>(flags) + 8;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
-    const uint32_t x_full = smem_u32(bars + 2 * kMaxStages), x_empty = x_full + 8;
     // zero row for ldmatrix lanes of absent tokens: the 16 bytes after the last X row
     const int pitch = x_pitch(GS);
     uint8_t* zero_row = xs + T * pitch;
+
+    const long long u0 = cta_begin(p, cta), u1 = cta_begin(p, cta + 1);
+    const SegOrder order = seg_order(p, u0, u1);
 
     if (tid == 0) {
         for (int i = 0; i < nstages; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, kConsumerWarps);
         }
-        mbar_init(x_full, 1);
-        mbar_init(x_empty, kConsumerWarps);
         flags[0] = 0;  // abort
+        for (int t = 0; t < 8; ++t) xmax[t] = 0;
         *reinterpret_cast<uint4*>(zero_row) = make_uint4(0, 0, 0, 0);
         mbar_fence_init();
     }
-    __syncthreads();
-    // Programmatic dependent launch: nothing below touches global memory that the
-    // preceding kernel in the stream may still write before this point.
-    grid_dependency_wait();
-    // Let the next kernel in the stream be scheduled as SMs free up; it waits in turn.
+    // Programmatic dependent launch: the next kernel in the stream may be scheduled as SMs
+    // free up. The consumers (which read X) and the epilogue warp (which writes Y, partial
+    // sums and tickets) wait for the preceding kernel to finish (grid_dependency_wait)
+    // before they touch global memory. The producer streams the weights at once: no kernel
+    // that writes them lets its dependents start early.
     grid_launch_dependents();
-
-    const long long u0 = cta_begin(p, cta), u1 = cta_begin(p, cta + 1);
-    const SegOrder order = seg_order(p, u0, u1);
+    __syncthreads();
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int it = 0, st = 0, nx = 0, cur_slab = -1;
+            int it = 0, st = 0;
             uint32_t phase = 0;
             bool ok = true;
             Segment nat;
             for (int si = 0; si < order.count && ok; ++si) {
                 const Segment sg = seg_pick(p, order, si, nat, u1);
-                if (sg.s != cur_slab) {
-                    if (!mbar_wait(x_empty, (nx & 1) ^ 1, flags, a.dev_err)) { ok = false; break; }
-                    const int gs = slab_groups(p, sg.s);
-                    const uint32_t row_bytes = gs * 128;
-                    mbar_arrive_expect_tx(x_full, row_bytes * T);
-                    for (int t = 0; t < T; ++t)
-                        bulk_g2s_keep(smem_u32(xs + t * pitch),
-                                      a.X + (size_t)t * p.K + (size_t)sg.s * GS * kGroup, row_bytes, x_full);
-                    ++nx;
-                    cur_slab = sg.s;
-                }
                 const int rt0 = SWIGLU ? sg.rp : 2 * sg.rp;
                 const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
                 const bool has1 = SWIGLU || rt1 < RT;
@@ -262,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 const int first = it > nstages ? it - nstages : 0;
                 for (int j = first; j < it; ++j)
                     mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, 100000000ull);
-                if (nx > 0) mbar_wait_drain(x_full, (nx - 1) & 1, 100000000ull);
             }
         }
         return;
@@ -273,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         // lane takes outputs o = lane + 32 q: q < 8 (gemm: 2 tiles x 128) or q < 4 (swiglu:
         // 128 gate/up pairs). o -> M tile o >> 7, token (o & 127) >> 4, row o & 15.
         constexpr int NQ = SWIGLU ? 4 : 8;
+        grid_dependency_wait();  // Y, partial sums and tickets may still be in the preceding kernel's use
         Segment nat;
         for (int si = 0; si < order.count; ++si) {
             const Segment sg = seg_pick(p, order, si, nat, u1);
@@ -354,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
 
     // The magic constant lives in a register so every decode output is a single LOP3.
     uint32_t magic;
-    asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kBf16Magic));
+    asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(F16 ? kF16Magic : kBf16Magic));
 
     // ldmatrix row addresses: lane l serves row (l & 7) of matrix (l >> 3); matrix mi covers
     // K step (mi >> 1) and its half (mi & 1). Absent tokens read the zero row.
@@ -368,22 +391,90 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     const uint32_t code_lane = lane * 16, scale_lane = BG * TB + (lane >> 2) * 4;
     const float* osum_lane = osum + 2 * (lane & 3);
 
-    int st = 0, nx = 0, cur_slab = -1;
+    int st = 0, cur_slab = -1;
     uint32_t phase = 0;
+    float tok_scale0 = 1.f, tok_scale1 = 1.f;
     Segment nat;
     for (int si = 0; si < order.count; ++si) {
         const Segment sg = seg_pick(p, order, si, nat, u1);
         if (sg.s != cur_slab) {
-            if (cur_slab >= 0) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(x_empty);
-            }
-            mbar_wait(x_full, nx & 1, flags, a.dev_err);
-            ++nx;
+            if (cur_slab >= 0)
+                named_bar_sync(kBarConsumers, kConsumerThreads);  // all done with the old slab
+            else
+                grid_dependency_wait();  // X may be the preceding kernel's output
             cur_slab = sg.s;
-            // O[gl][t]: the group MMA chain on the zero-point code, two groups per pass.
             const int gs = slab_groups(p, sg.s);
-            const uint32_t az[4] = {kZeroCode, kZeroCode, kZeroCode, kZeroCode};
+            const int chunks = gs * 8;  // 16-byte chunks per token row
+            // The X slab straight into shared memory (LSU path, not the producer's TMA queue,
+            // so it does not wait behind the weight stream).
+            const uint16_t* xg = a.X + (size_t)sg.s * GS * kGroup;
+            for (int t = 0; t < T; ++t)
+                for (int c = tid; c < chunks; c += kConsumerThreads)
+                    cp_async16(smem_u32(xs + t * pitch + c * 16), xg + (size_t)t * p.K + c * 8);
+            cp_async_wait_all();
+            // Per token, max |x| over the slab (bit patterns compare like magnitudes).
+            if (tid < 8) xmax[tid] = 0;
+            named_bar_sync(kBarConsumers, kConsumerThreads);
+            for (int t = 0; t < T; ++t) {
+                uint32_t mx = 0;
+                for (int c = tid; c < chunks; c += kConsumerThreads) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
+                    const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+                    mx = max(mx, max(m & 0xFFFFu, m >> 16));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                if (lane == 0) atomicMax(xmax + t, (int)mx);
+            }
+            named_bar_sync(kBarConsumers, kConsumerThreads);
+            if constexpr (F16) {
+                // X slab bf16 -> fp16 in place, times 2^-e (token_exponent); the upper-K half
+                // of every 16-wide K step is also divided by 16 (see decode_q4). Both exact.
+                for (int t = 0; t < T; ++t) {
+                    const int e = token_exponent(xmax[t]);
+                    const float lo_scale = __int_as_float((127 - e) << 23);
+                    const float hi_scale = lo_scale * 0.0625f;
+                    for (int c = tid; c < chunks; c += kConsumerThreads) {
+                        uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
+                        const uint4 v = *q;
+                        const float sc = (c & 1) ? hi_scale : lo_scale;
+                        uint4 o;
+                        uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+                        const uint32_t* iv = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __half2 h2 = __floats2half2_rn(__uint_as_float(iv[i] << 16) * sc,
+                                                                 __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
+                            ov[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        *q = o;
+                    }
+                }
+            } else {
+                // bf16 operands: only a token too large for the offset chains is rescaled.
+                for (int t = 0; t < T; ++t) {
+                    const int e = token_exponent_bf16(xmax[t]);
+                    if (e == 0) continue;
+                    const float sc = __int_as_float((127 - e) << 23);
+                    for (int c = tid; c < chunks; c += kConsumerThreads) {
+                        uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
+                        uint4 v = *q;
+                        uint32_t* iv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(iv[i] << 16) * sc,
+                                                                            __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
+                            iv[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        *q = v;
+                    }
+                }
+            }
+            named_bar_sync(kBarConsumers, kConsumerThreads);
+            if (tid < 8)   // e per token, for the handoff below
+                xmax[tid] = tid < T ? (F16 ? token_exponent(xmax[tid]) : token_exponent_bf16(xmax[tid])) : 0;
+            // O[gl][t]: the group MMA chain on the zero-point code, two groups per pass.
+            const uint32_t az[4] = {kZeroLo, kZeroLo, kZeroHi, kZeroHi};
             for (int gl = warp; gl < gs; gl += 2 * NW) {
                 const int gl2 = gl + NW < gs ? gl + NW : gl;
                 uint32_t xb[2][8];
@@ -393,9 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 ldsm_x4(ld_base + gl2 * ld_group_step + ld_half_step, xb[1] + 4);
                 float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int h = 0; h < 2; ++h) mma_zero_16816<F16>(d[h], az, xb[h][0], xb[h][1]);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) mma_bf16_16816(d[h], az, xb[h][2 * j], xb[h][2 * j + 1]);
+                for (int j = 1; j < 4; ++j)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) mma_acc<F16>(d[h], az, xb[h][2 * j], xb[h][2 * j + 1]);
                 if (lane < 4) {
                     osum[gl * 8 + 2 * lane] = d[0][0];
                     osum[gl * 8 + 2 * lane + 1] = d[0][1];
@@ -404,6 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 }
             }
             named_bar_sync(kBarConsumers, kConsumerThreads);
+            // 2^e of the lane's two token columns, applied when the run is handed over
+            tok_scale0 = __int_as_float((127 + xmax[2 * (lane & 3)]) << 23);
+            tok_scale1 = __int_as_float((127 + xmax[2 * (lane & 3) + 1]) << 23);
         }
 
         const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
@@ -415,52 +511,63 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             if (ok) {
                 const uint8_t* t0 = stage_mem + st * kStageBytes;
                 const int gl0 = b * BG - slab_g0;  // slab-local group of block index 0
+                // this warp's first group of the block: X fragment address and O pointer
+                const uint32_t la0 = ld_base + (gl0 + warp) * ld_group_step;
+                const float* o0 = osum_lane + (gl0 + warp) * 8;
                 if (i0 == 0 && i1 == BG) {
-                    // whole block: groups warp and warp + 8 of both M tiles, K-step-major
-                    uint32_t xb[2][8];
-                    float2 o[2];
+                    // whole block: this warp's GPW groups of both M tiles, K-step-major
+                    uint32_t xb[GPW][8];
+                    float2 o[GPW];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int gl = gl0 + warp + NW * h;
-                        ldsm_x4(ld_base + gl * ld_group_step, xb[h]);
-                        ldsm_x4(ld_base + gl * ld_group_step + ld_half_step, xb[h] + 4);
-                        o[h] = *reinterpret_cast<const float2*>(osum_lane + gl * 8);
+                    for (int h = 0; h < GPW; ++h) {
+                        const uint32_t la = la0 + (NW * h) * ld_group_step;
+                        ldsm_x4(la, xb[h]);
+                        ldsm_x4(la + ld_half_step, xb[h] + 4);
+                        o[h] = *reinterpret_cast<const float2*>(o0 + 8 * NW * h);
                     }
                     const uint8_t* c0 = t0 + warp * TB + code_lane;
                     const uint8_t* s0 = t0 + scale_lane + warp * kScaleTileBytes;
                     if (has1) {
-                        const uint8_t* const code[4] = {c0, c0 + NW * TB, c0 + kTileArea, c0 + kTileArea + NW * TB};
-                        const uint8_t* const scale[4] = {s0, s0 + NW * kScaleTileBytes, s0 + kTileArea,
-                                                         s0 + kTileArea + NW * kScaleTileBytes};
-                        tiles_mma<BITS, 2, 2>(code, scale, xb, o, magic, acc);
+                        const uint8_t* code[2 * GPW];
+                        const uint8_t* scale[2 * GPW];
+#pragma unroll
+                        for (int t = 0; t < 2 * GPW; ++t) {
+                            const int m = t / GPW, h = t % GPW;
+                            code[t] = c0 + m * kTileArea + NW * h * TB;
+                            scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
+                        }
+                        tiles_mma<BITS, F16, GPW, 2>(code, scale, xb, o, magic, acc);
                     } else {
-                        const uint8_t* const code[2] = {c0, c0 + NW * TB};
-                        const uint8_t* const scale[2] = {s0, s0 + NW * kScaleTileBytes};
-                        tiles_mma<BITS, 2, 1>(code, scale, xb, o, magic, acc);
+                        const uint8_t* code[GPW];
+                        const uint8_t* scale[GPW];
+#pragma unroll
+                        for (int t = 0; t < GPW; ++t) {
+                            code[t] = c0 + NW * t * TB;
+                            scale[t] = s0 + NW * t * kScaleTileBytes;
+                        }
+                        tiles_mma<BITS, F16, GPW, 1>(code, scale, xb, o, magic, acc);
                     }
                 } else {
                     // part of a block (first or last block of a run): group by group
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < GPW; ++h) {
                         const int i = warp + NW * h;
                         if (i >= i0 && i < i1) {
-                            const int gl = gl0 + i;
-                            uint32_t xb[2][8];
-                            ldsm_x4(ld_base + gl * ld_group_step, xb[0]);
-                            ldsm_x4(ld_base + gl * ld_group_step + ld_half_step, xb[0] + 4);
-                            float2 o[2];
-                            o[0] = *reinterpret_cast<const float2*>(osum_lane + gl * 8);
-                            o[1] = o[0];
+                            uint32_t xb[1][8];
+                            const uint32_t la = la0 + (NW * h) * ld_group_step;
+                            ldsm_x4(la, xb[0]);
+                            ldsm_x4(la + ld_half_step, xb[0] + 4);
+                            const float2 o[1] = {*reinterpret_cast<const float2*>(o0 + 8 * NW * h)};
                             const uint8_t* c0 = t0 + i * TB + code_lane;
                             const uint8_t* s0 = t0 + scale_lane + i * kScaleTileBytes;
                             if (has1) {
                                 const uint8_t* const code[2] = {c0, c0 + kTileArea};
                                 const uint8_t* const scale[2] = {s0, s0 + kTileArea};
-                                tiles_mma<BITS, 1, 2>(code, scale, xb, o, magic, acc);
+                                tiles_mma<BITS, F16, 1, 2>(code, scale, xb, o, magic, acc);
                             } else {
                                 const uint8_t* const code[1] = {c0};
                                 const uint8_t* const scale[1] = {s0};
-                                tiles_mma<BITS, 1, 1>(code, scale, xb, o, magic, acc);
+                                tiles_mma<BITS, F16, 1, 1>(code, scale, xb, o, magic, acc);
                             }
                         }
                     }
@@ -475,8 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         const int b = si & 1;
         if (si >= 2) named_bar_sync(kBarRedFree + b, kHandoffThreads);
         float4* r4 = reinterpret_cast<float4*>(red + b * kRedFloats);
-        r4[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-        r4[(warp * 2 + 1) * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+        r4[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0] * tok_scale0, acc[0][1] * tok_scale1,
+                                                     acc[0][2] * tok_scale0, acc[0][3] * tok_scale1);
+        r4[(warp * 2 + 1) * 32 + lane] = make_float4(acc[1][0] * tok_scale0, acc[1][1] * tok_scale1,
+                                                     acc[1][2] * tok_scale0, acc[1][3] * tok_scale1);
         named_bar_arrive(kBarRedFull + b, kHandoffThreads);
 #pragma unroll
         for (int m = 0; m < 2; ++m)
