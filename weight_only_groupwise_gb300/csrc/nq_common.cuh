@@ -38,8 +38,9 @@ constexpr int kBlockGroups = NQ_BLOCK_GROUPS;  // groups per packed block (= per
 #endif
 constexpr int kConsumerWarps = NQ_CONSUMER_WARPS;
 constexpr int kProducerWarp = kConsumerWarps;         // issues the bulk copies
-constexpr int kEpilogueWarp = kConsumerWarps + 1;     // reduces runs, stores, settles split-K
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;     // first of the warps that reduce runs,
+constexpr int kEpilogueWarps = 2;                     // store them and settle split-K (runs alternate)
+constexpr int kThreads = (kConsumerWarps + 1 + kEpilogueWarps) * 32;
 constexpr int kChunkGroups = kBlockGroups;           // K groups per pipeline stage
 constexpr int kGroupsPerWarp = kChunkGroups / kConsumerWarps;
 static_assert(kGroupsPerWarp * kConsumerWarps == kChunkGroups, "stage groups split evenly over warps");
@@ -48,6 +49,8 @@ constexpr int kSmemLimit = 227 * 1024;
 constexpr int kXBudget = 97 * 1024;  // on-chip activation slab (96 groups x 8 rows + padding)
 constexpr int kMinUnitsPerCta = 16;
 constexpr int kPartialFloats = 256;  // 2 M tiles x 16 rows x 8 tokens
+constexpr int kMaxRed = 4;           // most run hand-over buffers (consumers -> epilogue warps)
+constexpr int kRedBufBytes = kConsumerWarps * 2 * 512;  // one buffer: every warp's two accumulator tiles
 constexpr long long kWaitTimeoutNs = 2000000000LL;  // 2 s per bounded wait
 
 // Errors a kernel can raise through the workspace flag word.
@@ -86,6 +89,7 @@ struct Plan {
     long long slots;       // partial-sum slots: S * RP + P
     int tile_bytes, stage_bytes, x_bytes, corr_bytes, red_bytes, bar_bytes, smem_bytes;
     int f16;               // 1: fp16 MMA operands (X converted in shared memory), 0: bf16
+    int nred;              // run hand-over buffers (2..kMaxRed)
 };
 
 // Largest T that uses fp16 operands: one shift per code word instead of three, paid for by
@@ -124,13 +128,26 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
     p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
     p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
-    p.red_bytes = 2 * kConsumerWarps * 2 * 512;  // double-buffered run reduction
     p.bar_bytes = 512;                           // barriers, flags, per-token range data
-    const int fixed = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes;
-    int st = (kSmemLimit - fixed) / p.stage_bytes;
-    if (st > kMaxStages) st = kMaxStages;
+    // Run hand-over buffers: as many as fit (up to kMaxRed) without costing a pipeline stage
+    // against two; spare buffers let the consumers run ahead of a split-K settle.
+    int st = 0;
+    for (int nr = kMaxRed; nr >= 2; --nr) {
+        const int fixed = p.x_bytes + p.corr_bytes + nr * kRedBufBytes + p.bar_bytes;
+        int s2 = (kSmemLimit - fixed) / p.stage_bytes;
+        if (s2 > kMaxStages) s2 = kMaxStages;
+        const int fixed2 = p.x_bytes + p.corr_bytes + 2 * kRedBufBytes + p.bar_bytes;
+        int s_two = (kSmemLimit - fixed2) / p.stage_bytes;
+        if (s_two > kMaxStages) s_two = kMaxStages;
+        if (s2 == s_two || nr == 2) {
+            p.nred = nr;
+            st = s2;
+            break;
+        }
+    }
+    p.red_bytes = p.nred * kRedBufBytes;
     p.stages = st;
-    p.smem_bytes = fixed + st * p.stage_bytes;
+    p.smem_bytes = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes + st * p.stage_bytes;
     p.slots = (long long)p.S * p.RP + p.P;
     p.f16 = T <= NQ_F16_MAX_T ? 1 : 0;
     return st >= 2;
@@ -363,6 +380,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Acquire-release fence at GPU scope: orders this thread's earlier memory operations (and
+// those it has observed) before its later ones, as seen by any thread on the GPU.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 __device__ __forceinline__ void grid_dependency_wait() {

@@ -47,9 +47,10 @@ struct ProjArgs {
     Plan p;
 };
 
-// Named barriers: 1 = consumers only; 2,3 = run buffer b full (consumers arrive, epilogue
-// syncs); 4,5 = run buffer b free (epilogue arrives, consumers sync).
-constexpr int kBarConsumers = 1, kBarRedFull = 2, kBarRedFree = 4;
+// Named barriers: 1 = consumers only; 2 + b = run buffer b full (consumers arrive, the
+// epilogue warp of that run syncs); 2 + kMaxRed + b = run buffer b free (that epilogue warp
+// arrives, consumers sync).
+constexpr int kBarConsumers = 1, kBarRedFull = 2, kBarRedFree = 2 + kMaxRed;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kHandoffThreads = kConsumerThreads + 32;
 
@@ -290,52 +291,66 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         return;
     }
 
-    if (warp == kEpilogueWarp) {
+    if (warp >= kEpilogueWarp) {
         // ------------------------------------------------------------ epilogue
-        // lane takes outputs o = lane + 32 q: q < 8 (gemm: 2 tiles x 128) or q < 4 (swiglu:
-        // 128 gate/up pairs). o -> M tile o >> 7, token (o & 127) >> 4, row o & 15.
-        constexpr int NQ = SWIGLU ? 4 : 8;
+        // Two warps take alternate runs, so one run's split-K settle (publish, fence, ticket,
+        // fix-up: several L2 round trips under a saturated memory system) overlaps the next.
+        // A run has nout outputs o (gemm: M tile, token, row = o / 16TP, (o / 16) % TP,
+        // o % 16; swiglu: gate/up pairs, token, row = o / 16, o % 16) over the TP padded
+        // tokens only; lane takes o = lane + 32 j.
+        const int ew = warp - kEpilogueWarp;
+        const int TP = p.TP, nred = p.nred, tp_log = TP == 1 ? 0 : (TP == 2 ? 1 : (TP == 4 ? 2 : 3));
+        const int nout = (SWIGLU ? 16 : 32) * TP;
         grid_dependency_wait();  // Y, partial sums and tickets may still be in the preceding kernel's use
         Segment nat;
         for (int si = 0; si < order.count; ++si) {
             const Segment sg = seg_pick(p, order, si, nat, u1);
-            const int b = si & 1;
+            if ((si & 1) != ew) continue;
+            const int b = si % nred;
             named_bar_sync(kBarRedFull + b, kHandoffThreads);
             const float* rb = red + b * kRedFloats;
-            float v0[NQ], v1[NQ];
+            float v0[8], v1[8];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const int o = lane + 32 * q;
-                const int m = SWIGLU ? 0 : (o >> 7), tok = (o & 127) >> 4, row = o & 15;
+            for (int j = 0; j < 8; ++j) {
+                const int o = lane + 32 * j;
                 float s0 = 0.f, s1 = 0.f;
+                if (o < nout) {
+                    const int m = SWIGLU ? 0 : o >> (4 + tp_log), tok = (o >> 4) & (TP - 1), row = o & 15;
+                    const float* r0 = rb + red_index(0, m, tok, row);
 #pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    s0 += rb[red_index(w, m, tok, row)];
-                    if (SWIGLU) s1 += rb[red_index(w, 1, tok, row)];
+                    for (int w = 0; w < NW; ++w) {
+                        s0 += r0[w * 256];
+                        if (SWIGLU) s1 += r0[w * 256 + 128];
+                    }
                 }
-                v0[q] = s0;
-                v1[q] = s1;
+                v0[j] = s0;
+                v1[j] = s1;
             }
-            // buffer b is read: hand it back for the run two steps later
-            if (si + 2 < order.count) named_bar_arrive(kBarRedFree + b, kHandoffThreads);
+            // buffer b is read: hand it back for the run nred steps later
+            if (si + nred < order.count) named_bar_arrive(kBarRedFree + b, kHandoffThreads);
             if (flags[0]) continue;
             bool write = segment_complete(p, sg);
             if (!write) {
                 // split-K run: publish the partial, take the ticket, reduce if last
                 float* ws = a.partials + slot_of(p, sg.s, sg.rp, cta) * kPartialFloats;
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    ws[lane + 32 * q] = v0[q];
-                    if (SWIGLU) ws[128 + lane + 32 * q] = v1[q];
+                for (int j = 0; j < 8; ++j) {
+                    const int o = lane + 32 * j;
+                    if (o < nout) {
+                        ws[o] = v0[j];
+                        if (SWIGLU) ws[128 + o] = v1[j];
+                    }
                 }
-                __threadfence();
                 __syncwarp();
                 int last = 0;
-                if (lane == 0) last = ticket_add(a.tickets + sg.rp) == contributions(p, sg.rp) - 1;
+                if (lane == 0) {
+                    fence_acq_rel_gpu();  // the warp's partial stores before the ticket
+                    last = ticket_add(a.tickets + sg.rp) == contributions(p, sg.rp) - 1;
+                }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
 #pragma unroll
-                    for (int q = 0; q < NQ; ++q) v0[q] = v1[q] = 0.f;
+                    for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
                     for (int s = 0; s < p.S; ++s) {
                         const int gs = slab_groups(p, s);
                         const long long r0 = slab_base(p, s) + (long long)sg.rp * gs;
@@ -343,9 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         for (int c = cta_of(p, r0); c <= c_end; ++c) {
                             const float* src = a.partials + slot_of(p, s, sg.rp, c) * kPartialFloats;
 #pragma unroll
-                            for (int q = 0; q < NQ; ++q) {
-                                v0[q] += __ldcg(src + lane + 32 * q);
-                                if (SWIGLU) v1[q] += __ldcg(src + 128 + lane + 32 * q);
+                            for (int j = 0; j < 8; ++j) {
+                                const int o = lane + 32 * j;
+                                if (o < nout) {
+                                    v0[j] += __ldcg(src + o);
+                                    if (SWIGLU) v1[j] += __ldcg(src + 128 + o);
+                                }
                             }
                         }
                     }
@@ -355,13 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             }
             if (write) {
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const int o = lane + 32 * q;
-                    const int m = SWIGLU ? 0 : (o >> 7), tok = (o & 127) >> 4, row = o & 15;
+                for (int j = 0; j < 8; ++j) {
+                    const int o = lane + 32 * j;
+                    const int m = SWIGLU ? 0 : o >> (4 + tp_log), tok = (o >> 4) & (TP - 1), row = o & 15;
                     const int rt = SWIGLU ? sg.rp : 2 * sg.rp + m;
-                    if (tok < T && rt < RT)
+                    if (o < nout && tok < T && rt < RT)
                         a.Y[(size_t)tok * p.N + (size_t)rt * kTileRows + row] =
-                            SWIGLU ? bf16_bits_rn(silu_mul(v0[q], v1[q])) : bf16_bits_rn(v0[q]);
+                            SWIGLU ? bf16_bits_rn(silu_mul(v0[j], v1[j])) : bf16_bits_rn(v0[j]);
                 }
             }
         }
@@ -579,8 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         }
 
         // ------------------------------------------------------------ hand the run over
-        const int b = si & 1;
-        if (si >= 2) named_bar_sync(kBarRedFree + b, kHandoffThreads);
+        const int b = si % p.nred;
+        if (si >= p.nred) named_bar_sync(kBarRedFree + b, kHandoffThreads);
         float4* r4 = reinterpret_cast<float4*>(red + b * kRedFloats);
         r4[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0] * tok_scale0, acc[0][1] * tok_scale1,
                                                      acc[0][2] * tok_scale0, acc[0][3] * tok_scale1);
