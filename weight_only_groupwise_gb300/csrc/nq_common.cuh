@@ -129,10 +129,13 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
     p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
     p.bar_bytes = 512;                           // barriers, flags, per-token range data
-    // Run hand-over buffers: as many as fit (up to kMaxRed) without costing a pipeline stage
-    // against two; spare buffers let the consumers run ahead of a split-K settle.
+    // Run hand-over buffers: kMaxRed if they fit without costing a pipeline stage against
+    // two, else two; spare buffers let the consumers run ahead of a split-K settle. The count
+    // is a multiple of kEpilogueWarps, so each buffer is always served by the same epilogue
+    // warp (two warps never wait on one buffer's barrier at once).
+    static_assert(kMaxRed % kEpilogueWarps == 0 && 2 % kEpilogueWarps == 0, "buffers per epilogue warp");
     int st = 0;
-    for (int nr = kMaxRed; nr >= 2; --nr) {
+    for (int nr = kMaxRed; nr >= 2; nr -= 2) {
         const int fixed = p.x_bytes + p.corr_bytes + nr * kRedBufBytes + p.bar_bytes;
         int s2 = (kSmemLimit - fixed) / p.stage_bytes;
         if (s2 > kMaxStages) s2 = kMaxStages;
