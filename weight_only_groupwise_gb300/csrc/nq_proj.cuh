@@ -430,21 +430,36 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 for (int c = tid; c < chunks; c += kConsumerThreads)
                     cp_async16(smem_u32(xs + t * pitch + c * 16), xg + (size_t)t * p.K + c * 8);
             cp_async_wait_all();
-            // Per token, max |x| over the slab (bit patterns compare like magnitudes).
+            // Per token, max |x| over the slab (bit patterns compare like magnitudes). The bf16
+            // path needs it only when some |x| reaches 2^100 (bits 0x7180): one pass with a
+            // barrier OR-reduction decides, and the per-token pass runs only then.
             if (tid < 8) xmax[tid] = 0;
-            named_bar_sync(kBarConsumers, kConsumerThreads);
-            for (int t = 0; t < T; ++t) {
-                uint32_t mx = 0;
-                for (int c = tid; c < chunks; c += kConsumerThreads) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
-                    const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-                    mx = max(mx, max(m & 0xFFFFu, m >> 16));
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                if (lane == 0) atomicMax(xmax + t, (int)mx);
+            bool need_max = F16;
+            if constexpr (!F16) {
+                bool big = false;
+                for (int t = 0; t < T; ++t)
+                    for (int c = tid; c < chunks; c += kConsumerThreads) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
+                        const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+                        big |= max(m & 0xFFFFu, m >> 16) >= 0x7180u;
+                    }
+                need_max = named_bar_or(kBarConsumers, kConsumerThreads, big);
+            } else {
+                named_bar_sync(kBarConsumers, kConsumerThreads);
             }
-            named_bar_sync(kBarConsumers, kConsumerThreads);
+            if (need_max) {
+                for (int t = 0; t < T; ++t) {
+                    uint32_t mx = 0;
+                    for (int c = tid; c < chunks; c += kConsumerThreads) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
+                        const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+                        mx = max(mx, max(m & 0xFFFFu, m >> 16));
+                    }
+                    mx = __reduce_max_sync(0xffffffffu, mx);
+                    if (lane == 0) atomicMax(xmax + t, (int)mx);
+                }
+                named_bar_sync(kBarConsumers, kConsumerThreads);
+            }
             if constexpr (F16) {
                 // X slab bf16 -> fp16 in place, times 2^-e (token_exponent); the upper-K half
                 // of every 16-wide K step is also divided by 16 (see decode_q4). Both exact.
@@ -470,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 }
             } else {
                 // bf16 operands: only a token too large for the offset chains is rescaled.
-                for (int t = 0; t < T; ++t) {
+                for (int t = 0; t < T && need_max; ++t) {
                     const int e = token_exponent_bf16(xmax[t]);
                     if (e == 0) continue;
                     const float sc = __int_as_float((127 - e) << 23);
@@ -488,36 +503,43 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     }
                 }
             }
-            named_bar_sync(kBarConsumers, kConsumerThreads);
-            if (tid < 8)   // e per token, for the handoff below
-                xmax[tid] = tid < T ? (F16 ? token_exponent(xmax[tid]) : token_exponent_bf16(xmax[tid])) : 0;
-            // O[gl][t]: the group MMA chain on the zero-point code, two groups per pass.
+            if (F16 || need_max) named_bar_sync(kBarConsumers, kConsumerThreads);
+            // O[gl][t]: the group MMA chain on the zero-point code. A warp consumes only the
+            // groups gl = warp (mod NW) of the slab (blocks start on multiples of NW), so it
+            // computes exactly those, four chains per pass, and only it reads them back.
             const uint32_t az[4] = {kZeroLo, kZeroLo, kZeroHi, kZeroHi};
-            for (int gl = warp; gl < gs; gl += 2 * NW) {
-                const int gl2 = gl + NW < gs ? gl + NW : gl;
-                uint32_t xb[2][8];
-                ldsm_x4(ld_base + gl * ld_group_step, xb[0]);
-                ldsm_x4(ld_base + gl * ld_group_step + ld_half_step, xb[0] + 4);
-                ldsm_x4(ld_base + gl2 * ld_group_step, xb[1]);
-                ldsm_x4(ld_base + gl2 * ld_group_step + ld_half_step, xb[1] + 4);
-                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int gl = warp; gl < gs; gl += 4 * NW) {
+                int g[4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) mma_zero_16816<F16>(d[h], az, xb[h][0], xb[h][1]);
+                for (int c = 0; c < 4; ++c) g[c] = gl + c * NW < gs ? gl + c * NW : gl;
+                uint32_t xb[4][8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    ldsm_x4(ld_base + g[c] * ld_group_step, xb[c]);
+                    ldsm_x4(ld_base + g[c] * ld_group_step + ld_half_step, xb[c] + 4);
+                }
+                float d[4][4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mma_zero_16816<F16>(d[c], az, xb[c][0], xb[c][1]);
 #pragma unroll
                 for (int j = 1; j < 4; ++j)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) mma_acc<F16>(d[h], az, xb[h][2 * j], xb[h][2 * j + 1]);
+                    for (int c = 0; c < 4; ++c) mma_acc<F16>(d[c], az, xb[c][2 * j], xb[c][2 * j + 1]);
                 if (lane < 4) {
-                    osum[gl * 8 + 2 * lane] = d[0][0];
-                    osum[gl * 8 + 2 * lane + 1] = d[0][1];
-                    osum[gl2 * 8 + 2 * lane] = d[1][0];
-                    osum[gl2 * 8 + 2 * lane + 1] = d[1][1];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<float2*>(osum + g[c] * 8 + 2 * lane) = make_float2(d[c][0], d[c][1]);
                 }
             }
-            named_bar_sync(kBarConsumers, kConsumerThreads);
-            // 2^e of the lane's two token columns, applied when the run is handed over
-            tok_scale0 = __int_as_float((127 + xmax[2 * (lane & 3)]) << 23);
-            tok_scale1 = __int_as_float((127 + xmax[2 * (lane & 3) + 1]) << 23);
+            __syncwarp();
+            // 2^e of the lane's two token columns (from the max bits), applied at the hand-over
+            {
+                const int m0 = xmax[2 * (lane & 3)], m1 = xmax[2 * (lane & 3) + 1];
+                const int e0 = F16 ? token_exponent(m0) : token_exponent_bf16(m0);
+                const int e1 = F16 ? token_exponent(m1) : token_exponent_bf16(m1);
+                tok_scale0 = __int_as_float((127 + e0) << 23);
+                tok_scale1 = __int_as_float((127 + e1) << 23);
+            }
         }
 
         const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
