@@ -206,11 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     float* osum = reinterpret_cast<float*>(xs + p.x_bytes);  // O[gl][8]
     float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(osum) + p.corr_bytes);  // [2][kRedFloats]
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + p.red_bytes);
-    // bars: full[kMaxStages], empty[kMaxStages]; then flags
-    volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages);
+    // bars: full[kMaxStages], empty[kMaxStages], x_bar; then flags
+    volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 1);
     // per token: max |x| bits of the current slab, then its power-of-two range exponent
     int* xmax = const_cast<int*>(flags) + 8;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+    const uint32_t x_bar = smem_u32(bars + 2 * kMaxStages);  // an activation slab has landed
     // zero row for ldmatrix lanes of absent tokens: the 16 bytes after the last X row
     const int pitch = x_pitch(GS);
     uint8_t* zero_row = xs + T * pitch;
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, kConsumerWarps);
         }
+        mbar_init(x_bar, 1);
         flags[0] = 0;  // abort
         for (int t = 0; t < 8; ++t) xmax[t] = 0;
         *reinterpret_cast<uint4*>(zero_row) = make_uint4(0, 0, 0, 0);
@@ -278,6 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         }
                     }
                     ++it;
+                    // After the first stage, hold the weight stream until a bulk-copied first
+                    // activation slab has landed: its copies share this block's copy engine,
+                    // and behind a full ring of weight stages they would start the consumers late.
+                    if (!F16 && it == 1 && !mbar_wait(x_bar, 0, flags, a.dev_err)) {
+                        ok = false;
+                        break;
+                    }
                     if (++st == nstages) { st = 0; phase ^= 1; }
                 }
             }
@@ -351,19 +360,68 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 if (last) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
-                    for (int s = 0; s < p.S; ++s) {
-                        const int gs = slab_groups(p, s);
-                        const long long r0 = slab_base(p, s) + (long long)sg.rp * gs;
-                        const int c_end = cta_of(p, r0 + gs - 1);
-                        for (int c = cta_of(p, r0); c <= c_end; ++c) {
-                            const float* src = a.partials + slot_of(p, s, sg.rp, c) * kPartialFloats;
+                    // Every contribution of the pair, summed in fixed (slab, block) order.
+                    auto sum_in_order = [&]() {
+                        for (int s = 0; s < p.S; ++s) {
+                            const int gs = slab_groups(p, s);
+                            const long long r0 = slab_base(p, s) + (long long)sg.rp * gs;
+                            const int c_end = cta_of(p, r0 + gs - 1);
+                            for (int c = cta_of(p, r0); c <= c_end; ++c) {
+                                const float* src = a.partials + slot_of(p, s, sg.rp, c) * kPartialFloats;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int o = lane + 32 * j;
-                                if (o < nout) {
-                                    v0[j] += __ldcg(src + o);
-                                    if (SWIGLU) v1[j] += __ldcg(src + 128 + o);
+                                for (int j = 0; j < 8; ++j) {
+                                    const int o = lane + 32 * j;
+                                    if (o < nout) {
+                                        v0[j] += __ldcg(src + o);
+                                        if (SWIGLU) v1[j] += __ldcg(src + 128 + o);
+                                    }
                                 }
+                            }
+                        }
+                    };
+                    if constexpr (F16) {
+                        sum_in_order();  // one slab: two or three contributions
+                    } else {
+                        // Several slabs: the loads go out kBatch contributions at a time (same
+                        // order), so their L2 round trips overlap instead of queueing.
+                        constexpr int kFix = 16, kBatch = 4, JN = SWIGLU ? 4 : 8;
+                        int slots[kFix];
+                        int nc = 0;
+                        for (int s = 0; s < p.S; ++s) {
+                            const int gs = slab_groups(p, s);
+                            const long long r0 = slab_base(p, s) + (long long)sg.rp * gs;
+                            const int c_end = cta_of(p, r0 + gs - 1);
+                            for (int c = cta_of(p, r0); c <= c_end; ++c) {
+                                if (nc < kFix) slots[nc] = (int)slot_of(p, s, sg.rp, c);
+                                ++nc;
+                            }
+                        }
+                        if (nc > kFix) {
+                            sum_in_order();
+                        } else {
+                            for (int k0 = 0; k0 < nc; k0 += kBatch) {
+                                float t0[kBatch][JN], t1[kBatch][JN];
+#pragma unroll
+                                for (int u = 0; u < kBatch; ++u) {
+                                    const float* src = a.partials + (size_t)slots[k0 + u < nc ? k0 + u : k0] * kPartialFloats;
+#pragma unroll
+                                    for (int j = 0; j < JN; ++j) {
+                                        const int o = lane + 32 * j;
+                                        t0[u][j] = t1[u][j] = 0.f;
+                                        if (k0 + u < nc && o < nout) {
+                                            t0[u][j] = __ldcg(src + o);
+                                            if (SWIGLU) t1[u][j] = __ldcg(src + 128 + o);
+                                        }
+                                    }
+                                }
+#pragma unroll
+                                for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+                                    for (int j = 0; j < JN; ++j)
+                                        if (k0 + u < nc) {
+                                            v0[j] += t0[u][j];
+                                            v1[j] += t1[u][j];
+                                        }
                             }
                         }
                     }
@@ -409,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     const uint32_t code_lane = lane * 16, scale_lane = BG * TB + (lane >> 2) * 4;
     const float* osum_lane = osum + 2 * (lane & 3);
 
-    int st = 0, cur_slab = -1;
+    int st = 0, cur_slab = -1, nx = 0;
     uint32_t phase = 0;
     float tok_scale0 = 1.f, tok_scale1 = 1.f;
     Segment nat;
@@ -423,13 +481,27 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             cur_slab = sg.s;
             const int gs = slab_groups(p, sg.s);
             const int chunks = gs * 8;  // 16-byte chunks per token row
-            // The X slab straight into shared memory (LSU path, not the producer's TMA queue,
-            // so it does not wait behind the weight stream).
+            // The X slab into shared memory. fp16 operands (one or two token rows): 16-byte
+            // copies by every consumer thread (LSU path, off the weight stream's copy engine).
+            // bf16 operands (more rows): one bulk copy per row, since the LSU path stages
+            // through the L1 left beside this block's shared memory and would take several
+            // round trips.
             const uint16_t* xg = a.X + (size_t)sg.s * GS * kGroup;
-            for (int t = 0; t < T; ++t)
-                for (int c = tid; c < chunks; c += kConsumerThreads)
-                    cp_async16(smem_u32(xs + t * pitch + c * 16), xg + (size_t)t * p.K + c * 8);
-            cp_async_wait_all();
+            if constexpr (F16) {
+                for (int t = 0; t < T; ++t)
+                    for (int c = tid; c < chunks; c += kConsumerThreads)
+                        cp_async16(smem_u32(xs + t * pitch + c * 16), xg + (size_t)t * p.K + c * 8);
+                cp_async_wait_all();  // each thread's own chunks; the range pass below reads only those
+            } else {
+                if (tid == 0) {
+                    const uint32_t row_bytes = gs * 128;
+                    mbar_arrive_expect_tx(x_bar, row_bytes * T);
+                    for (int t = 0; t < T; ++t)
+                        bulk_g2s_plain(smem_u32(xs + t * pitch), xg + (size_t)t * p.K, row_bytes, x_bar);
+                }
+                mbar_wait(x_bar, nx & 1, flags, a.dev_err);
+                ++nx;
+            }
             // Per token, max |x| over the slab (bit patterns compare like magnitudes). The bf16
             // path needs it only when some |x| reaches 2^100 (bits 0x7180): one pass with a
             // barrier OR-reduction decides, and the per-token pass runs only then.
@@ -637,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         // Aborted: wait (bounded) for the stage copies that may still be in flight.
         for (int j = 0; j < nstages; ++j) mbar_wait_drain(full0 + 8 * j, 0, 100000000ull);
         for (int j = 0; j < nstages; ++j) mbar_wait_drain(full0 + 8 * j, 1, 100000000ull);
+        if (nx > 0) mbar_wait_drain(x_bar, (nx - 1) & 1, 100000000ull);
     }
 }
 
