@@ -614,8 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             }
         }
 
-        const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
-        const bool has1 = SWIGLU || rt1 < RT;
+        // Both M tiles always run: when the pair's second row tile does not exist (odd tile
+        // count, last pair) its chains run on whatever the stage holds there and the result is
+        // never stored (the epilogue drops rows past N). One code path keeps the loop small
+        // enough for the instruction cache.
         const int slab_g0 = sg.s * GS;
         for (int b = sg.ga / BG; b * BG < sg.gb; ++b) {
             const int i0 = max(sg.ga - b * BG, 0), i1 = min(sg.gb - b * BG, BG);
@@ -639,29 +641,19 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     }
                     const uint8_t* c0 = t0 + warp * TB + code_lane;
                     const uint8_t* s0 = t0 + scale_lane + warp * kScaleTileBytes;
-                    if (has1) {
-                        const uint8_t* code[2 * GPW];
-                        const uint8_t* scale[2 * GPW];
+                    const uint8_t* code[2 * GPW];
+                    const uint8_t* scale[2 * GPW];
 #pragma unroll
-                        for (int t = 0; t < 2 * GPW; ++t) {
-                            const int m = t / GPW, h = t % GPW;
-                            code[t] = c0 + m * kTileArea + NW * h * TB;
-                            scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
-                        }
-                        tiles_mma<BITS, F16, GPW, 2>(code, scale, xb, o, magic, acc);
-                    } else {
-                        const uint8_t* code[GPW];
-                        const uint8_t* scale[GPW];
-#pragma unroll
-                        for (int t = 0; t < GPW; ++t) {
-                            code[t] = c0 + NW * t * TB;
-                            scale[t] = s0 + NW * t * kScaleTileBytes;
-                        }
-                        tiles_mma<BITS, F16, GPW, 1>(code, scale, xb, o, magic, acc);
+                    for (int t = 0; t < 2 * GPW; ++t) {
+                        const int m = t / GPW, h = t % GPW;
+                        code[t] = c0 + m * kTileArea + NW * h * TB;
+                        scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
                     }
+                    tiles_mma<BITS, F16, GPW, 2>(code, scale, xb, o, magic, acc);
                 } else {
-                    // part of a block (first or last block of a run): group by group
-#pragma unroll
+                    // part of a block (first or last block of a run): group by group, in a
+                    // loop that is not unrolled (rare, and it keeps the code small)
+#pragma unroll 1
                     for (int h = 0; h < GPW; ++h) {
                         const int i = warp + NW * h;
                         if (i >= i0 && i < i1) {
@@ -672,15 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                             const float2 o[1] = {*reinterpret_cast<const float2*>(o0 + 8 * NW * h)};
                             const uint8_t* c0 = t0 + i * TB + code_lane;
                             const uint8_t* s0 = t0 + scale_lane + i * kScaleTileBytes;
-                            if (has1) {
-                                const uint8_t* const code[2] = {c0, c0 + kTileArea};
-                                const uint8_t* const scale[2] = {s0, s0 + kTileArea};
-                                tiles_mma<BITS, F16, 1, 2>(code, scale, xb, o, magic, acc);
-                            } else {
-                                const uint8_t* const code[1] = {c0};
-                                const uint8_t* const scale[1] = {s0};
-                                tiles_mma<BITS, F16, 1, 1>(code, scale, xb, o, magic, acc);
-                            }
+                            const uint8_t* const code[2] = {c0, c0 + kTileArea};
+                            const uint8_t* const scale[2] = {s0, s0 + kTileArea};
+                            tiles_mma<BITS, F16, 1, 2>(code, scale, xb, o, magic, acc);
                         }
                     }
                 }
