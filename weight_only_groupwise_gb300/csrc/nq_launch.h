@@ -13,9 +13,9 @@ cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
-template <int BITS, bool SWIGLU, bool F16>
+template <int BITS, bool SWIGLU, bool F16, bool ONE>
 cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    auto kern = proj_kernel<BITS, SWIGLU, F16>;
+    auto kern = proj_kernel<BITS, SWIGLU, F16, ONE>;
     // The shared-memory opt-in is per device; set it on every launch of a new size class
     // (cheap: the driver caches it) rather than tracking devices here.
     static thread_local int set_for_device = -1;
@@ -39,11 +39,13 @@ cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// The operand type is part of the plan (a.p.f16): fp16 operands for small T, bf16 otherwise.
+// The operand type is part of the plan (a.p.f16): fp16 operands for small T, bf16 otherwise;
+// a single token has its own fp16 instantiation.
 template <int BITS, bool SWIGLU>
 cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    return a.p.f16 ? launch_proj_t<BITS, SWIGLU, true>(a, stream, pdl)
-                   : launch_proj_t<BITS, SWIGLU, false>(a, stream, pdl);
+    if (!a.p.f16) return launch_proj_t<BITS, SWIGLU, false, false>(a, stream, pdl);
+    return a.p.T == 1 ? launch_proj_t<BITS, SWIGLU, true, true>(a, stream, pdl)
+                      : launch_proj_t<BITS, SWIGLU, true, false>(a, stream, pdl);
 }
 
 }  // namespace nq

@@ -97,7 +97,7 @@ __device__ __forceinline__ constexpr int mtile_of(int t) { return t / GROUPS; }
 // GROUPS x TILES tiles in one pass, K-step-major so their accumulator chains overlap. Each
 // tile's chain is "K step 0 from a zero accumulator, then K steps 1..3", exactly as for O.
 // code[t] / scale[t]: this lane's code bytes / scale pair of tile t.
-template <int BITS, bool F16, int GROUPS, int TILES>
+template <int BITS, bool F16, int GROUPS, int TILES, bool ONE = false>
 __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * TILES],
                                           const uint8_t* const (&scale)[GROUPS * TILES],
                                           const uint32_t (&xb)[GROUPS][8], const float2 (&o)[GROUPS],
@@ -141,9 +141,11 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * 
         const float2 s = __half22float2(sh);
         const int m = mtile_of<GROUPS>(t), h = group_of<GROUPS>(t);
         acc[m][0] = fmaf(s.x, d[t][0] - o[h].x, acc[m][0]);
-        acc[m][1] = fmaf(s.x, d[t][1] - o[h].y, acc[m][1]);
         acc[m][2] = fmaf(s.y, d[t][2] - o[h].x, acc[m][2]);
-        acc[m][3] = fmaf(s.y, d[t][3] - o[h].y, acc[m][3]);
+        if constexpr (!ONE) {  // token columns 2(l%4) + 1: none when there is one token
+            acc[m][1] = fmaf(s.x, d[t][1] - o[h].y, acc[m][1]);
+            acc[m][3] = fmaf(s.y, d[t][3] - o[h].y, acc[m][3]);
+        }
     }
 }
 
@@ -176,7 +178,8 @@ __device__ __forceinline__ int red_index(int w, int m, int tok, int row) {
     return ((w * 2 + m) * 32 + l) * 4 + j;
 }
 
-template <int BITS, bool SWIGLU, bool F16>
+// ONE: a single token (T = 1), whose odd token columns need no scaling.
+template <int BITS, bool SWIGLU, bool F16, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
@@ -649,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         code[t] = c0 + m * kTileArea + NW * h * TB;
                         scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
                     }
-                    tiles_mma<BITS, F16, GPW, 2>(code, scale, xb, o, magic, acc);
+                    tiles_mma<BITS, F16, GPW, 2, ONE>(code, scale, xb, o, magic, acc);
                 } else {
                     // part of a block (first or last block of a run): group by group, in a
                     // loop that is not unrolled (rare, and it keeps the code small)
@@ -666,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                             const uint8_t* s0 = t0 + scale_lane + i * kScaleTileBytes;
                             const uint8_t* const code[2] = {c0, c0 + kTileArea};
                             const uint8_t* const scale[2] = {s0, s0 + kTileArea};
-                            tiles_mma<BITS, F16, 1, 2>(code, scale, xb, o, magic, acc);
+                            tiles_mma<BITS, F16, 1, 2, ONE>(code, scale, xb, o, magic, acc);
                         }
                     }
                 }
