@@ -120,6 +120,14 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     long long P = p.U / kMinUnitsPerCta;
     if (P > num_sms) P = num_sms;
     if (P < 1) P = 1;
+    // Few row pairs, one slab: when they divide evenly into one or two per block and that
+    // still keeps most SMs streaming, give each block whole pairs. No pair is split, so no
+    // split-K settle (several L2 round trips at the end of a short kernel) is needed.
+    if (p.S == 1 && num_sms > 0) {
+        const int k = (p.RP + num_sms - 1) / num_sms;
+        if (k >= 1 && k <= 2 && p.RP % k == 0 && (long long)(p.RP / k) * 5 >= (long long)num_sms * 3)
+            P = p.RP / k;
+    }
     p.P = (int)P;
     p.Uq = (int)(p.U / p.P);
     p.Ur = (int)(p.U % p.P);
