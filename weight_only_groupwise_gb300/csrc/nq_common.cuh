@@ -3,13 +3,12 @@
 //
 // Packed layout (this library's definition; the pages give none):
 //   The K x N weight is cut into tiles of 16 output rows x one 64-wide K group, tile (rt, g)
-//   with rt = n / 16 and g = k / 64. Each row tile is a contiguous stream of blocks of 16
-//   groups (the last block of a row tile may hold fewer, nb = min(16, G - 16b)); a block is
+//   with rt = n / 16 and g = k / 64. Each row tile is a contiguous stream of blocks of 32
+//   groups (the last block of a row tile may hold fewer, nb = min(32, G - 32b)); a block is
 //   [nb tiles of codes][nb x 32 B of fp16 scales], so one bulk copy fetches a block's codes
 //   and scales together. Inside a code tile, lane l (0..31) of a warp owns 16 bytes = four
-//   uint32 words, one per 16-wide K step j: the word is exactly the lane's bf16 A-operand
-//   fragment of an m16n8k16 tensor-core MMA for that step once each nibble is widened to a
-//   16-bit half (see decode_q4). Q5 code tiles append one uint32 of high bits per lane (128
+//   uint32 words, one per 16-wide K step j: the word holds the lane's A-operand fragment of
+//   an m16n8k16 tensor-core MMA for that step, one LOP3 away per register (see decode_q4). Q5 code tiles append one uint32 of high bits per lane (128
 //   bytes per tile). A tile's 16 scales are ordered (row r, row r+8) for r = 0..7, so lane l
 //   reads one uint32 holding the scales of its rows l/4 and l/4+8.
 #pragma once

@@ -5,28 +5,32 @@
 // "与原版 NInfer 的对比": the Q5 K-split MMA path for verify rounds).
 //
 // Structure: one persistent block per SM with three roles.
-//   * Producer warp: its elected lane streams the block's units with 1-D TMA bulk copies
-//     into a ring of shared-memory stages (mbarrier full/empty pairs, L2 evict-first: every
-//     weight byte is read exactly once). A stage holds one 16-group packed block (codes and
-//     scales) of each of the two M tiles: one copy per tile, which keeps the copy engine at
-//     full rate. It also bulk-copies the activations of the current K slab (T rows, padded).
-//   * Consumer warps (kConsumerWarps): warp w takes K groups w and w + 8 of every stage, for
-//     both 16-row tiles of the row pair. A lane decodes its 16 code bytes into fp16 A
-//     fragments (1024 + q, or 1024 + 16 q against X / 16; exact), loads the B fragment of X
-//     with ldmatrix and runs four m16n8k16 MMAs from a zero accumulator: P. The MMAs of the
-//     warp's four tiles are issued K-step by K-step so the four accumulator chains overlap.
-//     The same four MMAs on the constant code z give O once per group and slab;
+//   * Producer warp: its elected lane initialises the mbarriers and streams the block's units
+//     with 1-D TMA bulk copies into a ring of shared-memory stages (mbarrier full/empty pairs,
+//     L2 evict-first: every weight byte is read exactly once). A stage holds one 32-group
+//     packed block (codes and scales) of each of the two M tiles: one copy per tile. It does
+//     not wait for the preceding kernel (weights are never written by a kernel that lets its
+//     dependents start early); with bf16 operands it holds the stream after the first stage
+//     until the activation slab has landed, so the slab's copies do not queue behind a ring.
+//   * Consumer warps (kConsumerWarps): they wait for the preceding kernel, stage the X slab
+//     of the current K range (fp16 path: cp.async by every thread, then an in-place fp16
+//     conversion with a per-token power-of-two range guard; bf16 path: one bulk copy per row)
+//     and compute O, the four-MMA chain on the constant zero-point code, for the groups they
+//     consume. Warp w then takes K groups w, w + 8, w + 16, w + 24 of every stage, for both
+//     16-row tiles of the row pair: a lane decodes its 16 code bytes into A fragments
+//     (fp16: 1024 + q, or 1024 + 16 q against X / 16; bf16: 128 + q; exact), loads the B
+//     fragment of X with ldmatrix and runs four m16n8k16 MMAs from a zero accumulator: P.
+//     The warp's eight tiles are issued K-step by K-step so their chains overlap.
 //     P - O = sum((q - z) * x) up to fp32 rounding, and exactly 0 where every code equals z
-//     (identical MMA inputs). The fp16 scale is applied with one FMA per group. X is turned
-//     into fp16 in shared memory once per slab (per-token power-of-two range guard).
-//   * Epilogue warp: at the end of each (slab, row pair) run the consumers drop their
-//     accumulators into one of two shared buffers and carry on. The epilogue warp reduces
-//     the warps' parts in a fixed order and writes Y directly when the run covers its whole
-//     pair; otherwise it stores an fp32 partial in the workspace and takes a ticket; the
+//     (identical MMA inputs). The fp16 scale is applied with one FMA per group.
+//   * Two epilogue warps, taking alternate runs: at the end of each (slab, row pair) run the
+//     consumers drop their accumulators into one of up to four shared hand-over buffers and
+//     carry on. The run's epilogue warp reduces the consumer warps' parts in a fixed order
+//     (padded tokens only) and writes Y directly when the run covers its whole pair;
+//     otherwise it stores an fp32 partial in the workspace, fences and takes a ticket; the
 //     block that takes the last ticket sums all partials of the pair in a fixed order
-//     (deterministic split-K, no spinning on other blocks) and writes Y. The block's
-//     partial runs are processed first, so split-K settles early and the block ends on a
-//     complete run.
+//     (deterministic split-K, no spinning on other blocks) and writes Y. The block's partial
+//     runs are processed first, so split-K settles early and the block ends on a complete run.
 #pragma once
 
 #include <cuda_bf16.h>
