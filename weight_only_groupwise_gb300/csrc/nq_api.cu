@@ -140,7 +140,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 bool g_pdl = true;
-int g_operands = -1;   // -1: by T (plan), 0: bf16, 1: fp16 (NQ_OPERANDS, for measurement)
 bool g_env_read = false;
 
 size_t ws_tickets_off() { return 256; }
@@ -157,9 +156,6 @@ nq_status current_device(DevState** out, int* dev_out) {
     if (!g_env_read) {
         const char* e = std::getenv("NQ_PDL");
         if (e && e[0] == '0') g_pdl = false;
-        const char* o = std::getenv("NQ_OPERANDS");
-        if (o && std::strcmp(o, "fp16") == 0) g_operands = 1;
-        if (o && std::strcmp(o, "bf16") == 0) g_operands = 0;
         g_env_read = true;
     }
     DevState& d = g_dev[dev];
@@ -256,7 +252,6 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     }
     ProjArgs a;
     if (!make_plan(bits, swiglu ? 1 : 0, T, K, N, d->sms, a.p)) return NQ_ERR_SHAPE;
-    if (g_operands >= 0) a.p.f16 = g_operands;
     st = ensure_workspace(*d, a.p.slots, a.p.RP);
     if (st != NQ_OK) return st;
     a.X = static_cast<const uint16_t*>(X);

@@ -317,6 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         const int ew = warp - kEpilogueWarp;
         const int TP = p.TP, nred = p.nred, tp_log = TP == 1 ? 0 : (TP == 2 ? 1 : (TP == 4 ? 2 : 3));
         const int nout = (SWIGLU ? 16 : 32) * TP;
+        // Outputs per lane at most: one token (16 or 32 outputs), fp16 path (T <= 2: up to
+        // 64), else 8 tokens (256). A compile-time bound keeps the epilogue code small.
+        constexpr int kF16TP = NQ_F16_MAX_T <= 1 ? 1 : (NQ_F16_MAX_T <= 2 ? 2 : (NQ_F16_MAX_T <= 4 ? 4 : 8));
+        constexpr int kMaxTP = ONE ? 1 : (F16 ? kF16TP : 8);
+        constexpr int JN8 = (SWIGLU ? 16 : 32) * kMaxTP / 32 > 0 ? (SWIGLU ? 16 : 32) * kMaxTP / 32 : 1;
         grid_dependency_wait();  // Y, partial sums and tickets may still be in the preceding kernel's use
         Segment nat;
         for (int si = 0; si < order.count; ++si) {
@@ -325,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             const int b = si % nred;
             named_bar_sync(kBarRedFull + b, kHandoffThreads);
             const float* rb = red + b * kRedFloats;
-            float v0[8], v1[8];
+            float v0[JN8], v1[JN8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < JN8; ++j) {
                 const int o = lane + 32 * j;
                 float s0 = 0.f, s1 = 0.f;
                 if (o < nout) {
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 // split-K run: publish the partial, take the ticket, reduce if last
                 float* ws = a.partials + slot_of(p, sg.s, sg.rp, cta) * kPartialFloats;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < JN8; ++j) {
                     const int o = lane + 32 * j;
                     if (o < nout) {
                         ws[o] = v0[j];
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
+                    for (int j = 0; j < JN8; ++j) v0[j] = v1[j] = 0.f;
                     // Every contribution of the pair, summed in fixed (slab, block) order.
                     auto sum_in_order = [&]() {
                         for (int s = 0; s < p.S; ++s) {
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                             for (int c = cta_of(p, r0); c <= c_end; ++c) {
                                 const float* src = a.partials + slot_of(p, s, sg.rp, c) * kPartialFloats;
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
+                                for (int j = 0; j < JN8; ++j) {
                                     const int o = lane + 32 * j;
                                     if (o < nout) {
                                         v0[j] += __ldcg(src + o);
@@ -438,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             }
             if (write) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < JN8; ++j) {
                     const int o = lane + 32 * j;
                     const int m = SWIGLU ? 0 : o >> (4 + tp_log), tok = (o >> 4) & (TP - 1), row = o & 15;
                     const int rt = SWIGLU ? sg.rp : 2 * sg.rp + m;
