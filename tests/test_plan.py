@@ -62,3 +62,24 @@ def test_partition_covers_every_unit_once(nq, bits, mode, T, K, N, sms):
         else:
             assert segs[0] == nat[0] and segs[1] == nat[-1] and segs[2:] == nat[1:-1]
             assert segs[-1][2] == 0 and segs[-1][3] == G
+
+
+@pytest.mark.parametrize("bits,T,K,N,sms,ctas", [
+    (5, 8, 5120, 6144, 152, 96),     # 192 pairs: two whole pairs per block
+    (5, 1, 5120, 6144, 152, 96),
+    (4, 1, 1024, 2432, 152, 76),     # 76 pairs: one per block (76 >= 60 % of 152)
+    (4, 1, 5120, 17408, 152, 152),   # 544 pairs: stream-K over every SM
+    (5, 8, 5120, 1024, 152, 152),    # 32 pairs: too few blocks, stream-K
+    (4, 8, 17408, 5120, 152, 152),   # several slabs: stream-K
+])
+def test_whole_pairs_when_they_divide_evenly(nq, bits, T, K, N, sms, ctas):
+    """With one slab and at most two row pairs per block, a grid that still covers 60 % of
+    the SMs takes whole pairs per block, and then no segment is a partial run."""
+    info = nq.plan_info(bits, 0, T, K, N, sms)
+    assert info["ctas"] == ctas
+    if ctas < sms:
+        G = K // 64
+        for c in range(ctas):
+            segs = nq.plan_segments(bits, 0, T, K, N, sms, c)
+            assert all(ga == 0 and gb == G for (_, _, ga, gb) in segs)
+            assert len(segs) == info["pairs"] // ctas
