@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         mbar_fence_init();
     }
     // Programmatic dependent launch: the next kernel in the stream may be scheduled as SMs
-    // free up. The consumers (which read X) and the epilogue warp (which writes Y, partial
+    // free up. The consumers (which read X) and the epilogue warps (which write Y, partial
     // sums and tickets) wait for the preceding kernel to finish (grid_dependency_wait)
     // before they touch global memory. The producer streams the weights at once: no kernel
     // that writes them lets its dependents start early.
