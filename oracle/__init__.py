@@ -53,6 +53,8 @@ def lib():
         L.orc_gemm_q5_rows.argtypes = [P, P, P, P, I, I, P, I, P]
         L.orc_swiglu_q4.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
         L.orc_swiglu_q4_rows.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P]
+        L.orc_swiglu_q5.argtypes = [P, P, P, P, P, P, P, I, I, I, P, P, P]
+        L.orc_swiglu_q5_rows.argtypes = [P, P, P, P, P, P, P, I, I, P, I, P, P, P]
         L.orc_num_threads.restype = I
         L.orc_set_num_threads.argtypes = [I]
         _lib = L
@@ -152,6 +154,33 @@ def swiglu_q4_rows(x, wg, sg, wu, su, T: int, K: int, rows):
     h = np.empty((len(r), T), np.uint16)
     lib().orc_swiglu_q4_rows(_p(x), _p(wg), _p(sg), _p(wu), _p(su), T, K, _p(r), len(r),
                              _p(g), _p(u), _p(h))
+    return g, u, h
+
+
+def swiglu_q5(x, wgn, wgh, sg, wun, wuh, su, T: int, K: int, N: int):
+    """(G, U, H) for 5-bit gate and up weights, as swiglu_q4."""
+    x = _c(x, np.uint16)
+    wgn, wgh, wun, wuh = (_c(a, np.uint32) for a in (wgn, wgh, wun, wuh))
+    sg, su = _c(sg, np.uint16), _c(su, np.uint16)
+    g = np.empty((T, N), np.float64)
+    u = np.empty((T, N), np.float64)
+    h = np.empty((T, N), np.uint16)
+    lib().orc_swiglu_q5(_p(x), _p(wgn), _p(wgh), _p(sg), _p(wun), _p(wuh), _p(su), T, K, N,
+                        _p(g), _p(u), _p(h))
+    return g, u, h
+
+
+def swiglu_q5_rows(x, wgn, wgh, sg, wun, wuh, su, T: int, K: int, rows):
+    """(G, U, H) on selected rows, each [len(rows)][T]."""
+    x = _c(x, np.uint16)
+    wgn, wgh, wun, wuh = (_c(a, np.uint32) for a in (wgn, wgh, wun, wuh))
+    sg, su = _c(sg, np.uint16), _c(su, np.uint16)
+    r = _c(rows, np.int32)
+    g = np.empty((len(r), T), np.float64)
+    u = np.empty((len(r), T), np.float64)
+    h = np.empty((len(r), T), np.uint16)
+    lib().orc_swiglu_q5_rows(_p(x), _p(wgn), _p(wgh), _p(sg), _p(wun), _p(wuh), _p(su), T, K,
+                             _p(r), len(r), _p(g), _p(u), _p(h))
     return g, u, h
 
 

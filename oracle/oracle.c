@@ -222,6 +222,24 @@ void orc_swiglu_q4_rows(const uint16_t* x, const uint32_t* wg, const uint16_t* s
     for (size_t i = 0; i < (size_t)count * T; ++i) h[i] = orc_round_bf16(orc_silu_mul(g[i], u[i]));
 }
 
+/* The same block for 5-bit gate and up weights (nibble plane + high plane each, z = 16). */
+void orc_swiglu_q5(const uint16_t* x, const uint32_t* wgn, const uint32_t* wgh, const uint16_t* sg,
+                   const uint32_t* wun, const uint32_t* wuh, const uint16_t* su, int T, int K, int N,
+                   double* g, double* u, uint16_t* h) {
+    orc_gemm_q5(x, wgn, wgh, sg, T, K, N, g);
+    orc_gemm_q5(x, wun, wuh, su, T, K, N, u);
+    for (size_t i = 0; i < (size_t)T * N; ++i) h[i] = orc_round_bf16(orc_silu_mul(g[i], u[i]));
+}
+
+void orc_swiglu_q5_rows(const uint16_t* x, const uint32_t* wgn, const uint32_t* wgh,
+                        const uint16_t* sg, const uint32_t* wun, const uint32_t* wuh,
+                        const uint16_t* su, int T, int K, const int* rows, int count, double* g,
+                        double* u, uint16_t* h) {
+    orc_gemm_q5_rows(x, wgn, wgh, sg, T, K, rows, count, g);
+    orc_gemm_q5_rows(x, wun, wuh, su, T, K, rows, count, u);
+    for (size_t i = 0; i < (size_t)count * T; ++i) h[i] = orc_round_bf16(orc_silu_mul(g[i], u[i]));
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

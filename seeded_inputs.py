@@ -89,6 +89,20 @@ def swiglu_problem(T: int, K: int, N: int, seed: int) -> dict:
     return {"T": T, "K": K, "N": N, "x": x, "wg": wg, "sg": sg, "wu": wu, "su": su}
 
 
+def swiglu_q5_problem(T: int, K: int, N: int, seed: int) -> dict:
+    """Gate and up Q5 weights (nibble and high planes each) and X, from one generator."""
+    g = rng(seed)
+    wgn = code_words(g, N, K // 8)
+    wgh = code_words(g, N, K // 32)
+    wun = code_words(g, N, K // 8)
+    wuh = code_words(g, N, K // 32)
+    sg = scales(g, N, K)
+    su = scales(g, N, K)
+    x = activations(g, T, K)
+    return {"T": T, "K": K, "N": N, "x": x, "wgn": wgn, "wgh": wgh, "sg": sg, "wun": wun,
+            "wuh": wuh, "su": su}
+
+
 # The five workloads. Shapes are those of a 27B-class dense decoder layer.
 TINY_Q4 = dict(T=1, K=256, N=128, seed=0)                  # tiny Q4 correctness case
 DECODE_Q4 = dict(T=1, K=5120, N=17408, seed=1)             # decode GEMV, FFN up-projection

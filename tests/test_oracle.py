@@ -167,6 +167,46 @@ def test_swiglu_vs_twin():
     assert np.array_equal(hr, h[:, [3, 40]].T) and np.array_equal(gr, g[:, [3, 40]].T)
 
 
+def test_swiglu_q5_vs_twin():
+    T, K, N = 5, 320, 32
+    p = si.swiglu_q5_problem(T, K, N, 37)
+    g, u, h = oracle.swiglu_q5(p["x"], p["wgn"], p["wgh"], p["sg"], p["wun"], p["wuh"], p["su"],
+                               T, K, N)
+    g_t = twin.gemm_q5(p["x"], p["wgn"], p["wgh"], p["sg"], K)
+    u_t = twin.gemm_q5(p["x"], p["wun"], p["wuh"], p["su"], K)
+    assert np.max(np.abs(g - g_t)) <= 1e-12 * np.max(np.abs(g_t))
+    assert np.max(np.abs(u - u_t)) <= 1e-12 * np.max(np.abs(u_t))
+    h_t = twin.silu(g_t) * u_t
+    h_ours = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.all(np.abs(h_ours - h_t) <= 2.0**-7 * np.abs(h_t) + 1e-30)
+    rows = [31, 0, 9]
+    gr, ur, hr = oracle.swiglu_q5_rows(p["x"], p["wgn"], p["wgh"], p["sg"], p["wun"], p["wuh"],
+                                       p["su"], T, K, rows)
+    assert np.array_equal(hr, h[:, rows].T) and np.array_equal(ur, u[:, rows].T)
+
+
+def test_swiglu_q5_closed_forms():
+    """Codes equal to the zero point (16: nibble 0, high bit 1) contribute exactly nothing:
+    an all-16 gate gives g = 0, so h = silu(0) * u is a zero carrying u's sign; an all-16 up
+    gives u = 0 and h a zero carrying g's sign.
+    A single code 17 (q - z = +1) in gate group 0 with a scale of 1 leaves g = x[t, k0]."""
+    T, K, N = 3, 128, 16
+    p = si.swiglu_q5_problem(T, K, N, 41)
+    zn = np.zeros_like(p["wgn"])
+    zh = np.full_like(p["wgh"], 0xFFFFFFFF)
+    g, u, h = oracle.swiglu_q5(p["x"], zn, zh, p["sg"], p["wun"], p["wuh"], p["su"], T, K, N)
+    assert np.all(g == 0.0) and np.array_equal(h, np.where(u < 0, 0x8000, 0).astype(np.uint16))
+    g, u, h = oracle.swiglu_q5(p["x"], p["wgn"], p["wgh"], p["sg"], zn, zh, p["su"], T, K, N)
+    assert np.all(u == 0.0) and np.array_equal(h, np.where(g < 0, 0x8000, 0).astype(np.uint16))
+    wgn = zn.copy()
+    wgn[:, 0] = 1 << 4 * 3          # row n, k0 = 3: nibble 1 with high bit 1 -> q = 17
+    sg = p["sg"].copy()
+    sg[:, 0] = np.float16(1.0).view(np.uint16)
+    g, u, h = oracle.swiglu_q5(p["x"], wgn, zh, sg, p["wun"], p["wuh"], p["su"], T, K, N)
+    xk0 = torch.from_numpy(p["x"][:, 3].view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(g, np.repeat(xk0[:, None], N, axis=1))
+
+
 def test_silu_closed_forms():
     assert oracle.silu_mul(0.0, 5.0) == 0.0
     assert oracle.silu_mul(50.0, 1.0) == pytest.approx(50.0, rel=1e-15)   # silu(g) -> g
