@@ -12,7 +12,7 @@ steps are replayed as one CUDA graph of K back-to-back launches (how a decode en
 them), bracketed by CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode_q4|verify_q5|swiglu_block|layer_stack] [--T T]
+                  [--workload decode_q4|verify_q5|swiglu_block|swiglu_block_q5|layer_stack] [--T T]
                   [--no-sweep] [--no-cpu-baseline]
 
 --impl reference times the CPU oracle (the deliberately slow fp64 definition) on the host
@@ -64,8 +64,8 @@ def proj_bytes(bits: int, T: int, K: int, N: int) -> int:
     return K * N * bits // 8 + N * (K // 64) * 2 + T * K * 2 + T * N * 2
 
 
-def swiglu_bytes(T: int, K: int, N: int) -> int:
-    return 2 * (K * N // 2 + N * (K // 64) * 2) + T * K * 2 + T * N * 2
+def swiglu_bytes(T: int, K: int, N: int, bits: int = 4) -> int:
+    return 2 * (K * N * bits // 8 + N * (K // 64) * 2) + T * K * 2 + T * N * 2
 
 
 WORKLOADS = {
@@ -75,6 +75,8 @@ WORKLOADS = {
                       desc="spec-verify Q5, T=8, K=5120, N=6144 (attention gate/value projection)"),
     "swiglu_block": dict(kind="swiglu", bits=4, T=8, K=5120, N=17408, Kd=17408, Nd=5120,
                          desc="SwiGLU block Q4, T=8: fused gate+up K=5120 N=17408, then down K=17408 N=5120"),
+    "swiglu_block_q5": dict(kind="swiglu", bits=5, T=8, K=5120, N=17408, Kd=17408, Nd=5120,
+                            desc="SwiGLU block Q5, T=8: fused gate+up K=5120 N=17408, then down K=17408 N=5120"),
     "layer_stack": dict(kind="stack", T=8, layers=64,
                         desc="64 independent 27B-class layers: fused gate+up and down (Q4), "
                              "q-gate 5120x6144, kv 5120x1024, out 6144x5120 (Q5)"),
@@ -85,9 +87,10 @@ def workload_bytes(w: dict) -> int:
     if w["kind"] == "proj":
         return proj_bytes(w["bits"], w["T"], w["K"], w["N"])
     if w["kind"] == "swiglu":
-        return swiglu_bytes(w["T"], w["K"], w["N"]) + proj_bytes(4, w["T"], w["Kd"], w["Nd"])
+        return (swiglu_bytes(w["T"], w["K"], w["N"], w["bits"])
+                + proj_bytes(w["bits"], w["T"], w["Kd"], w["Nd"]))
     T = w["T"]
-    per_layer = (swiglu_bytes(T, 5120, 17408) + proj_bytes(4, T, 17408, 5120) + proj_bytes(5, T, 5120, 6144)
+    per_layer = (swiglu_bytes(T, 5120, 17408, 4) + proj_bytes(4, T, 17408, 5120) + proj_bytes(5, T, 5120, 6144)
                  + proj_bytes(5, T, 5120, 1024) + proj_bytes(5, T, 6144, 5120))
     return per_layer * w["layers"]
 
@@ -231,20 +234,22 @@ def build_step(nq, w: dict, dev, T_override=None):
             fn(x, copies[i % R], N, out=y)
         return step, b, R, f"rotate {R} packed weight copies ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     if w["kind"] == "swiglu":
-        T, K, N, Kd, Nd = T_override or w["T"], w["K"], w["N"], w["Kd"], w["Nd"]
-        b = swiglu_bytes(T, K, N) + proj_bytes(4, T, Kd, Nd)
+        bits, T, K, N, Kd, Nd = w["bits"], T_override or w["T"], w["K"], w["N"], w["Kd"], w["Nd"]
+        b = swiglu_bytes(T, K, N, bits) + proj_bytes(bits, T, Kd, Nd)
         R = max(2, -(-3 * L2_BYTES // b))
-        gate = make_proj_copies(nq, 4, K, N, R, 3, dev)
-        up = make_proj_copies(nq, 4, K, N, R, 4, dev)
-        down = make_proj_copies(nq, 4, Kd, Nd, R, 5, dev)
+        gate = make_proj_copies(nq, bits, K, N, R, 3 + 10 * (bits - 4), dev)
+        up = make_proj_copies(nq, bits, K, N, R, 4 + 10 * (bits - 4), dev)
+        down = make_proj_copies(nq, bits, Kd, Nd, R, 5 + 10 * (bits - 4), dev)
+        fused = nq.swiglu_q4 if bits == 4 else nq.swiglu_q5
+        fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
         x = si.device_activations(T, K, gen, dev)
         h = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         y = torch.empty((T, Nd), dtype=torch.bfloat16, device=dev)
 
         def step(i):
             j = i % R
-            nq.swiglu_q4(x, gate[j], up[j], N, out=h)
-            nq.gemm_q4(h, down[j], Nd, out=y)
+            fused(x, gate[j], up[j], N, out=h)
+            fn(h, down[j], Nd, out=y)
         return step, b, R, f"rotate {R} weight sets ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     # layer stack: 64 independent layers, ~12 GB of packed weights (no reuse within a pass)
     T, L = T_override or w["T"], w["layers"]
@@ -496,7 +501,7 @@ def sweep(nq, dev, stream, peak):
     import torch
     out = []
     items = [("decode_q4", T) for T in (1, 2, 4, 8)] + [("verify_q5", T) for T in (1, 2, 4, 8)] + \
-            [("swiglu_block", 8)]
+            [("swiglu_block", 8), ("swiglu_block_q5", 8)]
     for name, T in items:
         w = dict(WORKLOADS[name], T=T)
         step, b, R, note, keep = build_step(nq, w, dev)

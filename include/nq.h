@@ -153,6 +153,16 @@ nq_status nq_gemm_q5(const void* X, const void* W, void* Y, int T, int K, int N,
 nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N,
                        void* stream);
 
+/*
+ * nq_swiglu_q5: as nq_swiglu_q4 for 5-bit gate and up weights packed by nq_pack_q5
+ * (z = 16): the pages run the SwiGLU path among the small-batch Q4/Q5 projections
+ * ("NInfer-4090" release post, section "V3 做了什么"; "ninfer-ext" README, the Q5
+ * small-batch path). Same arguments, layouts, ownership and errors; the down projection is
+ * nq_gemm_q4 or nq_gemm_q5 on H.
+ */
+nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N,
+                       void* stream);
+
 /* ---------------------------------------------------------------- debug dumps */
 
 /*

@@ -28,6 +28,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_swiglu_q4",
+                 "nq_swiglu_q5",
                  "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_status_string",
                  "nq_packed_bytes_q4", "nq_packed_bytes_q5"):
         assert must in names
@@ -61,6 +62,8 @@ def test_shape_errors_are_reported_before_any_cuda_call(L):
     assert L.nq_gemm_q5(p16, p16, p16, 1, 96, 16, None) == -2     # K % 64
     assert L.nq_gemm_q4(p16, p16, p16, 1, 64, 24, None) == -2     # N % 16
     assert L.nq_swiglu_q4(p16, p16, p16, p16, 1, 65, 16, None) == -2
+    assert L.nq_swiglu_q5(p16, p16, p16, p16, 9, 64, 16, None) == -2
+    assert L.nq_swiglu_q5(p16, p16, p16, p16, 1, 64, 40, None) == -2
     assert L.nq_pack_q4(p16, p16, 63, 16, p16, None) == -2
     assert L.nq_dequant_q5_debug(p16, p16, 64, 17, None) == -2
 
@@ -70,6 +73,7 @@ def test_empty_problems_launch_nothing(L):
     assert L.nq_gemm_q4(None, None, None, 0, 64, 16, None) == 0
     assert L.nq_gemm_q5(None, None, None, 4, 64, 0, None) == 0
     assert L.nq_swiglu_q4(None, None, None, None, 0, 64, 16, None) == 0
+    assert L.nq_swiglu_q5(None, None, None, None, 3, 64, 0, None) == 0
 
 
 def test_null_alignment_alias_errors(L):
@@ -87,6 +91,10 @@ def test_null_alignment_alias_errors(L):
     assert L.nq_gemm_q4(x, w, P(base + 1024 + 256), 1, 64, 16, None) == -4
     assert L.nq_gemm_q5(x, w, P(base + 1024 + 640), 2, 64, 16, None) == -4
     assert L.nq_swiglu_q4(x, w, s, P(base + 2048 + 512), 1, 64, 16, None) == -4
+    assert L.nq_swiglu_q5(x, w, None, y, 1, 64, 16, None) == -1
+    assert L.nq_swiglu_q5(x, w, P(base + 2056), y, 1, 64, 16, None) == -3   # Wu misaligned
+    # the packed Q5 64 x 16 weight is 64*16*5/8 + 16*2 = 672 bytes: H at Wu + 640 overlaps it
+    assert L.nq_swiglu_q5(x, w, s, P(base + 2048 + 640), 1, 64, 16, None) == -4
     assert L.nq_pack_q4(x, s, 64, 16, x, None) == -4
 
 
@@ -98,5 +106,5 @@ def test_plan_info_matches_workloads(L):
     assert p["slabs"] == 3 and p["slab_groups"] * 3 >= 272
     p = nq.plan_info(4, 1, 8, 5120, 17408, 152)   # swiglu pairs gate/up tiles
     assert p["pairs"] == 1088
-    with pytest.raises(Exception):
-        nq.plan_info(5, 1, 8, 5120, 17408, 152)   # no Q5 swiglu
+    p = nq.plan_info(5, 1, 8, 5120, 17408, 152)   # Q5 swiglu: same pairing, larger stages
+    assert p["pairs"] == 1088 and p["stages"] >= 2

@@ -109,6 +109,59 @@ def test_swiglu_q4_parity(nq, T, K, N, seed):
     assert gu.rel_err(h, h_exact) <= gu.TOL
 
 
+SWIGLU_Q5_SHAPES = [(8, 256, 48, 0), (1, 640, 16, 1), (2, 1024, 272, 2), (4, 17408, 64, 3),
+                    (8, 6208, 32, 4), (6, 320, 112, 5), (3, 5120, 1040, 6)]
+
+
+def _swiglu_q5_dev(nq, p, T, K, N):
+    wg = gu.pack_q5(nq, p["wgn"], p["wgh"], p["sg"], K, N)
+    wu = gu.pack_q5(nq, p["wun"], p["wuh"], p["su"], K, N)
+    return nq.swiglu_q5(gu.dev_bf16(p["x"]), wg, wu, N)
+
+
+@pytest.mark.parametrize("T,K,N,seed", SWIGLU_Q5_SHAPES)
+def test_swiglu_q5_parity(nq, T, K, N, seed):
+    p = si.swiglu_q5_problem(T, K, N, seed + 200)
+    h = gu.host_f64(_swiglu_q5_dev(nq, p, T, K, N))
+    g, u, _ = oracle.swiglu_q5(p["x"], p["wgn"], p["wgh"], p["sg"], p["wun"], p["wuh"], p["su"],
+                               T, K, N)
+    assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+
+
+def test_swiglu_q5_zero_point_codes_give_zero(nq):
+    """Gate codes all equal to z = 16 make g exactly 0, so every h is a zero; the same for
+    up codes. The kernel's zero-point correction must cancel exactly, not approximately."""
+    T, K, N = 8, 1024, 64
+    p = si.swiglu_q5_problem(T, K, N, 250)
+    zn, zh = np.zeros_like(p["wgn"]), np.full_like(p["wgh"], 0xFFFFFFFF)
+    q = dict(p, wgn=zn, wgh=zh)
+    assert np.all(gu.host_f64(_swiglu_q5_dev(nq, q, T, K, N)) == 0.0)
+    q = dict(p, wun=zn, wuh=zh)
+    assert np.all(gu.host_f64(_swiglu_q5_dev(nq, q, T, K, N)) == 0.0)
+
+
+def test_swiglu_q5_block_full_size_sampled(nq):
+    """The gate/up block of the SwiGLU workload (T=8, K=5120, N=17408) with 5-bit weights,
+    in the launch configuration of the full size, checked on sampled output rows; then the
+    down projection (Q5, K=17408 -> N=5120) on the GPU's own H."""
+    c = si.SWIGLU_Q4
+    T, K, N = c["T"], c["K"], c["N"]
+    p = si.swiglu_q5_problem(T, K, N, c["seed"] + 500)
+    h_dev = _swiglu_q5_dev(nq, p, T, K, N)
+    rows = gu.sample_rows(N, 256, 2)
+    g, u, _ = oracle.swiglu_q5_rows(p["x"], p["wgn"], p["wgh"], p["sg"], p["wun"], p["wuh"],
+                                    p["su"], T, K, rows)
+    assert gu.rel_err(gu.host_f64(h_dev)[:, rows], (g / (1.0 + np.exp(-g)) * u).T) <= gu.TOL
+    d = si.SWIGLU_DOWN
+    pd = si.q5_problem(T, d["K"], d["N"], c["seed"] + 1500)
+    wd = gu.pack_q5(nq, pd["wn"], pd["wh"], pd["s"], d["K"], d["N"])
+    y = gu.host_f64(nq.gemm_q5(h_dev, wd, d["N"]))
+    h_bits = h_dev.view(torch.int16).cpu().numpy().view(np.uint16)
+    rows = gu.sample_rows(d["N"], 256, 3)
+    y_ref = oracle.gemm_q5_rows(h_bits, pd["wn"], pd["wh"], pd["s"], T, d["K"], rows)
+    assert gu.rel_err(y[:, rows], y_ref.T) <= gu.TOL
+
+
 # ---------------------------------------------------------------- the five workloads
 
 def test_workload_tiny_q4(nq):

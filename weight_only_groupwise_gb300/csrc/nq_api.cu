@@ -231,7 +231,7 @@ int grid_for(long long work, int per_block) {
     return (int)(b < 1 ? 1 : b);
 }
 
-// Shared body of the three projection entry points.
+// Shared body of the projection entry points (Q4/Q5 GEMM, Q4/Q5 SwiGLU).
 nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* W1, void* Y, int T, int K,
                   int N, void* stream) {
     if (T < 0 || T > 8) return NQ_ERR_SHAPE;
@@ -263,7 +263,8 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
     cudaError_t e;
     if (swiglu)
-        e = launch_proj_swiglu_q4(a, as_stream(stream), g_pdl);
+        e = bits == 4 ? launch_proj_swiglu_q4(a, as_stream(stream), g_pdl)
+                      : launch_proj_swiglu_q5(a, as_stream(stream), g_pdl);
     else if (bits == 4)
         e = launch_proj_q4(a, as_stream(stream), g_pdl);
     else
@@ -362,6 +363,10 @@ nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, i
     return project(4, true, X, Wg, Wu, H, T, K, N, stream);
 }
 
+nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N, void* stream) {
+    return project(5, true, X, Wg, Wu, H, T, K, N, stream);
+}
+
 nq_status nq_dequant_q4_debug(const void* W, float* out, int K, int N, void* stream) {
     return dequant(4, W, out, K, N, stream);
 }
@@ -422,7 +427,7 @@ void nq_shutdown(void) {
 
 nq_status nq_plan_info(int bits, int mode, int T, int K, int N, int num_sms, int64_t out[8]) {
     if (!out) return NQ_ERR_NULL;
-    if ((bits != 4 && bits != 5) || (mode != 0 && mode != 1) || (mode == 1 && bits != 4)) return NQ_ERR_SHAPE;
+    if ((bits != 4 && bits != 5) || (mode != 0 && mode != 1)) return NQ_ERR_SHAPE;
     if (T < 1 || T > 8 || K < kGroup || N < kTileRows || num_sms < 1) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;

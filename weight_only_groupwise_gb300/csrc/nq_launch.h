@@ -12,6 +12,7 @@ namespace nq {
 cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
+cudaError_t launch_proj_swiglu_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
 template <int BITS, bool SWIGLU, bool F16, bool ONE>
 cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {

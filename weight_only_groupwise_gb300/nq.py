@@ -45,6 +45,7 @@ def lib() -> ctypes.CDLL:
         L.nq_gemm_q5.argtypes = [P, P, P, I, I, I, P]
         L.nq_gemm_q4_noalloc.argtypes = [P, P, P, I, I, I, P]
         L.nq_swiglu_q4.argtypes = [P, P, P, P, I, I, I, P]
+        L.nq_swiglu_q5.argtypes = [P, P, P, P, I, I, I, P]
         L.nq_dequant_q4_debug.argtypes = [P, P, I, I, P]
         L.nq_dequant_q5_debug.argtypes = [P, P, I, I, P]
         L.nq_reserve.argtypes = [I, I, I]
@@ -55,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_segments.restype = ctypes.c_int64
         for f in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_gemm_q4_noalloc", "nq_swiglu_q4",
+                  "nq_swiglu_q5",
                   "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_reserve", "nq_device_error",
                   "nq_plan_info"):
             getattr(L, f).restype = I
@@ -150,6 +152,15 @@ def swiglu_q4(x, wg, wu, N: int, out=None, stream=None):
     T, K = x.shape
     h = _out(x, N, out)
     _check(lib().nq_swiglu_q4(_ptr(x), _ptr(wg), _ptr(wu), _ptr(h), T, K, N, _stream(stream)))
+    return h
+
+
+def swiglu_q5(x, wg, wu, N: int, out=None, stream=None):
+    """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with both weights packed Q5."""
+    _cuda(x, "x")
+    T, K = x.shape
+    h = _out(x, N, out)
+    _check(lib().nq_swiglu_q5(_ptr(x), _ptr(wg), _ptr(wu), _ptr(h), T, K, N, _stream(stream)))
     return h
 
 
