@@ -333,3 +333,28 @@ def test_activation_range_outliers(nq, bits):
     for t in range(T):   # per token: each row has its own magnitude
         assert np.all(np.isfinite(y[t]))
         assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+def test_activation_outlier_in_a_later_slab(nq, bits):
+    """T=8 with K=17408 runs in three K slabs. One token carries an outlier near the bf16
+    maximum in the last slab only, in its last K group; another token is scaled by 1e30 in
+    the middle slab. Each slab's range check must see its own outliers."""
+    T, K, N = 8, 17408, 48
+    p = si.q4_problem(T, K, N, 93) if bits == 4 else si.q5_problem(T, K, N, 93)
+    g = np.random.default_rng(94)
+    x = g.standard_normal((T, K)).astype(np.float32)
+    x[5, K - 3] = -2.5e38
+    x[2, 7000:9000] *= 1.0e30
+    xb = si.bf16_bits(x)
+    if bits == 4:
+        w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+        y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(xb), w, N))
+        y_ref = oracle.gemm_q4(xb, p["wq"], p["s"], T, K, N)
+    else:
+        w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+        y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), w, N))
+        y_ref = oracle.gemm_q5(xb, p["wn"], p["wh"], p["s"], T, K, N)
+    for t in range(T):
+        assert np.all(np.isfinite(y[t]))
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t

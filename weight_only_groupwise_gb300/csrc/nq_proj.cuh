@@ -514,106 +514,114 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 mbar_wait(x_bar, nx & 1, flags, a.dev_err);
                 ++nx;
             }
-            // Per token, max |x| over the slab (bit patterns compare like magnitudes). The bf16
-            // path needs it only when some |x| reaches 2^100 (bits 0x7180): one pass with a
-            // barrier OR-reduction decides, and the per-token pass runs only then.
+            // Per token, max |x| over the slab (bit patterns compare like magnitudes), then the
+            // operand conversion and O[gl][t], the group MMA chain on the zero-point code. The
+            // fp16 path always needs the maximum. The bf16 path needs it only when some |x|
+            // reaches 2^100 (bits 0x7180): the O pass, which loads every group of the slab
+            // once across the warps, also tests its fragments; a barrier OR-reduction decides,
+            // and only then do the max pass, the rescale and a second O pass run.
             if (tid < 8) xmax[tid] = 0;
+            if constexpr (F16) named_bar_sync(kBarConsumers, kConsumerThreads);
             bool need_max = F16;
-            if constexpr (!F16) {
-                bool big = false;
-                for (int t = 0; t < T; ++t)
-                    for (int c = tid; c < chunks; c += kConsumerThreads) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
-                        const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-                        big |= max(m & 0xFFFFu, m >> 16) >= 0x7180u;
-                    }
-                need_max = named_bar_or(kBarConsumers, kConsumerThreads, big);
-            } else {
-                named_bar_sync(kBarConsumers, kConsumerThreads);
-            }
-            if (need_max) {
-                for (int t = 0; t < T; ++t) {
-                    uint32_t mx = 0;
-                    for (int c = tid; c < chunks; c += kConsumerThreads) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
-                        const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-                        mx = max(mx, max(m & 0xFFFFu, m >> 16));
-                    }
-                    mx = __reduce_max_sync(0xffffffffu, mx);
-                    if (lane == 0) atomicMax(xmax + t, (int)mx);
-                }
-                named_bar_sync(kBarConsumers, kConsumerThreads);
-            }
-            if constexpr (F16) {
-                // X slab bf16 -> fp16 in place, times 2^-e (token_exponent); the upper-K half
-                // of every 16-wide K step is also divided by 16 (see decode_q4). Both exact.
-                for (int t = 0; t < T; ++t) {
-                    const int e = token_exponent(xmax[t]);
-                    const float lo_scale = __int_as_float((127 - e) << 23);
-                    const float hi_scale = lo_scale * 0.0625f;
-                    for (int c = tid; c < chunks; c += kConsumerThreads) {
-                        uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
-                        const uint4 v = *q;
-                        const float sc = (c & 1) ? hi_scale : lo_scale;
-                        uint4 o;
-                        uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
-                        const uint32_t* iv = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const __half2 h2 = __floats2half2_rn(__uint_as_float(iv[i] << 16) * sc,
-                                                                 __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
-                            ov[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int rep = 0;; ++rep) {
+                if (need_max) {
+                    for (int t = 0; t < T; ++t) {
+                        uint32_t mx = 0;
+                        for (int c = tid; c < chunks; c += kConsumerThreads) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(xs + t * pitch + c * 16);
+                            const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                                   max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+                            mx = max(mx, max(m & 0xFFFFu, m >> 16));
                         }
-                        *q = o;
+                        mx = __reduce_max_sync(0xffffffffu, mx);
+                        if (lane == 0) atomicMax(xmax + t, (int)mx);
                     }
-                }
-            } else {
-                // bf16 operands: only a token too large for the offset chains is rescaled.
-                for (int t = 0; t < T && need_max; ++t) {
-                    const int e = token_exponent_bf16(xmax[t]);
-                    if (e == 0) continue;
-                    const float sc = __int_as_float((127 - e) << 23);
-                    for (int c = tid; c < chunks; c += kConsumerThreads) {
-                        uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
-                        uint4 v = *q;
-                        uint32_t* iv = reinterpret_cast<uint32_t*>(&v);
+                    named_bar_sync(kBarConsumers, kConsumerThreads);
+                    if constexpr (F16) {
+                        // X slab bf16 -> fp16 in place, times 2^-e (token_exponent); the upper-K
+                        // half of every 16-wide K step is also divided by 16 (see decode_q4).
+                        // Both exact.
+                        for (int t = 0; t < T; ++t) {
+                            const int e = token_exponent(xmax[t]);
+                            const float lo_scale = __int_as_float((127 - e) << 23);
+                            const float hi_scale = lo_scale * 0.0625f;
+                            for (int c = tid; c < chunks; c += kConsumerThreads) {
+                                uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
+                                const uint4 v = *q;
+                                const float sc = (c & 1) ? hi_scale : lo_scale;
+                                uint4 o;
+                                uint32_t* ov = reinterpret_cast<uint32_t*>(&o);
+                                const uint32_t* iv = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(iv[i] << 16) * sc,
-                                                                            __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
-                            iv[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                                for (int i = 0; i < 4; ++i) {
+                                    const __half2 h2 = __floats2half2_rn(__uint_as_float(iv[i] << 16) * sc,
+                                                                         __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
+                                    ov[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                                }
+                                *q = o;
+                            }
                         }
-                        *q = v;
+                    } else {
+                        // bf16 operands: only a token too large for the offset chains is rescaled.
+                        for (int t = 0; t < T; ++t) {
+                            const int e = token_exponent_bf16(xmax[t]);
+                            if (e == 0) continue;
+                            const float sc = __int_as_float((127 - e) << 23);
+                            for (int c = tid; c < chunks; c += kConsumerThreads) {
+                                uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
+                                uint4 v = *q;
+                                uint32_t* iv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(iv[i] << 16) * sc,
+                                                                                    __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
+                                    iv[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                                }
+                                *q = v;
+                            }
+                        }
+                    }
+                    named_bar_sync(kBarConsumers, kConsumerThreads);
+                }
+                // O[gl][t]: a warp consumes only the groups gl = warp (mod NW) of the slab
+                // (blocks start on multiples of NW), so it computes exactly those, four chains
+                // per pass, and only it reads them back. big: some half of a fragment has
+                // |x| >= 2^100 (a 15-bit magnitude m >= 0x7180 carries into bit 15 of
+                // m + 0x0E80, and no further).
+                uint32_t big = 0;
+                const uint32_t az[4] = {kZeroLo, kZeroLo, kZeroHi, kZeroHi};
+                for (int gl = warp; gl < gs; gl += 4 * NW) {
+                    int g[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) g[c] = gl + c * NW < gs ? gl + c * NW : gl;
+                    uint32_t xb[4][8];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        ldsm_x4(ld_base + g[c] * ld_group_step, xb[c]);
+                        ldsm_x4(ld_base + g[c] * ld_group_step + ld_half_step, xb[c] + 4);
+                    }
+                    if constexpr (!F16) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) big |= (xb[c][i] & 0x7FFF7FFFu) + 0x0E800E80u;
+                    }
+                    float d[4][4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mma_zero_16816<F16>(d[c], az, xb[c][0], xb[c][1]);
+#pragma unroll
+                    for (int j = 1; j < 4; ++j)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) mma_acc<F16>(d[c], az, xb[c][2 * j], xb[c][2 * j + 1]);
+                    if (lane < 4) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<float2*>(osum + g[c] * 8 + 2 * lane) = make_float2(d[c][0], d[c][1]);
                     }
                 }
-            }
-            if (F16 || need_max) named_bar_sync(kBarConsumers, kConsumerThreads);
-            // O[gl][t]: the group MMA chain on the zero-point code. A warp consumes only the
-            // groups gl = warp (mod NW) of the slab (blocks start on multiples of NW), so it
-            // computes exactly those, four chains per pass, and only it reads them back.
-            const uint32_t az[4] = {kZeroLo, kZeroLo, kZeroHi, kZeroHi};
-            for (int gl = warp; gl < gs; gl += 4 * NW) {
-                int g[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) g[c] = gl + c * NW < gs ? gl + c * NW : gl;
-                uint32_t xb[4][8];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    ldsm_x4(ld_base + g[c] * ld_group_step, xb[c]);
-                    ldsm_x4(ld_base + g[c] * ld_group_step + ld_half_step, xb[c] + 4);
-                }
-                float d[4][4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) mma_zero_16816<F16>(d[c], az, xb[c][0], xb[c][1]);
-#pragma unroll
-                for (int j = 1; j < 4; ++j)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) mma_acc<F16>(d[c], az, xb[c][2 * j], xb[c][2 * j + 1]);
-                if (lane < 4) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<float2*>(osum + g[c] * 8 + 2 * lane) = make_float2(d[c][0], d[c][1]);
-                }
+                if (F16 || rep > 0) break;
+                need_max = named_bar_or(kBarConsumers, kConsumerThreads, (big & 0x80008000u) != 0);
+                if (!need_max) break;
             }
             __syncwarp();
             // 2^e of the lane's two token columns (from the max bits), applied at the hand-over
