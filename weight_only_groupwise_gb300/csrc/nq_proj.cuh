@@ -670,6 +670,30 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
                     }
                     tiles_mma<BITS, F16, GPW, 2, ONE>(code, scale, xb, o, magic, acc);
+                } else if (i0 == 0 && i1 == BG / 2) {
+                    // the first half of a block (the 16-group tail of a row whose group count
+                    // is 16 mod 32, e.g. K = 5120): groups warp and warp + NW, unrolled
+                    constexpr int H = GPW / 2;
+                    uint32_t xb[H][8];
+                    float2 o[H];
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        const uint32_t la = la0 + (NW * h) * ld_group_step;
+                        ldsm_x4(la, xb[h]);
+                        ldsm_x4(la + ld_half_step, xb[h] + 4);
+                        o[h] = *reinterpret_cast<const float2*>(o0 + 8 * NW * h);
+                    }
+                    const uint8_t* c0 = t0 + warp * TB + code_lane;
+                    const uint8_t* s0 = t0 + scale_lane + warp * kScaleTileBytes;
+                    const uint8_t* code[2 * H];
+                    const uint8_t* scale[2 * H];
+#pragma unroll
+                    for (int t = 0; t < 2 * H; ++t) {
+                        const int m = t / H, h = t % H;
+                        code[t] = c0 + m * kTileArea + NW * h * TB;
+                        scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
+                    }
+                    tiles_mma<BITS, F16, H, 2, ONE>(code, scale, xb, o, magic, acc);
                 } else {
                     // part of a block (first or last block of a run): group by group, in a
                     // loop that is not unrolled (rare, and it keeps the code small)
