@@ -8,6 +8,7 @@ SHAPES = [
     (4, 0, 1, 256, 128), (4, 0, 1, 5120, 17408), (5, 0, 8, 5120, 6144), (4, 1, 8, 5120, 17408),
     (4, 0, 8, 17408, 5120), (5, 0, 8, 5120, 1024), (5, 0, 3, 6144, 5120), (4, 0, 8, 6208, 48),
     (4, 0, 5, 64, 16), (4, 0, 2, 1024, 272), (4, 1, 7, 17408, 48), (5, 0, 1, 64, 16),
+    (5, 1, 8, 5120, 17408), (5, 1, 4, 17408, 64), (5, 1, 1, 640, 16),
 ]
 
 
