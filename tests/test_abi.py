@@ -101,7 +101,7 @@ def test_null_alignment_alias_errors(L):
 def test_plan_info_matches_workloads(L):
     from weight_only_groupwise_gb300 import nq
     p = nq.plan_info(4, 0, 1, 5120, 17408, 152)
-    assert p["ctas"] == 152 and p["pairs"] == 544 and p["units"] == 544 * 80 and p["slabs"] == 1
+    assert p["ctas"] == 136 and p["pairs"] == 544 and p["units"] == 544 * 80 and p["slabs"] == 1  # 4 whole pairs each
     p = nq.plan_info(4, 0, 8, 17408, 5120, 152)   # T=8 down projection needs K slabs
     assert p["slabs"] == 3 and p["slab_groups"] * 3 >= 272
     p = nq.plan_info(4, 1, 8, 5120, 17408, 152)   # swiglu pairs gate/up tiles

@@ -68,14 +68,18 @@ def test_partition_covers_every_unit_once(nq, bits, mode, T, K, N, sms):
 @pytest.mark.parametrize("bits,T,K,N,sms,ctas", [
     (5, 8, 5120, 6144, 152, 96),     # 192 pairs: two whole pairs per block
     (5, 1, 5120, 6144, 152, 96),
-    (4, 1, 1024, 2432, 152, 76),     # 76 pairs: one per block (76 >= 60 % of 152)
-    (4, 1, 5120, 17408, 152, 152),   # 544 pairs: stream-K over every SM
-    (5, 8, 5120, 1024, 152, 152),    # 32 pairs: too few blocks, stream-K
+    (4, 1, 1024, 2432, 152, 76),     # 76 pairs: one per block
+    (4, 1, 5120, 17408, 152, 136),   # 544 pairs: four per block on 136 SMs
+    (5, 8, 5120, 1024, 152, 32),     # 32 pairs: the rings of 32 blocks hold the whole problem
+    (5, 1, 6144, 5120, 152, 80),     # 160 pairs, five stages per block: 80 blocks
+    (5, 8, 6144, 5120, 152, 152),    # the same at T=8: two stages, too little in flight
     (4, 8, 17408, 5120, 152, 152),   # several slabs: stream-K
+    (4, 1, 5120, 17408, 7, 7),       # 544 pairs on 7 SMs: 78 per block does not divide, stream-K
 ])
 def test_whole_pairs_when_they_divide_evenly(nq, bits, T, K, N, sms, ctas):
-    """With one slab and at most two row pairs per block, a grid that still covers 60 % of
-    the SMs takes whole pairs per block, and then no segment is a partial run."""
+    """With one slab and row pairs that divide evenly into at most four per block (the fewest
+    that fit the SMs), the grid takes whole pairs per block (no segment is a partial run)
+    when those blocks' rings hold at least 8 MB in flight or the whole problem."""
     info = nq.plan_info(bits, 0, T, K, N, sms)
     assert info["ctas"] == ctas
     if ctas < sms:
@@ -84,3 +88,10 @@ def test_whole_pairs_when_they_divide_evenly(nq, bits, T, K, N, sms, ctas):
             segs = nq.plan_segments(bits, 0, T, K, N, sms, c)
             assert all(ga == 0 and gb == G for (_, _, ga, gb) in segs)
             assert len(segs) == info["pairs"] // ctas
+
+
+def test_many_pairs_per_block_stay_stream_k(nq):
+    """The fused gate/up block of the SwiGLU workload has 1088 pairs: eight per block would
+    leave 16 SMs idle, so the plan keeps stream-K over every SM."""
+    assert nq.plan_info(4, 1, 8, 5120, 17408, 152)["ctas"] == 152
+    assert nq.plan_info(5, 1, 8, 5120, 17408, 152)["ctas"] == 152

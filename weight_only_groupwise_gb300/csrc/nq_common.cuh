@@ -45,6 +45,9 @@ constexpr int kGroupsPerWarp = kChunkGroups / kConsumerWarps;
 static_assert(kGroupsPerWarp * kConsumerWarps == kChunkGroups, "stage groups split evenly over warps");
 constexpr int kMaxStages = 12;
 constexpr int kSmemLimit = 227 * 1024;
+// Weight bytes that must be in flight to keep HBM busy (bandwidth x loaded latency, about
+// 6.8 TB/s x 1.2 us), measured: whole-pair grids below it streamed slower than stream-K.
+constexpr long long kSaturateBytes = 8ll << 20;
 constexpr int kXBudget = 97 * 1024;  // on-chip activation slab (96 groups x 8 rows + padding)
 constexpr int kMinUnitsPerCta = 16;
 constexpr int kPartialFloats = 256;  // 2 M tiles x 16 rows x 8 tokens
@@ -116,20 +119,6 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.GS = (p.G + p.S - 1) / p.S;
     if (p.S > 1) p.GS = (p.GS + kBlockGroups - 1) / kBlockGroups * kBlockGroups;  // slabs on block edges
     p.U = (long long)p.RP * p.G;
-    long long P = p.U / kMinUnitsPerCta;
-    if (P > num_sms) P = num_sms;
-    if (P < 1) P = 1;
-    // Few row pairs, one slab: when they divide evenly into one or two per block and that
-    // still keeps most SMs streaming, give each block whole pairs. No pair is split, so no
-    // split-K settle (several L2 round trips at the end of a short kernel) is needed.
-    if (p.S == 1 && num_sms > 0) {
-        const int k = (p.RP + num_sms - 1) / num_sms;
-        if (k >= 1 && k <= 2 && p.RP % k == 0 && (long long)(p.RP / k) * 5 >= (long long)num_sms * 3)
-            P = p.RP / k;
-    }
-    p.P = (int)P;
-    p.Uq = (int)(p.U / p.P);
-    p.Ur = (int)(p.U % p.P);
     p.CG = kChunkGroups;
     p.tile_bytes = bits == 4 ? kQ4TileBytes : kQ5TileBytes;
     p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
@@ -158,6 +147,27 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.red_bytes = p.nred * kRedBufBytes;
     p.stages = st;
     p.smem_bytes = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes + st * p.stage_bytes;
+    // Grid. Stream-K over all SMs by default. One slab and row pairs that divide evenly
+    // into k <= 4 per block (k = the fewest that fit the SMs): give each block whole pairs,
+    // so no pair is split and no split-K settle (several L2 round trips at the end of a
+    // short kernel) is needed, provided those blocks' rings can still keep HBM busy, i.e.
+    // hold kSaturateBytes in flight, or the whole problem. With more pairs per block the
+    // stream-K settles come early and overlap the stream, and the SMs a whole-pair grid
+    // leaves idle cost more (measured: 8 pairs per block on 136 SMs, +3 to +4 %).
+    long long P = p.U / kMinUnitsPerCta;
+    if (P > num_sms) P = num_sms;
+    if (P < 1) P = 1;
+    if (p.S == 1 && num_sms > 0 && st > 0) {
+        const int k = (p.RP + num_sms - 1) / num_sms;
+        if (k >= 1 && k <= 4 && p.RP % k == 0) {
+            const long long in_flight = (long long)(p.RP / k) * st * p.stage_bytes;
+            const long long weights = p.U * 2 * (p.tile_bytes + kScaleTileBytes);
+            if (in_flight >= kSaturateBytes || in_flight >= weights) P = p.RP / k;
+        }
+    }
+    p.P = (int)P;
+    p.Uq = (int)(p.U / p.P);
+    p.Ur = (int)(p.U % p.P);
     p.slots = (long long)p.S * p.RP + p.P;
     p.f16 = T <= NQ_F16_MAX_T ? 1 : 0;
     return st >= 2;
