@@ -217,6 +217,26 @@ nq_status nq_plan_info(int bits, int mode, int T, int K, int N, int num_sms, int
 int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, int cta,
                          int64_t* seg, int64_t cap);
 
+/*
+ * nq_plan_cluster_info / nq_plan_cluster_segments: the same for a slab-cluster launch,
+ * which the projection calls use (bf16 operands, T >= 3) when K needs 2..4 slabs, enough
+ * thread-block clusters fit the device, and the environment variable NQ_CLUSTER is not "0"
+ * at the first call. A cluster of S blocks takes a range of (row pair, slab-local group)
+ * work; block rank r takes slab r of it, stages that activation slab once, and the S parts
+ * of each run are added on chip by rank 0 (distributed shared memory) before the usual
+ * split-K settle between clusters. Host only; no device needed.
+ *   clusters: clusters to plan for (the calls use the device's resident count, at most
+ *   SMs / S).
+ *   info out[8]: [0] blocks, [1] cluster size S, [2] groups per slab, [3] row pairs,
+ *   [4] partial-sum slots, [5] pipeline stages, [6] cluster-level units, [7] clusters.
+ *   segments: as nq_plan_segments for block `cta` (cluster cta / S, rank cta % S): its
+ *   real (slab, pair, first group, end group) runs; a run may be empty (ga == gb) when the
+ *   last slab is shorter. Returns NQ_ERR_SHAPE when the shape has no slab-cluster plan.
+ */
+nq_status nq_plan_cluster_info(int bits, int mode, int T, int K, int N, int clusters, int64_t out[8]);
+int64_t nq_plan_cluster_segments(int bits, int mode, int T, int K, int N, int clusters, int cta,
+                                 int64_t* seg, int64_t cap);
+
 #ifdef __cplusplus
 }
 #endif

@@ -95,3 +95,48 @@ def test_many_pairs_per_block_stay_stream_k(nq):
     leave 16 SMs idle, so the plan keeps stream-K over every SM."""
     assert nq.plan_info(4, 1, 8, 5120, 17408, 152)["ctas"] == 152
     assert nq.plan_info(5, 1, 8, 5120, 17408, 152)["ctas"] == 152
+
+
+CLUSTER_SHAPES = [
+    # bits, mode, T, K, N, clusters
+    (4, 0, 8, 17408, 5120, 48), (5, 0, 8, 17408, 5120, 48), (4, 0, 4, 17408, 5120, 72),
+    (4, 0, 3, 17408, 64, 50), (4, 0, 8, 6208, 48, 7), (4, 1, 8, 17408, 48, 48),
+    (5, 1, 4, 17408, 64, 72), (4, 0, 8, 12352, 112, 3), (4, 0, 8, 24576, 16, 38),
+]
+
+
+@pytest.mark.parametrize("bits,mode,T,K,N,clusters", CLUSTER_SHAPES)
+def test_cluster_partition_covers_every_unit_once(nq, bits, mode, T, K, N, clusters):
+    """Slab clusters: block rank r only ever touches slab r; every (pair, group) of the
+    real problem is processed by exactly one block; the ranks of a cluster walk the same
+    runs (same pairs, same slab-local ranges before clipping to the shorter last slab)."""
+    import numpy as np
+    info = nq.plan_cluster_info(bits, mode, T, K, N, clusters)
+    S, gs, RP, G = info["cluster"], info["slab_groups"], info["pairs"], K // 64
+    assert 2 <= S <= 4 and gs % 8 == 0 and (S - 1) * gs < G <= S * gs
+    assert info["ctas"] == info["clusters"] * S and info["clusters"] <= clusters
+    assert info["stages"] >= 2
+    covered = np.zeros((RP, G), np.int32)
+    runs = {}
+    for cta in range(info["ctas"]):
+        c, r = divmod(cta, S)
+        segs = nq.plan_cluster_segments(bits, mode, T, K, N, clusters, cta)
+        lo, hi = r * gs, min((r + 1) * gs, G)
+        for (s, rp, ga, gb) in segs:
+            assert s == r and lo <= ga <= gb <= hi
+            covered[rp, ga:gb] += 1
+        runs.setdefault(c, []).append([(rp, ga - lo) for (s, rp, ga, gb) in segs])
+    assert (covered == 1).all()
+    for c, per_rank in runs.items():
+        pairs = [[rp for rp, _ in rr] for rr in per_rank]
+        assert all(p == pairs[0] for p in pairs)
+        starts0 = [a for _, a in per_rank[0]]
+        assert all([a for _, a in rr] == starts0 or r == S - 1 for r, rr in enumerate(per_rank))
+
+
+def test_no_cluster_plan_for_one_slab(nq):
+    from weight_only_groupwise_gb300.nq import NqError
+    with pytest.raises(NqError):
+        nq.plan_cluster_info(4, 0, 1, 5120, 17408, 48)     # one slab
+    with pytest.raises(NqError):
+        nq.plan_cluster_info(4, 0, 2, 17408, 5120, 48)     # fp16 operands, one slab

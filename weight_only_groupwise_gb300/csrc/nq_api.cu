@@ -134,12 +134,15 @@ struct DevState {
     uint8_t* ws = nullptr;     // [err: 256 B][tickets][partials]
     long long slots_cap = 0;
     long long tickets_cap = 0;
+    // resident slab clusters per [S][bits == 5][swiglu], -1 until queried
+    int cluster_cap[kMaxCluster + 1][2][2];
 };
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 bool g_pdl = true;
+bool g_cluster = true;
 bool g_env_read = false;
 
 size_t ws_tickets_off() { return 256; }
@@ -156,6 +159,8 @@ nq_status current_device(DevState** out, int* dev_out) {
     if (!g_env_read) {
         const char* e = std::getenv("NQ_PDL");
         if (e && e[0] == '0') g_pdl = false;
+        const char* c = std::getenv("NQ_CLUSTER");
+        if (c && c[0] == '0') g_cluster = false;
         g_env_read = true;
     }
     DevState& d = g_dev[dev];
@@ -164,6 +169,9 @@ nq_status current_device(DevState** out, int* dev_out) {
             cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return NQ_ERR_CUDA;
+        for (auto& a : d.cluster_cap)
+            for (auto& b : a)
+                for (int& c : b) c = -1;
         d.init = true;
     }
     if (d.major != 10 || d.minor != 3) return NQ_ERR_DEVICE;
@@ -231,6 +239,22 @@ int grid_for(long long work, int per_block) {
     return (int)(b < 1 ? 1 : b);
 }
 
+// Slab clusters of S blocks to launch: as many as can be resident at once (queried once per
+// device and instantiation; every plan of a slab-cluster instantiation needs more than half
+// of an SM's shared memory, so one block per SM), at most one block per SM.
+int resident_clusters(DevState& d, int bits, bool swiglu, int S) {
+    int& c = d.cluster_cap[S][bits == 5 ? 1 : 0][swiglu ? 1 : 0];
+    if (c < 0) {
+        const int smem = kSmemLimit;
+        if (bits == 4)
+            c = swiglu ? cluster_capacity_swiglu_q4(S, smem) : cluster_capacity_q4(S, smem);
+        else
+            c = swiglu ? cluster_capacity_swiglu_q5(S, smem) : cluster_capacity_q5(S, smem);
+    }
+    const int cap = d.sms / S;
+    return c < cap ? c : cap;
+}
+
 // Shared body of the projection entry points (Q4/Q5 GEMM, Q4/Q5 SwiGLU).
 nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* W1, void* Y, int T, int K,
                   int N, void* stream) {
@@ -252,7 +276,17 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     }
     ProjArgs a;
     if (!make_plan(bits, swiglu ? 1 : 0, T, K, N, d->sms, a.p)) return NQ_ERR_SHAPE;
-    st = ensure_workspace(*d, a.p.slots, a.p.RP);
+    a.q = a.p;
+    // K in several slabs (bf16 operands): slab clusters when enough of them fit at once.
+    if (g_cluster && a.p.S >= 2 && a.p.S <= kMaxCluster && !a.p.f16) {
+        Plan p2, q2;
+        const int C = resident_clusters(*d, bits, swiglu, a.p.S);
+        if (C > 0 && make_cluster_plans(bits, swiglu ? 1 : 0, T, K, N, C, p2, q2)) {
+            a.p = p2;
+            a.q = q2;
+        }
+    }
+    st = ensure_workspace(*d, a.q.slots, a.q.RP);
     if (st != NQ_OK) return st;
     a.X = static_cast<const uint16_t*>(X);
     a.W0 = static_cast<const uint8_t*>(W0);
@@ -460,6 +494,54 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
     Segment nat;
     for (int si = 0; si < order.count; ++si) {
         const Segment sg = seg_pick(p, order, si, nat, u1);
+        if (n < cap) {
+            seg[4 * n + 0] = sg.s;
+            seg[4 * n + 1] = sg.rp;
+            seg[4 * n + 2] = sg.ga;
+            seg[4 * n + 3] = sg.gb;
+        }
+        ++n;
+    }
+    return n;
+}
+
+nq_status nq_plan_cluster_info(int bits, int mode, int T, int K, int N, int clusters, int64_t out[8]) {
+    if (!out) return NQ_ERR_NULL;
+    if ((bits != 4 && bits != 5) || (mode != 0 && mode != 1)) return NQ_ERR_SHAPE;
+    if (T < 1 || T > 8 || K < kGroup || N < kTileRows || clusters < 1) return NQ_ERR_SHAPE;
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    Plan p, q;
+    if (!make_cluster_plans(bits, mode, T, K, N, clusters, p, q)) return NQ_ERR_SHAPE;
+    out[0] = p.P;
+    out[1] = p.cl;
+    out[2] = p.GS;
+    out[3] = p.RP;
+    out[4] = q.slots;
+    out[5] = p.stages;
+    out[6] = q.U;
+    out[7] = q.P;
+    return NQ_OK;
+}
+
+int64_t nq_plan_cluster_segments(int bits, int mode, int T, int K, int N, int clusters, int cta, int64_t* seg,
+                                 int64_t cap) {
+    int64_t info[8];
+    nq_status st = nq_plan_cluster_info(bits, mode, T, K, N, clusters, info);
+    if (st != NQ_OK) return st;
+    Plan p, q;
+    make_cluster_plans(bits, mode, T, K, N, clusters, p, q);
+    if (cta < 0 || cta >= p.P) return NQ_ERR_SHAPE;
+    if (cap > 0 && !seg) return NQ_ERR_NULL;
+    // Same walk as the kernels: the cluster's segments in processing order, mapped to the
+    // block's rank (its slab).
+    const int c = cta / p.cl, r = cta % p.cl;
+    int64_t n = 0;
+    const long long u0 = cta_begin(q, c), u1 = cta_begin(q, c + 1);
+    const SegOrder order = seg_order(q, u0, u1);
+    Segment nat;
+    for (int si = 0; si < order.count; ++si) {
+        const Segment sg = rank_segment(p, seg_pick(q, order, si, nat, u1), r);
         if (n < cap) {
             seg[4 * n + 0] = sg.s;
             seg[4 * n + 1] = sg.rp;

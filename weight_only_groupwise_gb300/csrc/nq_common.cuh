@@ -54,6 +54,7 @@ constexpr int kPartialFloats = 256;  // 2 M tiles x 16 rows x 8 tokens
 constexpr int kMaxRed = 4;           // most run hand-over buffers (consumers -> epilogue warps)
 constexpr int kRedBufBytes = kConsumerWarps * 2 * 512;  // one buffer: every warp's two accumulator tiles
 constexpr long long kWaitTimeoutNs = 2000000000LL;  // 2 s per bounded wait
+constexpr int kMaxCluster = 4;       // most K slabs handled by one thread-block cluster
 
 // Errors a kernel can raise through the workspace flag word.
 constexpr int kDevErrTimeout = 1;
@@ -92,13 +93,56 @@ struct Plan {
     int tile_bytes, stage_bytes, x_bytes, corr_bytes, red_bytes, bar_bytes, smem_bytes;
     int f16;               // 1: fp16 MMA operands (X converted in shared memory), 0: bf16
     int nred;              // run hand-over buffers (2..kMaxRed)
+    int cl;                // 1, or S: slab clusters (block rank r of a cluster takes slab r)
+    int cl_bytes;          // cluster exchange buffers at the end of shared memory (0 if cl == 1)
 };
+
+// Shared-memory bytes of the exchange buffers of a slab cluster of S blocks: per epilogue
+// warp, one partial run of each non-leading rank.
+NQ_HD int cluster_buffer_bytes(int S) { return S > 1 ? kEpilogueWarps * (S - 1) * kPartialFloats * 4 : 0; }
 
 // Largest T that uses fp16 operands: one shift per code word instead of three, paid for by
 // converting the activation slab to fp16 once per block, which grows with T.
 #ifndef NQ_F16_MAX_T
 #define NQ_F16_MAX_T 2
 #endif
+
+// Shared-memory layout of a plan whose slab geometry (GS) is set: activation slab,
+// zero-point sums, run hand-over buffers, barriers, cluster buffers (p.cl_bytes) and as many
+// pipeline stages as fit. Returns the stage count.
+NQ_HD int plan_smem(Plan& p) {
+    const int Tr = p.T > 0 ? p.T : 1;
+    p.CG = kChunkGroups;
+    p.tile_bytes = p.bits == 4 ? kQ4TileBytes : kQ5TileBytes;
+    p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
+    p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
+    p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
+    p.bar_bytes = 512;                           // barriers, flags, per-token range data
+    // Run hand-over buffers: kMaxRed if they fit without costing a pipeline stage against
+    // two, else two; spare buffers let the consumers run ahead of a split-K settle. The count
+    // is a multiple of kEpilogueWarps, so each buffer is always served by the same epilogue
+    // warp (two warps never wait on one buffer's barrier at once).
+    static_assert(kMaxRed % kEpilogueWarps == 0 && 2 % kEpilogueWarps == 0, "buffers per epilogue warp");
+    int st = 0;
+    for (int nr = kMaxRed; nr >= 2; nr -= 2) {
+        const int fixed = p.x_bytes + p.corr_bytes + nr * kRedBufBytes + p.bar_bytes + p.cl_bytes;
+        int s2 = (kSmemLimit - fixed) / p.stage_bytes;
+        if (s2 > kMaxStages) s2 = kMaxStages;
+        const int fixed2 = p.x_bytes + p.corr_bytes + 2 * kRedBufBytes + p.bar_bytes + p.cl_bytes;
+        int s_two = (kSmemLimit - fixed2) / p.stage_bytes;
+        if (s_two > kMaxStages) s_two = kMaxStages;
+        if (s2 == s_two || nr == 2) {
+            p.nred = nr;
+            st = s2;
+            break;
+        }
+    }
+    p.red_bytes = p.nred * kRedBufBytes;
+    p.stages = st;
+    p.smem_bytes = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes + p.cl_bytes + st * p.stage_bytes;
+    p.f16 = p.T <= NQ_F16_MAX_T ? 1 : 0;
+    return st;
+}
 
 NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan& p) {
     p.bits = bits;
@@ -119,34 +163,9 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.GS = (p.G + p.S - 1) / p.S;
     if (p.S > 1) p.GS = (p.GS + kBlockGroups - 1) / kBlockGroups * kBlockGroups;  // slabs on block edges
     p.U = (long long)p.RP * p.G;
-    p.CG = kChunkGroups;
-    p.tile_bytes = bits == 4 ? kQ4TileBytes : kQ5TileBytes;
-    p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
-    p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
-    p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
-    p.bar_bytes = 512;                           // barriers, flags, per-token range data
-    // Run hand-over buffers: kMaxRed if they fit without costing a pipeline stage against
-    // two, else two; spare buffers let the consumers run ahead of a split-K settle. The count
-    // is a multiple of kEpilogueWarps, so each buffer is always served by the same epilogue
-    // warp (two warps never wait on one buffer's barrier at once).
-    static_assert(kMaxRed % kEpilogueWarps == 0 && 2 % kEpilogueWarps == 0, "buffers per epilogue warp");
-    int st = 0;
-    for (int nr = kMaxRed; nr >= 2; nr -= 2) {
-        const int fixed = p.x_bytes + p.corr_bytes + nr * kRedBufBytes + p.bar_bytes;
-        int s2 = (kSmemLimit - fixed) / p.stage_bytes;
-        if (s2 > kMaxStages) s2 = kMaxStages;
-        const int fixed2 = p.x_bytes + p.corr_bytes + 2 * kRedBufBytes + p.bar_bytes;
-        int s_two = (kSmemLimit - fixed2) / p.stage_bytes;
-        if (s_two > kMaxStages) s_two = kMaxStages;
-        if (s2 == s_two || nr == 2) {
-            p.nred = nr;
-            st = s2;
-            break;
-        }
-    }
-    p.red_bytes = p.nred * kRedBufBytes;
-    p.stages = st;
-    p.smem_bytes = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes + st * p.stage_bytes;
+    p.cl = 1;
+    p.cl_bytes = 0;
+    const int st = plan_smem(p);
     // Grid. Stream-K over all SMs by default. One slab and row pairs that divide evenly
     // into k <= 4 per block (k = the fewest that fit the SMs): give each block whole pairs,
     // so no pair is split and no split-K settle (several L2 round trips at the end of a
@@ -169,8 +188,46 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
     p.Uq = (int)(p.U / p.P);
     p.Ur = (int)(p.U % p.P);
     p.slots = (long long)p.S * p.RP + p.P;
-    p.f16 = T <= NQ_F16_MAX_T ? 1 : 0;
     return st >= 2;
+}
+
+// Slab clusters (K split into S = 2..kMaxCluster slabs, bf16 operands): a thread-block
+// cluster of S blocks per range of work, block rank r taking slab r of every row pair in
+// the range, so each block stages one activation slab once and the S partial sums of a run
+// are added on chip (rank 0 gathers them through distributed shared memory) instead of
+// through the split-K workspace. p: the real plan (slab geometry, shared memory, P = C x S
+// blocks). q: the cluster-level plan, one virtual slab of GS groups with stream-K over the C
+// clusters; its segments, ticket counts and partial slots are those of the clusters, and a
+// virtual segment maps to rank r's real groups by rank_segment.
+NQ_HD bool make_cluster_plans(int bits, int mode, int T, int K, int N, int clusters, Plan& p, Plan& q) {
+    if (!make_plan(bits, mode, T, K, N, 1, p)) return false;
+    const int S = p.S;
+    if (S < 2 || S > kMaxCluster || clusters < 1 || p.f16) return false;
+    // Equal slabs on multiples of the consumer warp count (warp w consumes the groups that
+    // are w modulo kConsumerWarps from the slab start); never larger than the plain slabs.
+    int gs = (p.G + S - 1) / S;
+    gs = (gs + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+    if ((long long)(S - 1) * gs >= p.G || gs > p.GS) return false;
+    p.GS = gs;
+    p.cl = S;
+    p.cl_bytes = cluster_buffer_bytes(S);
+    if (plan_smem(p) < 2) return false;
+    q = p;
+    q.K = gs * kGroup;
+    q.G = gs;
+    q.S = 1;
+    q.GS = gs;
+    q.U = (long long)q.RP * gs;
+    q.P = (long long)clusters < q.U ? clusters : (int)q.U;
+    q.Uq = (int)(q.U / q.P);
+    q.Ur = (int)(q.U % q.P);
+    q.slots = (long long)q.RP + q.P;
+    p.P = q.P * S;
+    p.U = (long long)p.RP * p.G;
+    p.Uq = q.Uq;
+    p.Ur = q.Ur;
+    p.slots = q.slots;
+    return true;
 }
 
 NQ_HD int slab_groups(const Plan& p, int s) { return s < p.S - 1 ? p.GS : p.G - (p.S - 1) * p.GS; }
@@ -264,6 +321,18 @@ NQ_HD Segment seg_pick(const Plan& p, const SegOrder& o, int i, Segment& nat, lo
     return nat;
 }
 
+// Rank r's part of a cluster-level segment v (virtual groups [v.ga, v.gb) of one slab's
+// width): the same groups of slab r, clipped to that slab (the last slab may be shorter,
+// so the part may be empty).
+NQ_HD Segment rank_segment(const Plan& p, const Segment& v, int r) {
+    Segment sg = v;
+    const int gs = slab_groups(p, r);
+    sg.s = r;
+    sg.ga = r * p.GS + (v.ga < gs ? v.ga : gs);
+    sg.gb = r * p.GS + (v.gb < gs ? v.gb : gs);
+    return sg;
+}
+
 // A segment that covers its whole pair (one slab, all K groups) is the pair's only
 // contribution: its block writes the output directly.
 NQ_HD bool segment_complete(const Plan& p, const Segment& sg) {
@@ -355,6 +424,66 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
     while (!mbar_try_wait(bar, parity))
         if (global_timer_ns() - t0 > limit_ns) return false;
     return true;
+}
+
+// ---------------------------------------------------------------- cluster helpers
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_store_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Arrive on an mbarrier of another block of the cluster, releasing this thread's earlier
+// writes (and those it has observed) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase completed by other blocks of the cluster (acquire at cluster
+// scope). Same error behaviour as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  int* dev_err) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > (uint64_t)kWaitTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(dev_err, kDevErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Every thread of every block of the cluster (not .aligned: callers may have diverged).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

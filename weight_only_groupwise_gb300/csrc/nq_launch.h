@@ -14,9 +14,17 @@ cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
-template <int BITS, bool SWIGLU, bool F16, bool ONE>
+// Slab clusters of S blocks that can be resident at once for the slab-cluster
+// instantiation with `smem` bytes of shared memory per block (cudaOccupancyMaxActiveClusters);
+// 0 if none.
+int cluster_capacity_q4(int S, int smem);
+int cluster_capacity_q5(int S, int smem);
+int cluster_capacity_swiglu_q4(int S, int smem);
+int cluster_capacity_swiglu_q5(int S, int smem);
+
+template <int BITS, bool SWIGLU, bool F16, bool ONE, bool CLU>
 cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    auto kern = proj_kernel<BITS, SWIGLU, F16, ONE>;
+    auto kern = proj_kernel<BITS, SWIGLU, F16, ONE, CLU>;
     // The shared-memory opt-in is per device; set it on every launch of a new size class
     // (cheap: the driver caches it) rather than tracking devices here.
     static thread_local int set_for_device = -1;
@@ -32,21 +40,53 @@ cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = a.p.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (CLU) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = a.p.cl;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+template <int BITS, bool SWIGLU>
+int cluster_capacity_t(int S, int smem) {
+    auto kern = proj_kernel<BITS, SWIGLU, false, false, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // The operand type is part of the plan (a.p.f16): fp16 operands for small T, bf16 otherwise;
-// a single token has its own fp16 instantiation.
+// a single token has its own fp16 instantiation; slab clusters (a.p.cl > 1, bf16 only) theirs.
 template <int BITS, bool SWIGLU>
 cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    if (!a.p.f16) return launch_proj_t<BITS, SWIGLU, false, false>(a, stream, pdl);
-    return a.p.T == 1 ? launch_proj_t<BITS, SWIGLU, true, true>(a, stream, pdl)
-                      : launch_proj_t<BITS, SWIGLU, true, false>(a, stream, pdl);
+    if (a.p.cl > 1) return launch_proj_t<BITS, SWIGLU, false, false, true>(a, stream, pdl);
+    if (!a.p.f16) return launch_proj_t<BITS, SWIGLU, false, false, false>(a, stream, pdl);
+    return a.p.T == 1 ? launch_proj_t<BITS, SWIGLU, true, true, false>(a, stream, pdl)
+                      : launch_proj_t<BITS, SWIGLU, true, false, false>(a, stream, pdl);
 }
 
 }  // namespace nq

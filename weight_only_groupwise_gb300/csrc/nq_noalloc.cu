@@ -92,6 +92,7 @@ extern "C" nq_status nq_gemm_q4_noalloc(const void* X, const void* W, void* Y, i
     if (K == 0) return cudaMemsetAsync(Y, 0, yb, s) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
     ProjArgs a;
     if (!make_plan(4, 0, T, K, N, sms, a.p)) return NQ_ERR_SHAPE;
+    a.q = a.p;  // stream-K only (no slab clusters)
     if (a.p.slots > kStaticSlots || a.p.RP > kStaticTickets) return NQ_ERR_SCRATCH;
     uint8_t* base = static_cast<uint8_t*>(scratch);
     // The array keeps the previous call's contents: the error word and this call's tickets

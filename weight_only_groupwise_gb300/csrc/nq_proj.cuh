@@ -48,7 +48,9 @@ struct ProjArgs {
     float* partials;     // workspace: slots x kPartialFloats
     int* tickets;        // workspace: one per row pair, zero between calls
     int* dev_err;        // workspace: device error word
-    Plan p;
+    Plan p;              // the real plan (slab geometry, shared memory, grid)
+    Plan q;              // work split and split-K bookkeeping: p itself, or the cluster-level
+                         // plan of a slab-cluster launch (p.cl > 1)
 };
 
 // Named barriers: 1 = consumers only; 2 + b = run buffer b full (consumers arrive, the
@@ -183,7 +185,7 @@ __device__ __forceinline__ int red_index(int w, int m, int tok, int row) {
 }
 
 // ONE: a single token (T = 1), whose odd token columns need no scaling.
-template <int BITS, bool SWIGLU, bool F16, bool ONE>
+template <int BITS, bool SWIGLU, bool F16, bool ONE, bool CLU>
 __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
@@ -206,7 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     const long long row_tile_bytes = (long long)G * TBS;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cta = blockIdx.x;
+    // CLU: slab clusters of p.cl blocks; block rank crank takes slab crank of every run of
+    // cluster ccta, whose work split is q's. Otherwise q is p and ccta the block.
+    const Plan& q = CLU ? a.q : a.p;
+    const int crank = CLU ? (int)cluster_rank() : 0;
+    const int ccta = CLU ? (int)blockIdx.x / p.cl : (int)blockIdx.x;
 
     uint8_t* stage_mem = smem;
     uint8_t* xs = smem + nstages * kStageBytes;
@@ -219,11 +225,15 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     int* xmax = const_cast<int*>(flags) + 8;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
     const uint32_t x_bar = smem_u32(bars + 2 * kMaxStages);  // an activation slab has landed
+    // slab clusters: per epilogue warp, "the non-leading ranks' parts have arrived" (rank 0)
+    // and "rank 0 has read them" (other ranks); their partial runs land in cbuf of rank 0
+    const uint32_t cfull0 = smem_u32(bars + 40), cfree0 = smem_u32(bars + 40 + kEpilogueWarps);
+    float* cbuf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + p.bar_bytes);
     // zero row for ldmatrix lanes of absent tokens: the 16 bytes after the last X row
     const int pitch = x_pitch(GS);
     uint8_t* zero_row = xs + T * pitch;
 
-    const long long u0 = cta_begin(p, cta), u1 = cta_begin(p, cta + 1);
+    const long long u0 = cta_begin(q, ccta), u1 = cta_begin(q, ccta + 1);
     const SegOrder order = seg_order(p, u0, u1);
 
     if (tid == 0) {
@@ -232,6 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             mbar_init(empty0 + 8 * i, kConsumerWarps);
         }
         mbar_init(x_bar, 1);
+        if (CLU) {
+            for (int e = 0; e < kEpilogueWarps; ++e) {
+                mbar_init(cfull0 + 8 * e, p.cl - 1);
+                mbar_init(cfree0 + 8 * e, 1);
+            }
+        }
         flags[0] = 0;  // abort
         for (int t = 0; t < 8; ++t) xmax[t] = 0;
         *reinterpret_cast<uint4*>(zero_row) = make_uint4(0, 0, 0, 0);
@@ -243,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     // before they touch global memory. The producer streams the weights at once: no kernel
     // that writes them lets its dependents start early.
     grid_launch_dependents();
-    __syncthreads();
+    if constexpr (CLU)
+        cluster_sync_all();  // every block's barriers are initialised before any remote arrive
+    else
+        __syncthreads();
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -254,13 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             bool ok = true;
             Segment nat;
             for (int si = 0; si < order.count && ok; ++si) {
-                const Segment sg = seg_pick(p, order, si, nat, u1);
+                const Segment v = seg_pick(q, order, si, nat, u1);
+                const Segment sg = CLU ? rank_segment(p, v, crank) : v;
                 const int rt0 = SWIGLU ? sg.rp : 2 * sg.rp;
                 const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
                 const bool has1 = SWIGLU || rt1 < RT;
                 const uint8_t* w0 = a.W0 + rt0 * row_tile_bytes;
                 const uint8_t* w1 = a.W1 + rt1 * row_tile_bytes;
-                for (int b = sg.ga / BG; b * BG < sg.gb; ++b) {
+                for (int b = sg.ga / BG; sg.ga < sg.gb && b * BG < sg.gb; ++b) {
                     const int i0 = max(sg.ga - b * BG, 0), i1 = min(sg.gb - b * BG, BG);
                     const int nb = block_groups(b, G);
                     const bool whole = i0 == 0 && i1 == BG;   // implies nb == BG
@@ -304,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, 100000000ull);
             }
         }
+        if constexpr (CLU) cluster_sync_all();  // no block leaves while a peer may address it
         return;
     }
 
@@ -324,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         constexpr int JN8 = (SWIGLU ? 16 : 32) * kMaxTP / 32 > 0 ? (SWIGLU ? 16 : 32) * kMaxTP / 32 : 1;
         grid_dependency_wait();  // Y, partial sums and tickets may still be in the preceding kernel's use
         Segment nat;
+        int nrun = 0;  // runs this warp has exchanged within the cluster
         for (int si = 0; si < order.count; ++si) {
-            const Segment sg = seg_pick(p, order, si, nat, u1);
+            const Segment sg = seg_pick(q, order, si, nat, u1);  // cluster-level for CLU
             if ((si & 1) != ew) continue;
             const int b = si % nred;
             named_bar_sync(kBarRedFull + b, kHandoffThreads);
@@ -350,10 +372,52 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             // buffer b is read: hand it back for the run nred steps later
             if (si + nred < order.count) named_bar_arrive(kBarRedFree + b, kHandoffThreads);
             if (flags[0]) continue;
-            bool write = segment_complete(p, sg);
+            if constexpr (CLU) {
+                // Slab cluster: ranks 1..S-1 write their part of the run into rank 0's buffer
+                // for this warp and arrive on its barrier; rank 0 adds them in rank order and
+                // settles the run for the whole cluster. A rank writes its next part only
+                // after rank 0 has read the previous one.
+                const int S = p.cl;
+                const uint32_t fullb = cfull0 + 8 * ew, freeb = cfree0 + 8 * ew;
+                if (crank != 0) {
+                    if (nrun > 0 && !mbar_wait_cluster(freeb, (nrun - 1) & 1, flags, a.dev_err)) continue;
+                    const uint32_t dst =
+                        cluster_map(smem_u32(cbuf + (ew * (S - 1) + crank - 1) * kPartialFloats), 0);
+#pragma unroll
+                    for (int j = 0; j < JN8; ++j) {
+                        const int o = lane + 32 * j;
+                        if (o < nout) {
+                            cluster_store_f32(dst + 4 * o, v0[j]);
+                            if (SWIGLU) cluster_store_f32(dst + 4 * (128 + o), v1[j]);
+                        }
+                    }
+                    fence_acq_rel_cluster();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(cluster_map(fullb, 0));
+                    ++nrun;
+                    continue;
+                }
+                if (!mbar_wait_cluster(fullb, nrun & 1, flags, a.dev_err)) continue;
+                for (int r = 1; r < S; ++r) {
+                    const float* src = cbuf + (ew * (S - 1) + r - 1) * kPartialFloats;
+#pragma unroll
+                    for (int j = 0; j < JN8; ++j) {
+                        const int o = lane + 32 * j;
+                        if (o < nout) {
+                            v0[j] += src[o];
+                            if (SWIGLU) v1[j] += src[128 + o];
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    for (int r = 1; r < S; ++r) mbar_arrive_remote(cluster_map(freeb, r));
+                ++nrun;
+            }
+            bool write = segment_complete(q, sg);
             if (!write) {
                 // split-K run: publish the partial, take the ticket, reduce if last
-                float* ws = a.partials + slot_of(p, sg.s, sg.rp, cta) * kPartialFloats;
+                float* ws = a.partials + slot_of(q, sg.s, sg.rp, ccta) * kPartialFloats;
 #pragma unroll
                 for (int j = 0; j < JN8; ++j) {
                     const int o = lane + 32 * j;
@@ -366,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 int last = 0;
                 if (lane == 0) {
                     fence_acq_rel_gpu();  // the warp's partial stores before the ticket
-                    last = ticket_add(a.tickets + sg.rp) == contributions(p, sg.rp) - 1;
+                    last = ticket_add(a.tickets + sg.rp) == contributions(q, sg.rp) - 1;
                 }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
@@ -374,12 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     for (int j = 0; j < JN8; ++j) v0[j] = v1[j] = 0.f;
                     // Every contribution of the pair, summed in fixed (slab, block) order.
                     auto sum_in_order = [&]() {
-                        for (int s = 0; s < p.S; ++s) {
-                            const int gs = slab_groups(p, s);
-                            const long long r0 = slab_base(p, s) + (long long)sg.rp * gs;
-                            const int c_end = cta_of(p, r0 + gs - 1);
-                            for (int c = cta_of(p, r0); c <= c_end; ++c) {
-                                const float* src = a.partials + slot_of(p, s, sg.rp, c) * kPartialFloats;
+                        for (int s = 0; s < q.S; ++s) {
+                            const int gs = slab_groups(q, s);
+                            const long long r0 = slab_base(q, s) + (long long)sg.rp * gs;
+                            const int c_end = cta_of(q, r0 + gs - 1);
+                            for (int c = cta_of(q, r0); c <= c_end; ++c) {
+                                const float* src = a.partials + slot_of(q, s, sg.rp, c) * kPartialFloats;
 #pragma unroll
                                 for (int j = 0; j < JN8; ++j) {
                                     const int o = lane + 32 * j;
@@ -399,12 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         constexpr int kFix = 16, kBatch = 4, JN = SWIGLU ? 4 : 8;
                         int slots[kFix];
                         int nc = 0;
-                        for (int s = 0; s < p.S; ++s) {
-                            const int gs = slab_groups(p, s);
-                            const long long r0 = slab_base(p, s) + (long long)sg.rp * gs;
-                            const int c_end = cta_of(p, r0 + gs - 1);
-                            for (int c = cta_of(p, r0); c <= c_end; ++c) {
-                                if (nc < kFix) slots[nc] = (int)slot_of(p, s, sg.rp, c);
+                        for (int s = 0; s < q.S; ++s) {
+                            const int gs = slab_groups(q, s);
+                            const long long r0 = slab_base(q, s) + (long long)sg.rp * gs;
+                            const int c_end = cta_of(q, r0 + gs - 1);
+                            for (int c = cta_of(q, r0); c <= c_end; ++c) {
+                                if (nc < kFix) slots[nc] = (int)slot_of(q, s, sg.rp, c);
                                 ++nc;
                             }
                         }
@@ -453,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 }
             }
         }
+        if constexpr (CLU) cluster_sync_all();
         return;
     }
 
@@ -484,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     float tok_scale0 = 1.f, tok_scale1 = 1.f;
     Segment nat;
     for (int si = 0; si < order.count; ++si) {
-        const Segment sg = seg_pick(p, order, si, nat, u1);
+        const Segment v = seg_pick(q, order, si, nat, u1);
+        const Segment sg = CLU ? rank_segment(p, v, crank) : v;
         if (sg.s != cur_slab) {
             if (cur_slab >= 0)
                 named_bar_sync(kBarConsumers, kConsumerThreads);  // all done with the old slab
@@ -639,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         // never stored (the epilogue drops rows past N). One code path keeps the loop small
         // enough for the instruction cache.
         const int slab_g0 = sg.s * GS;
-        for (int b = sg.ga / BG; b * BG < sg.gb; ++b) {
+        for (int b = sg.ga / BG; sg.ga < sg.gb && b * BG < sg.gb; ++b) {
             const int i0 = max(sg.ga - b * BG, 0), i1 = min(sg.gb - b * BG, BG);
             const bool ok = mbar_wait(full0 + 8 * st, phase, flags, a.dev_err);
             if (ok) {
@@ -741,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         for (int j = 0; j < nstages; ++j) mbar_wait_drain(full0 + 8 * j, 1, 100000000ull);
         if (nx > 0) mbar_wait_drain(x_bar, (nx - 1) & 1, 100000000ull);
     }
+    if constexpr (CLU) cluster_sync_all();
 }
 
 }  // namespace nq

@@ -5,4 +5,5 @@ namespace nq {
 cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl) {
     return launch_proj<4, false>(a, stream, pdl);
 }
+int cluster_capacity_q4(int S, int smem) { return cluster_capacity_t<4, false>(S, smem); }
 }  // namespace nq

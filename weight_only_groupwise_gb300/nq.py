@@ -55,10 +55,13 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_info.argtypes = [I, I, I, I, I, I, P]
         L.nq_plan_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_segments.restype = ctypes.c_int64
+        L.nq_plan_cluster_info.argtypes = [I, I, I, I, I, I, P]
+        L.nq_plan_cluster_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
+        L.nq_plan_cluster_segments.restype = ctypes.c_int64
         for f in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_gemm_q4_noalloc", "nq_swiglu_q4",
                   "nq_swiglu_q5",
                   "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_reserve", "nq_device_error",
-                  "nq_plan_info"):
+                  "nq_plan_info", "nq_plan_cluster_info"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -205,6 +208,26 @@ def plan_segments(bits: int, mode: int, T: int, K: int, N: int, num_sms: int, ct
         _check(int(n))
     buf = (ctypes.c_int64 * (4 * max(n, 1)))()
     lib().nq_plan_segments(bits, mode, T, K, N, num_sms, cta, ctypes.cast(buf, ctypes.c_void_p), n)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+
+CLUSTER_KEYS = ("ctas", "cluster", "slab_groups", "pairs", "ws_slots", "stages", "cluster_units", "clusters")
+
+
+def plan_cluster_info(bits: int, mode: int, T: int, K: int, N: int, clusters: int) -> dict:
+    """The slab-cluster plan of a shape (host only); raises NqError if the shape has none."""
+    out = (ctypes.c_int64 * 8)()
+    _check(lib().nq_plan_cluster_info(bits, mode, T, K, N, clusters, ctypes.cast(out, ctypes.c_void_p)))
+    return dict(zip(CLUSTER_KEYS, list(out)))
+
+
+def plan_cluster_segments(bits: int, mode: int, T: int, K: int, N: int, clusters: int, cta: int):
+    """Real (slab, pair, ga, gb) runs of block `cta` of a slab-cluster plan, in order."""
+    n = lib().nq_plan_cluster_segments(bits, mode, T, K, N, clusters, cta, None, 0)
+    if n < 0:
+        _check(int(n))
+    buf = (ctypes.c_int64 * (4 * max(n, 1)))()
+    lib().nq_plan_cluster_segments(bits, mode, T, K, N, clusters, cta, ctypes.cast(buf, ctypes.c_void_p), n)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
 
