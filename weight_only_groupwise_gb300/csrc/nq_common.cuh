@@ -441,11 +441,16 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void cluster_store_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// 16-byte store into the shared memory of another block of the cluster that completes
+// 16 transaction bytes on that block's mbarrier `bar` once the data is there (no fence).
+__device__ __forceinline__ void cluster_store_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                                       uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+        "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+        "r"(bar)
+        : "memory");
 }
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Arrive on an mbarrier of another block of the cluster, releasing this thread's earlier
 // writes (and those it has observed) at cluster scope.

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         mbar_init(x_bar, 1);
         if (CLU) {
             for (int e = 0; e < kEpilogueWarps; ++e) {
-                mbar_init(cfull0 + 8 * e, p.cl - 1);
+                mbar_init(cfull0 + 8 * e, 1);  // rank 0's arrive with the expected bytes
                 mbar_init(cfree0 + 8 * e, 1);
             }
         }
@@ -373,40 +373,41 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             if (si + nred < order.count) named_bar_arrive(kBarRedFree + b, kHandoffThreads);
             if (flags[0]) continue;
             if constexpr (CLU) {
-                // Slab cluster: ranks 1..S-1 write their part of the run into rank 0's buffer
-                // for this warp and arrive on its barrier; rank 0 adds them in rank order and
-                // settles the run for the whole cluster. A rank writes its next part only
-                // after rank 0 has read the previous one.
+                // Slab cluster: ranks 1..S-1 store their part of the run into rank 0's buffer
+                // for this warp with st.async, which completes the transaction bytes on rank
+                // 0's barrier (armed by rank 0 for S-1 parts); rank 0 adds them in rank order
+                // and settles the run for the whole cluster. A rank stores its next part only
+                // after rank 0 has read the previous one. Layout of a part: [lane][8].
+                static_assert(JN8 <= 8 && (SWIGLU ? 2 * JN8 : JN8) <= 8, "one part: 8 values per lane");
                 const int S = p.cl;
                 const uint32_t fullb = cfull0 + 8 * ew, freeb = cfree0 + 8 * ew;
+                constexpr uint32_t kPartBytes = 32 * 8 * 4;
                 if (crank != 0) {
                     if (nrun > 0 && !mbar_wait_cluster(freeb, (nrun - 1) & 1, flags, a.dev_err)) continue;
-                    const uint32_t dst =
-                        cluster_map(smem_u32(cbuf + (ew * (S - 1) + crank - 1) * kPartialFloats), 0);
+                    float w[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) w[j] = 0.f;
 #pragma unroll
                     for (int j = 0; j < JN8; ++j) {
-                        const int o = lane + 32 * j;
-                        if (o < nout) {
-                            cluster_store_f32(dst + 4 * o, v0[j]);
-                            if (SWIGLU) cluster_store_f32(dst + 4 * (128 + o), v1[j]);
-                        }
+                        w[j] = v0[j];
+                        if (SWIGLU) w[JN8 + j] = v1[j];
                     }
-                    fence_acq_rel_cluster();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(cluster_map(fullb, 0));
+                    const uint32_t dst = cluster_map(
+                        smem_u32(cbuf + (ew * (S - 1) + crank - 1) * kPartialFloats + lane * 8), 0);
+                    const uint32_t rbar = cluster_map(fullb, 0);
+                    cluster_store_async_v4(dst, w[0], w[1], w[2], w[3], rbar);
+                    cluster_store_async_v4(dst + 16, w[4], w[5], w[6], w[7], rbar);
                     ++nrun;
                     continue;
                 }
+                if (lane == 0) mbar_arrive_expect_tx(fullb, (uint32_t)(S - 1) * kPartBytes);
                 if (!mbar_wait_cluster(fullb, nrun & 1, flags, a.dev_err)) continue;
                 for (int r = 1; r < S; ++r) {
-                    const float* src = cbuf + (ew * (S - 1) + r - 1) * kPartialFloats;
+                    const float* src = cbuf + (ew * (S - 1) + r - 1) * kPartialFloats + lane * 8;
 #pragma unroll
                     for (int j = 0; j < JN8; ++j) {
-                        const int o = lane + 32 * j;
-                        if (o < nout) {
-                            v0[j] += src[o];
-                            if (SWIGLU) v1[j] += src[128 + o];
-                        }
+                        v0[j] += src[j];
+                        if (SWIGLU) v1[j] += src[JN8 + j];
                     }
                 }
                 __syncwarp();
