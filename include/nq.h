@@ -218,10 +218,19 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
                          int64_t* seg, int64_t cap);
 
 /*
+ * nq_slab_clusters: turn slab clusters on (1) or off (0) for later projection calls of this
+ * process, or only query (-1); returns the previous setting. Off unless the environment
+ * variable NQ_CLUSTER is "1" at the first call. On GB300 a slab-cluster call is 8-23 %
+ * faster than the stream-K one when such calls follow each other, but was slower when it
+ * followed a different projection kernel under programmatic dependent launch, so it is
+ * opt-in. Not synchronised with calls in flight on other threads.
+ */
+int nq_slab_clusters(int enable);
+
+/*
  * nq_plan_cluster_info / nq_plan_cluster_segments: the same for a slab-cluster launch,
  * which the projection calls use (bf16 operands, T >= 3) when K needs 2..4 slabs, enough
- * thread-block clusters fit the device, and the environment variable NQ_CLUSTER is not "0"
- * at the first call. A cluster of S blocks takes a range of (row pair, slab-local group)
+ * thread-block clusters fit the device, and slab clusters are on (nq_slab_clusters). A cluster of S blocks takes a range of (row pair, slab-local group)
  * work; block rank r takes slab r of it, stages that activation slab once, and the S parts
  * of each run are added on chip by rank 0 (distributed shared memory) before the usual
  * split-K settle between clusters. Host only; no device needed.

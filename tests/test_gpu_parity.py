@@ -358,3 +358,38 @@ def test_activation_outlier_in_a_later_slab(nq, bits):
     for t in range(T):
         assert np.all(np.isfinite(y[t]))
         assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+
+
+SLAB_CLUSTER_SHAPES = [
+    # bits, T, K, N: two, three and four K slabs, a shorter last slab, SwiGLU pairs
+    (4, 8, 17408, 64), (5, 8, 17408, 48), (4, 3, 17408, 48), (5, 4, 17408, 32),
+    (4, 8, 6208, 80), (4, 8, 24576, 16),
+]
+
+
+@pytest.mark.parametrize("bits,T,K,N", SLAB_CLUSTER_SHAPES)
+def test_slab_cluster_parity(nq, bits, T, K, N):
+    """The slab-cluster launch (on for this test only) against the oracle."""
+    prev = nq.slab_clusters(1)
+    try:
+        seed = 300 + T + K // 64
+        if bits == 4:
+            p = si.q4_problem(T, K, N, seed)
+            w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), w, N))
+            y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+        else:
+            p = si.q5_problem(T, K, N, seed)
+            w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), w, N))
+            y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
+        assert gu.rel_err(y, y_ref) <= gu.TOL
+        s = si.swiglu_problem(T, K, 32, seed + 1)
+        wg = gu.pack_q4(nq, s["wg"], s["sg"], K, 32)
+        wu = gu.pack_q4(nq, s["wu"], s["su"], K, 32)
+        h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(s["x"]), wg, wu, 32))
+        g, u, _ = oracle.swiglu_q4(s["x"], s["wg"], s["sg"], s["wu"], s["su"], T, K, 32)
+        assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+        nq.device_error()
+    finally:
+        nq.slab_clusters(prev)

@@ -142,7 +142,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 bool g_pdl = true;
-bool g_cluster = true;
+bool g_cluster = false;
 bool g_env_read = false;
 
 size_t ws_tickets_off() { return 256; }
@@ -160,7 +160,7 @@ nq_status current_device(DevState** out, int* dev_out) {
         const char* e = std::getenv("NQ_PDL");
         if (e && e[0] == '0') g_pdl = false;
         const char* c = std::getenv("NQ_CLUSTER");
-        if (c && c[0] == '0') g_cluster = false;
+        if (c && c[0] == '1') g_cluster = true;
         g_env_read = true;
     }
     DevState& d = g_dev[dev];
@@ -503,6 +503,15 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
         ++n;
     }
     return n;
+}
+
+int nq_slab_clusters(int enable) {
+    DevState* d = nullptr;
+    current_device(&d, nullptr);  // reads the environment once, like every call
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int prev = g_cluster ? 1 : 0;
+    if (enable == 0 || enable == 1) g_cluster = enable == 1;
+    return prev;
 }
 
 nq_status nq_plan_cluster_info(int bits, int mode, int T, int K, int N, int clusters, int64_t out[8]) {

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_info.argtypes = [I, I, I, I, I, I, P]
         L.nq_plan_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_segments.restype = ctypes.c_int64
+        L.nq_slab_clusters.argtypes = [I]
+        L.nq_slab_clusters.restype = I
         L.nq_plan_cluster_info.argtypes = [I, I, I, I, I, I, P]
         L.nq_plan_cluster_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_cluster_segments.restype = ctypes.c_int64
@@ -209,6 +211,12 @@ def plan_segments(bits: int, mode: int, T: int, K: int, N: int, num_sms: int, ct
     buf = (ctypes.c_int64 * (4 * max(n, 1)))()
     lib().nq_plan_segments(bits, mode, T, K, N, num_sms, cta, ctypes.cast(buf, ctypes.c_void_p), n)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+
+def slab_clusters(enable: int = -1) -> int:
+    """Turn slab clusters on (1) / off (0) for later calls, or query (-1); returns the
+    previous setting."""
+    return int(lib().nq_slab_clusters(enable))
 
 
 CLUSTER_KEYS = ("ctas", "cluster", "slab_groups", "pairs", "ws_slots", "stages", "cluster_units", "clusters")
