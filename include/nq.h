@@ -44,7 +44,7 @@
  *     (different streams, no ordering) share it and race: order them on one stream.
  *   - Device-side waits are bounded; a wait that runs out sets a device error flag that
  *     nq_device_error reads.
- *   - nq_gemm_q4, nq_gemm_q5 and nq_swiglu_q4 launch with programmatic dependent launch:
+ *   - nq_gemm_q4, nq_gemm_q5, nq_swiglu_q4 and nq_swiglu_q5 launch with programmatic dependent launch:
  *     their kernel may start while the previous kernel on `stream` is finishing. It reads
  *     X and writes Y, H and its workspace only after that kernel has completed, but starts
  *     streaming the packed weights at once: the weights must not be written by a kernel
