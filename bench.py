@@ -355,7 +355,7 @@ def oracle_sample(w: dict, budget_s: float):
     import oracle
     import seeded_inputs as si
     if w["kind"] != "proj":
-        w = dict(kind="proj", bits=4, T=w.get("T", 8), K=5120, N=17408)
+        w = dict(kind="proj", bits=w.get("bits", 4), T=w.get("T", 8), K=5120, N=17408)
     bits, T, K, N = w["bits"], w["T"], w["K"], w["N"]
     p = si.q4_problem(T, K, N, 1) if bits == 4 else si.q5_problem(T, K, N, 2)
     rows_all = np.arange(N, dtype=np.int32)
