@@ -223,8 +223,8 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
  * variable NQ_CLUSTER is "1" at the first call. On GB300 a slab-cluster call is 8-23 %
  * faster than the stream-K one when such calls follow each other, but a slab-cluster launch
  * behind a different projection kernel under programmatic dependent launch started late
- * (with NQ_PDL=0 it was faster there too), so it is opt-in. Not synchronised with calls in
- * flight on other threads.
+ * (with NQ_PDL=0 it was faster there too), so slab-cluster launches go without dependent
+ * launch and the mode is opt-in. Not synchronised with calls in flight on other threads.
  */
 int nq_slab_clusters(int enable);
 

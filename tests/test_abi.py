@@ -108,3 +108,14 @@ def test_plan_info_matches_workloads(L):
     assert p["pairs"] == 1088
     p = nq.plan_info(5, 1, 8, 5120, 17408, 152)   # Q5 swiglu: same pairing, larger stages
     assert p["pairs"] == 1088 and p["stages"] >= 2
+
+
+def test_slab_cluster_switch(L):
+    """Query, set and restore the slab-cluster switch (host state only; no launch)."""
+    prev = L.nq_slab_clusters(-1)
+    assert prev in (0, 1)
+    assert L.nq_slab_clusters(1) == prev
+    assert L.nq_slab_clusters(-1) == 1
+    assert L.nq_slab_clusters(0) == 1
+    assert L.nq_slab_clusters(prev) == 0
+    assert L.nq_slab_clusters(-1) == prev
