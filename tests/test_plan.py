@@ -116,9 +116,9 @@ def test_cluster_partition_covers_every_unit_once(nq, bits, mode, T, K, N, clust
     assert 2 <= S <= 4 and gs % 8 == 0 and (S - 1) * gs < G <= S * gs
     assert info["ctas"] == info["clusters"] * S and info["clusters"] <= clusters
     assert info["stages"] >= 2
-    # the workspace reserved for the stream-K plan of the shape also holds the cluster plan's
-    # partial slots (nq_reserve sizes by stream-K plans)
-    assert info["ws_slots"] <= nq.plan_info(bits, mode, T, K, N, 152)["ws_slots"]
+    # split-K between clusters: one ticket per pair, one partial slot per (pair, cluster) run
+    # boundary, as a one-slab stream-K plan over the clusters
+    assert info["ws_slots"] == info["pairs"] + info["clusters"]
     covered = np.zeros((RP, G), np.int32)
     runs = {}
     for cta in range(info["ctas"]):

@@ -417,13 +417,19 @@ nq_status nq_reserve(int T_max, int K_max, int N_max) {
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
     long long slots = 0, tickets = 0;
-    // The largest plan over T <= T_max and both modes bounds every smaller call.
+    // The largest plan over T <= T_max and both modes bounds every smaller call; slab-cluster
+    // plans (at most SMs / S clusters) are counted as well.
     for (int T = 1; T <= T_max; ++T)
         for (int mode = 0; mode < 2; ++mode) {
+            const int K = K_max > 0 ? K_max : 64, N = N_max > 0 ? N_max : 16;
             Plan p;
-            make_plan(4, mode, T, K_max > 0 ? K_max : 64, N_max > 0 ? N_max : 16, d->sms, p);
+            make_plan(4, mode, T, K, N, d->sms, p);
             if (p.slots > slots) slots = p.slots;
             if (p.RP > tickets) tickets = p.RP;
+            Plan pc, qc;
+            if (p.S >= 2 && p.S <= kMaxCluster && make_cluster_plans(4, mode, T, K, N, d->sms / p.S, pc, qc) &&
+                qc.slots > slots)
+                slots = qc.slots;
         }
     return ensure_workspace(*d, slots, tickets);
 }
