@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     uint8_t* zero_row = xs + T * pitch;
 
     const long long u0 = cta_begin(q, ccta), u1 = cta_begin(q, ccta + 1);
-    const SegOrder order = seg_order(p, u0, u1);
+    const SegOrder order = seg_order(q, u0, u1);
 
     if (tid == 0) {
         for (int i = 0; i < nstages; ++i) {
