@@ -231,7 +231,7 @@ def build_step(nq, w: dict, dev, T_override=None):
         fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
 
         def step(i):
-            fn(x, copies[i % R], N, out=y)
+            fn(x, *copies[i % R], N, out=y)
         return step, b, R, f"rotate {R} packed weight copies ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     if w["kind"] == "swiglu":
         bits, T, K, N, Kd, Nd = w["bits"], T_override or w["T"], w["K"], w["N"], w["Kd"], w["Nd"]
@@ -248,8 +248,8 @@ def build_step(nq, w: dict, dev, T_override=None):
 
         def step(i):
             j = i % R
-            fused(x, gate[j], up[j], N, out=h)
-            fn(h, down[j], Nd, out=y)
+            fused(x, *gate[j], *up[j], N, out=h)
+            fn(h, *down[j], Nd, out=y)
         return step, b, R, f"rotate {R} weight sets ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     # layer stack: 64 independent layers, ~12 GB of packed weights (no reuse within a pass)
     T, L = T_override or w["T"], w["layers"]
@@ -273,18 +273,19 @@ def build_step(nq, w: dict, dev, T_override=None):
 
     def step(i):
         for ly in layers:
-            nq.swiglu_q4(x, ly["gate"], ly["up"], 17408, out=h)
-            nq.gemm_q4(h, ly["down"], 5120, out=yd)
-            nq.gemm_q5(x, ly["qg"], 6144, out=yq)
-            nq.gemm_q5(x, ly["kv"], 1024, out=ykv)
-            nq.gemm_q5(x6, ly["out"], 5120, out=yo)
+            nq.swiglu_q4(x, *ly["gate"], *ly["up"], 17408, out=h)
+            nq.gemm_q4(h, *ly["down"], 5120, out=yd)
+            nq.gemm_q5(x, *ly["qg"], 6144, out=yq)
+            nq.gemm_q5(x, *ly["kv"], 1024, out=ykv)
+            nq.gemm_q5(x6, *ly["out"], 5120, out=yo)
     w2 = dict(w, T=T)
     return step, workload_bytes(w2), 1, "64 distinct layers (~12 GB) per pass, no reuse", (x, y)
 
 
-def time_graph(step, steps: int, warmup: int, stream, soak_s: float = 0.0):
+def time_graph(step, steps: int, warmup: int, stream, soak_s: float = 0.0, reps: int = 5):
     """Eager warm-up, capture `steps` steps into one CUDA graph, replay it untimed (and for
-    `soak_s` seconds), then time one replay with events. Returns milliseconds."""
+    `soak_s` seconds), then time `reps` replays, each bracketed by CUDA events on the
+    launching stream. Returns the list of replay times in milliseconds."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -300,13 +301,17 @@ def time_graph(step, steps: int, warmup: int, stream, soak_s: float = 0.0):
     while time.time() < t_end:
         g.replay()
         torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        g.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    return start.elapsed_time(end)
+    out = []
+    for _ in range(reps):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            g.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        out.append(start.elapsed_time(end))
+    del g
+    return out
 
 
 def time_e2e(nq, w: dict, steps: int, warmup: int, stream, dev):
@@ -328,7 +333,7 @@ def time_e2e(nq, w: dict, steps: int, warmup: int, stream, dev):
 
     def step(i):
         xd.copy_(xs[i % 4], non_blocking=True)
-        fn(xd, copies[i % R], N, out=yd)
+        fn(xd, *copies[i % R], N, out=yd)
         ys[i % 4].copy_(yd, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -401,7 +406,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work")
     ap.add_argument("--soak", type=float, default=1.0,
-                    help="seconds of untimed graph replays before the timed one (clock sampling)")
+                    help="seconds of untimed graph replays before the timed ones (clock sampling)")
+    ap.add_argument("--reps", type=int, default=5, help="timed replays of the K-step graph (median reported)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -455,8 +461,8 @@ def main():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
-        ms = time_graph(step, args.steps, warmup, stream, soak_s=args.soak)
-    ms = max_over_ranks(ms, dev)
+        reps = time_graph(step, args.steps, warmup, stream, soak_s=args.soak, reps=args.reps)
+    ms = max_over_ranks(statistics.median(reps), dev)
     nq.device_error()
     ms_step = ms / args.steps
     value = job_rate_gbs(bytes_step, ms_step, world)
@@ -475,7 +481,11 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(args.workload)},
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": launches * args.steps * args.reps,
+        "spread": {"replays": args.reps, "statistic": "median",
+                   "us_per_step_min": round(1e3 * min(reps) / args.steps, 3),
+                   "us_per_step_median": round(1e3 * statistics.median(reps) / args.steps, 3),
+                   "us_per_step_max": round(1e3 * max(reps) / args.steps, 3)},
         "clocks": clk.summary(),
     }
     if not args.no_e2e and w["kind"] == "proj":
@@ -497,32 +507,50 @@ def main():
 
 
 def sweep(nq, dev, stream, peak):
-    """µs/call and GB/s of the other shapes at T = 1, 2, 4, 8 (context, not the headline)."""
+    """µs/call and GB/s of the other shapes (context, not the headline): the decode Q4 and
+    verify Q5 projections at every T = 1..8 (one weight set per shape, reused across T), the
+    Q4 and Q5 SwiGLU blocks at T=8 and the 64-layer stack at T = 1 and 8. Each entry is the
+    median of 5 timed graph replays."""
     import torch
     out = []
-    items = [("decode_q4", T) for T in (1, 2, 4, 8)] + [("verify_q5", T) for T in (1, 2, 4, 8)] + \
-            [("swiglu_block", 8), ("swiglu_block_q5", 8)]
-    for name, T in items:
-        w = dict(WORKLOADS[name], T=T)
-        step, b, R, note, keep = build_step(nq, w, dev)
-        steps = 100
-        ms = time_graph(step, steps, 5, stream)
-        us = 1e3 * ms / steps
+
+    def record(name, T, reps, steps, b, launches):
+        us = 1e3 * statistics.median(reps) / steps
         gbs = b / (us * 1e-6) / 1e9
         out.append({"workload": name, "T": T, "us_per_step": round(us, 3),
-                    "calls_per_step": launches_per_step(w), "GB_s": round(gbs, 1),
-                    "frac": round(gbs / peak, 4)})
+                    "us_min": round(1e3 * min(reps) / steps, 3), "us_max": round(1e3 * max(reps) / steps, 3),
+                    "calls_per_step": launches, "GB_s": round(gbs, 1), "frac": round(gbs / peak, 4)})
+
+    import seeded_inputs as si
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(777)
+    for name in ("decode_q4", "verify_q5"):
+        w = WORKLOADS[name]
+        bits, K, N = w["bits"], w["K"], w["N"]
+        R = max(2, -(-3 * L2_BYTES // proj_bytes(bits, 8, K, N)))
+        copies = make_proj_copies(nq, bits, K, N, R, 1 if bits == 4 else 2, dev)
+        fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
+        for T in range(1, 9):
+            x = si.device_activations(T, K, gen, dev)
+            y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+
+            def step(i, x=x, y=y):
+                fn(x, *copies[i % R], N, out=y)
+            steps = 100
+            record(name, T, time_graph(step, steps, 5, stream), steps, proj_bytes(bits, T, K, N), 1)
+        del copies
+        torch.cuda.empty_cache()
+    for name in ("swiglu_block", "swiglu_block_q5"):
+        w = dict(WORKLOADS[name], T=8)
+        step, b, R, note, keep = build_step(nq, w, dev)
+        steps = 100
+        record(name, 8, time_graph(step, steps, 5, stream), steps, b, launches_per_step(w))
         del step, keep
         torch.cuda.empty_cache()
     for T in (1, 8):
         w = dict(WORKLOADS["layer_stack"], T=T)
         step, b, R, note, keep = build_step(nq, w, dev)
-        ms = time_graph(step, 2, 1, stream)
-        us = 1e3 * ms / 2
-        gbs = b / (us * 1e-6) / 1e9
-        out.append({"workload": "layer_stack", "T": T, "us_per_step": round(us, 1),
-                    "calls_per_step": launches_per_step(w), "GB_s": round(gbs, 1),
-                    "frac": round(gbs / peak, 4)})
+        record("layer_stack", T, time_graph(step, 2, 1, stream), 2, b, launches_per_step(w))
         del step, keep
         torch.cuda.empty_cache()
     return out

@@ -21,11 +21,14 @@
  *   Wh   uint32 [N][K/32]  Q5 high bits: bit i of word j is bit 4 of q[n, 32j+i]
  *   S    fp16   [N][K/64]  one scale per (output row n, 64-wide group of K)
  *
- * Packed layout: nq_pack_* rewrites the canonical codes and scales into ONE opaque,
- * kernel-friendly buffer: tiles of 16 output rows x one 64-wide K group, in blocks of 32
- * groups per row tile, each block holding its codes followed by its scales, so one bulk copy
- * fetches both. Its size depends only on (bits, K, N), is exactly codes + scales (no padding,
- * no header) and is given by nq_packed_bytes_*. The projection calls take the packed form.
+ * Packed layout: nq_pack_* rewrites the canonical codes and scales into two kernel-friendly
+ * buffers, the packed codes Wq and the packed scales S: both are cut into tiles of 16 output
+ * rows x one 64-wide K group, stored row-tile-major and contiguous along K; inside a tile the
+ * codes are in the order of the tensor-core MMA operand fragments and the 16 scales in the
+ * order the fragments' rows use them. Sizes depend only on (bits, K, N) and are exactly the
+ * code bytes (nq_packed_bytes_*) and the scale bytes (nq_scale_bytes): no padding, no header.
+ * The projection calls take the packed pair (Wq, S); the pages name neither layout, so both
+ * are this library's definition.
  *
  * Conventions for every call:
  *   - Pointers are DEVICE pointers on the current CUDA device, owned by the caller; the
@@ -42,8 +45,8 @@
  *     synchronises the device and must not be made during stream capture. nq_reserve
  *     allocates it ahead of time. Projection calls that overlap in time on one device
  *     (different streams, no ordering) share it and race: order them on one stream.
- *   - Device-side waits are bounded; a wait that runs out sets a device error flag that
- *     nq_device_error reads.
+ *   - Device-side waits are bounded (2 s by default, see nq_wait_limit); a wait that runs
+ *     out sets a device error flag that nq_device_error reads.
  *   - nq_gemm_q4, nq_gemm_q5, nq_swiglu_q4 and nq_swiglu_q5 launch with programmatic dependent launch:
  *     their kernel may start while the previous kernel on `stream` is finishing. It reads
  *     X and writes Y, H and its workspace only after that kernel has completed, but starts
@@ -84,74 +87,89 @@ int nq_version(void);
 
 /* ---------------------------------------------------------------- packed sizes */
 
-/* Bytes of a packed Q4 weight (codes and scales): K*N/2 + 2*N*(K/64). 0 on a bad shape. */
+/* Bytes of the packed Q4 codes Wq: K*N/2. 0 on a bad shape (K % 64 or N % 16 nonzero). */
 size_t nq_packed_bytes_q4(int K, int N);
-/* Bytes of a packed Q5 weight (nibble plane, high plane, scales): 5*K*N/8 + 2*N*(K/64). */
+/* Bytes of the packed Q5 codes Wq (nibble plane and high plane): 5*K*N/8. 0 on a bad shape. */
 size_t nq_packed_bytes_q5(int K, int N);
+/* Bytes of the packed scales S (Q4 or Q5): 2*N*(K/64), the same as the canonical scales. */
+size_t nq_scale_bytes(int K, int N);
 
 /* ---------------------------------------------------------------- offline repack */
 
 /*
- * nq_pack_q4: canonical Q4 codes and scales -> packed weight (one-off, "offline repack").
- *   wq_canon  device uint32 [N][K/8]     canonical codes
- *   s_canon   device fp16   [N][K/64]    canonical scales (bit patterns)
- *   packed    device, nq_packed_bytes_q4(K, N) bytes, written
- * Pure bit permutation: nq_dequant_q4_debug(packed) reproduces the canonical weights.
+ * nq_pack_q4: canonical Q4 codes and scales -> packed pair (one-off "offline repack").
+ *   wq_canon   device uint32 [N][K/8]     canonical codes
+ *   s_canon    device fp16   [N][K/64]    canonical scales (bit patterns)
+ *   wq_packed  device, nq_packed_bytes_q4(K, N) bytes, written (packed codes)
+ *   s_packed   device, nq_scale_bytes(K, N) bytes, written (packed scales)
+ * Pure bit permutation: nq_dequant_q4_debug(wq_packed, s_packed) reproduces the canonical
+ * weights. Outputs must not overlap the inputs or each other (NQ_ERR_ALIAS).
  */
-nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* packed,
-                     void* stream);
+nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* wq_packed,
+                     void* s_packed, void* stream);
 
 /* nq_pack_q5: as nq_pack_q4 for 5-bit codes given as nibble plane wn_canon [N][K/8] and
- * high plane wh_canon [N][K/32]; packed holds nq_packed_bytes_q5(K, N) bytes. */
+ * high plane wh_canon [N][K/32]; wq_packed holds nq_packed_bytes_q5(K, N) bytes. */
 nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon,
-                     int K, int N, void* packed, void* stream);
+                     int K, int N, void* wq_packed, void* s_packed, void* stream);
 
 /* ---------------------------------------------------------------- projections */
 
 /*
- * nq_gemm_q4: Y = X * dequant(W) for 4-bit codes, 1 <= T <= 8 tokens.
- *   X  device bf16 [T][K];  W packed by nq_pack_q4 (codes and scales);
- *   Y  device bf16 [T][N], written.
+ * nq_gemm_q4: Y = X * dequant(Wq, S) for 4-bit codes, 1 <= T <= 8 tokens.
+ *   X   device bf16 [T][K]
+ *   Wq  device packed codes, S device packed fp16 scales (both from nq_pack_q4)
+ *   Y   device bf16 [T][N], written
  * Accumulation is fp32; Y is rounded once to bf16. Results are deterministic for a given
  * device (the split of K across thread blocks depends only on shape and SM count).
  */
-nq_status nq_gemm_q4(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
+nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                     void* stream);
 
 /*
  * nq_gemm_q4_noalloc: nq_gemm_q4 for callers that cannot allocate device memory. The pages
  * have no counterpart; this is a library convenience.
  *
  * nq_gemm_q4 allocates its split-K scratch with cudaMalloc the first time a shape needs it.
- * Code running during CUDA graph capture, plug-ins whose host framework owns all device
- * memory, and processes on a fixed memory budget cannot allow that. This call computes the
+ * Plug-ins whose host framework owns all device memory, and processes that must stay within
+ * a fixed memory budget once serving has started (where a late allocation can fail, or
+ * stall the device while it synchronises), cannot allow that. This call computes the
  * same Y with the same kernel but keeps its scratch in a fixed array of about 2.1 MB that
  * the library holds in every device's memory until the process exits; it calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *   Arguments, layouts, alignment and results: as nq_gemm_q4.
- *   Limit: the split-K plan must fit 2048 partial slots and 4096 tickets (for T <= 4 and
- *   K <= 24576 that is N up to about 60000); larger problems return NQ_ERR_SCRATCH before
- *   anything is launched.
+ *   Limit: the call's work split needs S*ceil(N/32) + P <= 2048 partial slots and
+ *   ceil(N/32) <= 4096 tickets, where S is the number of K slabs and P the number of thread
+ *   blocks (nq_plan_info out[2] and out[0]; P <= the SM count). K fits one slab up to
+ *   K = 49152 at T = 1, 24576 at T = 2, 16384 at T = 3, 12288 at T = 4, 8192 at T = 5..6 and
+ *   6144 at T = 7..8; there, on a 152-SM GB300, N may be up to 60672. Each further slab
+ *   divides the room: e.g. T = 8, K = 17408 (three slabs) allows N <= 20224. Larger
+ *   problems return NQ_ERR_SCRATCH before anything is launched.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *   with that device current; make that first call before any stream capture.
- *   Every call clears the part of the array that must start at zero (error word, tickets)
- *   on its own stream, then launches. All calls share the one array: calls that overlap on
- *   the GPU (unordered streams) race and give wrong results; order them on one stream.
+ *   Every call clears the tickets it uses on its own stream, then launches. All calls share
+ *   the one array: calls that overlap on the GPU (unordered streams) race and give wrong
+ *   results; order them on one stream.
+ *   A bounded wait that runs out inside this call's kernel sets the array's own error word;
+ *   it stays set until nq_device_error reports it (as NQ_ERR_TIMEOUT) and clears it.
  */
-nq_status nq_gemm_q4_noalloc(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
+nq_status nq_gemm_q4_noalloc(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                             void* stream);
 
 /* nq_gemm_q5: as nq_gemm_q4 for 5-bit codes packed by nq_pack_q5 (z = 16). */
-nq_status nq_gemm_q5(const void* X, const void* W, void* Y, int T, int K, int N, void* stream);
+nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
+                     void* stream);
 
 /*
  * nq_swiglu_q4: fused gate/up projection of the SwiGLU MLP ("NInfer-4090" release post,
  * section "V3 做了什么", SwiGLU path at T=8):
- *   g = X * dequant(Wg),  u = X * dequant(Wu)   (each [T][N], fp32 accumulation)
+ *   g = X * dequant(Wg, Sg),  u = X * dequant(Wu, Su)   (each [T][N], fp32 accumulation)
  *   H = bf16(silu(g) * u),    silu(g) = g / (1 + exp(-g)) in fp32
- *   X device bf16 [T][K]; Wg and Wu packed by nq_pack_q4 (K x N each);
+ *   X device bf16 [T][K]; (Wg, Sg) and (Wu, Su) packed by nq_pack_q4 (K x N each);
  *   H device bf16 [T][N], written. The down projection is nq_gemm_q4 on H.
  */
-nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N,
-                       void* stream);
+nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su,
+                       void* H, int T, int K, int N, void* stream);
 
 /*
  * nq_swiglu_q5: as nq_swiglu_q4 for 5-bit gate and up weights packed by nq_pack_q5
@@ -160,20 +178,30 @@ nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, i
  * small-batch path). Same arguments, layouts, ownership and errors; the down projection is
  * nq_gemm_q4 or nq_gemm_q5 on H.
  */
-nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N,
-                       void* stream);
+nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su,
+                       void* H, int T, int K, int N, void* stream);
 
 /* ---------------------------------------------------------------- debug dumps */
 
 /*
- * nq_dequant_q4_debug: decodes the PACKED weight with the projection kernels' own decode
- * and writes out[n][k] = (float)s * (float)(q - 8) in fp32, canonical order [N][K].
- * The value is exact, so it must equal the CPU definition bit for bit.
+ * nq_dequant_q4_debug: decodes the PACKED pair (Wq, S) with the decoder of the T <= 2
+ * projection kernels (fp16 operands: a code q becomes 1024 + q, or 1024 + 16 q at the upper
+ * half of each 16-wide K step) and writes out[n][k] = (float)s * (float)(q - 8) in fp32,
+ * canonical order [N][K]. The value is exact, so it must equal the CPU definition bit for bit.
  */
-nq_status nq_dequant_q4_debug(const void* W, float* out, int K, int N, void* stream);
+nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* out, int K, int N, void* stream);
 
-/* nq_dequant_q5_debug: as above for a Q5 packed weight (z = 16). */
-nq_status nq_dequant_q5_debug(const void* W, float* out, int K, int N, void* stream);
+/* nq_dequant_q5_debug: as above for a Q5 packed pair (z = 16). */
+nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* out, int K, int N, void* stream);
+
+/*
+ * nq_dequant_q4_debug_bf16 / nq_dequant_q5_debug_bf16: the same dump through the decoder of
+ * the T >= 3 projection kernels (bf16 operands: every code q becomes 128 + q). Same
+ * arguments and result; the two decoders must agree with each other and with the CPU
+ * definition bit for bit.
+ */
+nq_status nq_dequant_q4_debug_bf16(const void* Wq, const void* S, float* out, int K, int N, void* stream);
+nq_status nq_dequant_q5_debug_bf16(const void* Wq, const void* S, float* out, int K, int N, void* stream);
 
 /* ---------------------------------------------------------------- runtime */
 
@@ -186,11 +214,23 @@ nq_status nq_reserve(int T_max, int K_max, int N_max);
 
 /*
  * nq_device_error: synchronise the current device, then report and clear the device-side
- * error flag of its workspace: NQ_OK, or NQ_ERR_TIMEOUT if a bounded wait inside a kernel
- * ran out since the last check (that call's outputs are then undefined). Clears the
- * split-K tickets as well, so later calls start clean.
+ * error flags of its workspace and of nq_gemm_q4_noalloc's fixed scratch: NQ_OK, or
+ * NQ_ERR_TIMEOUT if a bounded wait inside a kernel ran out since the last check (that
+ * call's outputs are then undefined). Clears the split-K tickets as well, so later calls
+ * start clean.
  */
 nq_status nq_device_error(void);
+
+/*
+ * nq_wait_limit: the bound, in nanoseconds, of every device-side wait of later projection
+ * calls (a pipeline stage, an activation slab, a cluster peer). ns > 0 sets it; ns <= 0 only
+ * queries. Returns the previous bound. Default 2 s, or the environment variable NQ_WAIT_NS
+ * read at the first call. A wait that runs out aborts its thread block (its outputs are
+ * undefined, nq_device_error reports NQ_ERR_TIMEOUT) after the block has waited, on a
+ * separate fixed bound, for the copies it already issued. A bound far below a kernel's run
+ * time makes calls abort: that is how the tests reach this path.
+ */
+long long nq_wait_limit(long long ns);
 
 /* nq_shutdown: free every device workspace of this process (synchronises each device). */
 void nq_shutdown(void);

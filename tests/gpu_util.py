@@ -42,3 +42,23 @@ def sample_rows(N: int, count: int, seed: int) -> np.ndarray:
     fixed = [0, 7, 8, 15, 16, N // 2, N - 17, N - 16, N - 9, N - 1]
     rnd = g.choice(N, size=min(count, N), replace=False)
     return np.unique(np.clip(np.concatenate([fixed, rnd]), 0, N - 1)).astype(np.int32)
+
+
+def expect_timeout(nq, call, tries=5):
+    """Run `call` with a 1 ns wait bound until nq_device_error reports a timeout (a block
+    whose every wait is satisfied at the first look cannot time out, so allow a few tries)."""
+    import pytest
+    from weight_only_groupwise_gb300.nq import NqError
+    for _ in range(tries):
+        prev = nq.wait_limit(1)
+        try:
+            call()
+        finally:
+            nq.wait_limit(prev)
+        try:
+            nq.device_error()
+        except NqError as e:
+            assert e.status == -7, e
+            nq.device_error()          # reported once, then clear
+            return
+    pytest.fail("no bounded wait ran out with a 1 ns bound")

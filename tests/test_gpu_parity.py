@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path (called through the C ABI) against the fp64 CPU oracle on the
-same seeded inputs. Dequantised weights must match bit for bit; outputs within
-max|y - y_ref| / max|y_ref| <= 5e-3 (the bf16 output rounding alone is up to 2^-9 relative)."""
+same seeded inputs. Dequantised weights must match bit for bit, through both decoders the
+kernels use; outputs within max|y - y_ref| / max|y_ref| <= 5e-3. The bf16 output rounding
+alone is up to 2^-8 (3.9e-3) relative to |y| (8 significant bits, half an ulp of 2^-7), so
+the bound leaves about 1.1e-3 for fp32 accumulation in any order, where ~1e-6 is expected."""
 import numpy as np
 import pytest
 import torch
@@ -26,31 +28,68 @@ def nq():
 DEQ_SHAPES = [(256, 128, 0), (192, 48, 1), (64, 16, 2), (640, 272, 3), (5120, 6144, 4)]
 
 
+def _dequant_case(nq, bits, operands, K, N, seed):
+    if bits == 4:
+        p = si.q4_problem(1, K, N, seed)
+        w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+        w_gpu = nq.dequant_q4_debug(*w, K, N, operands=operands).cpu().numpy()
+        w_ref = oracle.dequant_q4(p["wq"], p["s"], K, N)
+    else:
+        p = si.q5_problem(1, K, N, seed)
+        w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+        w_gpu = nq.dequant_q5_debug(*w, K, N, operands=operands).cpu().numpy()
+        w_ref = oracle.dequant_q5(p["wn"], p["wh"], p["s"], K, N)
+    assert w_gpu.shape == w_ref.shape
+    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+
+
+# Both decoders: fp16 operands (the T <= 2 kernels: 1024 + q / 1024 + 16 q) and bf16
+# operands (the T >= 3 kernels: 128 + q), each dumped through the same decode routine the
+# projection kernels call, compared bit for bit with the CPU definition.
+@pytest.mark.parametrize("operands", ["f16", "bf16"])
+@pytest.mark.parametrize("bits", [4, 5])
 @pytest.mark.parametrize("K,N,seed", DEQ_SHAPES)
-def test_dequant_q4_bit_exact(nq, K, N, seed):
-    p = si.q4_problem(1, K, N, seed)
-    w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-    w_gpu = nq.dequant_q4_debug(w, K, N).cpu().numpy()
-    w_ref = oracle.dequant_q4(p["wq"], p["s"], K, N)
-    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+def test_dequant_bit_exact(nq, bits, operands, K, N, seed):
+    _dequant_case(nq, bits, operands, K, N, seed)
 
 
-@pytest.mark.parametrize("K,N,seed", DEQ_SHAPES)
-def test_dequant_q5_bit_exact(nq, K, N, seed):
-    p = si.q5_problem(1, K, N, seed)
-    w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-    w_gpu = nq.dequant_q5_debug(w, K, N).cpu().numpy()
-    w_ref = oracle.dequant_q5(p["wn"], p["wh"], p["s"], K, N)
-    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+# the full decode / verify weight shapes (K=5120 with N=17408 Q4 and N=6144 Q5)
+@pytest.mark.parametrize("operands", ["f16", "bf16"])
+@pytest.mark.parametrize("bits,K,N,seed", [(4, 5120, 17408, 1), (5, 5120, 6144, 2)])
+def test_dequant_bit_exact_full_size(nq, bits, operands, K, N, seed):
+    _dequant_case(nq, bits, operands, K, N, seed)
 
 
-def test_dequant_full_size_decode_q4(nq):
-    c = si.DECODE_Q4
-    p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
-    w = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
-    w_gpu = nq.dequant_q4_debug(w, c["K"], c["N"]).cpu().numpy()
-    w_ref = oracle.dequant_q4(p["wq"], p["s"], c["K"], c["N"])
-    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+def test_dequant_every_code_both_decoders(nq):
+    """Every code value at every position of a tile: codes cycle through 0..15 (Q4) and
+    0..31 (Q5) with the high plane driven by bit 4, so each nibble slot, each high-bit
+    position and each K step of the fragment layout sees every value, under scales that
+    include fp16 subnormals, the largest finite fp16 and negative values."""
+    K, N = 256, 32
+    k = np.arange(K)
+    n = np.arange(N)[:, None]
+    q4 = (k[None, :] + 3 * n) % 16
+    q5 = (k[None, :] * 7 + 5 * n) % 32
+    wq = np.zeros((N, K // 8), np.uint32)
+    wn = np.zeros((N, K // 8), np.uint32)
+    wh = np.zeros((N, K // 32), np.uint32)
+    for i in range(8):
+        wq |= (q4[:, i::8].astype(np.uint32) << np.uint32(4 * i))
+        wn |= ((q5[:, i::8] & 15).astype(np.uint32) << np.uint32(4 * i))
+    for i in range(32):
+        wh |= ((q5[:, i::32] >> 4).astype(np.uint32) << np.uint32(i))
+    scale_bits = np.array([0x0001, 0x03FF, 0x0400, 0x3C00, 0x7BFF, 0xBC00, 0x8001, 0x2E66], np.uint16)
+    s = scale_bits[(np.arange(N)[:, None] + np.arange(K // 64)[None, :]) % len(scale_bits)]
+    s = np.ascontiguousarray(s)
+    ref4 = oracle.dequant_q4(wq, s, K, N)
+    ref5 = oracle.dequant_q5(wn, wh, s, K, N)
+    w4 = gu.pack_q4(nq, wq, s, K, N)
+    w5 = gu.pack_q5(nq, wn, wh, s, K, N)
+    for operands in ("f16", "bf16"):
+        g4 = nq.dequant_q4_debug(*w4, K, N, operands=operands).cpu().numpy()
+        g5 = nq.dequant_q5_debug(*w5, K, N, operands=operands).cpu().numpy()
+        assert np.array_equal(g4.view(np.uint32), ref4.view(np.uint32)), operands
+        assert np.array_equal(g5.view(np.uint32), ref5.view(np.uint32)), operands
 
 
 # ---------------------------------------------------------------- projections, small/ragged
@@ -68,7 +107,7 @@ GEMM_SHAPES = [
 def test_gemm_q4_parity(nq, T, K, N, seed):
     p = si.q4_problem(T, K, N, seed)
     wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, N))
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *wq, N))
     y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
     assert gu.rel_err(y, y_ref) <= gu.TOL
 
@@ -77,7 +116,7 @@ def test_gemm_q4_parity(nq, T, K, N, seed):
 def test_gemm_q5_parity(nq, T, K, N, seed):
     p = si.q5_problem(T, K, N, seed + 100)
     wq = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, N))
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), *wq, N))
     y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
     assert gu.rel_err(y, y_ref) <= gu.TOL
 
@@ -87,11 +126,11 @@ def test_gemm_every_T(nq, T):
     K, N = 1536, 208
     p = si.q4_problem(T, K, N, 50 + T)
     wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, N))
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *wq, N))
     assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)) <= gu.TOL
     q = si.q5_problem(T, K, N, 60 + T)
     wq5 = gu.pack_q5(nq, q["wn"], q["wh"], q["s"], K, N)
-    y5 = gu.host_f64(nq.gemm_q5(gu.dev_bf16(q["x"]), wq5, N))
+    y5 = gu.host_f64(nq.gemm_q5(gu.dev_bf16(q["x"]), *wq5, N))
     assert gu.rel_err(y5, oracle.gemm_q5(q["x"], q["wn"], q["wh"], q["s"], T, K, N)) <= gu.TOL
 
 
@@ -103,7 +142,7 @@ def test_swiglu_q4_parity(nq, T, K, N, seed):
     p = si.swiglu_problem(T, K, N, seed)
     wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
     wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
-    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, wu, N))
+    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), *wg, *wu, N))
     g, u, h_ref_bits = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
     h_exact = g / (1.0 + np.exp(-g)) * u
     assert gu.rel_err(h, h_exact) <= gu.TOL
@@ -116,7 +155,7 @@ SWIGLU_Q5_SHAPES = [(8, 256, 48, 0), (1, 640, 16, 1), (2, 1024, 272, 2), (4, 174
 def _swiglu_q5_dev(nq, p, T, K, N):
     wg = gu.pack_q5(nq, p["wgn"], p["wgh"], p["sg"], K, N)
     wu = gu.pack_q5(nq, p["wun"], p["wuh"], p["su"], K, N)
-    return nq.swiglu_q5(gu.dev_bf16(p["x"]), wg, wu, N)
+    return nq.swiglu_q5(gu.dev_bf16(p["x"]), *wg, *wu, N)
 
 
 @pytest.mark.parametrize("T,K,N,seed", SWIGLU_Q5_SHAPES)
@@ -155,7 +194,7 @@ def test_swiglu_q5_block_full_size_sampled(nq):
     d = si.SWIGLU_DOWN
     pd = si.q5_problem(T, d["K"], d["N"], c["seed"] + 1500)
     wd = gu.pack_q5(nq, pd["wn"], pd["wh"], pd["s"], d["K"], d["N"])
-    y = gu.host_f64(nq.gemm_q5(h_dev, wd, d["N"]))
+    y = gu.host_f64(nq.gemm_q5(h_dev, *wd, d["N"]))
     h_bits = h_dev.view(torch.int16).cpu().numpy().view(np.uint16)
     rows = gu.sample_rows(d["N"], 256, 3)
     y_ref = oracle.gemm_q5_rows(h_bits, pd["wn"], pd["wh"], pd["s"], T, d["K"], rows)
@@ -168,7 +207,7 @@ def test_workload_tiny_q4(nq):
     c = si.TINY_Q4
     p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
     wq = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, c["N"]))
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *wq, c["N"]))
     assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], c["T"], c["K"], c["N"])) <= gu.TOL
 
 
@@ -176,7 +215,7 @@ def test_workload_decode_q4_full(nq):
     c = si.DECODE_Q4
     p = si.q4_problem(c["T"], c["K"], c["N"], c["seed"])
     wq = gu.pack_q4(nq, p["wq"], p["s"], c["K"], c["N"])
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), wq, c["N"]))
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *wq, c["N"]))
     assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], c["T"], c["K"], c["N"])) <= gu.TOL
 
 
@@ -185,7 +224,7 @@ def test_workload_verify_q5_full(nq, T):
     c = si.VERIFY_Q5
     p = si.q5_problem(T, c["K"], c["N"], c["seed"])
     wq = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], c["K"], c["N"])
-    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), wq, c["N"]))
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), *wq, c["N"]))
     y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, c["K"], c["N"])
     assert gu.rel_err(y, y_ref) <= gu.TOL
 
@@ -197,7 +236,7 @@ def test_workload_swiglu_block_full(nq):
     p = si.swiglu_problem(T, K, N, c["seed"])
     wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
     wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
-    h_dev = nq.swiglu_q4(gu.dev_bf16(p["x"]), wg, wu, N)
+    h_dev = nq.swiglu_q4(gu.dev_bf16(p["x"]), *wg, *wu, N)
     rows = gu.sample_rows(N, 384, 1)
     g, u, _ = oracle.swiglu_q4_rows(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, rows)
     h_exact = (g / (1.0 + np.exp(-g)) * u).T           # [T][rows]
@@ -207,10 +246,24 @@ def test_workload_swiglu_block_full(nq):
     d = si.SWIGLU_DOWN
     pd = si.q4_problem(T, d["K"], d["N"], c["seed"] + 1000)
     wd = gu.pack_q4(nq, pd["wq"], pd["s"], d["K"], d["N"])
-    y = gu.host_f64(nq.gemm_q4(h_dev, wd, d["N"]))
+    y = gu.host_f64(nq.gemm_q4(h_dev, *wd, d["N"]))
     h_bits = h_dev.view(torch.int16).cpu().numpy().view(np.uint16)
     y_ref = oracle.gemm_q4(h_bits, pd["wq"], pd["s"], T, d["K"], d["N"])
     assert gu.rel_err(y, y_ref) <= gu.TOL
+
+
+def test_swiglu_q4_fused_decode_full_size_sampled(nq):
+    """The fused gate/up call at T=1 with the decode shape (K=5120, N=17408): the call the
+    layer-stack benchmark times at T=1, in its full-size launch configuration, on sampled
+    rows (both halves of row tiles, both tiles of row pairs, first and last rows)."""
+    T, K, N = 1, 5120, 17408
+    p = si.swiglu_problem(T, K, N, 31)
+    wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), *wg, *wu, N))
+    rows = gu.sample_rows(N, 512, 5)
+    g, u, _ = oracle.swiglu_q4_rows(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, rows)
+    assert gu.rel_err(h[:, rows], (g / (1.0 + np.exp(-g)) * u).T) <= gu.TOL
 
 
 @pytest.mark.parametrize("layer", [0, 63])
@@ -225,12 +278,12 @@ def test_workload_layer_stack_sampled(nq, layer, T):
         if bits == 4:
             p = si.q4_problem(T, K, N, si.layer_seed(layer, j))
             wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, N))
+            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), *wq, N))
             y_ref = oracle.gemm_q4_rows(x, p["wq"], p["s"], T, K, rows).T
         else:
             p = si.q5_problem(T, K, N, si.layer_seed(layer, j))
             wq = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(x), wq, N))
+            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(x), *wq, N))
             y_ref = oracle.gemm_q5_rows(x, p["wn"], p["wh"], p["s"], T, K, rows).T
         assert gu.rel_err(y[:, rows], y_ref) <= gu.TOL, name
 
@@ -242,15 +295,15 @@ def test_deterministic_and_zero_point_exact(nq):
     p = si.q4_problem(T, K, N, 77)
     wq = gu.pack_q4(nq, p["wq"], p["s"], K, N)
     x = gu.dev_bf16(p["x"])
-    y1 = nq.gemm_q4(x, wq, N)
-    y2 = nq.gemm_q4(x, wq, N)
+    y1 = nq.gemm_q4(x, *wq, N)
+    y2 = nq.gemm_q4(x, *wq, N)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     # all codes at the zero point: exactly zero output, however K is split
     z4 = gu.pack_q4(nq, np.full((N, K // 8), 0x88888888, np.uint32), p["s"], K, N)
-    assert torch.count_nonzero(nq.gemm_q4(x, z4, N).float()) == 0
+    assert torch.count_nonzero(nq.gemm_q4(x, *z4, N).float()) == 0
     z5 = gu.pack_q5(nq, np.zeros((N, K // 8), np.uint32), np.full((N, K // 32), 0xFFFFFFFF, np.uint32),
                          p["s"], K, N)
-    assert torch.count_nonzero(nq.gemm_q5(x, z5, N).float()) == 0
+    assert torch.count_nonzero(nq.gemm_q5(x, *z5, N).float()) == 0
 
 
 def test_one_hot_x_selects_codes(nq):
@@ -264,7 +317,7 @@ def test_one_hot_x_selects_codes(nq):
     ks = [0, 1, 63, 64, 300, 500, 638, 639]
     for t, k in enumerate(ks):
         x[t, k] = 0x3F80
-    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), wq, N))
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(x), *wq, N))
     for t, k in enumerate(ks):
         assert np.array_equal(y[t], codes[:, k].astype(np.float64))
 
@@ -277,12 +330,12 @@ def test_empty_and_k0(nq):
     # K == 0: Y is an empty sum -> zeros
     from weight_only_groupwise_gb300.nq import _ptr, _stream, lib
     x16 = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    rc = lib().nq_gemm_q4(_ptr(x16), _ptr(dummy), _ptr(y), 2, 0, N, _stream(None))
+    rc = lib().nq_gemm_q4(_ptr(x16), _ptr(dummy), _ptr(dummy), _ptr(y), 2, 0, N, _stream(None))
     assert rc == 0
     assert torch.count_nonzero(y.float()) == 0
     # T == 0: nothing written
     y.fill_(3.0)
-    rc = lib().nq_gemm_q5(_ptr(x16), _ptr(dummy), _ptr(y), 0, 64, N, _stream(None))
+    rc = lib().nq_gemm_q5(_ptr(x16), _ptr(dummy), _ptr(dummy), _ptr(y), 0, 64, N, _stream(None))
     assert rc == 0 and bool((y.float() == 3.0).all())
 
 
@@ -294,14 +347,17 @@ def test_errors_leave_output_untouched(nq):
     y = torch.full((T, N), 5.0, dtype=torch.bfloat16, device="cuda")
     from weight_only_groupwise_gb300.nq import NqError
     with pytest.raises(NqError) as e:
-        nq.gemm_q4(x, wq, N + 1, out=y)        # N % 16 != 0
+        nq.gemm_q4(x, *wq, N + 1, out=y)        # N % 16 != 0
     assert e.value.status == -2
     xo = torch.empty(T * K + 8, dtype=torch.bfloat16, device="cuda")[1:1 + T * K].view(T, K)
     with pytest.raises(NqError) as e:
-        nq.gemm_q4(xo, wq, N, out=y)           # misaligned X
+        nq.gemm_q4(xo, *wq, N, out=y)           # misaligned X
     assert e.value.status == -3
     with pytest.raises(NqError) as e:
-        nq.gemm_q4(x, wq, N, out=x.view(-1)[:T * N].view(T, N))  # Y aliases X
+        nq.gemm_q4(x, *wq, N, out=x.view(-1)[:T * N].view(T, N))  # Y aliases X
+    assert e.value.status == -4
+    with pytest.raises(NqError) as e:                           # Y aliases the scales
+        nq.gemm_q4(x, wq[0], wq[1], N, out=wq[1][:T * N * 2].view(torch.bfloat16).view(T, N))
     assert e.value.status == -4
     torch.cuda.synchronize()
     assert bool((y.float() == 5.0).all())
@@ -324,11 +380,11 @@ def test_activation_range_outliers(nq, bits):
     xb = si.bf16_bits(x)
     if bits == 4:
         w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-        y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(xb), w, N))
+        y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(xb), *w, N))
         y_ref = oracle.gemm_q4(xb, p["wq"], p["s"], T, K, N)
     else:
         w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-        y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), w, N))
+        y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), *w, N))
         y_ref = oracle.gemm_q5(xb, p["wn"], p["wh"], p["s"], T, K, N)
     for t in range(T):   # per token: each row has its own magnitude
         assert np.all(np.isfinite(y[t]))
@@ -349,11 +405,11 @@ def test_activation_outlier_in_a_later_slab(nq, bits):
     xb = si.bf16_bits(x)
     if bits == 4:
         w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-        y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(xb), w, N))
+        y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(xb), *w, N))
         y_ref = oracle.gemm_q4(xb, p["wq"], p["s"], T, K, N)
     else:
         w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-        y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), w, N))
+        y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), *w, N))
         y_ref = oracle.gemm_q5(xb, p["wn"], p["wh"], p["s"], T, K, N)
     for t in range(T):
         assert np.all(np.isfinite(y[t]))
@@ -376,18 +432,18 @@ def test_slab_cluster_parity(nq, bits, T, K, N):
         if bits == 4:
             p = si.q4_problem(T, K, N, seed)
             w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
-            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), w, N))
+            y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *w, N))
             y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
         else:
             p = si.q5_problem(T, K, N, seed)
             w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
-            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), w, N))
+            y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(p["x"]), *w, N))
             y_ref = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
         assert gu.rel_err(y, y_ref) <= gu.TOL
         s = si.swiglu_problem(T, K, 32, seed + 1)
         wg = gu.pack_q4(nq, s["wg"], s["sg"], K, 32)
         wu = gu.pack_q4(nq, s["wu"], s["su"], K, 32)
-        h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(s["x"]), wg, wu, 32))
+        h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(s["x"]), *wg, *wu, 32))
         g, u, _ = oracle.swiglu_q4(s["x"], s["wg"], s["sg"], s["wu"], s["su"], T, K, 32)
         assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
         nq.device_error()

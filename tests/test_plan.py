@@ -143,3 +143,31 @@ def test_no_cluster_plan_for_one_slab(nq):
         nq.plan_cluster_info(4, 0, 1, 5120, 17408, 48)     # one slab
     with pytest.raises(NqError):
         nq.plan_cluster_info(4, 0, 2, 17408, 5120, 48)     # fp16 operands, one slab
+
+
+# The limit of nq_gemm_q4_noalloc's fixed scratch (2048 partial slots, 4096 tickets) as
+# stated in include/nq.h for a 152-SM GB300: the largest N per (T, K), from the planner.
+NOALLOC_LIMITS = [
+    # T, K, largest N
+    (1, 5120, 60672), (1, 49152, 60672), (2, 24576, 60672), (3, 16384, 60672), (4, 12288, 60672),
+    (6, 8192, 60672), (8, 6144, 60672), (4, 17408, 30336), (8, 12288, 30336), (8, 17408, 20224),
+    (8, 24576, 15168),
+]
+
+
+def _noalloc_fits(nq, T, K, N, sms=152):
+    p = nq.plan_info(4, 0, T, K, N, sms)
+    return p["ws_slots"] <= 2048 and p["pairs"] <= 4096
+
+
+@pytest.mark.parametrize("T,K,n_max", NOALLOC_LIMITS)
+def test_noalloc_limits_stated_in_header(nq, T, K, n_max):
+    assert _noalloc_fits(nq, T, K, n_max)
+    assert not _noalloc_fits(nq, T, K, n_max + 16)
+
+
+@pytest.mark.parametrize("T,k_max", [(1, 49152), (2, 24576), (3, 16384), (4, 12288), (5, 8192),
+                                     (6, 8192), (7, 6144), (8, 6144)])
+def test_one_slab_k_limits_stated_in_header(nq, T, k_max):
+    assert nq.plan_info(4, 0, T, k_max, 512, 152)["slabs"] == 1
+    assert nq.plan_info(4, 0, T, k_max + 64, 512, 152)["slabs"] == 2

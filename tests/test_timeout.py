@@ -1,0 +1,54 @@
+"""Bounded device-side waits. With the wait bound set far below a kernel's run time (1 ns),
+the projection kernels abort instead of waiting: nq_device_error then reports
+NQ_ERR_TIMEOUT once and clears the flag and the split-K tickets, and the next call with the
+default bound is correct. The wait runs out because of the bound alone: nothing faults, traps
+or spins without limit, and every aborted block still waits, on its own fixed bound, for the
+copies it has issued before it exits."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    return nq
+
+
+# decode (one slab, whole row pairs, fp16 operands) and a three-slab split-K shape (bf16
+# operands, every run a partial: an abort leaves tickets part-counted)
+@pytest.mark.parametrize("T,K,N,seed", [(1, 5120, 17408, 1), (8, 17408, 512, 3)])
+def test_timeout_is_reported_and_next_call_is_correct(nq, T, K, N, seed):
+    base = nq.wait_limit(0)
+    assert base >= 1_000_000
+    p = si.q4_problem(T, K, N, seed)
+    w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    x = gu.dev_bf16(p["x"])
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    gu.expect_timeout(nq, lambda: nq.gemm_q4(x, *w, N, out=y))
+    assert nq.wait_limit(0) == base
+    y = gu.host_f64(nq.gemm_q4(x, *w, N))
+    nq.device_error()
+    assert gu.rel_err(y, oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)) <= gu.TOL
+
+
+def test_timeout_in_fused_swiglu(nq):
+    T, K, N = 4, 2048, 2048
+    p = si.swiglu_problem(T, K, N, 17)
+    wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    x = gu.dev_bf16(p["x"])
+    gu.expect_timeout(nq, lambda: nq.swiglu_q4(x, *wg, *wu, N))
+    h = gu.host_f64(nq.swiglu_q4(x, *wg, *wu, N))
+    nq.device_error()
+    g, u, _ = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
+    assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL

@@ -55,15 +55,15 @@ __global__ void pack_codes_kernel(const uint32_t* __restrict__ wn, const uint32_
             }
             words[j] = wv;
         }
-        uint8_t* base = out + packed_code_off(rt, g, G, TB);
+        uint8_t* base = out + packed_code_off(rt, g, G, TB);  // codes buffer
         reinterpret_cast<uint4*>(base)[lane] = make_uint4(words[0], words[1], words[2], words[3]);
         if (BITS == 5) reinterpret_cast<uint32_t*>(base + 512)[lane] = hw;
     }
 }
 
-// Canonical [N][K/64] fp16 scales -> per tile 16 halves ordered (r, r+8) for r = 0..7, stored
-// after the codes of the tile's block.
-__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N, int TB, uint8_t* __restrict__ out) {
+// Canonical [N][K/64] fp16 scales -> the packed scale buffer: per tile 16 halves ordered
+// (r, r+8) for r = 0..7.
+__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N, uint8_t* __restrict__ out) {
     const int G = K / kGroup;
     const long long total = (long long)(N / kTileRows) * G * 16;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
@@ -72,19 +72,57 @@ __global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N,
         const long long tile = idx >> 4;
         const int rt = (int)(tile / G), g = (int)(tile % G);
         const int row = (e >> 1) + 8 * (e & 1);
-        reinterpret_cast<uint16_t*>(out + packed_scale_off(rt, g, G, TB))[e] = s[(size_t)(rt * kTileRows + row) * G + g];
+        reinterpret_cast<uint16_t*>(out + packed_scale_off(rt, g, G))[e] = s[(size_t)(rt * kTileRows + row) * G + g];
     }
 }
 
-// Packed -> fp32 W[n][k], decoding with the projection kernels' own decode_q4/decode_q5:
-// a lower-K half holds 1024 + q, an upper-K half 1024 + 16 q (fp16); w = (float)s * (q - z),
-// every step exact in fp32.
-template <int BITS>
-__global__ void dequant_kernel(const uint8_t* __restrict__ wq, int K, int N, float* __restrict__ w) {
+// Packed -> fp32 W[n][k], decoding with the projection kernels' own decoders:
+//   F16 (the T <= 2 kernels): decode_q4 / decode_q5<J>, a lower-K half holds 1024 + q and an
+//     upper-K half 1024 + 16 q (fp16);
+//   bf16 (the T >= 3 kernels): decode_q4_bf16 / decode_q5_bf16<J>, every half holds 128 + q.
+// Then w = (float)s * (q - z); every step is exact in fp32.
+template <int BITS, int J, bool F16>
+__device__ __forceinline__ void decode_for_dump(uint32_t w, uint32_t h, uint32_t a[4]) {
+    if constexpr (F16) {
+        if constexpr (BITS == 4) decode_q4(w, a); else decode_q5<J>(w, h, a);
+    } else {
+        if constexpr (BITS == 4) decode_q4_bf16(w, a); else decode_q5_bf16<J>(w, h, a);
+    }
+}
+
+template <int BITS, bool F16, int J>
+__device__ __forceinline__ void dump_step(uint32_t w, uint32_t hb, int rt, int g, int gid, int c, int K, float s_lo,
+                                          float s_hi, float* __restrict__ out) {
+    constexpr float z = BITS == 4 ? 8.0f : 16.0f;
+    uint32_t a[4];
+    decode_for_dump<BITS, J, F16>(w, hb, a);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        // register m: rows r (m even) / r+8 (m odd), K pair k (m < 2) / k+8 (m >= 2)
+        const int row = gid + 8 * (m & 1);
+        const int k = g * kGroup + 16 * J + 2 * c + 8 * (m >> 1);
+        const float s = (m & 1) ? s_hi : s_lo;
+        float v0, v1;
+        if constexpr (F16) {
+            const float step = m < 2 ? 1.0f : 16.0f;
+            v0 = (__half2float(__ushort_as_half((unsigned short)(a[m] & 0xFFFFu))) - 1024.0f) / step;
+            v1 = (__half2float(__ushort_as_half((unsigned short)(a[m] >> 16))) - 1024.0f) / step;
+        } else {
+            v0 = __bfloat162float(__ushort_as_bfloat16((unsigned short)(a[m] & 0xFFFFu))) - 128.0f;
+            v1 = __bfloat162float(__ushort_as_bfloat16((unsigned short)(a[m] >> 16))) - 128.0f;
+        }
+        float* dst = out + (size_t)(rt * kTileRows + row) * K + k;
+        dst[0] = s * (v0 - z);
+        dst[1] = s * (v1 - z);
+    }
+}
+
+template <int BITS, bool F16>
+__global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint8_t* __restrict__ sq, int K, int N,
+                               float* __restrict__ w) {
     const int G = K / kGroup;
     const long long total = (long long)(N / kTileRows) * G * 32;
     constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
-    constexpr float z = BITS == 4 ? 8.0f : 16.0f;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const int lane = (int)(idx & 31);
@@ -94,35 +132,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, int K, int N, flo
         const uint8_t* tb = wq + packed_code_off(rt, g, G, TB);
         const uint4 wv = reinterpret_cast<const uint4*>(tb)[lane];
         const uint32_t hb = BITS == 5 ? reinterpret_cast<const uint32_t*>(tb + 512)[lane] : 0u;
-        const uint16_t* st = reinterpret_cast<const uint16_t*>(wq + packed_scale_off(rt, g, G, TB));
+        const uint16_t* st = reinterpret_cast<const uint16_t*>(sq + packed_scale_off(rt, g, G));
         const float s_lo = __half2float(__ushort_as_half(st[2 * gid]));
         const float s_hi = __half2float(__ushort_as_half(st[2 * gid + 1]));
-        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t a[4];
-            if (BITS == 4) {
-                decode_q4(ws[j], a);
-            } else {
-                if (j == 0) decode_q5<0>(ws[j], hb, a);
-                if (j == 1) decode_q5<1>(ws[j], hb, a);
-                if (j == 2) decode_q5<2>(ws[j], hb, a);
-                if (j == 3) decode_q5<3>(ws[j], hb, a);
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                // register m: rows r (m even) / r+8 (m odd), K pair k (m < 2) / k+8 (m >= 2)
-                const int row = gid + 8 * (m & 1);
-                const int k = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1);
-                const float s = (m & 1) ? s_hi : s_lo;
-                const float step = m < 2 ? 1.0f : 16.0f;
-                const float v0 = __half2float(__ushort_as_half((unsigned short)(a[m] & 0xFFFFu)));
-                const float v1 = __half2float(__ushort_as_half((unsigned short)(a[m] >> 16)));
-                float* dst = w + (size_t)(rt * kTileRows + row) * K + k;
-                dst[0] = s * ((v0 - 1024.0f) / step - z);
-                dst[1] = s * ((v1 - 1024.0f) / step - z);
-            }
-        }
+        dump_step<BITS, F16, 0>(wv.x, hb, rt, g, gid, c, K, s_lo, s_hi, w);
+        dump_step<BITS, F16, 1>(wv.y, hb, rt, g, gid, c, K, s_lo, s_hi, w);
+        dump_step<BITS, F16, 2>(wv.z, hb, rt, g, gid, c, K, s_lo, s_hi, w);
+        dump_step<BITS, F16, 3>(wv.w, hb, rt, g, gid, c, K, s_lo, s_hi, w);
     }
 }
 
@@ -144,6 +160,22 @@ DevState g_dev[kMaxDevices];
 bool g_pdl = true;
 bool g_cluster = false;
 bool g_env_read = false;
+unsigned long long g_wait_ns = (unsigned long long)kWaitTimeoutNs;
+
+// Reads NQ_PDL, NQ_CLUSTER and NQ_WAIT_NS once (the first call that needs them). g_mu held.
+void read_env_locked() {
+    if (g_env_read) return;
+    const char* e = std::getenv("NQ_PDL");
+    if (e && e[0] == '0') g_pdl = false;
+    const char* c = std::getenv("NQ_CLUSTER");
+    if (c && c[0] == '1') g_cluster = true;
+    const char* w = std::getenv("NQ_WAIT_NS");
+    if (w) {
+        const long long v = std::atoll(w);
+        if (v > 0) g_wait_ns = (unsigned long long)v;
+    }
+    g_env_read = true;
+}
 
 size_t ws_tickets_off() { return 256; }
 size_t ws_partials_off(long long tickets_cap) {
@@ -156,13 +188,7 @@ nq_status current_device(DevState** out, int* dev_out) {
     if (cudaGetDevice(&dev) != cudaSuccess) return NQ_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return NQ_ERR_DEVICE;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_env_read) {
-        const char* e = std::getenv("NQ_PDL");
-        if (e && e[0] == '0') g_pdl = false;
-        const char* c = std::getenv("NQ_CLUSTER");
-        if (c && c[0] == '1') g_cluster = true;
-        g_env_read = true;
-    }
+    read_env_locked();
     DevState& d = g_dev[dev];
     if (!d.init) {
         if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -226,10 +252,9 @@ nq_status check_shape(int K, int N) {
     return NQ_OK;
 }
 
-// Packed bytes: codes (K*N/2 or 5*K*N/8) plus fp16 scales (N*K/32), interleaved per block.
-size_t packed_bytes(int bits, int K, int N) {
-    return (size_t)K * N / 8 * (bits == 4 ? 4 : 5) + (size_t)N * (K / kGroup) * 2;
-}
+// Packed code bytes (K*N/2 or 5*K*N/8) and packed scale bytes (N*K/32).
+size_t packed_bytes(int bits, int K, int N) { return (size_t)K * N / 8 * (bits == 4 ? 4 : 5); }
+size_t scale_bytes(int K, int N) { return (size_t)N * (K / kGroup) * 2; }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -255,18 +280,22 @@ int resident_clusters(DevState& d, int bits, bool swiglu, int S) {
     return c < cap ? c : cap;
 }
 
-// Shared body of the projection entry points (Q4/Q5 GEMM, Q4/Q5 SwiGLU).
-nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* W1, void* Y, int T, int K,
-                  int N, void* stream) {
+// Shared body of the projection entry points (Q4/Q5 GEMM, Q4/Q5 SwiGLU). W0/S0: the weight
+// (gemm) or the gate weight (swiglu); W1/S1: the up weight (swiglu only).
+nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
+                  const void* S1, void* Y, int T, int K, int N, void* stream) {
     if (T < 0 || T > 8) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
     if (T == 0 || N == 0) return NQ_OK;  // empty output
-    if (!X || !W0 || !Y || (swiglu && !W1)) return NQ_ERR_NULL;
-    if (misaligned(X) || misaligned(W0) || misaligned(Y) || (swiglu && misaligned(W1))) return NQ_ERR_ALIGN;
+    if (!X || !W0 || !S0 || !Y || (swiglu && (!W1 || !S1))) return NQ_ERR_NULL;
+    if (misaligned(X) || misaligned(W0) || misaligned(S0) || misaligned(Y) ||
+        (swiglu && (misaligned(W1) || misaligned(S1))))
+        return NQ_ERR_ALIGN;
     const size_t xb = (size_t)T * K * 2, yb = (size_t)T * N * 2;
-    const size_t wb = packed_bytes(bits, K, N);
-    if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, wb) || (swiglu && overlap(Y, yb, W1, wb)))
+    const size_t wb = packed_bytes(bits, K, N), sb = scale_bytes(K, N);
+    if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, wb) || overlap(Y, yb, S0, sb) ||
+        (swiglu && (overlap(Y, yb, W1, wb) || overlap(Y, yb, S1, sb))))
         return NQ_ERR_ALIAS;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
@@ -290,11 +319,14 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     if (st != NQ_OK) return st;
     a.X = static_cast<const uint16_t*>(X);
     a.W0 = static_cast<const uint8_t*>(W0);
+    a.S0 = static_cast<const uint8_t*>(S0);
     a.W1 = static_cast<const uint8_t*>(swiglu ? W1 : W0);
+    a.S1 = static_cast<const uint8_t*>(swiglu ? S1 : S0);
     a.Y = static_cast<uint16_t*>(Y);
     a.dev_err = reinterpret_cast<int*>(d->ws);
     a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
     a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
+    a.wait_ns = g_wait_ns;
     cudaError_t e;
     if (swiglu)
         e = bits == 4 ? launch_proj_swiglu_q4(a, as_stream(stream), g_pdl)
@@ -306,51 +338,71 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     return e == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N, void* packed,
-               void* stream) {
+nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N, void* wq_packed,
+               void* s_packed, void* stream) {
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
     if (K == 0 || N == 0) return NQ_OK;
-    if (!wn || !s || !packed || (bits == 5 && !wh)) return NQ_ERR_NULL;
-    if (misaligned(wn) || misaligned(s) || misaligned(packed) || (bits == 5 && misaligned(wh))) return NQ_ERR_ALIGN;
-    const size_t ob = packed_bytes(bits, K, N);
-    const size_t in_n = (size_t)N * K / 2, in_h = (size_t)N * K / 8, in_s = (size_t)N * (K / kGroup) * 2;
-    if (overlap(packed, ob, wn, in_n) || overlap(packed, ob, s, in_s) || (bits == 5 && overlap(packed, ob, wh, in_h)))
-        return NQ_ERR_ALIAS;
+    if (!wn || !s || !wq_packed || !s_packed || (bits == 5 && !wh)) return NQ_ERR_NULL;
+    if (misaligned(wn) || misaligned(s) || misaligned(wq_packed) || misaligned(s_packed) ||
+        (bits == 5 && misaligned(wh)))
+        return NQ_ERR_ALIGN;
+    const size_t ob = packed_bytes(bits, K, N), osb = scale_bytes(K, N);
+    const size_t in_n = (size_t)N * K / 2, in_h = (size_t)N * K / 8, in_s = scale_bytes(K, N);
+    const void* outs[2] = {wq_packed, s_packed};
+    const size_t out_n[2] = {ob, osb};
+    for (int i = 0; i < 2; ++i)
+        if (overlap(outs[i], out_n[i], wn, in_n) || overlap(outs[i], out_n[i], s, in_s) ||
+            (bits == 5 && overlap(outs[i], out_n[i], wh, in_h)))
+            return NQ_ERR_ALIAS;
+    if (overlap(wq_packed, ob, s_packed, osb)) return NQ_ERR_ALIAS;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
     const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
-    uint8_t* out = static_cast<uint8_t*>(packed);
+    uint8_t* out = static_cast<uint8_t*>(wq_packed);
     if (bits == 4)
         pack_codes_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(wn, nullptr, K, N, out);
     else
         pack_codes_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(wn, wh, K, N, out);
     if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
-    pack_scales_kernel<<<grid_for(lanes / 2, 256), 256, 0, as_stream(stream)>>>(
-        s, K, N, bits == 4 ? kQ4TileBytes : kQ5TileBytes, out);
+    pack_scales_kernel<<<grid_for(lanes / 2, 256), 256, 0, as_stream(stream)>>>(s, K, N,
+                                                                               static_cast<uint8_t*>(s_packed));
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
-nq_status dequant(int bits, const void* wq, float* w, int K, int N, void* stream) {
+nq_status dequant(int bits, bool f16, const void* wq, const void* sq, float* w, int K, int N, void* stream) {
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
     if (K == 0 || N == 0) return NQ_OK;
-    if (!wq || !w) return NQ_ERR_NULL;
-    if (misaligned(wq) || misaligned(w)) return NQ_ERR_ALIGN;
-    if (overlap(w, (size_t)N * K * 4, wq, packed_bytes(bits, K, N))) return NQ_ERR_ALIAS;
+    if (!wq || !sq || !w) return NQ_ERR_NULL;
+    if (misaligned(wq) || misaligned(sq) || misaligned(w)) return NQ_ERR_ALIGN;
+    if (overlap(w, (size_t)N * K * 4, wq, packed_bytes(bits, K, N)) || overlap(w, (size_t)N * K * 4, sq, scale_bytes(K, N)))
+        return NQ_ERR_ALIAS;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
     const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
-    if (bits == 4)
-        dequant_kernel<4><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(static_cast<const uint8_t*>(wq), K, N, w);
-    else
-        dequant_kernel<5><<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(static_cast<const uint8_t*>(wq), K, N, w);
+    const uint8_t* c = static_cast<const uint8_t*>(wq);
+    const uint8_t* sc = static_cast<const uint8_t*>(sq);
+    const int grid = grid_for(lanes, 256);
+    cudaStream_t s = as_stream(stream);
+    if (bits == 4 && f16) dequant_kernel<4, true><<<grid, 256, 0, s>>>(c, sc, K, N, w);
+    if (bits == 4 && !f16) dequant_kernel<4, false><<<grid, 256, 0, s>>>(c, sc, K, N, w);
+    if (bits == 5 && f16) dequant_kernel<5, true><<<grid, 256, 0, s>>>(c, sc, K, N, w);
+    if (bits == 5 && !f16) dequant_kernel<5, false><<<grid, 256, 0, s>>>(c, sc, K, N, w);
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace nq {
+unsigned long long wait_limit_ns() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    read_env_locked();
+    return g_wait_ns;
+}
+}  // namespace nq
 
 // ---------------------------------------------------------------- C ABI
 
@@ -371,42 +423,63 @@ const char* nq_status_string(nq_status s) {
     }
 }
 
-int nq_version(void) { return (1 << 16) | 0; }
+int nq_version(void) { return (2 << 16) | 0; }
 
 size_t nq_packed_bytes_q4(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_bytes(4, K, N) : 0; }
 size_t nq_packed_bytes_q5(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_bytes(5, K, N) : 0; }
 
-nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* packed, void* stream) {
-    return pack(4, wq_canon, nullptr, s_canon, K, N, packed, stream);
+size_t nq_scale_bytes(int K, int N) { return check_shape(K, N) == NQ_OK ? scale_bytes(K, N) : 0; }
+
+nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* wq_packed,
+                     void* s_packed, void* stream) {
+    return pack(4, wq_canon, nullptr, s_canon, K, N, wq_packed, s_packed, stream);
 }
 
 nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const uint16_t* s_canon, int K, int N,
-                     void* packed, void* stream) {
-    return pack(5, wn_canon, wh_canon, s_canon, K, N, packed, stream);
+                     void* wq_packed, void* s_packed, void* stream) {
+    return pack(5, wn_canon, wh_canon, s_canon, K, N, wq_packed, s_packed, stream);
 }
 
-nq_status nq_gemm_q4(const void* X, const void* W, void* Y, int T, int K, int N, void* stream) {
-    return project(4, false, X, W, nullptr, Y, T, K, N, stream);
+nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N, void* stream) {
+    return project(4, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
 }
 
-nq_status nq_gemm_q5(const void* X, const void* W, void* Y, int T, int K, int N, void* stream) {
-    return project(5, false, X, W, nullptr, Y, T, K, N, stream);
+nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N, void* stream) {
+    return project(5, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
 }
 
-nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N, void* stream) {
-    return project(4, true, X, Wg, Wu, H, T, K, N, stream);
+nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su, void* H, int T,
+                       int K, int N, void* stream) {
+    return project(4, true, X, Wg, Sg, Wu, Su, H, T, K, N, stream);
 }
 
-nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Wu, void* H, int T, int K, int N, void* stream) {
-    return project(5, true, X, Wg, Wu, H, T, K, N, stream);
+nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su, void* H, int T,
+                       int K, int N, void* stream) {
+    return project(5, true, X, Wg, Sg, Wu, Su, H, T, K, N, stream);
 }
 
-nq_status nq_dequant_q4_debug(const void* W, float* out, int K, int N, void* stream) {
-    return dequant(4, W, out, K, N, stream);
+nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
+    return dequant(4, true, Wq, S, W, K, N, stream);
 }
 
-nq_status nq_dequant_q5_debug(const void* W, float* out, int K, int N, void* stream) {
-    return dequant(5, W, out, K, N, stream);
+nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
+    return dequant(5, true, Wq, S, W, K, N, stream);
+}
+
+nq_status nq_dequant_q4_debug_bf16(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
+    return dequant(4, false, Wq, S, W, K, N, stream);
+}
+
+nq_status nq_dequant_q5_debug_bf16(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
+    return dequant(5, false, Wq, S, W, K, N, stream);
+}
+
+long long nq_wait_limit(long long ns) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    read_env_locked();
+    const long long prev = (long long)g_wait_ns;
+    if (ns > 0) g_wait_ns = (unsigned long long)ns;
+    return prev;
 }
 
 nq_status nq_reserve(int T_max, int K_max, int N_max) {
@@ -436,14 +509,18 @@ nq_status nq_reserve(int T_max, int K_max, int N_max) {
 
 nq_status nq_device_error(void) {
     DevState* d = nullptr;
-    nq_status st = current_device(&d, nullptr);
+    int dev = 0;
+    nq_status st = current_device(&d, &dev);
     if (st != NQ_OK) return st;
     if (cudaDeviceSynchronize() != cudaSuccess) return NQ_ERR_CUDA;
+    // The fixed scratch of nq_gemm_q4_noalloc has its own error word.
+    const nq_status st_static = noalloc_take_error(dev);
+    if (st_static == NQ_ERR_CUDA) return st_static;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!d->ws) return NQ_OK;
+    if (!d->ws) return st_static;
     int err = 0;
     if (cudaMemcpy(&err, d->ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NQ_ERR_CUDA;
-    if (err == 0) return NQ_OK;
+    if (err == 0) return st_static;
     if (cudaMemset(d->ws, 0, ws_partials_off(d->tickets_cap)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
         return NQ_ERR_CUDA;

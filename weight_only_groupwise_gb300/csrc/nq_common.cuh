@@ -1,16 +1,19 @@
 // nq_common.cuh -- layout constants, the work plan and PTX helpers shared by the kernels
 // of the groupwise int4/int5 small-batch projection (sm_103a).
 //
-// Packed layout (this library's definition; the pages give none):
-//   The K x N weight is cut into tiles of 16 output rows x one 64-wide K group, tile (rt, g)
-//   with rt = n / 16 and g = k / 64. Each row tile is a contiguous stream of blocks of 32
-//   groups (the last block of a row tile may hold fewer, nb = min(32, G - 32b)); a block is
-//   [nb tiles of codes][nb x 32 B of fp16 scales], so one bulk copy fetches a block's codes
-//   and scales together. Inside a code tile, lane l (0..31) of a warp owns 16 bytes = four
-//   uint32 words, one per 16-wide K step j: the word holds the lane's A-operand fragment of
-//   an m16n8k16 tensor-core MMA for that step, one LOP3 away per register (see decode_q4). Q5 code tiles append one uint32 of high bits per lane (128
-//   bytes per tile). A tile's 16 scales are ordered (row r, row r+8) for r = 0..7, so lane l
-//   reads one uint32 holding the scales of its rows l/4 and l/4+8.
+// Packed layout (this library's definition; the pages give none). A packed weight is two
+// buffers, the codes Wq and the scales S, both cut into tiles of 16 output rows x one
+// 64-wide K group, tile (rt, g) with rt = n / 16 and g = k / 64, stored row-tile-major
+// (tile (rt, g) is number rt * G + g, G = K / 64):
+//   Wq: TB bytes per tile (512 for Q4, 640 for Q5) at (rt * G + g) * TB. Inside a code
+//       tile, lane l (0..31) of a warp owns 16 bytes = four uint32 words, one per 16-wide
+//       K step j: the word holds the lane's A-operand fragment of an m16n8k16 tensor-core
+//       MMA for that step, one LOP3 away per register (see decode_q4). Q5 code tiles append
+//       one uint32 of high bits per lane (128 bytes per tile).
+//   S:  32 bytes per tile (16 fp16 scales) at (rt * G + g) * 32, ordered (row r, row r+8)
+//       for r = 0..7, so lane l reads one uint32 holding the scales of its rows l/4, l/4+8.
+// A row tile's codes and scales are each contiguous along K, so a pipeline stage of any
+// run of groups is one bulk copy of codes and one of scales per tile.
 #pragma once
 
 #include <cstdint>
@@ -31,7 +34,7 @@ constexpr int kScaleTileBytes = 32;  // 16 fp16
 #ifndef NQ_BLOCK_GROUPS
 #define NQ_BLOCK_GROUPS 32
 #endif
-constexpr int kBlockGroups = NQ_BLOCK_GROUPS;  // groups per packed block (= per pipeline stage)
+constexpr int kBlockGroups = NQ_BLOCK_GROUPS;  // groups per pipeline stage (stages start on multiples of it)
 #ifndef NQ_CONSUMER_WARPS
 #define NQ_CONSUMER_WARPS 8
 #endif
@@ -53,7 +56,8 @@ constexpr int kMinUnitsPerCta = 16;
 constexpr int kPartialFloats = 256;  // 2 M tiles x 16 rows x 8 tokens
 constexpr int kMaxRed = 4;           // most run hand-over buffers (consumers -> epilogue warps)
 constexpr int kRedBufBytes = kConsumerWarps * 2 * 512;  // one buffer: every warp's two accumulator tiles
-constexpr long long kWaitTimeoutNs = 2000000000LL;  // 2 s per bounded wait
+constexpr long long kWaitTimeoutNs = 2000000000LL;  // default bound of a device-side wait: 2 s
+constexpr unsigned long long kDrainNs = 100000000ull;  // bound of each wait for copies in flight on abort
 constexpr int kMaxCluster = 4;       // most K slabs handled by one thread-block cluster
 
 // Errors a kernel can raise through the workspace flag word.
@@ -61,21 +65,9 @@ constexpr int kDevErrTimeout = 1;
 
 NQ_HD int tpad(int T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
 
-// Byte offsets inside a packed matrix (TB = code bytes per tile, 512 or 640).
-NQ_HD long long packed_tile_stride(int TB) { return TB + kScaleTileBytes; }
-NQ_HD long long packed_row_tile_bytes(int G, int TB) { return (long long)G * packed_tile_stride(TB); }
-NQ_HD long long packed_block_off(int rt, int b, int G, int TB) {
-    return rt * packed_row_tile_bytes(G, TB) + (long long)b * kBlockGroups * packed_tile_stride(TB);
-}
-NQ_HD int block_groups(int b, int G) { return G - kBlockGroups * b < kBlockGroups ? G - kBlockGroups * b : kBlockGroups; }
-NQ_HD long long packed_code_off(int rt, int g, int G, int TB) {
-    return packed_block_off(rt, g / kBlockGroups, G, TB) + (long long)(g % kBlockGroups) * TB;
-}
-NQ_HD long long packed_scale_off(int rt, int g, int G, int TB) {
-    const int b = g / kBlockGroups;
-    return packed_block_off(rt, b, G, TB) + (long long)block_groups(b, G) * TB +
-           (long long)(g % kBlockGroups) * kScaleTileBytes;
-}
+// Byte offsets inside a packed weight (TB = code bytes per tile, 512 or 640).
+NQ_HD long long packed_code_off(int rt, int g, int G, int TB) { return ((long long)rt * G + g) * TB; }
+NQ_HD long long packed_scale_off(int rt, int g, int G) { return ((long long)rt * G + g) * kScaleTileBytes; }
 
 // The work split of one projection call. One "unit" is one 64-wide K group of one row pair
 // (two 16-row tiles; for SwiGLU the gate tile and the up tile of the same rows). Units are
@@ -401,16 +393,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Bounded wait on an mbarrier phase. Returns false (and raises the block's abort flag and
-// the device error word) if the phase does not complete within kWaitTimeoutNs, or at once if
-// the block has already aborted. Never spins forever.
+// the device error word) if the phase does not complete within limit_ns, or at once if the
+// block has already aborted. Never spins forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* dev_err) {
+                                          int* dev_err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (*abort_flag) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > (uint64_t)kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(dev_err, kDevErrTimeout);
             return false;
@@ -473,11 +465,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait on a phase completed by other blocks of the cluster (acquire at cluster
 // scope). Same error behaviour as mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  int* dev_err) {
+                                                  int* dev_err, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait_cluster(bar, parity)) {
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > (uint64_t)kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(dev_err, kDevErrTimeout);
             return false;

@@ -7,6 +7,13 @@
 
 namespace nq {
 
+// Bound of every device-side wait for later launches (nq_wait_limit; NQ_WAIT_NS).
+unsigned long long wait_limit_ns();
+
+// Reports and clears the error word of nq_gemm_q4_noalloc's fixed scratch on device `dev`
+// (NQ_OK if that device never ran it). The caller has synchronised the device.
+int noalloc_take_error(int dev);
+
 // Launch proj_kernel<BITS, SWIGLU> with a.p's grid and shared memory on `stream`.
 // pdl: allow programmatic dependent launch behind the preceding kernel of the stream.
 cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);

@@ -3,10 +3,9 @@
 //
 // nq_gemm_q4 keeps its split-K scratch (partial sums, tickets, an error word) in a workspace
 // that the library allocates with cudaMalloc on first use. Some callers cannot let that
-// happen: code that runs while a CUDA graph is being captured (an allocation is not a
-// stream operation and breaks the capture), plug-ins whose host framework owns all device
-// memory and forbids allocations after start-up, and processes on a fixed memory budget
-// where a late allocation could fail in the middle of serving. This entry point runs the
+// happen: plug-ins whose host framework owns all device memory and forbids allocations
+// after start-up, and processes on a fixed memory budget where a late allocation could fail
+// (or synchronise the device) in the middle of serving. This entry point runs the
 // same kernel with its scratch in a fixed-size array that exists in device memory for as
 // long as the library is loaded, so it never calls cudaMalloc, cudaFree or any allocating
 // routine.
@@ -74,16 +73,37 @@ nq_status device_setup(void** scratch, int* sms) {
 
 }  // namespace
 
-extern "C" nq_status nq_gemm_q4_noalloc(const void* X, const void* W, void* Y, int T, int K, int N,
+namespace nq {
+// The error word of the fixed scratch on device `dev`: a bounded wait that ran out inside an
+// nq_gemm_q4_noalloc kernel set it. Reported and cleared here (with the tickets, which an
+// aborted call may have left part-counted) for nq_device_error; the caller has synchronised.
+int noalloc_take_error(int dev) {
+    if (dev < 0 || dev >= kMaxDev) return NQ_OK;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        scratch = g_scratch[dev];
+    }
+    if (!scratch) return NQ_OK;
+    int err = 0;
+    if (cudaMemcpy(&err, scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NQ_ERR_CUDA;
+    if (err == 0) return NQ_OK;
+    if (cudaMemset(scratch, 0, kStaticPartialOff) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return NQ_ERR_CUDA;
+    return NQ_ERR_TIMEOUT;
+}
+}  // namespace nq
+
+extern "C" nq_status nq_gemm_q4_noalloc(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
                                         void* stream) {
     if (T < 0 || T > 8 || K < 0 || N < 0 || K > (1 << 20) || N > (1 << 20) || K % kGroup || N % kTileRows)
         return NQ_ERR_SHAPE;
     if (T == 0 || N == 0) return NQ_OK;
-    if (!X || !W || !Y) return NQ_ERR_NULL;
-    if (misaligned16(X) || misaligned16(W) || misaligned16(Y)) return NQ_ERR_ALIGN;
+    if (!X || !Wq || !S || !Y) return NQ_ERR_NULL;
+    if (misaligned16(X) || misaligned16(Wq) || misaligned16(S) || misaligned16(Y)) return NQ_ERR_ALIGN;
     const size_t xb = (size_t)T * K * 2, yb = (size_t)T * N * 2;
-    const size_t wb = (size_t)K * N / 2 + (size_t)N * (K / kGroup) * 2;
-    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W, wb)) return NQ_ERR_ALIAS;
+    const size_t wb = (size_t)K * N / 2, sb = (size_t)N * (K / kGroup) * 2;
+    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, Wq, wb) || overlaps(Y, yb, S, sb)) return NQ_ERR_ALIAS;
     void* scratch = nullptr;
     int sms = 0;
     nq_status st = device_setup(&scratch, &sms);
@@ -95,15 +115,19 @@ extern "C" nq_status nq_gemm_q4_noalloc(const void* X, const void* W, void* Y, i
     a.q = a.p;  // stream-K only (no slab clusters)
     if (a.p.slots > kStaticSlots || a.p.RP > kStaticTickets) return NQ_ERR_SCRATCH;
     uint8_t* base = static_cast<uint8_t*>(scratch);
-    // The array keeps the previous call's contents: the error word and this call's tickets
-    // must start at zero, so clear them on the call's stream (no allocation involved).
-    if (cudaMemsetAsync(base, 0, kStaticTicketOff + (size_t)a.p.RP * 4, s) != cudaSuccess) return NQ_ERR_CUDA;
+    // The array keeps the previous call's contents: this call's tickets must start at zero,
+    // so clear them on the call's stream (no allocation involved). The error word is left
+    // alone: it stays set until nq_device_error reports it.
+    if (cudaMemsetAsync(base + kStaticTicketOff, 0, (size_t)a.p.RP * 4, s) != cudaSuccess) return NQ_ERR_CUDA;
     a.X = static_cast<const uint16_t*>(X);
-    a.W0 = static_cast<const uint8_t*>(W);
-    a.W1 = static_cast<const uint8_t*>(W);
+    a.W0 = static_cast<const uint8_t*>(Wq);
+    a.W1 = static_cast<const uint8_t*>(Wq);
+    a.S0 = static_cast<const uint8_t*>(S);
+    a.S1 = static_cast<const uint8_t*>(S);
     a.Y = static_cast<uint16_t*>(Y);
     a.dev_err = reinterpret_cast<int*>(base);
     a.tickets = reinterpret_cast<int*>(base + kStaticTicketOff);
     a.partials = reinterpret_cast<float*>(base + kStaticPartialOff);
+    a.wait_ns = wait_limit_ns();
     return launch_proj_q4(a, s, false) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }

@@ -7,8 +7,8 @@
 // Structure: one persistent block per SM with three roles.
 //   * Producer warp: its elected lane initialises the mbarriers and streams the block's units
 //     with 1-D TMA bulk copies into a ring of shared-memory stages (mbarrier full/empty pairs,
-//     L2 evict-first: every weight byte is read exactly once). A stage holds one 32-group
-//     packed block (codes and scales) of each of the two M tiles: one copy per tile. It does
+//     L2 evict-first: every weight byte is read exactly once). A stage holds up to 32 groups
+//     of each of the two M tiles: one copy of codes and one of scales per tile. It does
 //     not wait for the preceding kernel (weights are never written by a kernel that lets its
 //     dependents start early); with bf16 operands it holds the stream after the first stage
 //     until the activation slab has landed, so the slab's copies do not queue behind a ring.
@@ -42,12 +42,15 @@ namespace nq {
 
 struct ProjArgs {
     const uint16_t* X;   // bf16 [T][K]
-    const uint8_t* W0;   // packed matrix of M tile 0 (codes and scales)
+    const uint8_t* W0;   // packed codes of M tile 0
     const uint8_t* W1;   // M tile 1 (gemm: same matrix, next row tile; swiglu: up matrix)
+    const uint8_t* S0;   // packed scales of M tile 0
+    const uint8_t* S1;   // packed scales of M tile 1
     uint16_t* Y;         // bf16 [T][N]
     float* partials;     // workspace: slots x kPartialFloats
     int* tickets;        // workspace: one per row pair, zero between calls
     int* dev_err;        // workspace: device error word
+    unsigned long long wait_ns;  // bound of every device-side wait
     Plan p;              // the real plan (slab geometry, shared memory, grid)
     Plan q;              // work split and split-K bookkeeping: p itself, or the cluster-level
                          // plan of a slab-cluster launch (p.cl > 1)
@@ -205,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     // plan fields used in loops, in registers
     const Plan& p = a.p;
     const int T = p.T, G = p.G, RT = p.RT, GS = p.GS, nstages = p.stages;
-    const long long row_tile_bytes = (long long)G * TBS;
+    const long long row_tile_codes = (long long)G * TB, row_tile_scales = (long long)G * kScaleTileBytes;
+    const uint64_t wait_ns = a.wait_ns;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // CLU: slab clusters of p.cl blocks; block rank crank takes slab crank of every run of
@@ -219,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     float* osum = reinterpret_cast<float*>(xs + p.x_bytes);  // O[gl][8]
     float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(osum) + p.corr_bytes);  // [2][kRedFloats]
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + p.red_bytes);
-    // bars: full[kMaxStages], empty[kMaxStages], x_bar; then flags
+    // bars: full[kMaxStages], empty[kMaxStages], x_bar; then flags: [0] abort, [1] stages the
+    // producer issued, [2] producer done (both written once the producer stops issuing)
     volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages + 1);
     // per token: max |x| bits of the current slab, then its power-of-two range exponent
     int* xmax = const_cast<int*>(flags) + 8;
@@ -249,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             }
         }
         flags[0] = 0;  // abort
+        flags[1] = 0;
+        flags[2] = 0;
         for (int t = 0; t < 8; ++t) xmax[t] = 0;
         *reinterpret_cast<uint4*>(zero_row) = make_uint4(0, 0, 0, 0);
         mbar_fence_init();
@@ -278,13 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 const int rt0 = SWIGLU ? sg.rp : 2 * sg.rp;
                 const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
                 const bool has1 = SWIGLU || rt1 < RT;
-                const uint8_t* w0 = a.W0 + rt0 * row_tile_bytes;
-                const uint8_t* w1 = a.W1 + rt1 * row_tile_bytes;
+                const uint8_t* w0 = a.W0 + rt0 * row_tile_codes;
+                const uint8_t* w1 = a.W1 + rt1 * row_tile_codes;
+                const uint8_t* s0 = a.S0 + rt0 * row_tile_scales;
+                const uint8_t* s1 = a.S1 + rt1 * row_tile_scales;
                 for (int b = sg.ga / BG; sg.ga < sg.gb && b * BG < sg.gb; ++b) {
                     const int i0 = max(sg.ga - b * BG, 0), i1 = min(sg.gb - b * BG, BG);
-                    const int nb = block_groups(b, G);
-                    const bool whole = i0 == 0 && i1 == BG;   // implies nb == BG
-                    if (!mbar_wait(empty0 + 8 * st, phase ^ 1, flags, a.dev_err)) {
+                    if (!mbar_wait(empty0 + 8 * st, phase ^ 1, flags, a.dev_err, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -292,25 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     const uint32_t fb = full0 + 8 * st;
                     const uint32_t per_tile = (i1 - i0) * TBS;
                     mbar_arrive_expect_tx(fb, (has1 ? 2u : 1u) * per_tile);
-                    const long long boff = (long long)b * BG * TBS;
+                    const long long g0 = (long long)b * BG + i0;  // first group of the copy
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         if (m == 1 && !has1) break;
-                        const uint8_t* blk = (m == 0 ? w0 : w1) + boff;
                         uint8_t* dst = sb + m * kTileArea;
-                        if (whole) {
-                            bulk_g2s(smem_u32(dst), blk, kTileArea, fb, pol);
-                        } else {
-                            bulk_g2s(smem_u32(dst + i0 * TB), blk + i0 * TB, (i1 - i0) * TB, fb, pol);
-                            bulk_g2s(smem_u32(dst + BG * TB + i0 * kScaleTileBytes),
-                                     blk + nb * TB + i0 * kScaleTileBytes, (i1 - i0) * kScaleTileBytes, fb, pol);
-                        }
+                        bulk_g2s(smem_u32(dst + i0 * TB), (m == 0 ? w0 : w1) + g0 * TB, (i1 - i0) * TB, fb, pol);
+                        bulk_g2s(smem_u32(dst + BG * TB + i0 * kScaleTileBytes),
+                                 (m == 0 ? s0 : s1) + g0 * kScaleTileBytes, (i1 - i0) * kScaleTileBytes, fb, pol);
                     }
                     ++it;
                     // After the first stage, hold the weight stream until a bulk-copied first
                     // activation slab has landed: its copies share this block's copy engine,
                     // and behind a full ring of weight stages they would start the consumers late.
-                    if (!F16 && it == 1 && !mbar_wait(x_bar, 0, flags, a.dev_err)) {
+                    if (!F16 && it == 1 && !mbar_wait(x_bar, 0, flags, a.dev_err, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -321,8 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 // Aborted: let copies already issued land before the block can exit.
                 const int first = it > nstages ? it - nstages : 0;
                 for (int j = first; j < it; ++j)
-                    mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, 100000000ull);
+                    mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, kDrainNs);
             }
+            // Tell the consumers how many stages were issued, for their drain on abort.
+            flags[1] = it;
+            __threadfence_block();
+            flags[2] = 1;
         }
         if constexpr (CLU) cluster_sync_all();  // no block leaves while a peer may address it
         return;
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 const uint32_t fullb = cfull0 + 8 * ew, freeb = cfree0 + 8 * ew;
                 constexpr uint32_t kPartBytes = 32 * 8 * 4;
                 if (crank != 0) {
-                    if (nrun > 0 && !mbar_wait_cluster(freeb, (nrun - 1) & 1, flags, a.dev_err)) continue;
+                    if (nrun > 0 && !mbar_wait_cluster(freeb, (nrun - 1) & 1, flags, a.dev_err, wait_ns)) continue;
                     float w[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) w[j] = 0.f;
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     continue;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(fullb, (uint32_t)(S - 1) * kPartBytes);
-                if (!mbar_wait_cluster(fullb, nrun & 1, flags, a.dev_err)) continue;
+                if (!mbar_wait_cluster(fullb, nrun & 1, flags, a.dev_err, wait_ns)) continue;
                 for (int r = 1; r < S; ++r) {
                     const float* src = cbuf + (ew * (S - 1) + r - 1) * kPartialFloats + lane * 8;
 #pragma unroll
@@ -545,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     const uint32_t code_lane = lane * 16, scale_lane = BG * TB + (lane >> 2) * 4;
     const float* osum_lane = osum + 2 * (lane & 3);
 
-    int st = 0, cur_slab = -1, nx = 0;
+    int st = 0, cur_slab = -1, nx = 0, nx_issued = 0;
     uint32_t phase = 0;
     float tok_scale0 = 1.f, tok_scale1 = 1.f;
     Segment nat;
@@ -573,12 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 cp_async_wait_all();  // each thread's own chunks; the range pass below reads only those
             } else {
                 if (tid == 0) {
-                    const uint32_t row_bytes = gs * 128;
-                    mbar_arrive_expect_tx(x_bar, row_bytes * T);
-                    for (int t = 0; t < T; ++t)
-                        bulk_g2s_plain(smem_u32(xs + t * pitch), xg + (size_t)t * p.K, row_bytes, x_bar);
+                    // The previous slab's copies have landed (every consumer waited for them,
+                    // unless the block aborted: then wait here, bounded), so phases never
+                    // overlap; after an abort no new slab is fetched.
+                    if (nx_issued > 0) mbar_wait_drain(x_bar, (nx_issued - 1) & 1, kDrainNs);
+                    if (!flags[0]) {
+                        const uint32_t row_bytes = gs * 128;
+                        mbar_arrive_expect_tx(x_bar, row_bytes * T);
+                        for (int t = 0; t < T; ++t)
+                            bulk_g2s_plain(smem_u32(xs + t * pitch), xg + (size_t)t * p.K, row_bytes, x_bar);
+                        ++nx_issued;
+                    }
                 }
-                mbar_wait(x_bar, nx & 1, flags, a.dev_err);
+                mbar_wait(x_bar, nx & 1, flags, a.dev_err, wait_ns);
                 ++nx;
             }
             // Per token, max |x| over the slab (bit patterns compare like magnitudes), then the
@@ -708,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         const int slab_g0 = sg.s * GS;
         for (int b = sg.ga / BG; sg.ga < sg.gb && b * BG < sg.gb; ++b) {
             const int i0 = max(sg.ga - b * BG, 0), i1 = min(sg.gb - b * BG, BG);
-            const bool ok = mbar_wait(full0 + 8 * st, phase, flags, a.dev_err);
+            const bool ok = mbar_wait(full0 + 8 * st, phase, flags, a.dev_err, wait_ns);
             if (ok) {
                 const uint8_t* t0 = stage_mem + st * kStageBytes;
                 const int gl0 = b * BG - slab_g0;  // slab-local group of block index 0
@@ -803,10 +816,17 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     }
 
     if (flags[0] && tid == 0) {
-        // Aborted: wait (bounded) for the stage copies that may still be in flight.
-        for (int j = 0; j < nstages; ++j) mbar_wait_drain(full0 + 8 * j, 0, 100000000ull);
-        for (int j = 0; j < nstages; ++j) mbar_wait_drain(full0 + 8 * j, 1, 100000000ull);
-        if (nx > 0) mbar_wait_drain(x_bar, (nx - 1) & 1, 100000000ull);
+        // Aborted: the consumers stopped waiting for their stages, so copies may still be in
+        // flight. Once the producer has stopped (bounded wait for its flag), wait (bounded)
+        // for the last copy issued into each stage -- a stage's phases complete in order --
+        // and for the last activation slab.
+        const uint64_t t0 = global_timer_ns();
+        while (!flags[2] && global_timer_ns() - t0 < 2 * kDrainNs) {
+        }
+        const int issued = flags[1];
+        for (int j = issued > nstages ? issued - nstages : 0; j < issued; ++j)
+            mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, kDrainNs);
+        if (nx_issued > 0) mbar_wait_drain(x_bar, (nx_issued - 1) & 1, kDrainNs);
     }
     if constexpr (CLU) cluster_sync_all();
 }

@@ -39,17 +39,23 @@ def lib() -> ctypes.CDLL:
         for f in ("nq_packed_bytes_q4", "nq_packed_bytes_q5"):
             getattr(L, f).argtypes = [I, I]
             getattr(L, f).restype = S
-        L.nq_pack_q4.argtypes = [P, P, I, I, P, P]
-        L.nq_pack_q5.argtypes = [P, P, P, I, I, P, P]
-        L.nq_gemm_q4.argtypes = [P, P, P, I, I, I, P]
-        L.nq_gemm_q5.argtypes = [P, P, P, I, I, I, P]
-        L.nq_gemm_q4_noalloc.argtypes = [P, P, P, I, I, I, P]
-        L.nq_swiglu_q4.argtypes = [P, P, P, P, I, I, I, P]
-        L.nq_swiglu_q5.argtypes = [P, P, P, P, I, I, I, P]
-        L.nq_dequant_q4_debug.argtypes = [P, P, I, I, P]
-        L.nq_dequant_q5_debug.argtypes = [P, P, I, I, P]
+        L.nq_scale_bytes.argtypes = [I, I]
+        L.nq_scale_bytes.restype = S
+        L.nq_pack_q4.argtypes = [P, P, I, I, P, P, P]
+        L.nq_pack_q5.argtypes = [P, P, P, I, I, P, P, P]
+        L.nq_gemm_q4.argtypes = [P, P, P, P, I, I, I, P]
+        L.nq_gemm_q5.argtypes = [P, P, P, P, I, I, I, P]
+        L.nq_gemm_q4_noalloc.argtypes = [P, P, P, P, I, I, I, P]
+        L.nq_swiglu_q4.argtypes = [P, P, P, P, P, P, I, I, I, P]
+        L.nq_swiglu_q5.argtypes = [P, P, P, P, P, P, I, I, I, P]
+        for f in ("nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_dequant_q4_debug_bf16",
+                  "nq_dequant_q5_debug_bf16"):
+            getattr(L, f).argtypes = [P, P, P, I, I, P]
+            getattr(L, f).restype = I
         L.nq_reserve.argtypes = [I, I, I]
         L.nq_device_error.argtypes = []
+        L.nq_wait_limit.argtypes = [ctypes.c_longlong]
+        L.nq_wait_limit.restype = ctypes.c_longlong
         L.nq_shutdown.argtypes = []
         L.nq_shutdown.restype = None
         L.nq_plan_info.argtypes = [I, I, I, I, I, I, P]
@@ -61,9 +67,7 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_cluster_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_cluster_segments.restype = ctypes.c_int64
         for f in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_gemm_q4_noalloc", "nq_swiglu_q4",
-                  "nq_swiglu_q5",
-                  "nq_dequant_q4_debug", "nq_dequant_q5_debug", "nq_reserve", "nq_device_error",
-                  "nq_plan_info", "nq_plan_cluster_info"):
+                  "nq_swiglu_q5", "nq_reserve", "nq_device_error", "nq_plan_info", "nq_plan_cluster_info"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -104,25 +108,37 @@ def packed_bytes_q5(K: int, N: int) -> int:
     return int(lib().nq_packed_bytes_q5(K, N))
 
 
+def scale_bytes(K: int, N: int) -> int:
+    return int(lib().nq_scale_bytes(K, N))
+
+
 # ---------------------------------------------------------------- repack
 
-def pack_q4(wq_canon: torch.Tensor, s_canon: torch.Tensor, K: int, N: int, stream=None) -> torch.Tensor:
+def _packed_pair(code_bytes: int, K: int, N: int, dev):
+    wq = torch.empty(max(code_bytes, 16), dtype=torch.uint8, device=dev)
+    s = torch.empty(max(scale_bytes(K, N), 16), dtype=torch.uint8, device=dev)
+    return wq, s
+
+
+def pack_q4(wq_canon: torch.Tensor, s_canon: torch.Tensor, K: int, N: int, stream=None):
     """Canonical Q4 codes (4-byte words [N][K/8]) and fp16 scales ([N][K/64]) on the GPU ->
-    packed weight (uint8 tensor holding codes and scales)."""
+    (packed codes, packed scales), two uint8 device tensors."""
     dev = _cuda(wq_canon, "wq_canon").device
     _cuda(s_canon, "s_canon")
-    w = torch.empty(max(packed_bytes_q4(K, N), 16), dtype=torch.uint8, device=dev)
-    _check(lib().nq_pack_q4(_ptr(wq_canon), _ptr(s_canon), K, N, _ptr(w), _stream(stream)))
-    return w
+    wq, s = _packed_pair(packed_bytes_q4(K, N), K, N, dev)
+    _check(lib().nq_pack_q4(_ptr(wq_canon), _ptr(s_canon), K, N, _ptr(wq), _ptr(s), _stream(stream)))
+    return wq, s
 
 
-def pack_q5(wn_canon, wh_canon, s_canon, K: int, N: int, stream=None) -> torch.Tensor:
+def pack_q5(wn_canon, wh_canon, s_canon, K: int, N: int, stream=None):
+    """Canonical Q5 nibble plane, high plane and fp16 scales -> (packed codes, packed scales)."""
     dev = _cuda(wn_canon, "wn_canon").device
     _cuda(wh_canon, "wh_canon")
     _cuda(s_canon, "s_canon")
-    w = torch.empty(max(packed_bytes_q5(K, N), 16), dtype=torch.uint8, device=dev)
-    _check(lib().nq_pack_q5(_ptr(wn_canon), _ptr(wh_canon), _ptr(s_canon), K, N, _ptr(w), _stream(stream)))
-    return w
+    wq, s = _packed_pair(packed_bytes_q5(K, N), K, N, dev)
+    _check(lib().nq_pack_q5(_ptr(wn_canon), _ptr(wh_canon), _ptr(s_canon), K, N, _ptr(wq), _ptr(s),
+                            _stream(stream)))
+    return wq, s
 
 
 # ---------------------------------------------------------------- projections
@@ -134,51 +150,70 @@ def _out(x: torch.Tensor, N: int, out):
     return _cuda(out, "out")
 
 
-def gemm_q4(x: torch.Tensor, w: torch.Tensor, N: int, out=None, stream=None):
-    """Y[T,N] (bf16) = X[T,K] (bf16) * dequant(packed Q4 weight)."""
+def gemm_q4(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, N: int, out=None, stream=None):
+    """Y[T,N] (bf16) = X[T,K] (bf16) * dequant(packed Q4 codes wq, packed scales s)."""
     _cuda(x, "x")
     T, K = x.shape
     y = _out(x, N, out)
-    _check(lib().nq_gemm_q4(_ptr(x), _ptr(w), _ptr(y), T, K, N, _stream(stream)))
+    _check(lib().nq_gemm_q4(_ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N, _stream(stream)))
     return y
 
 
-def gemm_q5(x: torch.Tensor, w: torch.Tensor, N: int, out=None, stream=None):
+def gemm_q5(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, N: int, out=None, stream=None):
+    """Y[T,N] (bf16) = X[T,K] (bf16) * dequant(packed Q5 codes wq, packed scales s)."""
     _cuda(x, "x")
     T, K = x.shape
     y = _out(x, N, out)
-    _check(lib().nq_gemm_q5(_ptr(x), _ptr(w), _ptr(y), T, K, N, _stream(stream)))
+    _check(lib().nq_gemm_q5(_ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N, _stream(stream)))
     return y
 
 
-def swiglu_q4(x, wg, wu, N: int, out=None, stream=None):
-    """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with both weights packed Q4."""
+def gemm_q4_noalloc(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, N: int, out=None, stream=None):
+    """gemm_q4 with its scratch in the library's fixed device array (no allocation by the
+    library; `out` is allocated here by torch when not given)."""
+    _cuda(x, "x")
+    T, K = x.shape
+    y = _out(x, N, out)
+    _check(lib().nq_gemm_q4_noalloc(_ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N, _stream(stream)))
+    return y
+
+
+def swiglu_q4(x, wg, sg, wu, su, N: int, out=None, stream=None):
+    """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with both weights packed Q4 (codes, scales)."""
     _cuda(x, "x")
     T, K = x.shape
     h = _out(x, N, out)
-    _check(lib().nq_swiglu_q4(_ptr(x), _ptr(wg), _ptr(wu), _ptr(h), T, K, N, _stream(stream)))
+    _check(lib().nq_swiglu_q4(_ptr(x), _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(h), T, K, N,
+                              _stream(stream)))
     return h
 
 
-def swiglu_q5(x, wg, wu, N: int, out=None, stream=None):
-    """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with both weights packed Q5."""
+def swiglu_q5(x, wg, sg, wu, su, N: int, out=None, stream=None):
+    """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with both weights packed Q5 (codes, scales)."""
     _cuda(x, "x")
     T, K = x.shape
     h = _out(x, N, out)
-    _check(lib().nq_swiglu_q5(_ptr(x), _ptr(wg), _ptr(wu), _ptr(h), T, K, N, _stream(stream)))
+    _check(lib().nq_swiglu_q5(_ptr(x), _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(h), T, K, N,
+                              _stream(stream)))
     return h
 
 
-def dequant_q4_debug(w, K: int, N: int, stream=None) -> torch.Tensor:
-    out = torch.empty((N, K), dtype=torch.float32, device=w.device)
-    _check(lib().nq_dequant_q4_debug(_ptr(w), _ptr(out), K, N, _stream(stream)))
+def _dequant(fn, wq, s, K: int, N: int, stream):
+    out = torch.empty((N, K), dtype=torch.float32, device=wq.device)
+    _check(fn(_ptr(wq), _ptr(s), _ptr(out), K, N, _stream(stream)))
     return out
 
 
-def dequant_q5_debug(w, K: int, N: int, stream=None) -> torch.Tensor:
-    out = torch.empty((N, K), dtype=torch.float32, device=w.device)
-    _check(lib().nq_dequant_q5_debug(_ptr(w), _ptr(out), K, N, _stream(stream)))
-    return out
+def dequant_q4_debug(wq, s, K: int, N: int, operands: str = "f16", stream=None) -> torch.Tensor:
+    """fp32 [N][K] dump of a packed Q4 pair through the decoder of the fp16-operand kernels
+    (T <= 2, operands="f16") or of the bf16-operand kernels (T >= 3, operands="bf16")."""
+    f = lib().nq_dequant_q4_debug if operands == "f16" else lib().nq_dequant_q4_debug_bf16
+    return _dequant(f, wq, s, K, N, stream)
+
+
+def dequant_q5_debug(wq, s, K: int, N: int, operands: str = "f16", stream=None) -> torch.Tensor:
+    f = lib().nq_dequant_q5_debug if operands == "f16" else lib().nq_dequant_q5_debug_bf16
+    return _dequant(f, wq, s, K, N, stream)
 
 
 # ---------------------------------------------------------------- runtime / plan
@@ -189,6 +224,11 @@ def reserve(T_max: int, K_max: int, N_max: int) -> None:
 
 def device_error() -> None:
     _check(lib().nq_device_error())
+
+
+def wait_limit(ns: int = 0) -> int:
+    """Set (ns > 0) or query (ns <= 0) the bound of device-side waits; returns the previous."""
+    return int(lib().nq_wait_limit(int(ns)))
 
 
 def shutdown() -> None:
@@ -241,7 +281,8 @@ def plan_cluster_segments(bits: int, mode: int, T: int, K: int, N: int, clusters
 
 # C names, for callers that prefer them
 nq_pack_q4, nq_pack_q5 = pack_q4, pack_q5
-nq_gemm_q4, nq_gemm_q5, nq_swiglu_q4 = gemm_q4, gemm_q5, swiglu_q4
+nq_gemm_q4, nq_gemm_q5, nq_gemm_q4_noalloc = gemm_q4, gemm_q5, gemm_q4_noalloc
+nq_swiglu_q4, nq_swiglu_q5 = swiglu_q4, swiglu_q5
 nq_dequant_q4_debug, nq_dequant_q5_debug = dequant_q4_debug, dequant_q5_debug
-nq_reserve, nq_device_error, nq_shutdown = reserve, device_error, shutdown
+nq_reserve, nq_device_error, nq_shutdown, nq_wait_limit = reserve, device_error, shutdown, wait_limit
 nq_plan_info, nq_plan_segments = plan_info, plan_segments
