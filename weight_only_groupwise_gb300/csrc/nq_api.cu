@@ -7,7 +7,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/nq.h"
+#include "nq.h"
 #include "nq_launch.h"
 
 using namespace nq;

@@ -58,6 +58,10 @@ constexpr int kMaxRed = 4;           // most run hand-over buffers (consumers ->
 constexpr int kRedBufBytes = kConsumerWarps * 2 * 512;  // one buffer: every warp's two accumulator tiles
 constexpr long long kWaitTimeoutNs = 2000000000LL;  // default bound of a device-side wait: 2 s
 constexpr unsigned long long kDrainNs = 100000000ull;  // bound of each wait for copies in flight on abort
+// Bounds below this poll the barrier without suspending (mbarrier.test_wait), so that they
+// are exact; longer bounds use the suspending mbarrier.try_wait, whose own hardware time
+// limit is far below this.
+constexpr unsigned long long kPollBelowNs = 1000000ull;
 constexpr int kMaxCluster = 4;       // most K slabs handled by one thread-block cluster
 
 // Errors a kernel can raise through the workspace flag word.
@@ -386,6 +390,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-suspending test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -397,11 +414,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // block has already aborted. Never spins forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* dev_err, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const bool poll = limit_ns < kPollBelowNs;
+    if (!poll && mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (*abort_flag) return false;
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(dev_err, kDevErrTimeout);
@@ -450,6 +468,18 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -466,8 +496,9 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // scope). Same error behaviour as mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                   int* dev_err, uint64_t limit_ns) {
+    const bool poll = limit_ns < kPollBelowNs;
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait_cluster(bar, parity)) {
+    while (!(poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity))) {
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
