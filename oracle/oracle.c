@@ -151,12 +151,13 @@ void orc_gemm_q4(const uint16_t* x, const uint32_t* wq, const uint16_t* s, int T
 #pragma omp parallel
     {
         float* wrow = (float*)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1));
-        double out[8];
+        double* out = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
 #pragma omp for schedule(static)
         for (int n = 0; n < N; ++n) {
             row_q4(x, wq, s, T, K, n, wrow, out);
             for (int t = 0; t < T; ++t) y[(size_t)t * N + n] = out[t];
         }
+        free(out);
         free(wrow);
     }
 }
@@ -167,12 +168,13 @@ void orc_gemm_q5(const uint16_t* x, const uint32_t* wn, const uint32_t* wh, cons
 #pragma omp parallel
     {
         float* wrow = (float*)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1));
-        double out[8];
+        double* out = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
 #pragma omp for schedule(static)
         for (int n = 0; n < N; ++n) {
             row_q5(x, wn, wh, s, T, K, n, wrow, out);
             for (int t = 0; t < T; ++t) y[(size_t)t * N + n] = out[t];
         }
+        free(out);
         free(wrow);
     }
 }

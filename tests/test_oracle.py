@@ -114,7 +114,9 @@ def test_golden_swiglu_closed_form():
 
 # ---------------------------------------------------------------- the twin
 
-TWIN_SHAPES = [(1, 256, 128, 0), (3, 192, 48, 11), (8, 640, 80, 12), (5, 64, 16, 13)]
+# up to 64 tokens: the larger speculative-verify batches (several requests x draft tokens)
+TWIN_SHAPES = [(1, 256, 128, 0), (3, 192, 48, 11), (8, 640, 80, 12), (5, 64, 16, 13), (9, 128, 32, 14),
+               (64, 192, 48, 15)]
 
 
 @pytest.mark.parametrize("T,K,N,seed", TWIN_SHAPES)
@@ -137,6 +139,23 @@ def test_q5_dequant_and_gemm_vs_twin(T, K, N, seed):
     y = oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
     y_twin = twin.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], K)
     assert np.max(np.abs(y - y_twin)) <= 1e-12 * np.max(np.abs(y_twin))
+
+
+def test_token_rows_are_independent():
+    """Row t of Y depends only on row t of X: a 40-token batch equals its 8-token slices
+    computed separately (and the rows variant agrees), for both code widths."""
+    T, K, N = 40, 256, 48
+    p = si.q4_problem(T, K, N, 16)
+    y = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+    for t0 in range(0, T, 8):
+        part = oracle.gemm_q4(np.ascontiguousarray(p["x"][t0:t0 + 8]), p["wq"], p["s"], 8, K, N)
+        assert np.array_equal(y[t0:t0 + 8], part)
+    rows = np.arange(N, dtype=np.int32)
+    assert np.array_equal(oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows).T, y)
+    q = si.q5_problem(T, K, N, 17)
+    y5 = oracle.gemm_q5(q["x"], q["wn"], q["wh"], q["s"], T, K, N)
+    part = oracle.gemm_q5(np.ascontiguousarray(q["x"][32:]), q["wn"], q["wh"], q["s"], 8, K, N)
+    assert np.array_equal(y5[32:], part)
 
 
 def test_rows_variant_matches_full():
