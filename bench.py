@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "µs/call and achieved HBM GB/s (% of roofline) for Q4/Q5 skinny GEMM, T=1..8"
+MAX_T = 64
 KERNEL_SOURCES = ["nq_common.cuh", "nq_proj.cuh", "nq_launch.h", "nq_api.cu"]
 
 
@@ -548,7 +549,9 @@ def main():
 
 def sweep(nq, dev, stream, peak):
     """µs/call and GB/s of the other shapes (context, not the headline): the decode Q4 and
-    verify Q5 projections at every T = 1..8 (one weight set per shape, reused across T), the
+    verify Q5 projections at every T = 1..8 and at T = 16, 32, 64 (larger verify batches, one
+    launch per 8-token slice; GB/s counts the weights once) with one weight set per shape,
+    reused across T; the
     Q4 and Q5 SwiGLU blocks at T=8 and the 64-layer stack at T = 1 and 8. Each entry is the
     median of 5 timed graph replays."""
     import torch
@@ -570,7 +573,7 @@ def sweep(nq, dev, stream, peak):
         R = max(2, -(-3 * L2_BYTES // proj_bytes(bits, 8, K, N)))
         copies = make_proj_copies(nq, bits, K, N, R, 1 if bits == 4 else 2, dev)
         fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
-        for T in range(1, 9):
+        for T in list(range(1, 9)) + [16, 32, 64]:
             x = si.device_activations(T, K, gen, dev)
             y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
 

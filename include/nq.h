@@ -4,7 +4,7 @@
  * The operation (what the pages tune for single-GPU decode and speculative verify rounds):
  *
  *     Y[t,n] = sum_k X[t,k] * W[k,n],   W[k,n] = s[n, k/64] * (q[n,k] - z),
- *     z = 8 for 4-bit codes (Q4), z = 16 for 5-bit codes (Q5),  t < T <= 8.
+ *     z = 8 for 4-bit codes (Q4), z = 16 for 5-bit codes (Q5),  t < T <= 64.
  *
  * Sources: "NInfer-4090" release post (lcz.me), section "V3 做了什么" -- small-batch Q4/Q5
  * projections with T=8 routing, used by the GDN projections, the attention Q5 projections
@@ -34,8 +34,12 @@
  *   - Pointers are DEVICE pointers on the current CUDA device, owned by the caller; the
  *     library never frees or retains them. `stream` is a cudaStream_t (NULL = the legacy
  *     default stream). Calls are asynchronous on `stream`; none synchronises or prints.
- *   - Shapes: K % 64 == 0, N % 16 == 0, 0 <= T <= 8. T == 0 or N == 0 is an empty problem
+ *   - Shapes: K % 64 == 0, N % 16 == 0, 0 <= T <= 64. T == 0 or N == 0 is an empty problem
  *     (NQ_OK, nothing launched). K == 0 makes Y an empty sum: zeros are written.
+ *   - Token batches: one kernel launch handles up to 8 tokens (decode, and the T = 8 verify
+ *     rounds the pages tune); a call with T > 8 (larger speculative-verify batches, e.g.
+ *     4 requests x 8 draft tokens) runs one launch per slice of 8 tokens, each streaming the
+ *     weights again, so its time grows with ceil(T / 8).
  *   - Alignment: every pointer 16-byte aligned.
  *   - All argument checks run on the host before anything is launched; a call that returns
  *     an error has launched nothing and left every output untouched.
@@ -70,7 +74,7 @@ typedef int nq_status;
 enum {
     NQ_OK = 0,
     NQ_ERR_NULL = -1,     /* a required pointer is NULL                                   */
-    NQ_ERR_SHAPE = -2,    /* K % 64, N % 16, T outside [0, 8], negative size, too large   */
+    NQ_ERR_SHAPE = -2,    /* K % 64, N % 16, T outside [0, 64], negative size, too large  */
     NQ_ERR_ALIGN = -3,    /* a pointer is not 16-byte aligned                             */
     NQ_ERR_ALIAS = -4,    /* an output range overlaps an input range                      */
     NQ_ERR_CUDA = -5,     /* a CUDA runtime call or kernel launch failed                  */
@@ -116,7 +120,7 @@ nq_status nq_pack_q5(const uint32_t* wn_canon, const uint32_t* wh_canon, const u
 /* ---------------------------------------------------------------- projections */
 
 /*
- * nq_gemm_q4: Y = X * dequant(Wq, S) for 4-bit codes, 1 <= T <= 8 tokens.
+ * nq_gemm_q4: Y = X * dequant(Wq, S) for 4-bit codes, 1 <= T <= 64 tokens.
  *   X   device bf16 [T][K]
  *   Wq  device packed codes, S device packed fp16 scales (both from nq_pack_q4)
  *   Y   device bf16 [T][N], written

@@ -85,13 +85,13 @@ def test_shape_errors_are_reported_before_any_cuda_call(L):
     P = ctypes.c_void_p
     buf = ctypes.create_string_buffer(64)
     p16 = P((ctypes.addressof(buf) + 15) & ~15)
-    assert L.nq_gemm_q4(p16, p16, p16, p16, 9, 64, 16, None) == -2     # T > 8
+    assert L.nq_gemm_q4(p16, p16, p16, p16, 65, 64, 16, None) == -2    # T > 64
     assert L.nq_gemm_q4(p16, p16, p16, p16, -1, 64, 16, None) == -2
     assert L.nq_gemm_q5(p16, p16, p16, p16, 1, 96, 16, None) == -2     # K % 64
     assert L.nq_gemm_q4(p16, p16, p16, p16, 1, 64, 24, None) == -2     # N % 16
-    assert L.nq_gemm_q4_noalloc(p16, p16, p16, p16, 9, 64, 16, None) == -2
+    assert L.nq_gemm_q4_noalloc(p16, p16, p16, p16, 65, 64, 16, None) == -2
     assert L.nq_swiglu_q4(p16, p16, p16, p16, p16, p16, 1, 65, 16, None) == -2
-    assert L.nq_swiglu_q5(p16, p16, p16, p16, p16, p16, 9, 64, 16, None) == -2
+    assert L.nq_swiglu_q5(p16, p16, p16, p16, p16, p16, 65, 64, 16, None) == -2
     assert L.nq_swiglu_q5(p16, p16, p16, p16, p16, p16, 1, 64, 40, None) == -2
     assert L.nq_pack_q4(p16, p16, 63, 16, p16, p16, None) == -2
     assert L.nq_dequant_q5_debug(p16, p16, p16, 64, 17, None) == -2

@@ -449,3 +449,52 @@ def test_slab_cluster_parity(nq, bits, T, K, N):
         nq.device_error()
     finally:
         nq.slab_clusters(prev)
+
+
+# ---------------------------------------------------------------- larger verify batches
+
+# T > 8 (several concurrent requests' verify rows): one launch per slice of 8 tokens; the
+# ragged last slice, a single extra token and the 64-token maximum.
+LARGE_T_SHAPES = [(9, 640, 48, 0), (16, 1024, 272, 1), (24, 256, 16, 2), (33, 6208, 80, 3), (64, 512, 64, 4),
+                  (40, 17408, 32, 5)]
+
+
+@pytest.mark.parametrize("T,K,N,seed", LARGE_T_SHAPES)
+def test_large_batches_parity(nq, T, K, N, seed):
+    p = si.q4_problem(T, K, N, 400 + seed)
+    w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *w, N))
+    y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+    for t in range(T):
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+    q = si.q5_problem(T, K, N, 450 + seed)
+    w5 = gu.pack_q5(nq, q["wn"], q["wh"], q["s"], K, N)
+    y5 = gu.host_f64(nq.gemm_q5(gu.dev_bf16(q["x"]), *w5, N))
+    assert gu.rel_err(y5, oracle.gemm_q5(q["x"], q["wn"], q["wh"], q["s"], T, K, N)) <= gu.TOL
+
+
+@pytest.mark.parametrize("T", [12, 64])
+def test_large_batches_swiglu(nq, T):
+    K, N = 1024, 96
+    p = si.swiglu_problem(T, K, N, 470 + T)
+    wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    h = gu.host_f64(nq.swiglu_q4(gu.dev_bf16(p["x"]), *wg, *wu, N))
+    g, u, _ = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
+    assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+    v = si.swiglu_q5_problem(T, K, N, 480 + T)
+    h5 = gu.host_f64(_swiglu_q5_dev(nq, v, T, K, N))
+    g5, u5, _ = oracle.swiglu_q5(v["x"], v["wgn"], v["wgh"], v["sg"], v["wun"], v["wuh"], v["su"], T, K, N)
+    assert gu.rel_err(h5, g5 / (1.0 + np.exp(-g5)) * u5) <= gu.TOL
+
+
+def test_large_batch_decode_shape_sampled(nq):
+    """T=64 (eight requests x eight verify tokens) on the decode weight shape K=5120,
+    N=17408, in its full-size launch configuration, on sampled output rows."""
+    T, K, N = 64, 5120, 17408
+    p = si.q4_problem(T, K, N, 490)
+    w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q4(gu.dev_bf16(p["x"]), *w, N))
+    rows = gu.sample_rows(N, 96, 6)
+    y_ref = oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows).T
+    assert gu.rel_err(y[:, rows], y_ref) <= gu.TOL

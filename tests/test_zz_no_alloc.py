@@ -32,7 +32,7 @@ def nq():
 
 # decode shape (one K slab, split-K runs at block edges) and the T=8 down projection shape
 # (three K slabs: every run is a split-K partial, so the scratch is really used)
-@pytest.mark.parametrize("T,K,N,seed", [(1, 5120, 17408, 1), (8, 17408, 5120, 3), (3, 640, 48, 9)])
+@pytest.mark.parametrize("T,K,N,seed", [(1, 5120, 17408, 1), (8, 17408, 5120, 3), (3, 640, 48, 9), (20, 1024, 272, 11)])
 def test_noalloc_matches_allocating_call_twice(nq, T, K, N, seed):
     p = si.q4_problem(T, K, N, seed)
     w = gu.pack_q4(nq, p["wq"], p["s"], K, N)

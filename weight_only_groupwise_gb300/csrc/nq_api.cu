@@ -280,11 +280,30 @@ int resident_clusters(DevState& d, int bits, bool swiglu, int S) {
     return c < cap ? c : cap;
 }
 
+// The work split of one launch of T <= kSliceT tokens: the stream-K plan, or slab clusters when
+// K needs 2..kMaxCluster slabs (bf16 operands), enough clusters fit and they are switched on.
+bool choose_plans(int bits, bool swiglu, int T, int K, int N, DevState& d, Plan& p, Plan& q) {
+    if (!make_plan(bits, swiglu ? 1 : 0, T, K, N, d.sms, p)) return false;
+    q = p;
+    if (g_cluster && p.S >= 2 && p.S <= kMaxCluster && !p.f16) {
+        Plan p2, q2;
+        const int C = resident_clusters(d, bits, swiglu, p.S);
+        if (C > 0 && make_cluster_plans(bits, swiglu ? 1 : 0, T, K, N, C, p2, q2)) {
+            p = p2;
+            q = q2;
+        }
+    }
+    return true;
+}
+
 // Shared body of the projection entry points (Q4/Q5 GEMM, Q4/Q5 SwiGLU). W0/S0: the weight
-// (gemm) or the gate weight (swiglu); W1/S1: the up weight (swiglu only).
+// (gemm) or the gate weight (swiglu); W1/S1: the up weight (swiglu only). T up to kSliceT runs
+// as one launch; larger batches (up to kMaxT) as one launch per slice of kSliceT tokens, each
+// streaming the weights again. Every slice's plan and the workspace are settled before the
+// first launch, so an error still launches nothing.
 nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
                   const void* S1, void* Y, int T, int K, int N, void* stream) {
-    if (T < 0 || T > 8) return NQ_ERR_SHAPE;
+    if (T < 0 || T > kMaxT) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
     if (T == 0 || N == 0) return NQ_OK;  // empty output
@@ -303,39 +322,40 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     if (K == 0) {  // empty sum
         return cudaMemsetAsync(Y, 0, yb, as_stream(stream)) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
     }
-    ProjArgs a;
-    if (!make_plan(bits, swiglu ? 1 : 0, T, K, N, d->sms, a.p)) return NQ_ERR_SHAPE;
-    a.q = a.p;
-    // K in several slabs (bf16 operands): slab clusters when enough of them fit at once.
-    if (g_cluster && a.p.S >= 2 && a.p.S <= kMaxCluster && !a.p.f16) {
-        Plan p2, q2;
-        const int C = resident_clusters(*d, bits, swiglu, a.p.S);
-        if (C > 0 && make_cluster_plans(bits, swiglu ? 1 : 0, T, K, N, C, p2, q2)) {
-            a.p = p2;
-            a.q = q2;
-        }
+    // At most two distinct slice sizes: full slices and the remainder.
+    const int full = T < kSliceT ? T : kSliceT, rest = T > kSliceT ? T % kSliceT : 0;
+    ProjArgs a_full, a_rest;
+    if (!choose_plans(bits, swiglu, full, K, N, *d, a_full.p, a_full.q)) return NQ_ERR_SHAPE;
+    long long slots = a_full.q.slots, tickets = a_full.q.RP;
+    if (rest > 0) {
+        if (!choose_plans(bits, swiglu, rest, K, N, *d, a_rest.p, a_rest.q)) return NQ_ERR_SHAPE;
+        if (a_rest.q.slots > slots) slots = a_rest.q.slots;
     }
-    st = ensure_workspace(*d, a.q.slots, a.q.RP);
+    st = ensure_workspace(*d, slots, tickets);
     if (st != NQ_OK) return st;
-    a.X = static_cast<const uint16_t*>(X);
-    a.W0 = static_cast<const uint8_t*>(W0);
-    a.S0 = static_cast<const uint8_t*>(S0);
-    a.W1 = static_cast<const uint8_t*>(swiglu ? W1 : W0);
-    a.S1 = static_cast<const uint8_t*>(swiglu ? S1 : S0);
-    a.Y = static_cast<uint16_t*>(Y);
-    a.dev_err = reinterpret_cast<int*>(d->ws);
-    a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
-    a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
-    a.wait_ns = g_wait_ns;
-    cudaError_t e;
-    if (swiglu)
-        e = bits == 4 ? launch_proj_swiglu_q4(a, as_stream(stream), g_pdl)
-                      : launch_proj_swiglu_q5(a, as_stream(stream), g_pdl);
-    else if (bits == 4)
-        e = launch_proj_q4(a, as_stream(stream), g_pdl);
-    else
-        e = launch_proj_q5(a, as_stream(stream), g_pdl);
-    return e == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+    for (int t0 = 0; t0 < T; t0 += kSliceT) {
+        ProjArgs a = T - t0 >= kSliceT || rest == 0 ? a_full : a_rest;
+        a.X = static_cast<const uint16_t*>(X) + (size_t)t0 * K;
+        a.W0 = static_cast<const uint8_t*>(W0);
+        a.S0 = static_cast<const uint8_t*>(S0);
+        a.W1 = static_cast<const uint8_t*>(swiglu ? W1 : W0);
+        a.S1 = static_cast<const uint8_t*>(swiglu ? S1 : S0);
+        a.Y = static_cast<uint16_t*>(Y) + (size_t)t0 * N;
+        a.dev_err = reinterpret_cast<int*>(d->ws);
+        a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
+        a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
+        a.wait_ns = g_wait_ns;
+        cudaError_t e;
+        if (swiglu)
+            e = bits == 4 ? launch_proj_swiglu_q4(a, as_stream(stream), g_pdl)
+                          : launch_proj_swiglu_q5(a, as_stream(stream), g_pdl);
+        else if (bits == 4)
+            e = launch_proj_q4(a, as_stream(stream), g_pdl);
+        else
+            e = launch_proj_q5(a, as_stream(stream), g_pdl);
+        if (e != cudaSuccess) return NQ_ERR_CUDA;
+    }
+    return NQ_OK;
 }
 
 nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N, void* wq_packed,
@@ -412,7 +432,7 @@ const char* nq_status_string(nq_status s) {
     switch (s) {
         case NQ_OK: return "NQ_OK";
         case NQ_ERR_NULL: return "NQ_ERR_NULL: a required pointer is NULL";
-        case NQ_ERR_SHAPE: return "NQ_ERR_SHAPE: need K % 64 == 0, N % 16 == 0, 0 <= T <= 8";
+        case NQ_ERR_SHAPE: return "NQ_ERR_SHAPE: need K % 64 == 0, N % 16 == 0, 0 <= T <= 64";
         case NQ_ERR_ALIGN: return "NQ_ERR_ALIGN: pointers must be 16-byte aligned";
         case NQ_ERR_ALIAS: return "NQ_ERR_ALIAS: an output overlaps an input";
         case NQ_ERR_CUDA: return "NQ_ERR_CUDA: a CUDA call or launch failed";
@@ -483,7 +503,8 @@ long long nq_wait_limit(long long ns) {
 }
 
 nq_status nq_reserve(int T_max, int K_max, int N_max) {
-    if (T_max < 1 || T_max > 8) return NQ_ERR_SHAPE;
+    if (T_max < 1 || T_max > kMaxT) return NQ_ERR_SHAPE;
+    if (T_max > kSliceT) T_max = kSliceT;  // larger batches run as slices of kSliceT tokens
     nq_status st = check_shape(K_max, N_max);
     if (st != NQ_OK) return st;
     DevState* d = nullptr;

@@ -63,6 +63,8 @@ constexpr unsigned long long kDrainNs = 100000000ull;  // bound of each wait for
 // limit is far below this.
 constexpr unsigned long long kPollBelowNs = 1000000ull;
 constexpr int kMaxCluster = 4;       // most K slabs handled by one thread-block cluster
+constexpr int kSliceT = 8;           // tokens one projection launch handles (MMA N = 8)
+constexpr int kMaxT = 64;            // tokens one projection call accepts (kSliceT per launch)
 
 // Errors a kernel can raise through the workspace flag word.
 constexpr int kDevErrTimeout = 1;

@@ -96,7 +96,7 @@ int noalloc_take_error(int dev) {
 
 extern "C" nq_status nq_gemm_q4_noalloc(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N,
                                         void* stream) {
-    if (T < 0 || T > 8 || K < 0 || N < 0 || K > (1 << 20) || N > (1 << 20) || K % kGroup || N % kTileRows)
+    if (T < 0 || T > kMaxT || K < 0 || N < 0 || K > (1 << 20) || N > (1 << 20) || K % kGroup || N % kTileRows)
         return NQ_ERR_SHAPE;
     if (T == 0 || N == 0) return NQ_OK;
     if (!X || !Wq || !S || !Y) return NQ_ERR_NULL;
@@ -110,24 +110,36 @@ extern "C" nq_status nq_gemm_q4_noalloc(const void* X, const void* Wq, const voi
     if (st != NQ_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return cudaMemsetAsync(Y, 0, yb, s) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
-    ProjArgs a;
-    if (!make_plan(4, 0, T, K, N, sms, a.p)) return NQ_ERR_SHAPE;
-    a.q = a.p;  // stream-K only (no slab clusters)
-    if (a.p.slots > kStaticSlots || a.p.RP > kStaticTickets) return NQ_ERR_SCRATCH;
+    // Batches above kSliceT tokens run as one launch per slice (as nq_gemm_q4). Both slice
+    // sizes (full slices and the remainder) are planned and checked before anything runs.
+    const int full = T < kSliceT ? T : kSliceT, rest = T > kSliceT ? T % kSliceT : 0;
+    Plan plans[2];
+    for (int i = 0; i < 2; ++i) {
+        const int tn = i == 0 ? full : rest;
+        if (tn == 0) continue;
+        if (!make_plan(4, 0, tn, K, N, sms, plans[i])) return NQ_ERR_SHAPE;
+        if (plans[i].slots > kStaticSlots || plans[i].RP > kStaticTickets) return NQ_ERR_SCRATCH;
+    }
     uint8_t* base = static_cast<uint8_t*>(scratch);
-    // The array keeps the previous call's contents: this call's tickets must start at zero,
-    // so clear them on the call's stream (no allocation involved). The error word is left
-    // alone: it stays set until nq_device_error reports it.
-    if (cudaMemsetAsync(base + kStaticTicketOff, 0, (size_t)a.p.RP * 4, s) != cudaSuccess) return NQ_ERR_CUDA;
-    a.X = static_cast<const uint16_t*>(X);
-    a.W0 = static_cast<const uint8_t*>(Wq);
-    a.W1 = static_cast<const uint8_t*>(Wq);
-    a.S0 = static_cast<const uint8_t*>(S);
-    a.S1 = static_cast<const uint8_t*>(S);
-    a.Y = static_cast<uint16_t*>(Y);
-    a.dev_err = reinterpret_cast<int*>(base);
-    a.tickets = reinterpret_cast<int*>(base + kStaticTicketOff);
-    a.partials = reinterpret_cast<float*>(base + kStaticPartialOff);
-    a.wait_ns = wait_limit_ns();
-    return launch_proj_q4(a, s, false) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+    for (int t0 = 0; t0 < T; t0 += kSliceT) {
+        ProjArgs a;
+        a.p = T - t0 >= kSliceT || rest == 0 ? plans[0] : plans[1];
+        a.q = a.p;  // stream-K only (no slab clusters)
+        // The array keeps the previous call's contents: this launch's tickets must start at
+        // zero, so clear them on the call's stream (no allocation involved). The error word is
+        // left alone: it stays set until nq_device_error reports it.
+        if (cudaMemsetAsync(base + kStaticTicketOff, 0, (size_t)a.p.RP * 4, s) != cudaSuccess) return NQ_ERR_CUDA;
+        a.X = static_cast<const uint16_t*>(X) + (size_t)t0 * K;
+        a.W0 = static_cast<const uint8_t*>(Wq);
+        a.W1 = static_cast<const uint8_t*>(Wq);
+        a.S0 = static_cast<const uint8_t*>(S);
+        a.S1 = static_cast<const uint8_t*>(S);
+        a.Y = static_cast<uint16_t*>(Y) + (size_t)t0 * N;
+        a.dev_err = reinterpret_cast<int*>(base);
+        a.tickets = reinterpret_cast<int*>(base + kStaticTicketOff);
+        a.partials = reinterpret_cast<float*>(base + kStaticPartialOff);
+        a.wait_ns = wait_limit_ns();
+        if (launch_proj_q4(a, s, false) != cudaSuccess) return NQ_ERR_CUDA;
+    }
+    return NQ_OK;
 }
