@@ -55,6 +55,13 @@ def lib():
         L.orc_swiglu_q4_rows.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P]
         L.orc_swiglu_q5.argtypes = [P, P, P, P, P, P, P, I, I, I, P, P, P]
         L.orc_swiglu_q5_rows.argtypes = [P, P, P, P, P, P, P, I, I, P, I, P, P, P]
+        L.orc_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_e2m1_to_f64.restype = ctypes.c_double
+        L.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_to_f64.restype = ctypes.c_double
+        L.orc_dequant_fp4.argtypes = [P, P, ctypes.c_float, I, I, P]
+        L.orc_gemm_fp4.argtypes = [P, P, P, ctypes.c_float, I, I, I, P]
+        L.orc_gemm_fp4_rows.argtypes = [P, P, P, ctypes.c_float, I, I, P, I, P]
         L.orc_num_threads.restype = I
         L.orc_set_num_threads.argtypes = [I]
         _lib = L
@@ -182,6 +189,38 @@ def swiglu_q5_rows(x, wgn, wgh, sg, wun, wuh, su, T: int, K: int, rows):
     lib().orc_swiglu_q5_rows(_p(x), _p(wgn), _p(wgh), _p(sg), _p(wun), _p(wuh), _p(su), T, K,
                              _p(r), len(r), _p(g), _p(u), _p(h))
     return g, u, h
+
+
+def e2m1_to_f64(c: int) -> float:
+    return lib().orc_e2m1_to_f64(int(c))
+
+
+def e4m3_to_f64(b: int) -> float:
+    return lib().orc_e4m3_to_f64(int(b))
+
+
+def dequant_fp4(codes, sf, g: float, K: int, N: int) -> np.ndarray:
+    """NVFP4 weights in fp32 [N][K]: codes uint32 [N][K/8], e4m3 scales uint8 [N][K/16]."""
+    codes, sf = _c(codes, np.uint32), _c(sf, np.uint8)
+    w = np.empty((N, K), np.float32)
+    lib().orc_dequant_fp4(_p(codes), _p(sf), float(g), K, N, _p(w))
+    return w
+
+
+def gemm_fp4(x, codes, sf, g: float, T: int, K: int, N: int) -> np.ndarray:
+    x, codes, sf = _c(x, np.uint16), _c(codes, np.uint32), _c(sf, np.uint8)
+    y = np.empty((T, N), np.float64)
+    lib().orc_gemm_fp4(_p(x), _p(codes), _p(sf), float(g), T, K, N, _p(y))
+    return y
+
+
+def gemm_fp4_rows(x, codes, sf, g: float, T: int, K: int, rows) -> np.ndarray:
+    """Y[t, rows[i]] as an array [len(rows)][T]."""
+    x, codes, sf = _c(x, np.uint16), _c(codes, np.uint32), _c(sf, np.uint8)
+    r = _c(rows, np.int32)
+    y = np.empty((len(r), T), np.float64)
+    lib().orc_gemm_fp4_rows(_p(x), _p(codes), _p(sf), float(g), T, K, _p(r), len(r), _p(y))
+    return y
 
 
 def num_threads() -> int:

@@ -242,6 +242,92 @@ void orc_swiglu_q5_rows(const uint16_t* x, const uint32_t* wgn, const uint32_t* 
     for (size_t i = 0; i < (size_t)count * T; ++i) h[i] = orc_round_bf16(orc_silu_mul(g[i], u[i]));
 }
 
+/* ---------------------------------------------------------------- NVFP4 weights
+ *
+ * The 4-bit floating-point weight format the pages name beside groupwise int ("ninfer-ext"
+ * README, section "与原版 NInfer 的对比": the NVFP4 MLP-projection A16 tensor-core kernel).
+ * The pages print no layout; the plain reading of NVFP4 is used:
+ *   element  e2m1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0;
+ *            exponent 0 is subnormal: value = m * 0.5; otherwise 2^(e-1) * (1 + m/2)
+ *   block    16 consecutive elements along K share one scale,
+ *   scale    e4m3 (the "fn" variant): sign bit 7, exponent bits 6..3 (bias 7), mantissa
+ *            bits 2..0; exponent 0 is subnormal: m * 2^-9; S.1111.111 is NaN; no infinity
+ *   tensor   one fp32 scale g for the whole matrix
+ *   W[n,k] = g * scale(sf[n, k/16]) * e2m1(c[n,k]),  Y[t,n] = sum_k X[t,k] * W[n,k]
+ * Canonical layout: codes uint32 [N][K/8] with nibble i of word j the code of k = 8j+i (the
+ * same rule as the 4-bit integer codes), scales uint8 [N][K/16] e4m3 bit patterns.
+ * Dequantised weight in fp32: (float)g * (float)(scale * element); the inner product is
+ * exact in fp32 (at most 2 + 4 significant bits), so it is rounded once. */
+
+double orc_e2m1_to_f64(uint8_t c) {
+    int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+double orc_e4m3_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);           /* m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+static inline float fp4_weight(const uint32_t* codes, const uint8_t* sf, float g, int K, int n, int k) {
+    uint8_t c = (uint8_t)q4_code(codes, K, n, k);
+    float inner = (float)(orc_e4m3_to_f64(sf[(size_t)n * (K / 16) + (k >> 4)]) * orc_e2m1_to_f64(c));
+    return g * inner;
+}
+
+/* Step "dequantise" for NVFP4: W32[n][k]. */
+void orc_dequant_fp4(const uint32_t* codes, const uint8_t* sf, float g, int K, int N, float* w) {
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) w[(size_t)n * K + k] = fp4_weight(codes, sf, g, K, n, k);
+}
+
+static void row_fp4(const uint16_t* x, const uint32_t* codes, const uint8_t* sf, float g, int T, int K, int n,
+                    float* wrow, double* out) {
+    for (int k = 0; k < K; ++k) wrow[k] = fp4_weight(codes, sf, g, K, n, k);
+    for (int t = 0; t < T; ++t) {
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k) acc += (double)wrow[k] * orc_bf16_to_f64(x[(size_t)t * K + k]);
+        out[t] = acc;
+    }
+}
+
+/* Y[t][n] in fp64 for NVFP4 weights (dequantise + contract, k order). */
+void orc_gemm_fp4(const uint16_t* x, const uint32_t* codes, const uint8_t* sf, float g, int T, int K, int N,
+                  double* y) {
+#pragma omp parallel
+    {
+        float* wrow = (float*)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1));
+        double* out = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+#pragma omp for schedule(static)
+        for (int n = 0; n < N; ++n) {
+            row_fp4(x, codes, sf, g, T, K, n, wrow, out);
+            for (int t = 0; t < T; ++t) y[(size_t)t * N + n] = out[t];
+        }
+        free(out);
+        free(wrow);
+    }
+}
+
+void orc_gemm_fp4_rows(const uint16_t* x, const uint32_t* codes, const uint8_t* sf, float g, int T, int K,
+                       const int* rows, int count, double* y /* [count][T] */) {
+#pragma omp parallel
+    {
+        float* wrow = (float*)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1));
+#pragma omp for schedule(dynamic)
+        for (int i = 0; i < count; ++i) row_fp4(x, codes, sf, g, T, K, rows[i], wrow, y + (size_t)i * T);
+        free(wrow);
+    }
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -59,3 +59,34 @@ def gemm_q5(x, wn, wh, s, K):
 def silu(g: np.ndarray) -> np.ndarray:
     """silu via the logistic function of torch (a library routine), in fp64."""
     return np.asarray(g) * torch.sigmoid(torch.from_numpy(np.asarray(g, np.float64))).numpy()
+
+
+# ---------------------------------------------------------------- NVFP4
+
+def e4m3_f32(b: np.ndarray) -> np.ndarray:
+    """e4m3 ("fn") bit patterns -> fp32 through PyTorch's float8_e4m3fn type."""
+    t = torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float32).numpy()
+
+
+def e2m1_f32(c: np.ndarray) -> np.ndarray:
+    """e2m1 codes -> fp32 without a formula of our own: the fields of a 4-bit code widen into
+    an e4m3 bit pattern (same sign; exponent re-biased from 1 to 7; mantissa moved to the top
+    of e4m3's three bits; the one subnormal, 0.5, is the normal e4m3 2^-1), which PyTorch
+    decodes."""
+    c = np.asarray(c, dtype=np.uint8)
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    E = np.where(e == 0, np.where(m == 1, 6, 0), e + 6).astype(np.uint8)
+    M = np.where(e == 0, 0, m << 2).astype(np.uint8)
+    return e4m3_f32(((s << 7) | (E << 3) | M).astype(np.uint8))
+
+
+def weights_fp4(codes: np.ndarray, sf: np.ndarray, g: float, K: int) -> np.ndarray:
+    """fp32 W[n][k] = g * (scale * element); the inner product is exact in fp32."""
+    elem = e2m1_f32(codes_q4(codes, K).astype(np.uint8))
+    scale = np.repeat(e4m3_f32(sf), 16, axis=1)
+    return np.float32(g) * (scale * elem)
+
+
+def gemm_fp4(x, codes, sf, g, K):
+    return gemm(x, weights_fp4(codes, sf, g, K))

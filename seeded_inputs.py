@@ -103,6 +103,27 @@ def swiglu_q5_problem(T: int, K: int, N: int, seed: int) -> dict:
             "wuh": wuh, "su": su}
 
 
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> e4m3 ("fn", round to nearest even, PyTorch cast) as uint8 bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+FP4_BLOCK = 16
+FP4_GLOBAL_SCALE = 0.0078125  # 2^-7: the per-tensor fp32 scale of the synthetic NVFP4 weights
+
+
+def fp4_problem(T: int, K: int, N: int, seed: int, g: float = FP4_GLOBAL_SCALE) -> dict:
+    """One seeded NVFP4 projection: e2m1 code words (uniform 32-bit words: every 4-bit code,
+    both zeros included, equally likely), then one e4m3 block scale per 16 elements of a row
+    (fp32 exp(N(0, 0.25)) cast to e4m3), then X ~ N(0,1) in bf16; g is the tensor scale."""
+    rg = rng(seed)
+    codes = code_words(rg, N, K // 8)
+    sf = e4m3_bits(np.exp(SCALE_SIGMA * rg.standard_normal((N, K // FP4_BLOCK))).astype(np.float32))
+    x = activations(rg, T, K)
+    return {"T": T, "K": K, "N": N, "x": x, "codes": codes, "sf": sf, "g": float(g)}
+
+
 # The five workloads. Shapes are those of a 27B-class dense decoder layer.
 TINY_Q4 = dict(T=1, K=256, N=128, seed=0)                  # tiny Q4 correctness case
 DECODE_Q4 = dict(T=1, K=5120, N=17408, seed=1)             # decode GEMV, FFN up-projection
@@ -132,6 +153,11 @@ def device_code_words(rows: int, words: int, gen: "torch.Generator", device) -> 
 def device_scales(N: int, K: int, gen, device) -> "torch.Tensor":
     z = torch.randn((N, K // GROUP), generator=gen, device=device, dtype=torch.float32)
     return (SCALE_BASE * torch.exp(SCALE_SIGMA * z)).to(torch.float16).view(torch.int16)
+
+
+def device_fp4_scales(N: int, K: int, gen, device) -> "torch.Tensor":
+    z = torch.randn((N, K // FP4_BLOCK), generator=gen, device=device, dtype=torch.float32)
+    return torch.exp(SCALE_SIGMA * z).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
 def device_activations(T: int, K: int, gen, device) -> "torch.Tensor":

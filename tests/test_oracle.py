@@ -313,6 +313,64 @@ def test_dequant_is_exact_product():
     assert np.array_equal(w, exact)
 
 
+# ---------------------------------------------------------------- NVFP4
+
+def test_e4m3_decoder_exhaustive_vs_torch():
+    ours = np.array([oracle.e4m3_to_f64(b) for b in range(256)])
+    ref = twin.e4m3_f32(np.arange(256, dtype=np.uint8)).astype(np.float64)
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.array_equal(np.signbit(ours[ok]), np.signbit(ref[ok]))   # -0 stays -0
+
+
+def test_e2m1_decoder_all_codes():
+    ours = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
+    assert np.array_equal(ours, twin.e2m1_f32(np.arange(16, dtype=np.uint8)).astype(np.float64))
+    # the format's value set: eight magnitudes, the negative codes mirror the positive ones
+    assert list(ours[:8]) == sorted(ours[:8]) and ours[1] == 0.5 and ours[2] == 1.0 and ours[7] == 6.0
+    assert np.array_equal(ours[8:], -ours[:8]) and np.signbit(ours[8]) and ours[8] == 0.0
+
+
+FP4_SHAPES = [(1, 256, 32, 0), (3, 192, 48, 1), (8, 640, 16, 2), (20, 64, 32, 3)]
+
+
+@pytest.mark.parametrize("T,K,N,seed", FP4_SHAPES)
+def test_fp4_dequant_and_gemm_vs_twin(T, K, N, seed):
+    p = si.fp4_problem(T, K, N, 60 + seed)
+    w = oracle.dequant_fp4(p["codes"], p["sf"], p["g"], K, N)
+    w_twin = twin.weights_fp4(p["codes"], p["sf"], p["g"], K)
+    assert np.array_equal(w.view(np.uint32), w_twin.view(np.uint32))
+    y = oracle.gemm_fp4(p["x"], p["codes"], p["sf"], p["g"], T, K, N)
+    y_twin = twin.gemm_fp4(p["x"], p["codes"], p["sf"], p["g"], K)
+    assert np.max(np.abs(y - y_twin)) <= 1e-12 * np.max(np.abs(y_twin))
+    rows = np.array([0, N - 1, N // 2], np.int32)
+    assert np.array_equal(oracle.gemm_fp4_rows(p["x"], p["codes"], p["sf"], p["g"], T, K, rows).T, y[:, rows])
+
+
+def test_fp4_block_structure():
+    """One scale per 16 elements: a block scale of 2 doubles exactly its own 16 weights; the
+    tensor scale multiplies every weight; the weights are the exact products (fp64 check)."""
+    K, N = 128, 16
+    p = si.fp4_problem(1, K, N, 70, g=1.0)
+    w = oracle.dequant_fp4(p["codes"], p["sf"], 1.0, K, N).astype(np.float64)
+    sf2 = p["sf"].copy()
+    sf2[3, 5] = 0x40                                   # e4m3 2.0
+    sf1 = p["sf"].copy()
+    sf1[3, 5] = 0x38                                   # e4m3 1.0
+    w2 = oracle.dequant_fp4(p["codes"], sf2, 1.0, K, N).astype(np.float64)
+    w1 = oracle.dequant_fp4(p["codes"], sf1, 1.0, K, N).astype(np.float64)
+    assert np.array_equal(w2[3, 80:96], 2.0 * w1[3, 80:96])
+    mask = np.ones_like(w, bool)
+    mask[3, 80:96] = False
+    assert np.array_equal(w2[mask], w[mask])
+    wg = oracle.dequant_fp4(p["codes"], p["sf"], 0.25, K, N).astype(np.float64)
+    assert np.array_equal(wg, 0.25 * w)
+    exact = np.repeat(twin.e4m3_f32(p["sf"]).astype(np.float64), 16, axis=1) * \
+        twin.e2m1_f32(twin.codes_q4(p["codes"], K).astype(np.uint8)).astype(np.float64)
+    assert np.array_equal(w, exact)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 MUTATIONS = [
@@ -323,6 +381,9 @@ MUTATIONS = [
     ("x row stride transposed", "orc_bf16_to_f64(x[(size_t)t * K + k]);\n        out[t] = acc;\n    }\n}\n\nstatic void row_q5",
      "orc_bf16_to_f64(x[(size_t)k * T + t]);\n        out[t] = acc;\n    }\n}\n\nstatic void row_q5"),
     ("fp16 subnormal off by one", "ldexp((double)f, -24)", "ldexp((double)f, -23)"),
+    ("fp4 block of 32", "sf[(size_t)n * (K / 16) + (k >> 4)]", "sf[(size_t)n * (K / 16) + (k >> 5)]"),
+    ("e2m1 exponent bias 0", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
+    ("e4m3 subnormal scale", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
 ]
 
 
@@ -337,6 +398,7 @@ def _build_mutant(src: str, tmp: str) -> "ctypes.CDLL":
     P, I = ctypes.c_void_p, ctypes.c_int
     L.orc_gemm_q4.argtypes = [P, P, P, I, I, I, P]
     L.orc_gemm_q5.argtypes = [P, P, P, P, I, I, I, P]
+    L.orc_gemm_fp4.argtypes = [P, P, P, ctypes.c_float, I, I, I, P]
     return L
 
 
@@ -365,4 +427,12 @@ def test_planted_mistake_is_caught(name, old, new):
         yf = np.empty((f["T"], f["N"]))
         L.orc_gemm_q4(oracle._p(x), oracle._p(wq), oracle._p(s), f["T"], f["K"], f["N"], oracle._p(yf))
         caught |= not np.array_equal(yf, np.array(f["y_expected"]))
+        # NVFP4 vs its twin, with block scales that include e4m3 subnormals
+        r = si.fp4_problem(T, K, N, 42)
+        r["sf"][:, ::3] = np.arange(1, 8, dtype=np.uint8)[np.arange(r["sf"][:, ::3].size) % 7].reshape(
+            r["sf"][:, ::3].shape)
+        y4 = np.empty((T, N))
+        L.orc_gemm_fp4(oracle._p(r["x"]), oracle._p(r["codes"]), oracle._p(r["sf"]), r["g"], T, K, N,
+                       oracle._p(y4))
+        caught |= not np.allclose(y4, twin.gemm_fp4(r["x"], r["codes"], r["sf"], r["g"], K), rtol=1e-9, atol=0)
         assert caught, name
