@@ -65,6 +65,11 @@ def proj_bytes(bits: int, T: int, K: int, N: int) -> int:
     return K * N * bits // 8 + N * (K // 64) * 2 + T * K * 2 + T * N * 2
 
 
+def fp4_bytes(T: int, K: int, N: int) -> int:
+    """NVFP4: e2m1 codes (K*N/2) + e4m3 block scales (N*K/16) + X + Y."""
+    return K * N // 2 + N * K // 16 + T * K * 2 + T * N * 2
+
+
 def swiglu_bytes(T: int, K: int, N: int, bits: int = 4) -> int:
     return 2 * (K * N * bits // 8 + N * (K // 64) * 2) + T * K * 2 + T * N * 2
 
@@ -212,6 +217,21 @@ def make_proj_copies(nq, bits, K, N, copies, seed, dev):
         else:
             out.append(nq.pack_q5(wn, wh, s, K, N))
         del wn, s
+    torch.cuda.synchronize()
+    return out
+
+
+def make_fp4_copies(nq, K, N, copies, seed, dev):
+    import torch
+    import seeded_inputs as si
+    gen = torch.Generator(device=dev)
+    out = []
+    for r in range(copies):
+        gen.manual_seed(seed * 1000 + r)
+        codes = si.device_code_words(N, K // 8, gen, dev)
+        sf = si.device_fp4_scales(N, K, gen, dev)
+        out.append(nq.pack_fp4(codes, sf, K, N))
+        del codes, sf
     torch.cuda.synchronize()
     return out
 
@@ -583,6 +603,19 @@ def sweep(nq, dev, stream, peak):
             record(name, T, time_graph(step, steps, 5, stream), steps, proj_bytes(bits, T, K, N), 1)
         del copies
         torch.cuda.empty_cache()
+    # NVFP4 weights on the decode shape (the pages' NVFP4 MLP-projection A16 kernel)
+    K, N = 5120, 17408
+    R = max(2, -(-3 * L2_BYTES // fp4_bytes(8, K, N)))
+    copies = make_fp4_copies(nq, K, N, R, 9, dev)
+    for T in (1, 2, 4, 8):
+        x = si.device_activations(T, K, gen, dev)
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+
+        def step(i, x=x, y=y):
+            nq.gemm_fp4(x, *copies[i % R], si.FP4_GLOBAL_SCALE, N, out=y)
+        record("decode_fp4", T, time_graph(step, 100, 5, stream), 100, fp4_bytes(T, K, N), 1)
+    del copies
+    torch.cuda.empty_cache()
     for name in ("swiglu_block", "swiglu_block_q5"):
         w = dict(WORKLOADS[name], T=8)
         step, b, R, note, keep = build_step(nq, w, dev)

@@ -185,6 +185,43 @@ nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void
 nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su,
                        void* H, int T, int K, int N, void* stream);
 
+/* ---------------------------------------------------------------- NVFP4 weights */
+
+/*
+ * NVFP4 weights: the 4-bit floating-point format the pages run beside groupwise int
+ * ("ninfer-ext" README, section "与原版 NInfer 的对比": an NVFP4 MLP-projection tensor-core
+ * kernel with 16-bit activations, "A16"). The pages print no layout; this library reads NVFP4
+ * as: e2m1 elements (sign, 2 exponent bits with bias 1, 1 mantissa bit; values 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6 and their negatives), one e4m3 scale (bias 7, the "fn" variant) per 16
+ * consecutive elements along K, and one fp32 tensor scale g:
+ *     W[k,n] = g * e4m3(sf[n, k/16]) * e2m1(c[n,k]),   Y[t,n] = sum_k X[t,k] * W[k,n].
+ * Canonical layouts: codes uint32 [N][K/8], nibble i of word j the code of k = 8j+i (the Q4
+ * rule); scales uint8 [N][K/16] e4m3 bit patterns. K % 64 == 0, N % 16 == 0 as above.
+ * The kernels decode each weight pair into fp16 exactly (scale times element has at most 6
+ * significant bits) and run fp16 tensor-core MMAs against X converted to fp16 with a
+ * per-token power-of-two range factor; accumulation is fp32, Y is rounded once to bf16.
+ */
+
+/* Bytes of packed NVFP4 codes (K*N/2) and of packed NVFP4 block scales (N*K/16). */
+size_t nq_packed_bytes_fp4(int K, int N);
+size_t nq_scale_bytes_fp4(int K, int N);
+
+/* nq_pack_fp4: canonical NVFP4 codes and e4m3 scales (device) -> packed pair (device, sizes
+ * above); outputs must not overlap the inputs or each other. */
+nq_status nq_pack_fp4(const uint32_t* codes_canon, const uint8_t* sf_canon, int K, int N, void* wq_packed,
+                      void* s_packed, void* stream);
+
+/* nq_gemm_fp4: Y = X * W for NVFP4 weights packed by nq_pack_fp4, global_scale = g,
+ * 1 <= T <= 64 (slices of 8 tokens as the other projections). Arguments, alignment, errors
+ * and launch behaviour as nq_gemm_q4. */
+nq_status nq_gemm_fp4(const void* X, const void* Wq, const void* S, float global_scale, void* Y, int T, int K,
+                      int N, void* stream);
+
+/* nq_dequant_fp4_debug: out[n][k] = g * (scale * element) in fp32 through the kernels' own
+ * decoder; exact, so it must equal the CPU definition bit for bit. */
+nq_status nq_dequant_fp4_debug(const void* Wq, const void* S, float global_scale, float* out, int K, int N,
+                               void* stream);
+
 /* ---------------------------------------------------------------- debug dumps */
 
 /*

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     for must in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_swiglu_q4",
                  "nq_swiglu_q5", "nq_dequant_q4_debug", "nq_dequant_q5_debug",
                  "nq_dequant_q4_debug_bf16", "nq_dequant_q5_debug_bf16", "nq_status_string",
-                 "nq_packed_bytes_q4", "nq_packed_bytes_q5", "nq_scale_bytes", "nq_wait_limit"):
+                 "nq_packed_bytes_q4", "nq_packed_bytes_q5", "nq_scale_bytes", "nq_wait_limit",
+                 "nq_pack_fp4", "nq_gemm_fp4", "nq_dequant_fp4_debug", "nq_packed_bytes_fp4", "nq_scale_bytes_fp4"):
         assert must in names
 
 
@@ -65,6 +66,9 @@ def test_sizes_and_strings(L):
     assert nq.packed_bytes_q4(100, 16) == 0          # K % 64 != 0
     assert nq.packed_bytes_q4(64, 8) == 0            # N % 16 != 0
     assert nq.scale_bytes(64, 8) == 0
+    assert nq.packed_bytes_fp4(5120, 17408) == 5120 * 17408 // 2
+    assert nq.scale_bytes_fp4(5120, 17408) == 17408 * 5120 // 16
+    assert nq.scale_bytes_fp4(96, 16) == 0
     for s in range(-8, 1):
         assert nq.status_string(s).startswith("NQ_")
     assert nq.status_string(-99) == "NQ_ERR_UNKNOWN"
@@ -96,6 +100,9 @@ def test_shape_errors_are_reported_before_any_cuda_call(L):
     assert L.nq_pack_q4(p16, p16, 63, 16, p16, p16, None) == -2
     assert L.nq_dequant_q5_debug(p16, p16, p16, 64, 17, None) == -2
     assert L.nq_dequant_q4_debug_bf16(p16, p16, p16, 32, 16, None) == -2
+    assert L.nq_gemm_fp4(p16, p16, p16, ctypes.c_float(1.0), p16, 65, 64, 16, None) == -2
+    assert L.nq_gemm_fp4(p16, p16, p16, ctypes.c_float(1.0), p16, 1, 64, 24, None) == -2
+    assert L.nq_pack_fp4(p16, p16, 96, 16, p16, p16, None) == -2
 
 
 def test_empty_problems_launch_nothing(L):
@@ -132,6 +139,12 @@ def test_null_alignment_alias_errors(L):
     assert L.nq_swiglu_q5(x, w, s, P(base + 3080), s2, y, 1, 64, 16, None) == -3   # Wu misaligned
     # the packed Q5 64 x 16 codes are 640 bytes: H at Wu + 624 overlaps them
     assert L.nq_swiglu_q5(x, w, s, w2, s2, P(base + 3072 + 624), 1, 64, 16, None) == -4
+    # NVFP4 64 x 16: 512 code bytes, 64 scale bytes
+    g1 = ctypes.c_float(1.0)
+    assert L.nq_gemm_fp4(x, w, None, g1, y, 1, 64, 16, None) == -1
+    assert L.nq_gemm_fp4(x, w, s, g1, P(base + 5128), 1, 64, 16, None) == -3
+    assert L.nq_gemm_fp4(x, w, s, g1, P(base + 2048 + 48), 1, 64, 16, None) == -4   # Y overlaps the scales
+    assert L.nq_gemm_fp4(None, None, None, g1, None, 0, 64, 16, None) == 0
     # pack outputs overlapping an input or each other
     assert L.nq_pack_q4(x, s, 64, 16, x, s2, None) == -4
     assert L.nq_pack_q4(x, s, 64, 16, w2, P(base + 3072 + 256), None) == -4

@@ -1,0 +1,112 @@
+"""GPU parity of the NVFP4 weight path (e2m1 elements, e4m3 scale per 16, fp32 tensor scale)
+against the fp64 CPU oracle on the same seeded inputs: the decoded weights bit for bit
+(through the kernels' own decoder), the projection within max|y - y_ref| / max|y_ref| <= 5e-3
+(per token row)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    return nq
+
+
+def pack(nq, p, K, N):
+    return nq.pack_fp4(gu.dev_u32(p["codes"]), torch.from_numpy(np.ascontiguousarray(p["sf"])).cuda(), K, N)
+
+
+@pytest.mark.parametrize("K,N,seed", [(64, 16, 0), (256, 48, 1), (640, 272, 2), (5120, 17408, 3)])
+def test_fp4_dequant_bit_exact(nq, K, N, seed):
+    p = si.fp4_problem(1, K, N, 500 + seed)
+    w = pack(nq, p, K, N)
+    w_gpu = nq.dequant_fp4_debug(*w, p["g"], K, N).cpu().numpy()
+    w_ref = oracle.dequant_fp4(p["codes"], p["sf"], p["g"], K, N)
+    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+
+
+def test_fp4_dequant_every_code_and_scale_edges(nq):
+    """Every e2m1 code at every fragment position, under e4m3 scales that include the
+    subnormals (0x01..0x07), the smallest normal, 1.0, the largest finite value (448), and a
+    tensor scale that is not a power of two."""
+    K, N = 256, 32
+    k = np.arange(K)
+    n = np.arange(N)[:, None]
+    c = (k[None, :] * 5 + 3 * n) % 16
+    codes = np.zeros((N, K // 8), np.uint32)
+    for i in range(8):
+        codes |= c[:, i::8].astype(np.uint32) << np.uint32(4 * i)
+    edge = np.array([0x01, 0x02, 0x07, 0x08, 0x38, 0x7E, 0x3F, 0x10, 0x55, 0x5E], np.uint8)
+    sf = np.ascontiguousarray(edge[(np.arange(N)[:, None] + np.arange(K // 16)[None, :]) % len(edge)])
+    g = 0.3
+    p = {"codes": codes, "sf": sf}
+    w = pack(nq, p, K, N)
+    w_gpu = nq.dequant_fp4_debug(*w, g, K, N).cpu().numpy()
+    w_ref = oracle.dequant_fp4(codes, sf, g, K, N)
+    assert np.array_equal(w_gpu.view(np.uint32), w_ref.view(np.uint32))
+
+
+FP4_GEMM_SHAPES = [(1, 256, 128, 0), (2, 640, 48, 1), (3, 192, 80, 2), (5, 1024, 272, 3), (8, 5120, 96, 4),
+                   (8, 17408, 48, 5), (7, 6208, 32, 6), (12, 512, 64, 7), (1, 17408, 32, 8)]
+
+
+@pytest.mark.parametrize("T,K,N,seed", FP4_GEMM_SHAPES)
+def test_fp4_gemm_parity(nq, T, K, N, seed):
+    p = si.fp4_problem(T, K, N, 520 + seed)
+    w = pack(nq, p, K, N)
+    y = gu.host_f64(nq.gemm_fp4(gu.dev_bf16(p["x"]), *w, p["g"], N))
+    y_ref = oracle.gemm_fp4(p["x"], p["codes"], p["sf"], p["g"], T, K, N)
+    for t in range(T):
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_fp4_decode_shape_full_size_sampled(nq, T):
+    """The 27B-class FFN up-projection shape (K=5120, N=17408) in NVFP4, full-size launch,
+    sampled output rows."""
+    K, N = 5120, 17408
+    p = si.fp4_problem(T, K, N, 540 + T)
+    w = pack(nq, p, K, N)
+    y = gu.host_f64(nq.gemm_fp4(gu.dev_bf16(p["x"]), *w, p["g"], N))
+    rows = gu.sample_rows(N, 256, 7)
+    y_ref = oracle.gemm_fp4_rows(p["x"], p["codes"], p["sf"], p["g"], T, K, rows).T
+    assert gu.rel_err(y[:, rows], y_ref) <= gu.TOL
+
+
+def test_fp4_activation_range_outliers(nq):
+    T, K, N = 6, 1280, 96
+    p = si.fp4_problem(T, K, N, 560)
+    g = np.random.default_rng(561)
+    x = g.standard_normal((T, K)).astype(np.float32)
+    x[0, 5] = 3.0e38
+    x[1, :] *= 1.0e6
+    x[2, 100:200] = 70000.0
+    x[3, :] *= 1.0e-30
+    xb = si.bf16_bits(x)
+    w = pack(nq, p, K, N)
+    y = gu.host_f64(nq.gemm_fp4(gu.dev_bf16(xb), *w, p["g"], N))
+    y_ref = oracle.gemm_fp4(xb, p["codes"], p["sf"], p["g"], T, K, N)
+    for t in range(T):
+        assert np.all(np.isfinite(y[t]))
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+
+
+def test_fp4_deterministic(nq):
+    T, K, N = 8, 6208, 272
+    p = si.fp4_problem(T, K, N, 570)
+    w = pack(nq, p, K, N)
+    x = gu.dev_bf16(p["x"])
+    y1 = nq.gemm_fp4(x, *w, p["g"], N)
+    y2 = nq.gemm_fp4(x, *w, p["g"], N)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    nq.device_error()

@@ -72,7 +72,91 @@ __global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int K, int N,
         const long long tile = idx >> 4;
         const int rt = (int)(tile / G), g = (int)(tile % G);
         const int row = (e >> 1) + 8 * (e & 1);
-        reinterpret_cast<uint16_t*>(out + packed_scale_off(rt, g, G))[e] = s[(size_t)(rt * kTileRows + row) * G + g];
+        reinterpret_cast<uint16_t*>(out + packed_scale_off(rt, g, G, kScaleTileBytes))[e] =
+            s[(size_t)(rt * kTileRows + row) * G + g];
+    }
+}
+
+// Canonical NVFP4 codes [N][K/8] (nibble i of word j = element 8j+i) -> packed code tiles:
+// lane l's word j holds its registers 0..3 of K step j in bytes 0..3, register m = (row
+// l/4 + 8 (m & 1), K pair 2(l%4) + 8 (m >> 1)), the even element in the low nibble.
+__global__ void pack_fp4_codes_kernel(const uint32_t* __restrict__ wn, int K, int N, uint8_t* __restrict__ out) {
+    const int G = K / kGroup;
+    const long long total = (long long)(N / kTileRows) * G * 32;
+    const int kw8 = K / 8;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx & 31);
+        const long long tile = idx >> 5;
+        const int rt = (int)(tile / G), g = (int)(tile % G);
+        const int gid = lane >> 2, c = lane & 3;
+        uint32_t words[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t wv = 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int n = rt * kTileRows + gid + 8 * (m & 1);
+                const int k0 = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = k0 + e;
+                    const uint32_t code = (wn[(size_t)n * kw8 + (k >> 3)] >> (4 * (k & 7))) & 0xFu;
+                    wv |= code << (8 * m + 4 * e);
+                }
+            }
+            words[j] = wv;
+        }
+        reinterpret_cast<uint4*>(out + packed_code_off(rt, g, G, kQ4TileBytes))[lane] =
+            make_uint4(words[0], words[1], words[2], words[3]);
+    }
+}
+
+// Canonical e4m3 block scales [N][K/16] -> packed scale tiles: byte 8 r + 2 j + h of tile (rt, g)
+// is the scale of row 16 rt + r + 8 h, K step j of group g.
+__global__ void pack_fp4_scales_kernel(const uint8_t* __restrict__ sf, int K, int N, uint8_t* __restrict__ out) {
+    const int G = K / kGroup;
+    const long long total = (long long)(N / kTileRows) * G * kFp4ScaleTileBytes;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int b = (int)(idx % kFp4ScaleTileBytes);
+        const long long tile = idx / kFp4ScaleTileBytes;
+        const int rt = (int)(tile / G), g = (int)(tile % G);
+        const int r = b >> 3, j = (b >> 1) & 3, h = b & 1;
+        out[packed_scale_off(rt, g, G, kFp4ScaleTileBytes) + b] =
+            sf[(size_t)(rt * kTileRows + r + 8 * h) * (K / 16) + g * 4 + j];
+    }
+}
+
+// Packed NVFP4 pair -> fp32 W[n][k] = g * (fp16 register value), through decode_fp4, the
+// projection kernel's own decoder (the register value is exactly scale * element).
+__global__ void dequant_fp4_kernel(const uint8_t* __restrict__ wq, const uint8_t* __restrict__ sq, float gs, int K,
+                                   int N, float* __restrict__ w) {
+    const int G = K / kGroup;
+    const long long total = (long long)(N / kTileRows) * G * 32;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(idx & 31);
+        const long long tile = idx >> 5;
+        const int rt = (int)(tile / G), g = (int)(tile % G);
+        const int gid = lane >> 2, c = lane & 3;
+        const uint4 wv = reinterpret_cast<const uint4*>(wq + packed_code_off(rt, g, G, kQ4TileBytes))[lane];
+        const uint2 sc = *reinterpret_cast<const uint2*>(sq + packed_scale_off(rt, g, G, kFp4ScaleTileBytes) + gid * 8);
+        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+        const uint32_t ss[4] = {sc.x, sc.x >> 16, sc.y, sc.y >> 16};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t a[4];
+            decode_fp4(ws[j], ss[j], a);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int row = gid + 8 * (m & 1);
+                const int k = g * kGroup + 16 * j + 2 * c + 8 * (m >> 1);
+                float* dst = w + (size_t)(rt * kTileRows + row) * K + k;
+                dst[0] = gs * __half2float(__ushort_as_half((unsigned short)(a[m] & 0xFFFFu)));
+                dst[1] = gs * __half2float(__ushort_as_half((unsigned short)(a[m] >> 16)));
+            }
+        }
     }
 }
 
@@ -132,7 +216,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint8_t* __
         const uint8_t* tb = wq + packed_code_off(rt, g, G, TB);
         const uint4 wv = reinterpret_cast<const uint4*>(tb)[lane];
         const uint32_t hb = BITS == 5 ? reinterpret_cast<const uint32_t*>(tb + 512)[lane] : 0u;
-        const uint16_t* st = reinterpret_cast<const uint16_t*>(sq + packed_scale_off(rt, g, G));
+        const uint16_t* st = reinterpret_cast<const uint16_t*>(sq + packed_scale_off(rt, g, G, kScaleTileBytes));
         const float s_lo = __half2float(__ushort_as_half(st[2 * gid]));
         const float s_hi = __half2float(__ushort_as_half(st[2 * gid + 1]));
         dump_step<BITS, F16, 0>(wv.x, hb, rt, g, gid, c, K, s_lo, s_hi, w);
@@ -252,9 +336,12 @@ nq_status check_shape(int K, int N) {
     return NQ_OK;
 }
 
-// Packed code bytes (K*N/2 or 5*K*N/8) and packed scale bytes (N*K/32).
-size_t packed_bytes(int bits, int K, int N) { return (size_t)K * N / 8 * (bits == 4 ? 4 : 5); }
-size_t scale_bytes(int K, int N) { return (size_t)N * (K / kGroup) * 2; }
+// Packed code bytes (K*N/2, or 5*K*N/8 for Q5) and packed scale bytes (N*K/32: fp16 per 64;
+// NVFP4: N*K/16, e4m3 per 16).
+size_t packed_bytes(int bits, int K, int N) { return (size_t)K * N / 8 * (bits == 5 ? 5 : 4); }
+size_t scale_bytes(int K, int N, int bits = 4) {
+    return bits == kFp4 ? (size_t)N * (K / 16) : (size_t)N * (K / kGroup) * 2;
+}
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -302,7 +389,7 @@ bool choose_plans(int bits, bool swiglu, int T, int K, int N, DevState& d, Plan&
 // streaming the weights again. Every slice's plan and the workspace are settled before the
 // first launch, so an error still launches nothing.
 nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
-                  const void* S1, void* Y, int T, int K, int N, void* stream) {
+                  const void* S1, void* Y, int T, int K, int N, void* stream, float gscale = 1.f) {
     if (T < 0 || T > kMaxT) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
@@ -312,7 +399,7 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
         (swiglu && (misaligned(W1) || misaligned(S1))))
         return NQ_ERR_ALIGN;
     const size_t xb = (size_t)T * K * 2, yb = (size_t)T * N * 2;
-    const size_t wb = packed_bytes(bits, K, N), sb = scale_bytes(K, N);
+    const size_t wb = packed_bytes(bits, K, N), sb = scale_bytes(K, N, bits);
     if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, wb) || overlap(Y, yb, S0, sb) ||
         (swiglu && (overlap(Y, yb, W1, wb) || overlap(Y, yb, S1, sb))))
         return NQ_ERR_ALIAS;
@@ -345,8 +432,11 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
         a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
         a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
         a.wait_ns = g_wait_ns;
+        a.gscale = gscale;
         cudaError_t e;
-        if (swiglu)
+        if (bits == kFp4)
+            e = launch_proj_fp4(a, as_stream(stream), g_pdl);
+        else if (swiglu)
             e = bits == 4 ? launch_proj_swiglu_q4(a, as_stream(stream), g_pdl)
                           : launch_proj_swiglu_q5(a, as_stream(stream), g_pdl);
         else if (bits == 4)
@@ -414,6 +504,49 @@ nq_status dequant(int bits, bool f16, const void* wq, const void* sq, float* w, 
     return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
 }
 
+nq_status pack_fp4(const uint32_t* codes, const uint8_t* sf, int K, int N, void* wq_packed, void* s_packed,
+                   void* stream) {
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    if (K == 0 || N == 0) return NQ_OK;
+    if (!codes || !sf || !wq_packed || !s_packed) return NQ_ERR_NULL;
+    if (misaligned(codes) || misaligned(sf) || misaligned(wq_packed) || misaligned(s_packed)) return NQ_ERR_ALIGN;
+    const size_t cb = packed_bytes(kFp4, K, N), sb = scale_bytes(K, N, kFp4);
+    const void* outs[2] = {wq_packed, s_packed};
+    const size_t out_n[2] = {cb, sb};
+    for (int i = 0; i < 2; ++i)
+        if (overlap(outs[i], out_n[i], codes, cb) || overlap(outs[i], out_n[i], sf, sb)) return NQ_ERR_ALIAS;
+    if (overlap(wq_packed, cb, s_packed, sb)) return NQ_ERR_ALIAS;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
+    pack_fp4_codes_kernel<<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(codes, K, N,
+                                                                               static_cast<uint8_t*>(wq_packed));
+    if (cudaGetLastError() != cudaSuccess) return NQ_ERR_CUDA;
+    pack_fp4_scales_kernel<<<grid_for(lanes * 2, 256), 256, 0, as_stream(stream)>>>(sf, K, N,
+                                                                                    static_cast<uint8_t*>(s_packed));
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
+nq_status dequant_fp4(const void* wq, const void* sq, float gs, float* w, int K, int N, void* stream) {
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    if (K == 0 || N == 0) return NQ_OK;
+    if (!wq || !sq || !w) return NQ_ERR_NULL;
+    if (misaligned(wq) || misaligned(sq) || misaligned(w)) return NQ_ERR_ALIGN;
+    if (overlap(w, (size_t)N * K * 4, wq, packed_bytes(kFp4, K, N)) ||
+        overlap(w, (size_t)N * K * 4, sq, scale_bytes(K, N, kFp4)))
+        return NQ_ERR_ALIAS;
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    const long long lanes = (long long)(N / kTileRows) * (K / kGroup) * 32;
+    dequant_fp4_kernel<<<grid_for(lanes, 256), 256, 0, as_stream(stream)>>>(
+        static_cast<const uint8_t*>(wq), static_cast<const uint8_t*>(sq), gs, K, N, w);
+    return cudaGetLastError() == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace nq {
@@ -449,6 +582,23 @@ size_t nq_packed_bytes_q4(int K, int N) { return check_shape(K, N) == NQ_OK ? pa
 size_t nq_packed_bytes_q5(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_bytes(5, K, N) : 0; }
 
 size_t nq_scale_bytes(int K, int N) { return check_shape(K, N) == NQ_OK ? scale_bytes(K, N) : 0; }
+size_t nq_packed_bytes_fp4(int K, int N) { return check_shape(K, N) == NQ_OK ? packed_bytes(kFp4, K, N) : 0; }
+size_t nq_scale_bytes_fp4(int K, int N) { return check_shape(K, N) == NQ_OK ? scale_bytes(K, N, kFp4) : 0; }
+
+nq_status nq_pack_fp4(const uint32_t* codes_canon, const uint8_t* sf_canon, int K, int N, void* wq_packed,
+                      void* s_packed, void* stream) {
+    return pack_fp4(codes_canon, sf_canon, K, N, wq_packed, s_packed, stream);
+}
+
+nq_status nq_gemm_fp4(const void* X, const void* Wq, const void* S, float global_scale, void* Y, int T, int K, int N,
+                      void* stream) {
+    return project(kFp4, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream, global_scale);
+}
+
+nq_status nq_dequant_fp4_debug(const void* Wq, const void* S, float global_scale, float* W, int K, int N,
+                               void* stream) {
+    return dequant_fp4(Wq, S, global_scale, W, K, N, stream);
+}
 
 nq_status nq_pack_q4(const uint32_t* wq_canon, const uint16_t* s_canon, int K, int N, void* wq_packed,
                      void* s_packed, void* stream) {

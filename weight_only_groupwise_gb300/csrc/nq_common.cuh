@@ -14,6 +14,12 @@
 //       for r = 0..7, so lane l reads one uint32 holding the scales of its rows l/4, l/4+8.
 // A row tile's codes and scales are each contiguous along K, so a pipeline stage of any
 // run of groups is one bulk copy of codes and one of scales per tile.
+//
+// NVFP4 weights (format tag kFp4) use the same tiles: a code tile holds 16 rows x 64 e2m1
+// codes (512 B), lane l's word j holding its four A registers of K step j in bytes 0..3
+// (register m's two codes in byte m, the even-K element in the low nibble); a scale tile
+// holds the 16 x 4 e4m3 block scales (one per 16-wide K step, 64 B), byte 8 r + 2 j + h for
+// row r + 8 h, so lane l reads its rows' scales of all four K steps as 8 bytes at 8 (l/4).
 #pragma once
 
 #include <cstdint>
@@ -31,6 +37,8 @@ constexpr int kTileRows = 16;        // output rows per tile (MMA M)
 constexpr int kQ4TileBytes = 512;    // 16 x 64 nibbles
 constexpr int kQ5TileBytes = 640;    // + 16 x 64 high bits
 constexpr int kScaleTileBytes = 32;  // 16 fp16
+constexpr int kFp4 = 14;             // format tag of NVFP4 weights (template argument BITS)
+constexpr int kFp4ScaleTileBytes = 64;  // 16 rows x 4 e4m3 block scales
 #ifndef NQ_BLOCK_GROUPS
 #define NQ_BLOCK_GROUPS 32
 #endif
@@ -73,7 +81,9 @@ NQ_HD int tpad(int T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
 
 // Byte offsets inside a packed weight (TB = code bytes per tile, 512 or 640).
 NQ_HD long long packed_code_off(int rt, int g, int G, int TB) { return ((long long)rt * G + g) * TB; }
-NQ_HD long long packed_scale_off(int rt, int g, int G) { return ((long long)rt * G + g) * kScaleTileBytes; }
+NQ_HD int code_tile_bytes(int bits) { return bits == 5 ? kQ5TileBytes : kQ4TileBytes; }
+NQ_HD int scale_tile_bytes(int bits) { return bits == kFp4 ? kFp4ScaleTileBytes : kScaleTileBytes; }
+NQ_HD long long packed_scale_off(int rt, int g, int G, int STB) { return ((long long)rt * G + g) * STB; }
 
 // The work split of one projection call. One "unit" is one 64-wide K group of one row pair
 // (two 16-row tiles; for SwiGLU the gate tile and the up tile of the same rows). Units are
@@ -111,8 +121,8 @@ NQ_HD int cluster_buffer_bytes(int S) { return S > 1 ? kEpilogueWarps * (S - 1) 
 NQ_HD int plan_smem(Plan& p) {
     const int Tr = p.T > 0 ? p.T : 1;
     p.CG = kChunkGroups;
-    p.tile_bytes = p.bits == 4 ? kQ4TileBytes : kQ5TileBytes;
-    p.stage_bytes = 2 * p.CG * (p.tile_bytes + kScaleTileBytes);
+    p.tile_bytes = code_tile_bytes(p.bits);
+    p.stage_bytes = 2 * p.CG * (p.tile_bytes + scale_tile_bytes(p.bits));
     p.x_bytes = (Tr * (p.GS * 128 + 16) + 16 + 127) / 128 * 128;  // T rows of pitch GS*128+16, zero row
     p.corr_bytes = (p.GS * 8 * 4 + 127) / 128 * 128;  // O[gl][8 tokens] fp32
     p.bar_bytes = 512;                           // barriers, flags, per-token range data
@@ -138,7 +148,7 @@ NQ_HD int plan_smem(Plan& p) {
     p.red_bytes = p.nred * kRedBufBytes;
     p.stages = st;
     p.smem_bytes = p.x_bytes + p.corr_bytes + p.red_bytes + p.bar_bytes + p.cl_bytes + st * p.stage_bytes;
-    p.f16 = p.T <= NQ_F16_MAX_T ? 1 : 0;
+    p.f16 = p.bits == kFp4 || p.T <= NQ_F16_MAX_T ? 1 : 0;  // NVFP4: fp16 weights at every T
     return st;
 }
 
@@ -178,7 +188,7 @@ NQ_HD bool make_plan(int bits, int mode, int T, int K, int N, int num_sms, Plan&
         const int k = (p.RP + num_sms - 1) / num_sms;
         if (k >= 1 && k <= 4 && p.RP % k == 0) {
             const long long in_flight = (long long)(p.RP / k) * st * p.stage_bytes;
-            const long long weights = p.U * 2 * (p.tile_bytes + kScaleTileBytes);
+            const long long weights = p.U * 2 * (p.tile_bytes + scale_tile_bytes(p.bits));
             if (in_flight >= kSaturateBytes || in_flight >= weights) P = p.RP / k;
         }
     }
@@ -685,6 +695,51 @@ __device__ __forceinline__ void decode_q5_bf16(uint32_t w, uint32_t h, uint32_t 
     a[2] = and_or<0x000F000Fu>(w >> 4, and_or<0x00100010u>(h >> J, magic));
     a[1] = and_or<0x000F000Fu>(w >> 8, and_or<0x00100010u>(h >> (4 + J), magic));
     a[3] = and_or<0x000F000Fu>(w >> 12, and_or<0x00100010u>(h >> (8 + J), magic));
+}
+
+// ---------------------------------------------------------------- NVFP4 decode
+//
+// Each A register is exact in fp16: an e2m1 element (at most 2 significant bits, 0.5 .. 6)
+// times its e4m3 block scale (at most 4 significant bits, 2^-9 .. 448) has at most 6
+// significant bits and lies inside fp16's normal range, so one fp16 multiply is exact.
+
+// Two e2m1 codes (low byte of x, the first in bits 0..3) -> fp16x2.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(d) : "r"(x));
+    return d;
+}
+
+// Two e4m3 values (low 16 bits of x, the first in bits 0..7) -> fp16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(x));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The low (H0) or high (H1) half of x in both halves.
+template <int H>
+__device__ __forceinline__ uint32_t half_bcast(uint32_t x) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(x), "n"(H == 0 ? 0x1010 : 0x3232));
+    return d;
+}
+
+// K step of an NVFP4 tile: w holds registers 0..3 in bytes 0..3 (rows r, r+8, r, r+8; lower
+// then upper K pairs), sc the e4m3 scales of rows r (low byte) and r+8 (high byte).
+__device__ __forceinline__ void decode_fp4(uint32_t w, uint32_t sc, uint32_t a[4]) {
+    const uint32_t s2 = e4m3x2_to_f16x2(sc);
+    const uint32_t s_r = half_bcast<0>(s2), s_r8 = half_bcast<1>(s2);
+    a[0] = hmul2(e2m1x2_to_f16x2(w), s_r);
+    a[1] = hmul2(e2m1x2_to_f16x2(w >> 8), s_r8);
+    a[2] = hmul2(e2m1x2_to_f16x2(w >> 16), s_r);
+    a[3] = hmul2(e2m1x2_to_f16x2(w >> 24), s_r8);
 }
 
 // Q5: as decode_q4, plus bit 4 of each code from the lane's high word h, which lands on bit 4

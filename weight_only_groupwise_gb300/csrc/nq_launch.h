@@ -20,6 +20,7 @@ cudaError_t launch_proj_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
+cudaError_t launch_proj_fp4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
 // Slab clusters of S blocks that can be resident at once for the slab-cluster
 // instantiation with `smem` bytes of shared memory per block (cudaOccupancyMaxActiveClusters);
@@ -96,6 +97,14 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
     if (!a.p.f16) return launch_proj_t<BITS, SWIGLU, false, false, false>(a, stream, pdl);
     return a.p.T == 1 ? launch_proj_t<BITS, SWIGLU, true, true, false>(a, stream, pdl)
                       : launch_proj_t<BITS, SWIGLU, true, false, false>(a, stream, pdl);
+}
+
+// NVFP4 weights decode to fp16 at every T: only the fp16-operand instantiations exist (one
+// token, or up to eight).
+template <int BITS>
+cudaError_t launch_proj_f16_only(const ProjArgs& a, cudaStream_t stream, bool pdl) {
+    return a.p.T == 1 ? launch_proj_t<BITS, false, true, true, false>(a, stream, pdl)
+                      : launch_proj_t<BITS, false, true, false, false>(a, stream, pdl);
 }
 
 }  // namespace nq

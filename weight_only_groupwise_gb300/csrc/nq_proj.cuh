@@ -51,6 +51,7 @@ struct ProjArgs {
     int* tickets;        // workspace: one per row pair, zero between calls
     int* dev_err;        // workspace: device error word
     unsigned long long wait_ns;  // bound of every device-side wait
+    float gscale = 1.f;  // tensor scale of NVFP4 weights (1 for the integer formats)
     Plan p;              // the real plan (slab geometry, shared memory, grid)
     Plan q;              // work split and split-K bookkeeping: p itself, or the cluster-level
                          // plan of a slab-cluster launch (p.cl > 1)
@@ -81,8 +82,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4& w) {
 // A fragment of K step J: fp16 pairs (1024 + q lower-K, 1024 + 16 q upper-K) or bf16 pairs
 // (128 + q everywhere).
 template <int BITS, bool F16, int J>
-__device__ __forceinline__ void decode_step(const uint4& w, uint32_t hb, uint32_t a[4], uint32_t magic) {
-    if constexpr (F16) {
+__device__ __forceinline__ void decode_step(const uint4& w, uint32_t hb, const uint2& sc, uint32_t a[4],
+                                            uint32_t magic) {
+    if constexpr (BITS == kFp4) {
+        // the e4m3 scales of rows (r, r+8) for K step J: bytes 2J, 2J+1 of the lane's 8
+        decode_fp4(word_of<J>(w), J < 2 ? (J == 0 ? sc.x : sc.x >> 16) : (J == 2 ? sc.y : sc.y >> 16), a);
+    } else if constexpr (F16) {
         if constexpr (BITS == 4) decode_q4(word_of<J>(w), a, magic);
         else decode_q5<J>(word_of<J>(w), hb, a, magic);
     } else {
@@ -105,55 +110,73 @@ __device__ __forceinline__ constexpr int mtile_of(int t) { return t / GROUPS; }
 
 // GROUPS x TILES tiles in one pass, K-step-major so their accumulator chains overlap. Each
 // tile's chain is "K step 0 from a zero accumulator, then K steps 1..3", exactly as for O.
-// code[t] / scale[t]: this lane's code bytes / scale pair of tile t.
+// code[t] / scale[t]: this lane's code bytes / scales of tile t. Integer codes: the tile's
+// partial P, minus the zero-point chain O of its group, times the group scale, is added to
+// the accumulator. NVFP4: the A registers already carry their block scales (exact fp16), so
+// the tile's partial is added as is.
 template <int BITS, bool F16, int GROUPS, int TILES, bool ONE = false>
 __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * TILES],
                                           const uint8_t* const (&scale)[GROUPS * TILES],
                                           const uint32_t (&xb)[GROUPS][8], const float2 (&o)[GROUPS],
                                           uint32_t magic, float (&acc)[2][4]) {
     constexpr int NT = GROUPS * TILES;
+    constexpr bool FP4 = BITS == kFp4;
     uint4 w[NT];
-    uint32_t hb[NT], sw[NT];
+    uint32_t hb[NT];
+    uint2 sw[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         w[t] = *reinterpret_cast<const uint4*>(code[t]);
         // high-bit word of the lane: after the tile's 512 nibble bytes, 4 bytes per lane
         hb[t] = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code[t] + 512 - (threadIdx.x & 31) * 12) : 0u;
-        sw[t] = *reinterpret_cast<const uint32_t*>(scale[t]);
+        if constexpr (FP4)
+            sw[t] = *reinterpret_cast<const uint2*>(scale[t]);
+        else
+            sw[t] = make_uint2(*reinterpret_cast<const uint32_t*>(scale[t]), 0u);
     }
     float d[NT][4];
     uint32_t a[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        decode_step<BITS, F16, 0>(w[t], hb[t], a[t], magic);
+        decode_step<BITS, F16, 0>(w[t], hb[t], sw[t], a[t], magic);
         mma_zero_16816<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][0], xb[group_of<GROUPS>(t)][1]);
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        decode_step<BITS, F16, 1>(w[t], hb[t], a[t], magic);
+        decode_step<BITS, F16, 1>(w[t], hb[t], sw[t], a[t], magic);
         mma_acc<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][2], xb[group_of<GROUPS>(t)][3]);
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        decode_step<BITS, F16, 2>(w[t], hb[t], a[t], magic);
+        decode_step<BITS, F16, 2>(w[t], hb[t], sw[t], a[t], magic);
         mma_acc<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][4], xb[group_of<GROUPS>(t)][5]);
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        decode_step<BITS, F16, 3>(w[t], hb[t], a[t], magic);
+        decode_step<BITS, F16, 3>(w[t], hb[t], sw[t], a[t], magic);
         mma_acc<F16>(d[t], a[t], xb[group_of<GROUPS>(t)][6], xb[group_of<GROUPS>(t)][7]);
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        __half2 sh;
-        *reinterpret_cast<uint32_t*>(&sh) = sw[t];
-        const float2 s = __half22float2(sh);
-        const int m = mtile_of<GROUPS>(t), h = group_of<GROUPS>(t);
-        acc[m][0] = fmaf(s.x, d[t][0] - o[h].x, acc[m][0]);
-        acc[m][2] = fmaf(s.y, d[t][2] - o[h].x, acc[m][2]);
-        if constexpr (!ONE) {  // token columns 2(l%4) + 1: none when there is one token
-            acc[m][1] = fmaf(s.x, d[t][1] - o[h].y, acc[m][1]);
-            acc[m][3] = fmaf(s.y, d[t][3] - o[h].y, acc[m][3]);
+        const int m = mtile_of<GROUPS>(t);
+        if constexpr (FP4) {
+            acc[m][0] += d[t][0];
+            acc[m][2] += d[t][2];
+            if constexpr (!ONE) {
+                acc[m][1] += d[t][1];
+                acc[m][3] += d[t][3];
+            }
+        } else {
+            __half2 sh;
+            *reinterpret_cast<uint32_t*>(&sh) = sw[t].x;
+            const float2 s = __half22float2(sh);
+            const int h = group_of<GROUPS>(t);
+            acc[m][0] = fmaf(s.x, d[t][0] - o[h].x, acc[m][0]);
+            acc[m][2] = fmaf(s.y, d[t][2] - o[h].x, acc[m][2]);
+            if constexpr (!ONE) {  // token columns 2(l%4) + 1: none when there is one token
+                acc[m][1] = fmaf(s.x, d[t][1] - o[h].y, acc[m][1]);
+                acc[m][3] = fmaf(s.y, d[t][3] - o[h].y, acc[m][3]);
+            }
         }
     }
 }
@@ -191,8 +214,10 @@ __device__ __forceinline__ int red_index(int w, int m, int tok, int row) {
 template <int BITS, bool SWIGLU, bool F16, bool ONE, bool CLU>
 __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int TB = BITS == 4 ? kQ4TileBytes : kQ5TileBytes;
-    constexpr int TBS = TB + kScaleTileBytes;         // code + scale bytes per tile
+    constexpr bool FP4 = BITS == kFp4;
+    constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
+    constexpr int STB = FP4 ? kFp4ScaleTileBytes : kScaleTileBytes;  // scale bytes per tile
+    constexpr int TBS = TB + STB;                     // code + scale bytes per tile
     constexpr int BG = kBlockGroups;                  // groups per block = per stage
     constexpr int kTileArea = BG * TBS;               // one M tile's share of a stage
     constexpr int kStageBytes = 2 * kTileArea;
@@ -208,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     // plan fields used in loops, in registers
     const Plan& p = a.p;
     const int T = p.T, G = p.G, RT = p.RT, GS = p.GS, nstages = p.stages;
-    const long long row_tile_codes = (long long)G * TB, row_tile_scales = (long long)G * kScaleTileBytes;
+    const long long row_tile_codes = (long long)G * TB, row_tile_scales = (long long)G * STB;
     const uint64_t wait_ns = a.wait_ns;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -305,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         if (m == 1 && !has1) break;
                         uint8_t* dst = sb + m * kTileArea;
                         bulk_g2s(smem_u32(dst + i0 * TB), (m == 0 ? w0 : w1) + g0 * TB, (i1 - i0) * TB, fb, pol);
-                        bulk_g2s(smem_u32(dst + BG * TB + i0 * kScaleTileBytes),
-                                 (m == 0 ? s0 : s1) + g0 * kScaleTileBytes, (i1 - i0) * kScaleTileBytes, fb, pol);
+                        bulk_g2s(smem_u32(dst + BG * TB + i0 * STB), (m == 0 ? s0 : s1) + g0 * STB, (i1 - i0) * STB,
+                                 fb, pol);
                     }
                     ++it;
                     // After the first stage, hold the weight stream until a bulk-copied first
@@ -347,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         // Outputs per lane at most: one token (16 or 32 outputs), fp16 path (T <= 2: up to
         // 64), else 8 tokens (256). A compile-time bound keeps the epilogue code small.
         constexpr int kF16TP = NQ_F16_MAX_T <= 1 ? 1 : (NQ_F16_MAX_T <= 2 ? 2 : (NQ_F16_MAX_T <= 4 ? 4 : 8));
-        constexpr int kMaxTP = ONE ? 1 : (F16 ? kF16TP : 8);
+        constexpr int kMaxTP = ONE ? 1 : ((F16 && !FP4) ? kF16TP : 8);
         constexpr int JN8 = (SWIGLU ? 16 : 32) * kMaxTP / 32 > 0 ? (SWIGLU ? 16 : 32) * kMaxTP / 32 : 1;
         grid_dependency_wait();  // Y, partial sums and tickets may still be in the preceding kernel's use
         Segment nat;
@@ -548,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     const uint32_t ld_group_step = lt_valid ? 128u : 0u;
     const uint32_t ld_half_step = lt_valid ? 64u : 0u;  // K steps 2,3 are 32 elements further
     // per-lane byte offsets inside a stage's tile area
-    const uint32_t code_lane = lane * 16, scale_lane = BG * TB + (lane >> 2) * 4;
+    const uint32_t code_lane = lane * 16, scale_lane = BG * TB + (lane >> 2) * (FP4 ? 8 : 4);
     const float* osum_lane = osum + 2 * (lane & 3);
 
     int st = 0, cur_slab = -1, nx = 0, nx_issued = 0;
@@ -624,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         for (int t = 0; t < T; ++t) {
                             const int e = token_exponent(xmax[t]);
                             const float lo_scale = __int_as_float((127 - e) << 23);
-                            const float hi_scale = lo_scale * 0.0625f;
+                            const float hi_scale = FP4 ? lo_scale : lo_scale * 0.0625f;
                             for (int c = tid; c < chunks; c += kConsumerThreads) {
                                 uint4* q = reinterpret_cast<uint4*>(xs + t * pitch + c * 16);
                                 const uint4 v = *q;
@@ -670,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 // m + 0x0E80, and no further).
                 uint32_t big = 0;
                 const uint32_t az[4] = {kZeroLo, kZeroLo, kZeroHi, kZeroHi};
-                for (int gl = warp; gl < gs; gl += 4 * NW) {
+                for (int gl = warp; !FP4 && gl < gs; gl += 4 * NW) {  // NVFP4 has no zero point
                     int g[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) g[c] = gl + c * NW < gs ? gl + c * NW : gl;
@@ -711,6 +736,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 const int e1 = F16 ? token_exponent(m1) : token_exponent_bf16(m1);
                 tok_scale0 = __int_as_float((127 + e0) << 23);
                 tok_scale1 = __int_as_float((127 + e1) << 23);
+                if constexpr (FP4) {
+                    tok_scale0 *= a.gscale;
+                    tok_scale1 *= a.gscale;
+                }
             }
         }
 
@@ -740,14 +769,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         o[h] = *reinterpret_cast<const float2*>(o0 + 8 * NW * h);
                     }
                     const uint8_t* c0 = t0 + warp * TB + code_lane;
-                    const uint8_t* s0 = t0 + scale_lane + warp * kScaleTileBytes;
+                    const uint8_t* s0 = t0 + scale_lane + warp * STB;
                     const uint8_t* code[2 * GPW];
                     const uint8_t* scale[2 * GPW];
 #pragma unroll
                     for (int t = 0; t < 2 * GPW; ++t) {
                         const int m = t / GPW, h = t % GPW;
                         code[t] = c0 + m * kTileArea + NW * h * TB;
-                        scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
+                        scale[t] = s0 + m * kTileArea + NW * h * STB;
                     }
                     tiles_mma<BITS, F16, GPW, 2, ONE>(code, scale, xb, o, magic, acc);
                 } else if (i0 == 0 && i1 == BG / 2) {
@@ -764,14 +793,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         o[h] = *reinterpret_cast<const float2*>(o0 + 8 * NW * h);
                     }
                     const uint8_t* c0 = t0 + warp * TB + code_lane;
-                    const uint8_t* s0 = t0 + scale_lane + warp * kScaleTileBytes;
+                    const uint8_t* s0 = t0 + scale_lane + warp * STB;
                     const uint8_t* code[2 * H];
                     const uint8_t* scale[2 * H];
 #pragma unroll
                     for (int t = 0; t < 2 * H; ++t) {
                         const int m = t / H, h = t % H;
                         code[t] = c0 + m * kTileArea + NW * h * TB;
-                        scale[t] = s0 + m * kTileArea + NW * h * kScaleTileBytes;
+                        scale[t] = s0 + m * kTileArea + NW * h * STB;
                     }
                     tiles_mma<BITS, F16, H, 2, ONE>(code, scale, xb, o, magic, acc);
                 } else {
@@ -787,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                             ldsm_x4(la + ld_half_step, xb[0] + 4);
                             const float2 o[1] = {*reinterpret_cast<const float2*>(o0 + 8 * NW * h)};
                             const uint8_t* c0 = t0 + i * TB + code_lane;
-                            const uint8_t* s0 = t0 + scale_lane + i * kScaleTileBytes;
+                            const uint8_t* s0 = t0 + scale_lane + i * STB;
                             const uint8_t* const code[2] = {c0, c0 + kTileArea};
                             const uint8_t* const scale[2] = {s0, s0 + kTileArea};
                             tiles_mma<BITS, F16, 1, 2, ONE>(code, scale, xb, o, magic, acc);

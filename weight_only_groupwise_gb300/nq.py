@@ -52,6 +52,16 @@ def lib() -> ctypes.CDLL:
                   "nq_dequant_q5_debug_bf16"):
             getattr(L, f).argtypes = [P, P, P, I, I, P]
             getattr(L, f).restype = I
+        L.nq_packed_bytes_fp4.argtypes = [I, I]
+        L.nq_packed_bytes_fp4.restype = S
+        L.nq_scale_bytes_fp4.argtypes = [I, I]
+        L.nq_scale_bytes_fp4.restype = S
+        L.nq_pack_fp4.argtypes = [P, P, I, I, P, P, P]
+        L.nq_pack_fp4.restype = I
+        L.nq_gemm_fp4.argtypes = [P, P, P, ctypes.c_float, P, I, I, I, P]
+        L.nq_gemm_fp4.restype = I
+        L.nq_dequant_fp4_debug.argtypes = [P, P, ctypes.c_float, P, I, I, P]
+        L.nq_dequant_fp4_debug.restype = I
         L.nq_reserve.argtypes = [I, I, I]
         L.nq_device_error.argtypes = []
         L.nq_wait_limit.argtypes = [ctypes.c_longlong]
@@ -216,6 +226,46 @@ def dequant_q5_debug(wq, s, K: int, N: int, operands: str = "f16", stream=None) 
     return _dequant(f, wq, s, K, N, stream)
 
 
+# ---------------------------------------------------------------- NVFP4
+
+def packed_bytes_fp4(K: int, N: int) -> int:
+    return int(lib().nq_packed_bytes_fp4(K, N))
+
+
+def scale_bytes_fp4(K: int, N: int) -> int:
+    return int(lib().nq_scale_bytes_fp4(K, N))
+
+
+def pack_fp4(codes_canon: torch.Tensor, sf_canon: torch.Tensor, K: int, N: int, stream=None):
+    """Canonical NVFP4 codes (4-byte words [N][K/8]) and e4m3 scales (bytes [N][K/16]) on the
+    GPU -> (packed codes, packed scales), two uint8 device tensors."""
+    dev = _cuda(codes_canon, "codes_canon").device
+    _cuda(sf_canon, "sf_canon")
+    wq = torch.empty(max(packed_bytes_fp4(K, N), 16), dtype=torch.uint8, device=dev)
+    s = torch.empty(max(scale_bytes_fp4(K, N), 16), dtype=torch.uint8, device=dev)
+    _check(lib().nq_pack_fp4(_ptr(codes_canon), _ptr(sf_canon), K, N, _ptr(wq), _ptr(s), _stream(stream)))
+    return wq, s
+
+
+def gemm_fp4(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, global_scale: float, N: int, out=None,
+             stream=None):
+    """Y[T,N] (bf16) = X[T,K] (bf16) * NVFP4 weight (packed codes wq, packed scales s, tensor
+    scale global_scale)."""
+    _cuda(x, "x")
+    T, K = x.shape
+    y = _out(x, N, out)
+    _check(lib().nq_gemm_fp4(_ptr(x), _ptr(wq), _ptr(s), ctypes.c_float(global_scale), _ptr(y), T, K, N,
+                             _stream(stream)))
+    return y
+
+
+def dequant_fp4_debug(wq, s, global_scale: float, K: int, N: int, stream=None) -> torch.Tensor:
+    out = torch.empty((N, K), dtype=torch.float32, device=wq.device)
+    _check(lib().nq_dequant_fp4_debug(_ptr(wq), _ptr(s), ctypes.c_float(global_scale), _ptr(out), K, N,
+                                      _stream(stream)))
+    return out
+
+
 # ---------------------------------------------------------------- runtime / plan
 
 def reserve(T_max: int, K_max: int, N_max: int) -> None:
@@ -284,5 +334,6 @@ nq_pack_q4, nq_pack_q5 = pack_q4, pack_q5
 nq_gemm_q4, nq_gemm_q5, nq_gemm_q4_noalloc = gemm_q4, gemm_q5, gemm_q4_noalloc
 nq_swiglu_q4, nq_swiglu_q5 = swiglu_q4, swiglu_q5
 nq_dequant_q4_debug, nq_dequant_q5_debug = dequant_q4_debug, dequant_q5_debug
+nq_pack_fp4, nq_gemm_fp4, nq_dequant_fp4_debug = pack_fp4, gemm_fp4, dequant_fp4_debug
 nq_reserve, nq_device_error, nq_shutdown, nq_wait_limit = reserve, device_error, shutdown, wait_limit
 nq_plan_info, nq_plan_segments = plan_info, plan_segments
