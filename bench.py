@@ -102,7 +102,8 @@ def workload_bytes(w: dict) -> int:
 
 
 def launches_per_step(w: dict) -> int:
-    return {"proj": 1, "swiglu": 2, "stack": 5 * w.get("layers", 1)}[w["kind"]]
+    """Kernel launches per step (T <= 8: one per call; the stack's q-gate and kv share one)."""
+    return {"proj": 1, "swiglu": 2, "stack": 4 * w.get("layers", 1)}[w["kind"]]
 
 
 # ---------------------------------------------------------------- environment helpers
@@ -273,7 +274,15 @@ def build_step(nq, w: dict, dev, T_override=None):
             fn(h, *down[j], Nd, out=y)
         return step, b, R, f"rotate {R} weight sets ({R * b / 1e6:.0f} MB > 3x L2)", (x, y)
     # layer stack: 64 independent layers, ~12 GB of packed weights (no reuse within a pass)
-    T, L = T_override or w["T"], w["layers"]
+    T = T_override or w["T"]
+    layers = build_layers(nq, w["layers"], dev)
+    step, keep = stack_step(nq, layers, T, dev, grouped=True)
+    w2 = dict(w, T=T)
+    return step, workload_bytes(w2), 1, "64 distinct layers (~12 GB) per pass, no reuse", (keep, layers)
+
+
+def build_layers(nq, L: int, dev):
+    import seeded_inputs as si
     layers = []
     for l in range(L):
         layers.append(dict(
@@ -283,6 +292,16 @@ def build_step(nq, w: dict, dev, T_override=None):
             qg=make_proj_copies(nq, 5, 5120, 6144, 1, si.layer_seed(l, 3), dev)[0],
             kv=make_proj_copies(nq, 5, 5120, 1024, 1, si.layer_seed(l, 4), dev)[0],
             out=make_proj_copies(nq, 5, 6144, 5120, 1, si.layer_seed(l, 5), dev)[0]))
+    return layers
+
+
+def stack_step(nq, layers, T: int, dev, grouped: bool):
+    """One pass over the layers: fused gate/up + down (Q4); q-gate and kv (Q5, the same X) as
+    one grouped launch or two calls; out (Q5)."""
+    import torch
+    import seeded_inputs as si
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(12345)
     x = si.device_activations(T, 5120, gen, dev)
     x6 = si.device_activations(T, 6144, gen, dev)
     h = torch.empty((T, 17408), dtype=torch.bfloat16, device=dev)
@@ -290,17 +309,18 @@ def build_step(nq, w: dict, dev, T_override=None):
     yq = torch.empty((T, 6144), dtype=torch.bfloat16, device=dev)
     ykv = torch.empty((T, 1024), dtype=torch.bfloat16, device=dev)
     yo = torch.empty((T, 5120), dtype=torch.bfloat16, device=dev)
-    y = (yd, yq, ykv, yo)
 
     def step(i):
         for ly in layers:
             nq.swiglu_q4(x, *ly["gate"], *ly["up"], 17408, out=h)
             nq.gemm_q4(h, *ly["down"], 5120, out=yd)
-            nq.gemm_q5(x, *ly["qg"], 6144, out=yq)
-            nq.gemm_q5(x, *ly["kv"], 1024, out=ykv)
+            if grouped:
+                nq.gemm_q5_grouped(x, [(*ly["qg"], 6144), (*ly["kv"], 1024)], outs=[yq, ykv])
+            else:
+                nq.gemm_q5(x, *ly["qg"], 6144, out=yq)
+                nq.gemm_q5(x, *ly["kv"], 1024, out=ykv)
             nq.gemm_q5(x6, *ly["out"], 5120, out=yo)
-    w2 = dict(w, T=T)
-    return step, workload_bytes(w2), 1, "64 distinct layers (~12 GB) per pass, no reuse", (x, y)
+    return step, (x, x6, h, yd, yq, ykv, yo)
 
 
 def time_graph(step, steps: int, warmup: int, stream, soak_s: float = 0.0, reps: int = 5):
@@ -623,12 +643,16 @@ def sweep(nq, dev, stream, peak):
         record(name, 8, time_graph(step, steps, 5, stream), steps, b, launches_per_step(w))
         del step, keep
         torch.cuda.empty_cache()
+    layers = build_layers(nq, WORKLOADS["layer_stack"]["layers"], dev)
     for T in (1, 8):
         w = dict(WORKLOADS["layer_stack"], T=T)
-        step, b, R, note, keep = build_step(nq, w, dev)
-        record("layer_stack", T, time_graph(step, 2, 1, stream), 2, b, launches_per_step(w))
-        del step, keep
-        torch.cuda.empty_cache()
+        for grouped in (True, False):
+            step, keep = stack_step(nq, layers, T, dev, grouped)
+            record("layer_stack" if grouped else "layer_stack_ungrouped", T, time_graph(step, 2, 1, stream), 2,
+                   workload_bytes(w), launches_per_step(w) + (0 if grouped else w["layers"]))
+            del step, keep
+    del layers
+    torch.cuda.empty_cache()
     return out
 
 

@@ -165,6 +165,30 @@ nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int 
                      void* stream);
 
 /*
+ * Grouped projections: several matrices applied to the same X in one launch (e.g. the
+ * attention q-gate 5120 x 6144 and kv 5120 x 1024 projections of a layer, which read the same
+ * activations). One launch per 8-token slice carries all groups, so the per-launch start-up
+ * and tail are paid once instead of once per matrix. No counterpart call on the pages, which
+ * rely on CUDA graphs to chain a layer's launches ("NInfer-4090" post / NInfer digest,
+ * decode with CUDA Graphs); this is the launch-level part of fusing a layer.
+ */
+typedef struct nq_group {
+    const void* Wq;  /* packed codes of a K x N matrix (nq_pack_q4 / nq_pack_q5)            */
+    const void* S;   /* its packed scales                                                  */
+    void* Y;         /* bf16 [T][N] output, written                                        */
+    int N;           /* outputs of this group: N % 16 == 0, N > 0                          */
+} nq_group;
+
+/*
+ * nq_gemm_q4_grouped / nq_gemm_q5_grouped: Y_g = X * dequant(Wq_g, S_g) for each of `count`
+ * groups (1..4, host array), all with the same X (device bf16 [T][K]) and code width.
+ * Results equal those of one nq_gemm_q4 / nq_gemm_q5 call per group. Outputs must not overlap
+ * X, any group's weights or each other. Errors and launch behaviour as nq_gemm_q4.
+ */
+nq_status nq_gemm_q4_grouped(const void* X, const nq_group* groups, int count, int T, int K, void* stream);
+nq_status nq_gemm_q5_grouped(const void* X, const nq_group* groups, int count, int T, int K, void* stream);
+
+/*
  * nq_swiglu_q4: fused gate/up projection of the SwiGLU MLP ("NInfer-4090" release post,
  * section "V3 做了什么", SwiGLU path at T=8):
  *   g = X * dequant(Wg, Sg),  u = X * dequant(Wu, Su)   (each [T][N], fp32 accumulation)

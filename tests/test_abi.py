@@ -171,3 +171,36 @@ def test_slab_cluster_switch(L):
     assert L.nq_slab_clusters(0) == 1
     assert L.nq_slab_clusters(prev) == 0
     assert L.nq_slab_clusters(-1) == prev
+
+
+def test_grouped_argument_errors(L):
+    from weight_only_groupwise_gb300.nq import NqGroup
+    P = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(16384)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    x = base
+    gs = (NqGroup * 5)()
+    # Q4 64 x 32: 1024 code bytes, 64 scale bytes; outputs 64 bytes each at T=1
+    for i in range(5):
+        gs[i] = NqGroup(base + 1024 + 2048 * i, base + 1024 + 2048 * i + 1536, base + 12288 + 128 * i, 32)
+    arr = ctypes.cast(gs, P)
+    assert L.nq_gemm_q4_grouped(P(x), None, 1, 1, 64, None) == -1
+    assert L.nq_gemm_q4_grouped(P(x), arr, 0, 1, 64, None) == -2
+    assert L.nq_gemm_q4_grouped(P(x), arr, 5, 1, 64, None) == -2
+    assert L.nq_gemm_q5_grouped(P(x), arr, 2, 65, 64, None) == -2
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 1, 96, None) == -2        # K % 64
+    saved = gs[1].N
+    gs[1].N = 40
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 1, 64, None) == -2        # N % 16
+    gs[1].N = 0
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 1, 64, None) == -2        # empty group
+    gs[1].N = saved
+    assert L.nq_gemm_q4_grouped(None, arr, 2, 1, 64, None) == -1
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 0, 64, None) == 0         # T == 0: nothing to do
+    y1 = gs[1].Y
+    gs[1].Y = base + 12288 + 32                                        # overlaps group 0's Y
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 1, 64, None) == -4
+    gs[1].Y = gs[0].Wq + 16                                            # overlaps group 0's codes
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 1, 64, None) == -4
+    gs[1].Y = y1 + 2                                                   # misaligned
+    assert L.nq_gemm_q4_grouped(P(x), arr, 2, 1, 64, None) == -3

@@ -498,3 +498,51 @@ def test_large_batch_decode_shape_sampled(nq):
     rows = gu.sample_rows(N, 96, 6)
     y_ref = oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows).T
     assert gu.rel_err(y[:, rows], y_ref) <= gu.TOL
+
+
+# ---------------------------------------------------------------- grouped projections
+
+GROUPED_CASES = [
+    # bits, T, K, [N per group]: the q-gate + kv pair of a layer (scaled down), odd tile counts,
+    # four groups, K slabs at T=8, several 8-token slices
+    (5, 8, 1024, [192, 32]), (4, 1, 640, [48, 16, 80]), (5, 3, 5120, [96, 48, 16, 272]),
+    (4, 8, 17408, [64, 48]), (5, 12, 512, [32, 112]), (4, 2, 256, [16]),
+]
+
+
+@pytest.mark.parametrize("bits,T,K,Ns", GROUPED_CASES)
+def test_grouped_projections_parity(nq, bits, T, K, Ns):
+    x = si.activations(si.rng(700 + T + K), T, K)
+    groups, refs = [], []
+    for j, N in enumerate(Ns):
+        if bits == 4:
+            p = si.q4_problem(T, K, N, 710 + j)
+            groups.append((*gu.pack_q4(nq, p["wq"], p["s"], K, N), N))
+            refs.append(oracle.gemm_q4(x, p["wq"], p["s"], T, K, N))
+        else:
+            p = si.q5_problem(T, K, N, 720 + j)
+            groups.append((*gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N), N))
+            refs.append(oracle.gemm_q5(x, p["wn"], p["wh"], p["s"], T, K, N))
+    fn = nq.gemm_q4_grouped if bits == 4 else nq.gemm_q5_grouped
+    ys = fn(gu.dev_bf16(x), groups)
+    for y, r in zip(ys, refs):
+        y = gu.host_f64(y)
+        for t in range(T):
+            assert gu.rel_err(y[t], r[t]) <= gu.TOL, t
+    nq.device_error()
+
+
+def test_grouped_layer_qkv_full_size_sampled(nq):
+    """The layer's q-gate (5120 x 6144) and kv (5120 x 1024) Q5 projections as one grouped
+    launch at T=8, full size, sampled rows of both outputs."""
+    T, K = 8, 5120
+    x = si.activations(si.rng(730), T, K)
+    pq = si.q5_problem(T, K, 6144, 731)
+    pk = si.q5_problem(T, K, 1024, 732)
+    groups = [(*gu.pack_q5(nq, pq["wn"], pq["wh"], pq["s"], K, 6144), 6144),
+              (*gu.pack_q5(nq, pk["wn"], pk["wh"], pk["s"], K, 1024), 1024)]
+    yq, yk = nq.gemm_q5_grouped(gu.dev_bf16(x), groups)
+    for y, p, N, seed in ((yq, pq, 6144, 8), (yk, pk, 1024, 9)):
+        rows = gu.sample_rows(N, 128, seed)
+        ref = oracle.gemm_q5_rows(x, p["wn"], p["wh"], p["s"], T, K, rows).T
+        assert gu.rel_err(gu.host_f64(y)[:, rows], ref) <= gu.TOL

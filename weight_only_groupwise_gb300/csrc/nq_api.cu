@@ -448,6 +448,88 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     return NQ_OK;
 }
 
+// Several projections of the same X in one launch per slice (gemm only, no slab clusters):
+// group g owns ceil(N_g / 32) consecutive row pairs of the work split.
+nq_status project_grouped(int bits, const void* X, const nq_group* groups, int count, int T, int K, void* stream) {
+    if (!groups) return NQ_ERR_NULL;
+    if (count < 1 || count > kMaxGroups || T < 0 || T > kMaxT) return NQ_ERR_SHAPE;
+    for (int g = 0; g < count; ++g) {
+        nq_status st = check_shape(K, groups[g].N);
+        if (st != NQ_OK) return st;
+        if (groups[g].N == 0) return NQ_ERR_SHAPE;
+    }
+    nq_status st = check_shape(K, 16);
+    if (st != NQ_OK) return st;
+    if (T == 0) return NQ_OK;
+    if (!X) return NQ_ERR_NULL;
+    if (misaligned(X)) return NQ_ERR_ALIGN;
+    const size_t xb = (size_t)T * K * 2;
+    for (int g = 0; g < count; ++g) {
+        const nq_group& G = groups[g];
+        if (!G.Wq || !G.S || !G.Y) return NQ_ERR_NULL;
+        if (misaligned(G.Wq) || misaligned(G.S) || misaligned(G.Y)) return NQ_ERR_ALIGN;
+    }
+    for (int g = 0; g < count; ++g) {
+        const size_t yb = (size_t)T * groups[g].N * 2;
+        if (overlap(groups[g].Y, yb, X, xb)) return NQ_ERR_ALIAS;
+        for (int h = 0; h < count; ++h) {
+            if (overlap(groups[g].Y, yb, groups[h].Wq, packed_bytes(bits, K, groups[h].N)) ||
+                overlap(groups[g].Y, yb, groups[h].S, scale_bytes(K, groups[h].N, bits)))
+                return NQ_ERR_ALIAS;
+            if (h != g && overlap(groups[g].Y, yb, groups[h].Y, (size_t)T * groups[h].N * 2)) return NQ_ERR_ALIAS;
+        }
+    }
+    DevState* d = nullptr;
+    st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    if (K == 0) {  // empty sums
+        for (int g = 0; g < count; ++g)
+            if (cudaMemsetAsync(groups[g].Y, 0, (size_t)T * groups[g].N * 2, as_stream(stream)) != cudaSuccess)
+                return NQ_ERR_CUDA;
+        return NQ_OK;
+    }
+    int gpair[kMaxGroups + 1];
+    gpair[0] = 0;
+    for (int g = 0; g < count; ++g) gpair[g + 1] = gpair[g] + (groups[g].N + 2 * kTileRows - 1) / (2 * kTileRows);
+    const int n_pairs = gpair[count];
+    if ((long long)n_pairs * 2 * kTileRows > kMaxDim) return NQ_ERR_SHAPE;
+    const int full = T < kSliceT ? T : kSliceT, rest = T > kSliceT ? T % kSliceT : 0;
+    Plan plans[2];
+    for (int i = 0; i < 2; ++i) {
+        const int tn = i == 0 ? full : rest;
+        if (tn > 0 && !make_plan(bits, 0, tn, K, n_pairs * 2 * kTileRows, d->sms, plans[i])) return NQ_ERR_SHAPE;
+    }
+    long long slots = plans[0].slots;
+    if (rest > 0 && plans[1].slots > slots) slots = plans[1].slots;
+    st = ensure_workspace(*d, slots, n_pairs);
+    if (st != NQ_OK) return st;
+    for (int t0 = 0; t0 < T; t0 += kSliceT) {
+        ProjArgs a;
+        a.p = T - t0 >= kSliceT || rest == 0 ? plans[0] : plans[1];
+        a.q = a.p;
+        a.X = static_cast<const uint16_t*>(X) + (size_t)t0 * K;
+        a.W0 = a.W1 = static_cast<const uint8_t*>(groups[0].Wq);
+        a.S0 = a.S1 = static_cast<const uint8_t*>(groups[0].S);
+        a.Y = static_cast<uint16_t*>(groups[0].Y);
+        a.ngroups = count;
+        for (int g = 0; g <= count; ++g) a.gpair[g] = gpair[g];
+        for (int g = 0; g < count; ++g) {
+            a.gW[g] = static_cast<const uint8_t*>(groups[g].Wq);
+            a.gS[g] = static_cast<const uint8_t*>(groups[g].S);
+            a.gY[g] = static_cast<uint16_t*>(groups[g].Y) + (size_t)t0 * groups[g].N;
+            a.gN[g] = groups[g].N;
+        }
+        a.dev_err = reinterpret_cast<int*>(d->ws);
+        a.tickets = reinterpret_cast<int*>(d->ws + ws_tickets_off());
+        a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
+        a.wait_ns = g_wait_ns;
+        const cudaError_t e = bits == 4 ? launch_proj_q4(a, as_stream(stream), g_pdl)
+                                        : launch_proj_q5(a, as_stream(stream), g_pdl);
+        if (e != cudaSuccess) return NQ_ERR_CUDA;
+    }
+    return NQ_OK;
+}
+
 nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N, void* wq_packed,
                void* s_packed, void* stream) {
     nq_status st = check_shape(K, N);
@@ -616,6 +698,14 @@ nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int 
 
 nq_status nq_gemm_q5(const void* X, const void* Wq, const void* S, void* Y, int T, int K, int N, void* stream) {
     return project(5, false, X, Wq, S, nullptr, nullptr, Y, T, K, N, stream);
+}
+
+nq_status nq_gemm_q4_grouped(const void* X, const nq_group* groups, int count, int T, int K, void* stream) {
+    return project_grouped(4, X, groups, count, T, K, stream);
+}
+
+nq_status nq_gemm_q5_grouped(const void* X, const nq_group* groups, int count, int T, int K, void* stream) {
+    return project_grouped(5, X, groups, count, T, K, stream);
 }
 
 nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su, void* H, int T,

@@ -40,6 +40,8 @@
 
 namespace nq {
 
+constexpr int kMaxGroups = 4;  // projections one grouped launch may carry
+
 struct ProjArgs {
     const uint16_t* X;   // bf16 [T][K]
     const uint8_t* W0;   // packed codes of M tile 0
@@ -52,10 +54,35 @@ struct ProjArgs {
     int* dev_err;        // workspace: device error word
     unsigned long long wait_ns;  // bound of every device-side wait
     float gscale = 1.f;  // tensor scale of NVFP4 weights (1 for the integer formats)
+    // Grouped launch (gemm only): ngroups > 0 projections of the same X, group g owning the
+    // global row pairs [gpair[g], gpair[g+1]) with its own packed weight, scales and output
+    // (N = gN[g]); W0/W1/S0/S1/Y are then unused. ngroups == 0: one matrix.
+    int ngroups = 0;
+    int gpair[kMaxGroups + 1];
+    int gN[kMaxGroups];
+    const uint8_t* gW[kMaxGroups];
+    const uint8_t* gS[kMaxGroups];
+    uint16_t* gY[kMaxGroups];
     Plan p;              // the real plan (slab geometry, shared memory, grid)
     Plan q;              // work split and split-K bookkeeping: p itself, or the cluster-level
                          // plan of a slab-cluster launch (p.cl > 1)
 };
+
+// The matrix a row pair belongs to: its packed codes and scales, output and width, and the
+// pair's index inside it.
+struct PairLoc {
+    const uint8_t* W;
+    const uint8_t* S;
+    uint16_t* Y;
+    int N, RT, rp;
+};
+
+__device__ __forceinline__ PairLoc locate_pair(const ProjArgs& a, int rp) {
+    if (a.ngroups == 0) return PairLoc{a.W0, a.S0, a.Y, a.p.N, a.p.RT, rp};
+    int g = 0;
+    while (g + 1 < a.ngroups && rp >= a.gpair[g + 1]) ++g;
+    return PairLoc{a.gW[g], a.gS[g], a.gY[g], a.gN[g], a.gN[g] / kTileRows, rp - a.gpair[g]};
+}
 
 // Named barriers: 1 = consumers only; 2 + b = run buffer b full (consumers arrive, the
 // epilogue warp of that run syncs); 2 + kMaxRed + b = run buffer b free (that epilogue warp
@@ -232,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
 
     // plan fields used in loops, in registers
     const Plan& p = a.p;
-    const int T = p.T, G = p.G, RT = p.RT, GS = p.GS, nstages = p.stages;
+    const int T = p.T, G = p.G, GS = p.GS, nstages = p.stages;
     const long long row_tile_codes = (long long)G * TB, row_tile_scales = (long long)G * STB;
     const uint64_t wait_ns = a.wait_ns;
 
@@ -307,13 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             for (int si = 0; si < order.count && ok; ++si) {
                 const Segment v = seg_pick(q, order, si, nat, u1);
                 const Segment sg = CLU ? rank_segment(p, v, crank) : v;
-                const int rt0 = SWIGLU ? sg.rp : 2 * sg.rp;
-                const int rt1 = SWIGLU ? sg.rp : 2 * sg.rp + 1;
-                const bool has1 = SWIGLU || rt1 < RT;
-                const uint8_t* w0 = a.W0 + rt0 * row_tile_codes;
-                const uint8_t* w1 = a.W1 + rt1 * row_tile_codes;
-                const uint8_t* s0 = a.S0 + rt0 * row_tile_scales;
-                const uint8_t* s1 = a.S1 + rt1 * row_tile_scales;
+                // SwiGLU: tile sg.rp of the gate matrix and of the up matrix; gemm: tiles
+                // 2 rp, 2 rp + 1 of the pair's matrix (the second may not exist)
+                const PairLoc L = SWIGLU ? PairLoc{a.W0, a.S0, a.Y, p.N, p.RT, sg.rp} : locate_pair(a, sg.rp);
+                const int rt0 = SWIGLU ? sg.rp : 2 * L.rp;
+                const int rt1 = SWIGLU ? sg.rp : 2 * L.rp + 1;
+                const bool has1 = SWIGLU || rt1 < L.RT;
+                const uint8_t* w0 = L.W + rt0 * row_tile_codes;
+                const uint8_t* w1 = (SWIGLU ? a.W1 : L.W) + rt1 * row_tile_codes;
+                const uint8_t* s0 = L.S + rt0 * row_tile_scales;
+                const uint8_t* s1 = (SWIGLU ? a.S1 : L.S) + rt1 * row_tile_scales;
                 for (int b = sg.ga / BG; sg.ga < sg.gb && b * BG < sg.gb; ++b) {
                     const int i0 = max(sg.ga - b * BG, 0), i1 = min(sg.gb - b * BG, BG);
                     if (!mbar_wait(empty0 + 8 * st, phase ^ 1, flags, a.dev_err, wait_ns)) {
@@ -538,13 +568,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 }
             }
             if (write) {
+                const PairLoc L = SWIGLU ? PairLoc{a.W0, a.S0, a.Y, p.N, p.RT, sg.rp} : locate_pair(a, sg.rp);
 #pragma unroll
                 for (int j = 0; j < JN8; ++j) {
                     const int o = lane + 32 * j;
                     const int m = SWIGLU ? 0 : o >> (4 + tp_log), tok = (o >> 4) & (TP - 1), row = o & 15;
-                    const int rt = SWIGLU ? sg.rp : 2 * sg.rp + m;
-                    if (o < nout && tok < T && rt < RT)
-                        a.Y[(size_t)tok * p.N + (size_t)rt * kTileRows + row] =
+                    const int rt = SWIGLU ? sg.rp : 2 * L.rp + m;
+                    if (o < nout && tok < T && rt < L.RT)
+                        L.Y[(size_t)tok * L.N + (size_t)rt * kTileRows + row] =
                             SWIGLU ? bf16_bits_rn(silu_mul(v0[j], v1[j])) : bf16_bits_rn(v0[j]);
                 }
             }

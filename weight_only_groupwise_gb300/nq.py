@@ -18,6 +18,11 @@ STATUS = {0: "NQ_OK", -1: "NQ_ERR_NULL", -2: "NQ_ERR_SHAPE", -3: "NQ_ERR_ALIGN",
           -5: "NQ_ERR_CUDA", -6: "NQ_ERR_DEVICE", -7: "NQ_ERR_TIMEOUT", -8: "NQ_ERR_SCRATCH"}
 
 
+class NqGroup(ctypes.Structure):
+    """struct nq_group of include/nq.h."""
+    _fields_ = [("Wq", ctypes.c_void_p), ("S", ctypes.c_void_p), ("Y", ctypes.c_void_p), ("N", ctypes.c_int)]
+
+
 class NqError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(msg)
@@ -62,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.nq_gemm_fp4.restype = I
         L.nq_dequant_fp4_debug.argtypes = [P, P, ctypes.c_float, P, I, I, P]
         L.nq_dequant_fp4_debug.restype = I
+        for f in ("nq_gemm_q4_grouped", "nq_gemm_q5_grouped"):
+            getattr(L, f).argtypes = [P, P, I, I, I, P]
+            getattr(L, f).restype = I
         L.nq_reserve.argtypes = [I, I, I]
         L.nq_device_error.argtypes = []
         L.nq_wait_limit.argtypes = [ctypes.c_longlong]
@@ -186,6 +194,28 @@ def gemm_q4_noalloc(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, N: int, 
     y = _out(x, N, out)
     _check(lib().nq_gemm_q4_noalloc(_ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N, _stream(stream)))
     return y
+
+
+def _grouped(fn, x, groups, outs, stream):
+    _cuda(x, "x")
+    T, K = x.shape
+    if outs is None:
+        outs = [torch.empty((T, N), dtype=torch.bfloat16, device=x.device) for (_, _, N) in groups]
+    arr = (NqGroup * len(groups))()
+    for i, ((wq, s, N), y) in enumerate(zip(groups, outs)):
+        _cuda(y, "out")
+        arr[i] = NqGroup(wq.data_ptr(), s.data_ptr(), y.data_ptr(), N)
+    _check(fn(_ptr(x), ctypes.cast(arr, ctypes.c_void_p), len(groups), T, K, _stream(stream)))
+    return outs
+
+
+def gemm_q4_grouped(x, groups, outs=None, stream=None):
+    """[Y_g] for groups [(packed codes, packed scales, N_g), ...] sharing X, one launch."""
+    return _grouped(lib().nq_gemm_q4_grouped, x, groups, outs, stream)
+
+
+def gemm_q5_grouped(x, groups, outs=None, stream=None):
+    return _grouped(lib().nq_gemm_q5_grouped, x, groups, outs, stream)
 
 
 def swiglu_q4(x, wg, sg, wu, su, N: int, out=None, stream=None):
@@ -333,6 +363,7 @@ def plan_cluster_segments(bits: int, mode: int, T: int, K: int, N: int, clusters
 nq_pack_q4, nq_pack_q5 = pack_q4, pack_q5
 nq_gemm_q4, nq_gemm_q5, nq_gemm_q4_noalloc = gemm_q4, gemm_q5, gemm_q4_noalloc
 nq_swiglu_q4, nq_swiglu_q5 = swiglu_q4, swiglu_q5
+nq_gemm_q4_grouped, nq_gemm_q5_grouped = gemm_q4_grouped, gemm_q5_grouped
 nq_dequant_q4_debug, nq_dequant_q5_debug = dequant_q4_debug, dequant_q5_debug
 nq_pack_fp4, nq_gemm_fp4, nq_dequant_fp4_debug = pack_fp4, gemm_fp4, dequant_fp4_debug
 nq_reserve, nq_device_error, nq_shutdown, nq_wait_limit = reserve, device_error, shutdown, wait_limit
