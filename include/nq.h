@@ -323,6 +323,26 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
                          int64_t* seg, int64_t cap);
 
 /*
+ * nq_tensor_core_batches: how plain Q4/Q5 projections with 8 < T <= 64 run. On (1, the
+ * default; the environment variable NQ_TC=0 read at the first call turns it off): one launch of
+ * the tensor-core kernel, which decodes the weights once into the fifth-generation tensor
+ * cores' memory (TMEM) and multiplies them with all T tokens (tcgen05.mma, M = 128 rows,
+ * N = 16, 32 or 64 padded tokens), so the weights stream from HBM once. Off (0): one launch of
+ * the 8-token kernel per slice of 8 tokens. -1 only queries. Returns the previous setting.
+ * Either way the results agree with the oracle within the same tolerance. The SwiGLU, NVFP4 and
+ * no-allocation calls use slices at every T. Not synchronised with calls in flight.
+ */
+int nq_tensor_core_batches(int enable);
+
+/*
+ * nq_plan_tc_info: the work split the tensor-core kernel would use (host only): out[0] blocks,
+ * [1] row blocks of 128 rows, [2] K pieces per row block (their fp32 partials are added in
+ * fixed order by the row block's last piece), [3] padded token count, [4] pipeline stages,
+ * [5] shared-memory bytes, [6] 64-wide K groups, [7] groups per stage. bits 4 or 5, 8 < T <= 64.
+ */
+nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t out[8]);
+
+/*
  * nq_slab_clusters: turn slab clusters on (1) or off (0) for later projection calls of this
  * process, or only query (-1); returns the previous setting. Off unless the environment
  * variable NQ_CLUSTER is "1" at the first call. On GB300 a slab-cluster call is 8-23 %

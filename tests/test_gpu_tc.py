@@ -1,0 +1,122 @@
+"""GPU parity of the large-batch tensor-core kernel (8 < T <= 64: tcgen05.mma with the decoded
+weights in TMEM) against the fp64 CPU oracle, per token row within 5e-3, and against the
+8-token-slice path. Shapes cover partial 128-row blocks, a K split across blocks (fp32 partials
+added in fixed order), a single K group, every padded token count (16, 32, 64) and both code
+widths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    assert nq.tensor_core_batches(-1) == 1
+    return nq
+
+
+TC_SHAPES = [
+    # T, K, N, seed
+    (9, 64, 16, 0), (16, 256, 128, 1), (17, 640, 272, 2), (32, 1024, 48, 3), (33, 5120, 384, 4),
+    (48, 1536, 1040, 5), (64, 512, 144, 6), (64, 17408, 96, 7), (24, 6208, 2064, 8), (12, 192, 4096, 9),
+]
+
+
+def _problem(bits, T, K, N, seed):
+    if bits == 4:
+        p = si.q4_problem(T, K, N, seed)
+        return p, lambda nq: gu.pack_q4(nq, p["wq"], p["s"], K, N), \
+            lambda: oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+    p = si.q5_problem(T, K, N, seed)
+    return p, lambda nq: gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N), \
+        lambda: oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("T,K,N,seed", TC_SHAPES)
+def test_tc_parity(nq, bits, T, K, N, seed):
+    p, pack, ref = _problem(bits, T, K, N, 800 + seed + 50 * bits)
+    w = pack(nq)
+    fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
+    y = gu.host_f64(fn(gu.dev_bf16(p["x"]), *w, N))
+    y_ref = ref()
+    for t in range(T):
+        assert np.all(np.isfinite(y[t]))
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+    nq.device_error()
+
+
+def test_tc_matches_slices_and_is_deterministic(nq):
+    T, K, N = 40, 2048, 1152
+    p = si.q4_problem(T, K, N, 880)
+    w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+    x = gu.dev_bf16(p["x"])
+    y1 = nq.gemm_q4(x, *w, N)
+    y2 = nq.gemm_q4(x, *w, N)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    prev = nq.tensor_core_batches(0)
+    try:
+        ys = nq.gemm_q4(x, *w, N)
+    finally:
+        nq.tensor_core_batches(prev)
+    y_ref = oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+    for y in (y1, ys):
+        yh = gu.host_f64(y)
+        for t in range(T):
+            assert gu.rel_err(yh[t], y_ref[t]) <= gu.TOL
+    nq.device_error()
+
+
+def test_tc_zero_point_codes_give_exact_zero(nq):
+    """Codes equal to z decode to exact bf16 zeros, so every product and sum is exactly 0."""
+    T, K, N = 24, 1024, 272
+    p = si.q4_problem(T, K, N, 881)
+    x = gu.dev_bf16(p["x"])
+    z4 = gu.pack_q4(nq, np.full((N, K // 8), 0x88888888, np.uint32), p["s"], K, N)
+    assert torch.count_nonzero(nq.gemm_q4(x, *z4, N).float()) == 0
+    z5 = gu.pack_q5(nq, np.zeros((N, K // 8), np.uint32), np.full((N, K // 32), 0xFFFFFFFF, np.uint32), p["s"], K, N)
+    assert torch.count_nonzero(nq.gemm_q5(x, *z5, N).float()) == 0
+
+
+@pytest.mark.parametrize("bits,K,N", [(4, 5120, 17408), (5, 5120, 6144)])
+def test_tc_full_size_sampled(nq, bits, K, N):
+    """T=64 on the decode (Q4) and verify (Q5) weight shapes, full-size launch, sampled rows."""
+    T = 64
+    p, pack, _ = _problem(bits, T, K, N, 890 + bits)
+    w = pack(nq)
+    fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
+    y = gu.host_f64(fn(gu.dev_bf16(p["x"]), *w, N))
+    rows = gu.sample_rows(N, 128, 11)
+    if bits == 4:
+        y_ref = oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows).T
+    else:
+        y_ref = oracle.gemm_q5_rows(p["x"], p["wn"], p["wh"], p["s"], T, K, rows).T
+    for t in range(T):
+        assert gu.rel_err(y[t, rows], y_ref[t]) <= gu.TOL, t
+
+
+def test_tc_activation_outliers(nq):
+    T, K, N = 20, 1280, 160
+    p = si.q5_problem(T, K, N, 895)
+    g = np.random.default_rng(896)
+    x = g.standard_normal((T, K)).astype(np.float32)
+    x[0, 5] = 3.0e38
+    x[1, :] *= 1.0e6
+    x[3, :] *= 1.0e-30
+    x[17, 700] = -2.0e37
+    xb = si.bf16_bits(x)
+    w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+    y = gu.host_f64(nq.gemm_q5(gu.dev_bf16(xb), *w, N))
+    y_ref = oracle.gemm_q5(xb, p["wn"], p["wh"], p["s"], T, K, N)
+    for t in range(T):
+        assert np.all(np.isfinite(y[t]))
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t

@@ -171,3 +171,21 @@ def test_noalloc_limits_stated_in_header(nq, T, K, n_max):
 def test_one_slab_k_limits_stated_in_header(nq, T, k_max):
     assert nq.plan_info(4, 0, T, k_max, 512, 152)["slabs"] == 1
     assert nq.plan_info(4, 0, T, k_max + 64, 512, 152)["slabs"] == 2
+
+
+@pytest.mark.parametrize("bits,T,K,N", [(4, 64, 5120, 17408), (5, 16, 5120, 6144), (4, 33, 17408, 5120),
+                                        (5, 9, 64, 16), (4, 64, 192, 4096), (5, 48, 6208, 1040)])
+@pytest.mark.parametrize("sms", [152, 148, 7])
+def test_tc_plan(nq, bits, T, K, N, sms):
+    """The tensor-core kernel's split: every (row block, K piece) is one block, the pieces of a
+    row block cover its K groups once, at most one block per SM when there are enough row
+    blocks, and the stages fit the shared memory."""
+    p = nq.plan_tc_info(bits, T, K, N, sms)
+    G = K // 64
+    assert p["groups"] == G and p["row_blocks"] == -(-N // 128)
+    assert p["ctas"] == p["row_blocks"] * p["k_pieces"]
+    assert p["ctas"] <= max(sms, p["row_blocks"])
+    bounds = [kp * G // p["k_pieces"] for kp in range(p["k_pieces"] + 1)]
+    assert bounds[0] == 0 and bounds[-1] == G and all(b1 > b0 for b0, b1 in zip(bounds, bounds[1:]))
+    assert p["tokens_padded"] in (16, 32, 64) and p["tokens_padded"] >= T > p["tokens_padded"] // 2 - (8 if T <= 16 else 0)
+    assert 2 <= p["stages"] and p["smem_bytes"] <= 227 * 1024

@@ -236,6 +236,9 @@ struct DevState {
     long long tickets_cap = 0;
     // resident slab clusters per [S][bits == 5][swiglu], -1 until queried
     int cluster_cap[kMaxCluster + 1][2][2];
+    // large-batch tensor-core kernel: [tickets: 4 B per row block, 256-B rounded][partials]
+    uint8_t* tc_ws = nullptr;
+    long long tc_tickets = 0, tc_floats = 0;
 };
 
 constexpr int kMaxDevices = 64;
@@ -244,6 +247,7 @@ DevState g_dev[kMaxDevices];
 bool g_pdl = true;
 bool g_cluster = false;
 bool g_env_read = false;
+bool g_tc = true;
 unsigned long long g_wait_ns = (unsigned long long)kWaitTimeoutNs;
 
 // Reads NQ_PDL, NQ_CLUSTER and NQ_WAIT_NS once (the first call that needs them). g_mu held.
@@ -253,6 +257,8 @@ void read_env_locked() {
     if (e && e[0] == '0') g_pdl = false;
     const char* c = std::getenv("NQ_CLUSTER");
     if (c && c[0] == '1') g_cluster = true;
+    const char* tcv = std::getenv("NQ_TC");
+    if (tcv && tcv[0] == '0') g_tc = false;
     const char* w = std::getenv("NQ_WAIT_NS");
     if (w) {
         const long long v = std::atoll(w);
@@ -315,6 +321,34 @@ nq_status ensure_workspace(DevState& d, long long slots, long long tickets) {
     d.ws = static_cast<uint8_t*>(p);
     d.slots_cap = sc;
     d.tickets_cap = tc;
+    return NQ_OK;
+}
+
+// The tensor-core kernel's scratch: tickets (zero between calls) and fp32 partial slots.
+// Growing it synchronises the device.
+nq_status ensure_tc_workspace(DevState& d, long long tickets, long long floats) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d.tc_ws && tickets <= d.tc_tickets && floats <= d.tc_floats) return NQ_OK;
+    long long tc = d.tc_tickets > tickets ? d.tc_tickets : tickets;
+    long long fc = d.tc_floats > floats ? d.tc_floats : floats;
+    if (tc < 1024) tc = 1024;
+    const size_t toff = (((size_t)tc * 4 + 255) / 256) * 256;
+    const size_t bytes = toff + (size_t)fc * sizeof(float);
+    if (d.tc_ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return NQ_ERR_CUDA;
+        cudaFree(d.tc_ws);
+        d.tc_ws = nullptr;
+        d.tc_tickets = d.tc_floats = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return NQ_ERR_CUDA;
+    if (cudaMemset(p, 0, toff) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(p);
+        return NQ_ERR_CUDA;
+    }
+    d.tc_ws = static_cast<uint8_t*>(p);
+    d.tc_tickets = tc;
+    d.tc_floats = fc;
     return NQ_OK;
 }
 
@@ -408,6 +442,24 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     if (st != NQ_OK) return st;
     if (K == 0) {  // empty sum
         return cudaMemsetAsync(Y, 0, yb, as_stream(stream)) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+    }
+    // Larger batches of a plain projection: the tensor-core kernel, one weight pass.
+    if (g_tc && !swiglu && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
+        alignas(64) TcArgs ta;
+        if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP)) {
+            st = ensure_workspace(*d, 1, 1);
+            if (st != NQ_OK) return st;
+            st = ensure_tc_workspace(*d, ta.p.RB, ta.p.KS > 1 ? (long long)ta.p.P * kTcRows * ta.p.TP : 1);
+            if (st != NQ_OK) return st;
+            ta.W = static_cast<const uint8_t*>(W0);
+            ta.S = static_cast<const uint8_t*>(S0);
+            ta.Y = static_cast<uint16_t*>(Y);
+            ta.tickets = reinterpret_cast<int*>(d->tc_ws);
+            ta.partials = reinterpret_cast<float*>(d->tc_ws + (((size_t)d->tc_tickets * 4 + 255) / 256) * 256);
+            ta.dev_err = reinterpret_cast<int*>(d->ws);
+            ta.wait_ns = g_wait_ns;
+            return launch_tc_proj(bits, ta, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+        }
     }
     // At most two distinct slice sizes: full slices and the remainder.
     const int full = T < kSliceT ? T : kSliceT, rest = T > kSliceT ? T % kSliceT : 0;
@@ -783,6 +835,7 @@ nq_status nq_device_error(void) {
     if (cudaMemcpy(&err, d->ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NQ_ERR_CUDA;
     if (err == 0) return st_static;
     if (cudaMemset(d->ws, 0, ws_partials_off(d->tickets_cap)) != cudaSuccess ||
+        (d->tc_ws && cudaMemset(d->tc_ws, 0, (size_t)d->tc_tickets * 4) != cudaSuccess) ||
         cudaDeviceSynchronize() != cudaSuccess)
         return NQ_ERR_CUDA;
     return NQ_ERR_TIMEOUT;
@@ -793,12 +846,15 @@ void nq_shutdown(void) {
     int cur = 0;
     cudaGetDevice(&cur);
     for (int i = 0; i < kMaxDevices; ++i) {
-        if (!g_dev[i].ws) continue;
+        if (!g_dev[i].ws && !g_dev[i].tc_ws) continue;
         cudaSetDevice(i);
         cudaDeviceSynchronize();
         cudaFree(g_dev[i].ws);
         g_dev[i].ws = nullptr;
         g_dev[i].slots_cap = g_dev[i].tickets_cap = 0;
+        cudaFree(g_dev[i].tc_ws);
+        g_dev[i].tc_ws = nullptr;
+        g_dev[i].tc_tickets = g_dev[i].tc_floats = 0;
     }
     cudaSetDevice(cur);
 }
@@ -847,6 +903,34 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
         ++n;
     }
     return n;
+}
+
+int nq_tensor_core_batches(int enable) {
+    DevState* d = nullptr;
+    current_device(&d, nullptr);  // reads the environment once, like every call
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int prev = g_tc ? 1 : 0;
+    if (enable == 0 || enable == 1) g_tc = enable == 1;
+    return prev;
+}
+
+nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t out[8]) {
+    if (!out) return NQ_ERR_NULL;
+    if ((bits != 4 && bits != 5) || T <= kSliceT || T > kTcMaxT || num_sms < 1 || K < kGroup || N < kTileRows)
+        return NQ_ERR_SHAPE;
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    TcPlan p;
+    if (!make_tc_plan(bits, T, K, N, num_sms, p)) return NQ_ERR_SHAPE;
+    out[0] = p.P;
+    out[1] = p.RB;
+    out[2] = p.KS;
+    out[3] = p.TP;
+    out[4] = p.stages;
+    out[5] = p.smem_bytes;
+    out[6] = p.G;
+    out[7] = kTcStageGroups;
+    return NQ_OK;
 }
 
 int nq_slab_clusters(int enable) {

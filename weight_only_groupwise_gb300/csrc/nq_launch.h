@@ -4,8 +4,14 @@
 #include <cuda_runtime.h>
 
 #include "nq_proj.cuh"
+#include "nq_tc.cuh"
 
 namespace nq {
+
+// Large-batch tensor-core kernel (nq_tc.cuh): the activation tensor map (false if the driver
+// entry point is missing or rejects the view) and the launch.
+bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP);
+cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl);
 
 // Bound of every device-side wait for later launches (nq_wait_limit; NQ_WAIT_NS).
 unsigned long long wait_limit_ns();

@@ -1,0 +1,516 @@
+// nq_tc.cuh -- the large-batch projection kernel: Y[T,N] = X[T,K] * dequant(W) for
+// 8 < T <= 64 tokens (several concurrent requests' speculative-verify rows: "ninfer-ext"
+// README, section "与原版 NInfer 的对比", C = 1..8 requests; "NInfer-4090" post, section
+// "实测数据", C2/C4/C8), 4- or 5-bit codes with one fp16 scale per 64-wide K group, on the
+// fifth-generation tensor cores (tcgen05) so that the weights stream from HBM once whatever T.
+//
+// One block per (128-row block, K piece), 10 warps:
+//   * warp 0, one lane -- producer: 1-D bulk copies of the eight 16-row tiles' codes and scales
+//     of each stage (kTcStageGroups groups) and one 3-D TMA copy of the stage's activation
+//     chunk, laid out as the tensor core's K-major core matrices (8 tokens x 16 bytes), tokens
+//     past T filled with zeros by the copy. A ring of shared-memory stages, mbarriers.
+//   * warps 1..4 -- decoders: warp w owns TMEM lanes 32 (w % 4) .. + 31, i.e. row tiles
+//     2 (w % 4) and + 1. A lane decodes its fragment words of a group into bf16 (q - z), exact,
+//     and stores them with tcgen05.st.16x128b.x2, which places the mma.sync A-fragment
+//     registers of lane t at TMEM lanes t/4, t/4 + 8 and columns t%4, 4 + t%4: K in natural
+//     order, one row per TMEM lane. Buffers of 32 columns (64 K) per group, kTcA of them.
+//   * warp 5, one lane -- MMA issuer: per group, four tcgen05.mma.kind::f16 (M = 128, N = TP,
+//     K = 16; A from TMEM, B = the activation chunk through a shared-memory descriptor; D in
+//     TMEM, fp32, a fresh accumulator per group: P = sum over the group of (q - z) x, exact
+//     products), then tcgen05.commit to the barriers that free the A buffer and publish P.
+//   * warps 6..9 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
+//     adds s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y, or,
+//     when K is split across blocks, an fp32 partial; the last block of a row block (ticket)
+//     adds the partials in fixed order and stores Y.
+// Every wait is bounded (the abort protocol of the small-batch kernel); TMEM is allocated and
+// freed by warp 0, after the issuer has waited for its last MMAs.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "nq_common.cuh"
+
+namespace nq {
+
+constexpr int kTcRows = 128;                      // rows per block = MMA M
+constexpr int kTcTiles = kTcRows / kTileRows;     // 16-row tiles per block
+constexpr int kTcStageGroups = 4;                 // 64-wide K groups per pipeline stage
+constexpr int kTcMaxStages = 8;
+constexpr int kTcA = 4;                           // A buffers in TMEM (32 columns each)
+constexpr int kTcP = 2;                           // P buffers in TMEM (TP columns each)
+constexpr int kTcWarps = 10;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcMinT = 9, kTcMaxT = 64;
+
+// Shared-memory bytes of one stage: codes and scales of kTcTiles tiles x kTcStageGroups groups,
+// then the activation chunk (kTcStageGroups * 64 K x TP tokens, bf16).
+NQ_HD int tc_weight_bytes(int bits) { return kTcTiles * kTcStageGroups * (code_tile_bytes(bits) + kScaleTileBytes); }
+NQ_HD int tc_x_bytes(int TP) { return TP * kTcStageGroups * kGroup * 2; }
+NQ_HD int tc_stage_bytes(int bits, int TP) { return tc_weight_bytes(bits) + tc_x_bytes(TP); }
+// Per stage: TP token exponents and a flag (the activation range check), after the barriers.
+NQ_HD int tc_extra_bytes(int TP) { return 1024 + kTcMaxStages * (TP + 1) * 4; }
+NQ_HD int tc_stages(int bits, int TP) {
+    int s = (kSmemLimit - tc_extra_bytes(TP)) / tc_stage_bytes(bits, TP);
+    return s > kTcMaxStages ? kTcMaxStages : s;
+}
+NQ_HD int tc_tpad(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
+
+// Work split of a large-batch call: RB row blocks of 128 rows, each K cut into KS pieces so
+// that RB * KS blocks about fill the SMs.
+struct TcPlan {
+    int T, TP, K, N, G, RT, RB, KS, P, stages, smem_bytes;
+};
+
+NQ_HD bool make_tc_plan(int bits, int T, int K, int N, int num_sms, TcPlan& p) {
+    p.T = T;
+    p.TP = tc_tpad(T);
+    p.K = K;
+    p.N = N;
+    p.G = K / kGroup;
+    p.RT = N / kTileRows;
+    p.RB = (N + kTcRows - 1) / kTcRows;
+    int ks = num_sms / (p.RB > 0 ? p.RB : 1);
+    const int max_ks = p.G / (2 * kTcStageGroups) > 0 ? p.G / (2 * kTcStageGroups) : 1;  // >= 8 groups a piece
+    if (ks > max_ks) ks = max_ks;
+    if (ks < 1) ks = 1;
+    p.KS = ks;
+    p.P = p.RB * p.KS;
+    p.stages = tc_stages(bits, p.TP);
+    p.smem_bytes = p.stages * tc_stage_bytes(bits, p.TP) + tc_extra_bytes(p.TP);
+    return p.stages >= 2 && p.G > 0;
+}
+
+struct alignas(64) TcArgs {
+    CUtensorMap xmap;        // X viewed as [K/8][T][8] bf16 (tokens past T read as zeros)
+    const uint8_t* W;        // packed codes
+    const uint8_t* S;        // packed scales
+    uint16_t* Y;             // bf16 [T][N]
+    float* partials;         // RB * KS slots of kTcRows x TP floats (K split only)
+    int* tickets;            // one per row block, zero between calls
+    int* dev_err;
+    unsigned long long wait_ns;
+    TcPlan p;
+};
+
+// ---------------------------------------------------------------- tcgen05 helpers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// The four A-fragment registers of a lane (rows r, r+8; K pairs c, c+4 of a 16-wide K step)
+// into TMEM: lanes taddr.lane + r, + r + 8; columns taddr.col + c, + 4 + c.
+__device__ __forceinline__ void tmem_st_frag(uint32_t taddr, const uint32_t a[4]) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a[0]),
+                 "r"(a[1]), "r"(a[2]), "r"(a[3])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive columns of the thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// D (+)= A * B: M = 128, N from idesc, K = 16; A in TMEM, B through a shared-memory descriptor.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on an mbarrier when all tcgen05 operations this thread issued so far are done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand without swizzle: core matrices of 8 rows x 16
+// bytes, lbo = bytes between K-adjacent cores, sbo = bytes between 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+           (1ull << 46);
+}
+
+// Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t tc_idesc_bf16(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint16_t bf16_bits_rn_tc(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// K step J of a lane's code word as four bf16x2 registers holding q - z exactly.
+template <int BITS, int J>
+__device__ __forceinline__ void tc_decode(const uint4& w, uint32_t hb, uint32_t a[4]) {
+    constexpr uint32_t kOff = BITS == 4 ? 0x43084308u : 0x43104310u;  // 128 + z in both halves
+    uint32_t magic;
+    asm("mov.b32 %0, %1;" : "=r"(magic) : "n"(kBf16Magic));
+    const uint32_t word = J == 0 ? w.x : (J == 1 ? w.y : (J == 2 ? w.z : w.w));
+    if constexpr (BITS == 4)
+        decode_q4_bf16(word, a, magic);
+    else
+        decode_q5_bf16<J>(word, hb, a, magic);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = bf16x2_sub(a[i], kOff);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int BITS, int TP>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_constant__ TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
+    constexpr int BG = kTcStageGroups;
+    constexpr int kWBytes = kTcTiles * BG * (TB + kScaleTileBytes);
+    constexpr int kXBytes = TP * BG * kGroup * 2;
+    constexpr int kStageBytes = kWBytes + kXBytes;
+    constexpr uint32_t kCols = 256;                   // TMEM columns: A buffers, then P buffers
+    static_assert(kTcA * 32 + kTcP * TP <= (int)kCols, "TMEM budget");
+    constexpr uint32_t kIdesc = tc_idesc_bf16(TP);
+
+    const TcPlan& p = a.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nstages = p.stages;
+    const int rb = (int)blockIdx.x / p.KS, kp = (int)blockIdx.x % p.KS;
+    const int g0 = (int)((long long)kp * p.G / p.KS), g1 = (int)((long long)(kp + 1) * p.G / p.KS);
+    const int ngroups = g1 - g0;
+    const int nst = (ngroups + BG - 1) / BG;          // stages this block streams
+    const uint64_t wait_ns = a.wait_ns;
+
+    uint8_t* stage_mem = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + nstages * kStageBytes);
+    // bars: full[S], empty[S], xchk[S], a_full[A], a_empty[A], p_full[P], p_empty[P], done;
+    // then flags, then per stage the token exponents of the range check
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kTcMaxStages, xchk0 = empty0 + 8 * kTcMaxStages;
+    const uint32_t afull0 = xchk0 + 8 * kTcMaxStages, aempty0 = afull0 + 8 * kTcA;
+    const uint32_t pfull0 = aempty0 + 8 * kTcA, pempty0 = pfull0 + 8 * kTcP, done_bar = pempty0 + 8 * kTcP;
+    volatile int* flags = reinterpret_cast<volatile int*>(bars + 3 * kTcMaxStages + 2 * kTcA + 2 * kTcP + 1);
+    // flags: [0] abort, [1] stages issued, [2] producer done, [3] TMEM base, [4] last ticket
+    // xexp: per stage, TP token exponents e (the chunk holds x * 2^-e) and [TP] = any e > 0
+    int* xexp = const_cast<int*>(flags) + 16;
+    const int kDecoders = 4, kEpilogue = 4;
+
+    if (tid == 0) {
+        for (int i = 0; i < nstages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kDecoders + 1 + kEpilogue);
+            mbar_init(xchk0 + 8 * i, kDecoders);
+        }
+        for (int i = 0; i < kTcA; ++i) {
+            mbar_init(afull0 + 8 * i, kDecoders);
+            mbar_init(aempty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < kTcP; ++i) {
+            mbar_init(pfull0 + 8 * i, 1);
+            mbar_init(pempty0 + 8 * i, kEpilogue);
+        }
+        mbar_init(done_bar, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        flags[2] = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(const_cast<int*>(flags) + 3), kCols);
+    grid_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)flags[3];
+    const uint32_t a_col0 = 0, p_col0 = kTcA * 32;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int it = 0;
+            bool ok = true;
+            for (int si = 0; si < nst && ok; ++si) {
+                const int st = si % nstages;
+                if (si >= nstages && !mbar_wait(empty0 + 8 * st, ((si / nstages) - 1) & 1, flags, a.dev_err, wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int g = g0 + si * BG, ng = g1 - g < BG ? g1 - g : BG;
+                uint8_t* sb = stage_mem + st * kStageBytes;
+                uint32_t bytes = (uint32_t)kXBytes;
+                for (int m = 0; m < kTcTiles; ++m)
+                    if (rb * kTcTiles + m < p.RT) bytes += (uint32_t)ng * (TB + kScaleTileBytes);
+                const uint32_t fb = full0 + 8 * st;
+                mbar_arrive_expect_tx(fb, bytes);
+                for (int m = 0; m < kTcTiles; ++m) {
+                    const int rt = rb * kTcTiles + m;
+                    if (rt >= p.RT) continue;
+                    bulk_g2s(smem_u32(sb + m * BG * TB), a.W + packed_code_off(rt, g, p.G, TB), ng * TB, fb, pol);
+                    bulk_g2s(smem_u32(sb + kTcTiles * BG * TB + m * BG * kScaleTileBytes),
+                             a.S + packed_scale_off(rt, g, p.G, kScaleTileBytes), ng * kScaleTileBytes, fb, pol);
+                }
+                // the weights are never written by a kernel that lets its dependents start
+                // early; X may be the preceding kernel's output
+                if (si == 0) grid_dependency_wait();
+                tma_load_3d(smem_u32(sb + kWBytes), &a.xmap, 0, 0, g * (kGroup / 8), fb);
+                ++it;
+            }
+            if (!ok) {
+                const int first = it > nstages ? it - nstages : 0;
+                for (int j = first; j < it; ++j)
+                    mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, kDrainNs);
+            }
+            flags[1] = it;
+            __threadfence_block();
+            flags[2] = 1;
+        }
+    } else if (warp <= kDecoders) {
+        // ------------------------------------------------------------ decoders
+        const int q = warp & 3;                        // TMEM lane quarter: rows 32q .. 32q+31
+        const int dt = tid - 32;                       // decoder thread 0..127
+        for (int gi = 0; gi < ngroups; ++gi) {
+            const int si = gi / BG, gs = gi % BG, st = si % nstages;
+            const int ab = gi % kTcA;
+            bool ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+            if (gs == 0) {
+                // Range check of the stage's activation chunk (every decoder thread, every stage,
+                // so the named barriers below always match): the group partials sum (q - z) x
+                // in fp32, so a token with some |x| >= 2^100 (bits 0x7180) is scaled by 2^-e,
+                // e = exponent(max |x|) - 99, exact in bf16; the epilogue multiplies its
+                // partials back by 2^e. Chunk c of the [K/8][TP][8] layout belongs to token c % TP.
+                uint4* xc = reinterpret_cast<uint4*>(stage_mem + st * kStageBytes + kWBytes);
+                int* ex = xexp + st * (TP + 1);
+                constexpr int kChunks = kXBytes / 16;
+                uint32_t big = 0;
+                for (int c = dt; c < kChunks; c += kDecoders * 32) {
+                    const uint4 v = xc[c];
+                    big |= ((v.x & 0x7FFF7FFFu) + 0x0E800E80u) | ((v.y & 0x7FFF7FFFu) + 0x0E800E80u) |
+                           ((v.z & 0x7FFF7FFFu) + 0x0E800E80u) | ((v.w & 0x7FFF7FFFu) + 0x0E800E80u);
+                }
+                if (named_bar_or(2, kDecoders * 32, (big & 0x80008000u) != 0)) {
+                    for (int t = dt; t < TP; t += kDecoders * 32) ex[t] = 0;
+                    named_bar_sync(2, kDecoders * 32);
+                    for (int c = dt; c < kChunks; c += kDecoders * 32) {
+                        const uint4 v = xc[c];
+                        const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                               max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+                        atomicMax(ex + c % TP, (int)max(m & 0xFFFFu, m >> 16));
+                    }
+                    named_bar_sync(2, kDecoders * 32);
+                    for (int c = dt; c < kChunks; c += kDecoders * 32) {
+                        const int e = ((ex[c % TP] >> 7) & 0xFF) - 127 - 99;
+                        if (e <= 0) continue;
+                        const float sc = __int_as_float((127 - e) << 23);
+                        uint4 v = xc[c];
+                        uint32_t* iv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(iv[i] << 16) * sc,
+                                                                            __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
+                            iv[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        xc[c] = v;
+                    }
+                    named_bar_sync(2, kDecoders * 32);
+                    for (int t = dt; t < TP; t += kDecoders * 32) {
+                        const int e = ((ex[t] >> 7) & 0xFF) - 127 - 99;
+                        ex[t] = e > 0 ? e : 0;
+                    }
+                    if (dt == 0) ex[TP] = 1;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tensor core reads it next
+                } else if (dt == 0) {
+                    ex[TP] = 0;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xchk0 + 8 * st);
+            }
+            if (gi >= kTcA)
+                ok = mbar_wait(aempty0 + 8 * ab, ((gi / kTcA) - 1) & 1, flags, a.dev_err, wait_ns) && ok;
+            if (ok) {
+                const uint8_t* sb = stage_mem + st * kStageBytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = 2 * q + h;
+                    const uint8_t* code = sb + m * BG * TB + gs * TB + lane * 16;
+                    const uint4 w = *reinterpret_cast<const uint4*>(code);
+                    const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
+                    const uint32_t base = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col0 + 32 * ab;
+                    uint32_t r[4];
+                    tc_decode<BITS, 0>(w, hb, r);
+                    tmem_st_frag(base + 0, r);
+                    tc_decode<BITS, 1>(w, hb, r);
+                    tmem_st_frag(base + 8, r);
+                    tc_decode<BITS, 2>(w, hb, r);
+                    tmem_st_frag(base + 16, r);
+                    tc_decode<BITS, 3>(w, hb, r);
+                    tmem_st_frag(base + 24, r);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(afull0 + 8 * ab);
+                if (gs == BG - 1 || gi == ngroups - 1) mbar_arrive(empty0 + 8 * st);
+            }
+        }
+    } else if (warp == kDecoders + 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            for (int gi = 0; gi < ngroups; ++gi) {
+                const int si = gi / BG, gs = gi % BG, st = si % nstages;
+                const int ab = gi % kTcA, pb = gi % kTcP;
+                bool ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+                ok = ok && mbar_wait(afull0 + 8 * ab, (gi / kTcA) & 1, flags, a.dev_err, wait_ns);
+                if (gi >= kTcP) ok = ok && mbar_wait(pempty0 + 8 * pb, ((gi / kTcP) - 1) & 1, flags, a.dev_err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t xbase = smem_u32(stage_mem + st * kStageBytes + kWBytes);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // K step j of group gs: core-matrix column (8 K) blocks 8 gs + 2 j, + 1
+                    const uint64_t bd = smem_desc(xbase + (uint32_t)(8 * gs + 2 * j) * (TP * 16), TP * 16, 128);
+                    tc_mma(tmem + p_col0 + TP * pb, tmem + a_col0 + 32 * ab + 8 * j, bd, kIdesc, j > 0 ? 1u : 0u);
+                }
+                tc_commit(aempty0 + 8 * ab);
+                tc_commit(pfull0 + 8 * pb);
+                if (gs == BG - 1 || gi == ngroups - 1) tc_commit(empty0 + 8 * st);
+            }
+            // every MMA this thread issued has completed before TMEM can be freed
+            tc_commit(done_bar);
+            mbar_wait_drain(done_bar, 0, kDrainNs);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = 32 * q + lane;                 // row of the block = TMEM lane
+        const int m = row >> 4, rr = row & 15;
+        const int sidx = 2 * (rr & 7) + (rr >> 3);     // the row's place in a packed scale tile
+        grid_dependency_wait();                        // Y, partials and tickets may be in use before
+        float acc[TP];
+#pragma unroll
+        for (int t = 0; t < TP; ++t) acc[t] = 0.f;
+        for (int gi = 0; gi < ngroups; ++gi) {
+            const int si = gi / BG, gs = gi % BG, st = si % nstages;
+            const int pb = gi % kTcP;
+            bool ok = true;
+            if (gs == 0) ok = mbar_wait(xchk0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+            ok = mbar_wait(pfull0 + 8 * pb, (gi / kTcP) & 1, flags, a.dev_err, wait_ns) && ok;
+            tc_fence_after();
+            if (ok) {
+                const uint8_t* sb = stage_mem + st * kStageBytes;
+                const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
+                    sb + kTcTiles * BG * TB + m * BG * kScaleTileBytes + gs * kScaleTileBytes + 2 * sidx)));
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + TP * pb;
+                const int* ex = xexp + st * (TP + 1);
+                const bool scaled = ex[TP] != 0;
+#pragma unroll
+                for (int c = 0; c < TP; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(base + c, v);
+                    tmem_wait_ld();
+                    if (!scaled) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[c + i] = fmaf(s * __int_as_float((127 + ex[c + i]) << 23), __uint_as_float(v[i]),
+                                              acc[c + i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(pempty0 + 8 * pb);
+                if (gs == BG - 1 || gi == ngroups - 1) mbar_arrive(empty0 + 8 * st);
+            }
+        }
+        // outputs: rows past N and tokens past T are not stored. The four epilogue warps agree on
+        // whether the block aborted before any of them enters the barriers below.
+        const int nrow = rb * kTcRows + row;
+        if (!named_bar_or(1, kEpilogue * 32, flags[0] != 0)) {
+            if (p.KS == 1) {
+                if (nrow < p.N) {
+#pragma unroll
+                    for (int t = 0; t < TP; ++t)
+                        if (t < p.T) a.Y[(size_t)t * p.N + nrow] = bf16_bits_rn_tc(acc[t]);
+                }
+            } else {
+                float* part = a.partials + ((size_t)rb * p.KS + kp) * (kTcRows * TP);
+#pragma unroll
+                for (int t = 0; t < TP; ++t) part[t * kTcRows + row] = acc[t];
+                named_bar_sync(1, kEpilogue * 32);     // the block's partial is complete
+                if (tid == (kDecoders + 2) * 32) {
+                    fence_acq_rel_gpu();
+                    flags[4] = ticket_add(a.tickets + rb) == p.KS - 1;
+                }
+                named_bar_sync(1, kEpilogue * 32);
+                if (flags[4]) {
+                    fence_acq_rel_gpu();
+                    float sum[TP];
+#pragma unroll
+                    for (int t = 0; t < TP; ++t) sum[t] = 0.f;
+                    for (int k2 = 0; k2 < p.KS; ++k2) {   // fixed order: deterministic
+                        const float* src = a.partials + ((size_t)rb * p.KS + k2) * (kTcRows * TP);
+#pragma unroll
+                        for (int t = 0; t < TP; ++t) sum[t] += __ldcg(src + t * kTcRows + row);
+                    }
+                    if (nrow < p.N) {
+#pragma unroll
+                        for (int t = 0; t < TP; ++t)
+                            if (t < p.T) a.Y[(size_t)t * p.N + nrow] = bf16_bits_rn_tc(sum[t]);
+                    }
+                    if (tid == (kDecoders + 2) * 32) a.tickets[rb] = 0;
+                }
+            }
+        }
+    }
+
+    if (flags[0] && tid == 0) {
+        // Aborted: wait (bounded) for the producer to stop, then for its last copy into each stage.
+        const uint64_t t0 = global_timer_ns();
+        while (!flags[2] && global_timer_ns() - t0 < 2 * kDrainNs) {
+        }
+        const int issued = flags[1];
+        for (int j = issued > nstages ? issued - nstages : 0; j < issued; ++j)
+            mbar_wait_drain(full0 + 8 * (j % nstages), (j / nstages) & 1, kDrainNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kCols);
+    }
+}
+
+}  // namespace nq

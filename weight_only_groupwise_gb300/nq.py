@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_info.argtypes = [I, I, I, I, I, I, P]
         L.nq_plan_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_segments.restype = ctypes.c_int64
+        L.nq_tensor_core_batches.argtypes = [I]
+        L.nq_tensor_core_batches.restype = I
+        L.nq_plan_tc_info.argtypes = [I, I, I, I, I, P]
+        L.nq_plan_tc_info.restype = I
         L.nq_slab_clusters.argtypes = [I]
         L.nq_slab_clusters.restype = I
         L.nq_plan_cluster_info.argtypes = [I, I, I, I, I, I, P]
@@ -331,6 +335,21 @@ def plan_segments(bits: int, mode: int, T: int, K: int, N: int, num_sms: int, ct
     buf = (ctypes.c_int64 * (4 * max(n, 1)))()
     lib().nq_plan_segments(bits, mode, T, K, N, num_sms, cta, ctypes.cast(buf, ctypes.c_void_p), n)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+
+def tensor_core_batches(enable: int = -1) -> int:
+    """Large batches (8 < T <= 64) on the tensor-core kernel (1) or in 8-token slices (0); -1
+    queries. Returns the previous setting."""
+    return int(lib().nq_tensor_core_batches(enable))
+
+
+TC_KEYS = ("ctas", "row_blocks", "k_pieces", "tokens_padded", "stages", "smem_bytes", "groups", "stage_groups")
+
+
+def plan_tc_info(bits: int, T: int, K: int, N: int, num_sms: int) -> dict:
+    out = (ctypes.c_int64 * 8)()
+    _check(lib().nq_plan_tc_info(bits, T, K, N, num_sms, ctypes.cast(out, ctypes.c_void_p)))
+    return dict(zip(TC_KEYS, list(out)))
 
 
 def slab_clusters(enable: int = -1) -> int:
