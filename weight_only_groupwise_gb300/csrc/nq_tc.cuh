@@ -4,26 +4,29 @@
 // "实测数据", C2/C4/C8), 4- or 5-bit codes with one fp16 scale per 64-wide K group, on the
 // fifth-generation tensor cores (tcgen05) so that the weights stream from HBM once whatever T.
 //
-// One block per (128-row block, K piece), 10 warps:
+// One block per (128-row block, K piece), 14 warps, in steps of two 64-wide groups:
 //   * warp 0, one lane -- producer: 1-D bulk copies of the eight 16-row tiles' codes and scales
 //     of each stage (kTcStageGroups groups) and one 3-D TMA copy of the stage's activation
 //     chunk, laid out as the tensor core's K-major core matrices (8 tokens x 16 bytes), tokens
 //     past T filled with zeros by the copy. A ring of shared-memory stages, mbarriers.
-//   * warps 1..4 -- decoders: warp w owns TMEM lanes 32 (w % 4) .. + 31, i.e. row tiles
-//     2 (w % 4) and + 1. A lane decodes its fragment words of a group into bf16 (q - z), exact,
-//     and stores them with tcgen05.st.16x128b.x2, which places the mma.sync A-fragment
-//     registers of lane t at TMEM lanes t/4, t/4 + 8 and columns t%4, 4 + t%4: K in natural
-//     order, one row per TMEM lane. Buffers of 32 columns (64 K) per group, kTcA of them.
-//   * warp 5, one lane -- MMA issuer: per group, four tcgen05.mma.kind::f16 (M = 128, N = TP,
+//   * warps 1..8 -- decoders: warp w owns one 16-row tile, TMEM lanes 32 (w % 4) + 16 h .. + 15
+//     (h = 0 for warps 1..4, 1 for 5..8). A lane decodes its fragment words of a group into
+//     bf16 (q - z), exact, and stores all four K steps with one tcgen05.st.16x128b.x8, which
+//     places the mma.sync A-fragment registers of lane t at TMEM lanes t/4, t/4 + 8 and columns
+//     8 j + t%4, 8 j + 4 + t%4: K in natural order, one row per TMEM lane. A buffer holds a
+//     step (2 groups, 64 columns); one wait for the stores and one hand-off per step.
+//   * warp 9, one lane -- MMA issuer: per group, four tcgen05.mma.kind::f16 (M = 128, N = TP,
 //     K = 16; A from TMEM, B = the activation chunk through a shared-memory descriptor; D in
 //     TMEM, fp32, a fresh accumulator per group: P = sum over the group of (q - z) x, exact
-//     products), then tcgen05.commit to the barriers that free the A buffer and publish P.
-//   * warps 6..9 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
+//     products), then per step one tcgen05.commit to the barriers that free the A buffer and
+//     publish the step's two P.
+//   * warps 10..13 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
 //     adds s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y, or,
 //     when K is split across blocks, an fp32 partial; the last block of a row block (ticket)
 //     adds the partials in fixed order and stores Y.
 // Every wait is bounded (the abort protocol of the small-batch kernel); TMEM is allocated and
-// freed by warp 0, after the issuer has waited for its last MMAs.
+// freed by warp 0, after the issuer has waited for its last MMAs. With one block per SM the
+// kernel takes all 512 TMEM columns.
 #pragma once
 
 #include <cuda.h>
@@ -38,9 +41,12 @@ constexpr int kTcRows = 128;                      // rows per block = MMA M
 constexpr int kTcTiles = kTcRows / kTileRows;     // 16-row tiles per block
 constexpr int kTcStageGroups = 4;                 // 64-wide K groups per pipeline stage
 constexpr int kTcMaxStages = 8;
-constexpr int kTcA = 4;                           // A buffers in TMEM (32 columns each)
-constexpr int kTcP = 2;                           // P buffers in TMEM (TP columns each)
-constexpr int kTcWarps = 10;
+constexpr int kTcPair = 2;                        // groups per pipeline step (one hand-off)
+constexpr int kTcA = 4;                           // A buffers in TMEM (a step: 64 columns each)
+constexpr int kTcP = 2;                           // P buffers in TMEM (a step: 2 TP columns each)
+constexpr int kTcDecoders = 8;                    // decoder warps: one 16-row tile each
+constexpr int kTcEpilogue = 4;                    // epilogue warps: one TMEM lane quarter each
+constexpr int kTcWarps = 2 + kTcDecoders + kTcEpilogue;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcMinT = 9, kTcMaxT = 64;
 
@@ -107,12 +113,17 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// The four A-fragment registers of a lane (rows r, r+8; K pairs c, c+4 of a 16-wide K step)
-// into TMEM: lanes taddr.lane + r, + r + 8; columns taddr.col + c, + 4 + c.
-__device__ __forceinline__ void tmem_st_frag(uint32_t taddr, const uint32_t a[4]) {
-    asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a[0]),
-                 "r"(a[1]), "r"(a[2]), "r"(a[3])
-                 : "memory");
+// The A-fragment registers of a lane for the four K steps of a group (rows r, r+8; K pairs
+// c, c+4 of each 16-wide step; 16 registers) into TMEM: step j's registers land at lanes
+// taddr.lane + r, + r + 8 and columns taddr.col + 8 j + c, + 8 j + 4 + c, i.e. 64 K in natural
+// order across 32 columns of 16 lanes (the 16x128b pattern repeated 8 times along columns).
+__device__ __forceinline__ void tmem_st_group(uint32_t taddr, const uint32_t (&a)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]),
+        "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15])
+        : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -194,12 +205,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
     constexpr int BG = kTcStageGroups;
+    static_assert(BG % kTcPair == 0, "steps do not straddle stages");
     constexpr int kWBytes = kTcTiles * BG * (TB + kScaleTileBytes);
     constexpr int kXBytes = TP * BG * kGroup * 2;
     constexpr int kStageBytes = kWBytes + kXBytes;
-    constexpr uint32_t kCols = 256;                   // TMEM columns: A buffers, then P buffers
-    static_assert(kTcA * 32 + kTcP * TP <= (int)kCols, "TMEM budget");
+    constexpr uint32_t kCols = 512;                   // TMEM columns: A buffers, then P buffers
+    constexpr int kACols = kTcPair * 32, kPCols = kTcPair * TP;
+    static_assert(kTcA * kACols + kTcP * kPCols <= (int)kCols, "TMEM budget");
     constexpr uint32_t kIdesc = tc_idesc_bf16(TP);
+    constexpr int kDec = kTcDecoders, kEpi = kTcEpilogue;
+    constexpr int kMmaWarp = 1 + kDec;
 
     const TcPlan& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -208,6 +223,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     const int g0 = (int)((long long)kp * p.G / p.KS), g1 = (int)((long long)(kp + 1) * p.G / p.KS);
     const int ngroups = g1 - g0;
     const int nst = (ngroups + BG - 1) / BG;          // stages this block streams
+    const int nsteps = (ngroups + kTcPair - 1) / kTcPair;
     const uint64_t wait_ns = a.wait_ns;
 
     uint8_t* stage_mem = smem;
@@ -221,21 +237,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     // flags: [0] abort, [1] stages issued, [2] producer done, [3] TMEM base, [4] last ticket
     // xexp: per stage, TP token exponents e (the chunk holds x * 2^-e) and [TP] = any e > 0
     int* xexp = const_cast<int*>(flags) + 16;
-    const int kDecoders = 4, kEpilogue = 4;
 
     if (tid == 0) {
         for (int i = 0; i < nstages; ++i) {
             mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, kDecoders + 1 + kEpilogue);
-            mbar_init(xchk0 + 8 * i, kDecoders);
+            mbar_init(empty0 + 8 * i, kDec + 1 + kEpi);
+            mbar_init(xchk0 + 8 * i, kDec);
         }
         for (int i = 0; i < kTcA; ++i) {
-            mbar_init(afull0 + 8 * i, kDecoders);
+            mbar_init(afull0 + 8 * i, kDec);
             mbar_init(aempty0 + 8 * i, 1);
         }
         for (int i = 0; i < kTcP; ++i) {
             mbar_init(pfull0 + 8 * i, 1);
-            mbar_init(pempty0 + 8 * i, kEpilogue);
+            mbar_init(pempty0 + 8 * i, kEpi);
         }
         mbar_init(done_bar, 1);
         flags[0] = 0;
@@ -249,8 +264,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = (uint32_t)flags[3];
-    const uint32_t a_col0 = 0, p_col0 = kTcA * 32;
+    const uint32_t a_col0 = 0, p_col0 = kTcA * kACols;
 
+    // Step k covers groups 2k, 2k+1 of the block (the second may be past its end), both in
+    // stage k / 2 at positions gs0 = 2 (k % 2), gs0 + 1.
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -292,15 +309,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
             __threadfence_block();
             flags[2] = 1;
         }
-    } else if (warp <= kDecoders) {
+    } else if (warp <= kDec) {
         // ------------------------------------------------------------ decoders
-        const int q = warp & 3;                        // TMEM lane quarter: rows 32q .. 32q+31
-        const int dt = tid - 32;                       // decoder thread 0..127
-        for (int gi = 0; gi < ngroups; ++gi) {
-            const int si = gi / BG, gs = gi % BG, st = si % nstages;
-            const int ab = gi % kTcA;
-            bool ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
-            if (gs == 0) {
+        const int q = warp & 3, h = (warp - 1) >> 2;  // TMEM lane quarter, and which half of it
+        const int m = 2 * q + h;                       // the warp's 16-row tile of the block
+        const int dt = tid - 32;                       // decoder thread 0 .. 32 kDec - 1
+        for (int k = 0; k < nsteps; ++k) {
+            const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
+            const int ab = k % kTcA;
+            const bool first = k % 2 == 0, last = k % 2 == 1 || k == nsteps - 1;
+            bool ok = true;
+            if (first) {
+                ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
                 // Range check of the stage's activation chunk (every decoder thread, every stage,
                 // so the named barriers below always match): the group partials sum (q - z) x
                 // in fp32, so a token with some |x| >= 2^100 (bits 0x7180) is scaled by 2^-e,
@@ -310,22 +330,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 int* ex = xexp + st * (TP + 1);
                 constexpr int kChunks = kXBytes / 16;
                 uint32_t big = 0;
-                for (int c = dt; c < kChunks; c += kDecoders * 32) {
+                for (int c = dt; c < kChunks; c += kDec * 32) {
                     const uint4 v = xc[c];
                     big |= ((v.x & 0x7FFF7FFFu) + 0x0E800E80u) | ((v.y & 0x7FFF7FFFu) + 0x0E800E80u) |
                            ((v.z & 0x7FFF7FFFu) + 0x0E800E80u) | ((v.w & 0x7FFF7FFFu) + 0x0E800E80u);
                 }
-                if (named_bar_or(2, kDecoders * 32, (big & 0x80008000u) != 0)) {
-                    for (int t = dt; t < TP; t += kDecoders * 32) ex[t] = 0;
-                    named_bar_sync(2, kDecoders * 32);
-                    for (int c = dt; c < kChunks; c += kDecoders * 32) {
+                if (named_bar_or(2, kDec * 32, (big & 0x80008000u) != 0)) {
+                    for (int t = dt; t < TP; t += kDec * 32) ex[t] = 0;
+                    named_bar_sync(2, kDec * 32);
+                    for (int c = dt; c < kChunks; c += kDec * 32) {
                         const uint4 v = xc[c];
-                        const uint32_t m = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                               max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-                        atomicMax(ex + c % TP, (int)max(m & 0xFFFFu, m >> 16));
+                        const uint32_t mx = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                                max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+                        atomicMax(ex + c % TP, (int)max(mx & 0xFFFFu, mx >> 16));
                     }
-                    named_bar_sync(2, kDecoders * 32);
-                    for (int c = dt; c < kChunks; c += kDecoders * 32) {
+                    named_bar_sync(2, kDec * 32);
+                    for (int c = dt; c < kChunks; c += kDec * 32) {
                         const int e = ((ex[c % TP] >> 7) & 0xFF) - 127 - 99;
                         if (e <= 0) continue;
                         const float sc = __int_as_float((127 - e) << 23);
@@ -339,8 +359,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                         }
                         xc[c] = v;
                     }
-                    named_bar_sync(2, kDecoders * 32);
-                    for (int t = dt; t < TP; t += kDecoders * 32) {
+                    named_bar_sync(2, kDec * 32);
+                    for (int t = dt; t < TP; t += kDec * 32) {
                         const int e = ((ex[t] >> 7) & 0xFF) - 127 - 99;
                         ex[t] = e > 0 ? e : 0;
                     }
@@ -352,26 +372,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xchk0 + 8 * st);
             }
-            if (gi >= kTcA)
-                ok = mbar_wait(aempty0 + 8 * ab, ((gi / kTcA) - 1) & 1, flags, a.dev_err, wait_ns) && ok;
+            if (k >= kTcA) ok = mbar_wait(aempty0 + 8 * ab, ((k / kTcA) - 1) & 1, flags, a.dev_err, wait_ns) && ok;
             if (ok) {
                 const uint8_t* sb = stage_mem + st * kStageBytes;
+                const uint32_t base = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col0 + kACols * ab;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int m = 2 * q + h;
-                    const uint8_t* code = sb + m * BG * TB + gs * TB + lane * 16;
+                for (int gp = 0; gp < kTcPair; ++gp) {
+                    if (2 * k + gp >= ngroups) break;
+                    const uint8_t* code = sb + m * BG * TB + (gs0 + gp) * TB + lane * 16;
                     const uint4 w = *reinterpret_cast<const uint4*>(code);
                     const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
-                    const uint32_t base = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col0 + 32 * ab;
-                    uint32_t r[4];
-                    tc_decode<BITS, 0>(w, hb, r);
-                    tmem_st_frag(base + 0, r);
-                    tc_decode<BITS, 1>(w, hb, r);
-                    tmem_st_frag(base + 8, r);
-                    tc_decode<BITS, 2>(w, hb, r);
-                    tmem_st_frag(base + 16, r);
-                    tc_decode<BITS, 3>(w, hb, r);
-                    tmem_st_frag(base + 24, r);
+                    uint32_t r[16];
+                    tc_decode<BITS, 0>(w, hb, r + 0);
+                    tc_decode<BITS, 1>(w, hb, r + 4);
+                    tc_decode<BITS, 2>(w, hb, r + 8);
+                    tc_decode<BITS, 3>(w, hb, r + 12);
+                    tmem_st_group(base + 32 * gp, r);
                 }
                 tmem_wait_st();
             }
@@ -379,30 +395,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(afull0 + 8 * ab);
-                if (gs == BG - 1 || gi == ngroups - 1) mbar_arrive(empty0 + 8 * st);
+                if (last) mbar_arrive(empty0 + 8 * st);
             }
         }
-    } else if (warp == kDecoders + 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            for (int gi = 0; gi < ngroups; ++gi) {
-                const int si = gi / BG, gs = gi % BG, st = si % nstages;
-                const int ab = gi % kTcA, pb = gi % kTcP;
+            for (int k = 0; k < nsteps; ++k) {
+                const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
+                const int ab = k % kTcA, pb = k % kTcP;
+                const bool last = k % 2 == 1 || k == nsteps - 1;
                 bool ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
-                ok = ok && mbar_wait(afull0 + 8 * ab, (gi / kTcA) & 1, flags, a.dev_err, wait_ns);
-                if (gi >= kTcP) ok = ok && mbar_wait(pempty0 + 8 * pb, ((gi / kTcP) - 1) & 1, flags, a.dev_err, wait_ns);
+                ok = ok && mbar_wait(afull0 + 8 * ab, (k / kTcA) & 1, flags, a.dev_err, wait_ns);
+                if (k >= kTcP) ok = ok && mbar_wait(pempty0 + 8 * pb, ((k / kTcP) - 1) & 1, flags, a.dev_err, wait_ns);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t xbase = smem_u32(stage_mem + st * kStageBytes + kWBytes);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // K step j of group gs: core-matrix column (8 K) blocks 8 gs + 2 j, + 1
-                    const uint64_t bd = smem_desc(xbase + (uint32_t)(8 * gs + 2 * j) * (TP * 16), TP * 16, 128);
-                    tc_mma(tmem + p_col0 + TP * pb, tmem + a_col0 + 32 * ab + 8 * j, bd, kIdesc, j > 0 ? 1u : 0u);
+                for (int gp = 0; gp < kTcPair; ++gp) {
+                    if (2 * k + gp >= ngroups) break;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        // K step j of group gs0 + gp: core-matrix (8 K) columns 8 (gs0 + gp) + 2 j, + 1
+                        const uint64_t bd =
+                            smem_desc(xbase + (uint32_t)(8 * (gs0 + gp) + 2 * j) * (TP * 16), TP * 16, 128);
+                        tc_mma(tmem + p_col0 + kPCols * pb + TP * gp, tmem + a_col0 + kACols * ab + 32 * gp + 8 * j,
+                               bd, kIdesc, j > 0 ? 1u : 0u);
+                    }
                 }
                 tc_commit(aempty0 + 8 * ab);
                 tc_commit(pfull0 + 8 * pb);
-                if (gs == BG - 1 || gi == ngroups - 1) tc_commit(empty0 + 8 * st);
+                if (last) tc_commit(empty0 + 8 * st);
             }
             // every MMA this thread issued has completed before TMEM can be freed
             tc_commit(done_bar);
@@ -418,33 +441,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         float acc[TP];
 #pragma unroll
         for (int t = 0; t < TP; ++t) acc[t] = 0.f;
-        for (int gi = 0; gi < ngroups; ++gi) {
-            const int si = gi / BG, gs = gi % BG, st = si % nstages;
-            const int pb = gi % kTcP;
+        for (int k = 0; k < nsteps; ++k) {
+            const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
+            const int pb = k % kTcP;
+            const bool first = k % 2 == 0, last = k % 2 == 1 || k == nsteps - 1;
             bool ok = true;
-            if (gs == 0) ok = mbar_wait(xchk0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
-            ok = mbar_wait(pfull0 + 8 * pb, (gi / kTcP) & 1, flags, a.dev_err, wait_ns) && ok;
+            if (first) ok = mbar_wait(xchk0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+            ok = mbar_wait(pfull0 + 8 * pb, (k / kTcP) & 1, flags, a.dev_err, wait_ns) && ok;
             tc_fence_after();
             if (ok) {
                 const uint8_t* sb = stage_mem + st * kStageBytes;
-                const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
-                    sb + kTcTiles * BG * TB + m * BG * kScaleTileBytes + gs * kScaleTileBytes + 2 * sidx)));
-                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + TP * pb;
                 const int* ex = xexp + st * (TP + 1);
                 const bool scaled = ex[TP] != 0;
 #pragma unroll
-                for (int c = 0; c < TP; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(base + c, v);
-                    tmem_wait_ld();
-                    if (!scaled) {
+                for (int gp = 0; gp < kTcPair; ++gp) {
+                    if (2 * k + gp >= ngroups) break;
+                    const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
+                        sb + kTcTiles * BG * TB + m * BG * kScaleTileBytes + (gs0 + gp) * kScaleTileBytes + 2 * sidx)));
+                    const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb + TP * gp;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
-                    } else {
+                    for (int c = 0; c < TP; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(base + c, v);
+                        tmem_wait_ld();
+                        if (!scaled) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[c + i] = fmaf(s * __int_as_float((127 + ex[c + i]) << 23), __uint_as_float(v[i]),
-                                              acc[c + i]);
+                            for (int i = 0; i < 16; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                acc[c + i] = fmaf(s * __int_as_float((127 + ex[c + i]) << 23), __uint_as_float(v[i]),
+                                                  acc[c + i]);
+                        }
                     }
                 }
             }
@@ -452,13 +480,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(pempty0 + 8 * pb);
-                if (gs == BG - 1 || gi == ngroups - 1) mbar_arrive(empty0 + 8 * st);
+                if (last) mbar_arrive(empty0 + 8 * st);
             }
         }
         // outputs: rows past N and tokens past T are not stored. The four epilogue warps agree on
         // whether the block aborted before any of them enters the barriers below.
         const int nrow = rb * kTcRows + row;
-        if (!named_bar_or(1, kEpilogue * 32, flags[0] != 0)) {
+        if (!named_bar_or(1, kEpi * 32, flags[0] != 0)) {
             if (p.KS == 1) {
                 if (nrow < p.N) {
 #pragma unroll
@@ -469,12 +497,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 float* part = a.partials + ((size_t)rb * p.KS + kp) * (kTcRows * TP);
 #pragma unroll
                 for (int t = 0; t < TP; ++t) part[t * kTcRows + row] = acc[t];
-                named_bar_sync(1, kEpilogue * 32);     // the block's partial is complete
-                if (tid == (kDecoders + 2) * 32) {
+                named_bar_sync(1, kEpi * 32);          // the block's partial is complete
+                const int leader = (kMmaWarp + 1) * 32;
+                if (tid == leader) {
                     fence_acq_rel_gpu();
                     flags[4] = ticket_add(a.tickets + rb) == p.KS - 1;
                 }
-                named_bar_sync(1, kEpilogue * 32);
+                named_bar_sync(1, kEpi * 32);
                 if (flags[4]) {
                     fence_acq_rel_gpu();
                     float sum[TP];
@@ -490,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                         for (int t = 0; t < TP; ++t)
                             if (t < p.T) a.Y[(size_t)t * p.N + nrow] = bf16_bits_rn_tc(sum[t]);
                     }
-                    if (tid == (kDecoders + 2) * 32) a.tickets[rb] = 0;
+                    if (tid == leader) a.tickets[rb] = 0;
                 }
             }
         }
