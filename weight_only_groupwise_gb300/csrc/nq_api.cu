@@ -446,7 +446,8 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     // Larger batches of a plain projection: the tensor-core kernel, one weight pass.
     if (g_tc && !swiglu && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
         alignas(64) TcArgs ta;
-        if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP)) {
+        if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP) &&
+            encode_weight_maps(&ta.wmap, &ta.smap, W0, S0, bits, K, N)) {
             st = ensure_workspace(*d, 1, 1);
             if (st != NQ_OK) return st;
             st = ensure_tc_workspace(*d, ta.p.RB, ta.p.KS > 1 ? (long long)ta.p.P * kTcRows * ta.p.TP : 1);

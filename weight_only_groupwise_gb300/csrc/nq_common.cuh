@@ -81,8 +81,8 @@ NQ_HD int tpad(int T) { return T <= 1 ? 1 : (T <= 2 ? 2 : (T <= 4 ? 4 : 8)); }
 
 // Byte offsets inside a packed weight (TB = code bytes per tile, 512 or 640).
 NQ_HD long long packed_code_off(int rt, int g, int G, int TB) { return ((long long)rt * G + g) * TB; }
-NQ_HD int code_tile_bytes(int bits) { return bits == 5 ? kQ5TileBytes : kQ4TileBytes; }
-NQ_HD int scale_tile_bytes(int bits) { return bits == kFp4 ? kFp4ScaleTileBytes : kScaleTileBytes; }
+NQ_HD constexpr int code_tile_bytes(int bits) { return bits == 5 ? kQ5TileBytes : kQ4TileBytes; }
+NQ_HD constexpr int scale_tile_bytes(int bits) { return bits == kFp4 ? kFp4ScaleTileBytes : kScaleTileBytes; }
 NQ_HD long long packed_scale_off(int rt, int g, int G, int STB) { return ((long long)rt * G + g) * STB; }
 
 // The work split of one projection call. One "unit" is one 64-wide K group of one row pair
@@ -388,6 +388,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One arrive by the lanes whose pred is true, issued by the whole warp with the predicate inside
+// the instruction: no branch, so the warp does not reconverge behind the arrive (a branch around
+// an arrive costs ~160 cycles per hand-off on sm_103 when the warp reconverges after it).
+__device__ __forceinline__ void mbar_arrive_if(uint32_t bar, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+        "r"((uint32_t)pred)
+        : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

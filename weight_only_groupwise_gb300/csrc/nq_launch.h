@@ -11,6 +11,7 @@ namespace nq {
 // Large-batch tensor-core kernel (nq_tc.cuh): the activation tensor map (false if the driver
 // entry point is missing or rejects the view) and the launch.
 bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP);
+bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N);
 cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl);
 
 // Bound of every device-side wait for later launches (nq_wait_limit; NQ_WAIT_NS).

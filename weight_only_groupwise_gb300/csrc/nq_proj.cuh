@@ -856,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            mbar_arrive_if(empty0 + 8 * st, lane == 0);
             if (++st == nstages) { st = 0; phase ^= 1; }
         }
 

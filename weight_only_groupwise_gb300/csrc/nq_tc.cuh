@@ -5,25 +5,31 @@
 // fifth-generation tensor cores (tcgen05) so that the weights stream from HBM once whatever T.
 //
 // One block per (128-row block, K piece), 14 warps, in steps of two 64-wide groups:
-//   * warp 0, one lane -- producer: 1-D bulk copies of the eight 16-row tiles' codes and scales
-//     of each stage (kTcStageGroups groups) and one 3-D TMA copy of the stage's activation
-//     chunk, laid out as the tensor core's K-major core matrices (8 tokens x 16 bytes), tokens
-//     past T filled with zeros by the copy. A ring of shared-memory stages, mbarriers.
+//   * warp 0, one lane -- producer: per stage (kTcStageGroups groups) three 3-D TMA copies:
+//     the codes and the scales of the eight 16-row tiles (tiles and groups past the matrix
+//     read as zeros), and the stage's activation chunk, one [TP][64] block per group in the tensor core's K-major 128-byte-swizzled
+//     layout, tokens past T filled with zeros by the copy. A ring of shared-memory stages
+//     (1024-byte aligned), mbarriers.
 //   * warps 1..8 -- decoders: warp w owns one 16-row tile, TMEM lanes 32 (w % 4) + 16 h .. + 15
 //     (h = 0 for warps 1..4, 1 for 5..8). A lane decodes its fragment words of a group into
-//     bf16 (q - z), exact, and stores all four K steps with one tcgen05.st.16x128b.x8, which
-//     places the mma.sync A-fragment registers of lane t at TMEM lanes t/4, t/4 + 8 and columns
-//     8 j + t%4, 8 j + 4 + t%4: K in natural order, one row per TMEM lane. A buffer holds a
-//     step (2 groups, 64 columns); one wait for the stores and one hand-off per step.
-//   * warp 9, one lane -- MMA issuer: per group, four tcgen05.mma.kind::f16 (M = 128, N = TP,
-//     K = 16; A from TMEM, B = the activation chunk through a shared-memory descriptor; D in
-//     TMEM, fp32, a fresh accumulator per group: P = sum over the group of (q - z) x, exact
-//     products), then per step one tcgen05.commit to the barriers that free the A buffer and
-//     publish the step's two P.
+//     bf16 (q - z) 2^-12, exact, and stores all four K steps with one tcgen05.st.16x128b.x8,
+//     which places the mma.sync A-fragment registers of lane t at TMEM lanes t/4, t/4 + 8 and
+//     columns 8 j + t%4, 8 j + 4 + t%4: K in natural order, one row per TMEM lane. A buffer
+//     holds a step (2 groups, 64 columns). Software-pipelined: the next step is loaded and
+//     decoded while the current step's stores complete.
+//   * warp 9 -- MMA issuer (the whole warp runs the loop, one elected lane issues): per group,
+//     four tcgen05.mma.kind::f16 (M = 128, N = TP, K = 16; A from TMEM, B = the activation
+//     chunk through a shared-memory descriptor; D in TMEM, fp32, a fresh accumulator per group:
+//     P = 2^-12 sum over the group of (q - z) x), then per step tcgen05.commit to the barriers
+//     that free the A buffer and publish the step's two P.
 //   * warps 10..13 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
-//     adds s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y, or,
-//     when K is split across blocks, an fp32 partial; the last block of a row block (ticket)
-//     adds the partials in fixed order and stores Y.
+//     adds 2^12 s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y,
+//     or, when K is split across blocks, an fp32 partial; the last block of a row block
+//     (ticket) adds the partials in fixed order and stores Y.
+// The 2^-12 in the decoded weights keeps every group partial finite for any finite bf16
+// activation: |q - z| 2^-12 <= 2^-8 and |x| < 2^128, so 64 products stay below 2^126 (fp32
+// overflows at 2^128); 2^12 s is exact in fp32, so the result is the unscaled one. No range
+// pass over the activations is needed.
 // Every wait is bounded (the abort protocol of the small-batch kernel); TMEM is allocated and
 // freed by warp 0, after the issuer has waited for its last MMAs. With one block per SM the
 // kernel takes all 512 TMEM columns.
@@ -41,9 +47,11 @@ constexpr int kTcRows = 128;                      // rows per block = MMA M
 constexpr int kTcTiles = kTcRows / kTileRows;     // 16-row tiles per block
 constexpr int kTcStageGroups = 4;                 // 64-wide K groups per pipeline stage
 constexpr int kTcMaxStages = 8;
-constexpr int kTcPair = 2;                        // groups per pipeline step (one hand-off)
-constexpr int kTcA = 4;                           // A buffers in TMEM (a step: 64 columns each)
-constexpr int kTcP = 2;                           // P buffers in TMEM (a step: 2 TP columns each)
+constexpr int kTcPair = 2;                        // groups per P buffer (one MMA-to-epilogue hand-off)
+constexpr int kTcA = 2;                           // A buffers in TMEM (a stage: 128 columns each)
+constexpr int kTcPCols = 256;                     // TMEM columns of the P buffers (2 TP each)
+constexpr int kTcMaxP = kTcPCols / (kTcPair * 16);
+constexpr int kTcScaleExp = 12;                   // decoded weights carry 2^-12
 constexpr int kTcDecoders = 8;                    // decoder warps: one 16-row tile each
 constexpr int kTcEpilogue = 4;                    // epilogue warps: one TMEM lane quarter each
 constexpr int kTcWarps = 2 + kTcDecoders + kTcEpilogue;
@@ -52,16 +60,16 @@ constexpr int kTcMinT = 9, kTcMaxT = 64;
 
 // Shared-memory bytes of one stage: codes and scales of kTcTiles tiles x kTcStageGroups groups,
 // then the activation chunk (kTcStageGroups * 64 K x TP tokens, bf16).
-NQ_HD int tc_weight_bytes(int bits) { return kTcTiles * kTcStageGroups * (code_tile_bytes(bits) + kScaleTileBytes); }
-NQ_HD int tc_x_bytes(int TP) { return TP * kTcStageGroups * kGroup * 2; }
-NQ_HD int tc_stage_bytes(int bits, int TP) { return tc_weight_bytes(bits) + tc_x_bytes(TP); }
-// Per stage: TP token exponents and a flag (the activation range check), after the barriers.
-NQ_HD int tc_extra_bytes(int TP) { return 1024 + kTcMaxStages * (TP + 1) * 4; }
-NQ_HD int tc_stages(int bits, int TP) {
+NQ_HD constexpr int tc_weight_bytes(int bits) { return kTcTiles * kTcStageGroups * (code_tile_bytes(bits) + kScaleTileBytes); }
+NQ_HD constexpr int tc_x_bytes(int TP) { return TP * kTcStageGroups * kGroup * 2; }
+NQ_HD constexpr int tc_stage_bytes(int bits, int TP) { return tc_weight_bytes(bits) + tc_x_bytes(TP); }
+// Alignment of the stages to 1024 bytes (the swizzle atom), then barriers and flags after them.
+NQ_HD constexpr int tc_extra_bytes(int) { return 2048; }
+NQ_HD constexpr int tc_stages(int bits, int TP) {
     int s = (kSmemLimit - tc_extra_bytes(TP)) / tc_stage_bytes(bits, TP);
     return s > kTcMaxStages ? kTcMaxStages : s;
 }
-NQ_HD int tc_tpad(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
+NQ_HD constexpr int tc_tpad(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 
 // Work split of a large-batch call: RB row blocks of 128 rows, each K cut into KS pieces so
 // that RB * KS blocks about fill the SMs.
@@ -89,7 +97,9 @@ NQ_HD bool make_tc_plan(int bits, int T, int K, int N, int num_sms, TcPlan& p) {
 }
 
 struct alignas(64) TcArgs {
-    CUtensorMap xmap;        // X viewed as [K/8][T][8] bf16 (tokens past T read as zeros)
+    CUtensorMap xmap;        // X viewed as [K/64][T][64] bf16 (tokens past T read as zeros)
+    CUtensorMap wmap;        // packed codes viewed as [RT][G][tile bytes / 8] (8-byte elements)
+    CUtensorMap smap;        // packed scales viewed as [RT][G][4] (8-byte elements)
     const uint8_t* W;        // packed codes
     const uint8_t* S;        // packed scales
     uint16_t* Y;             // bf16 [T][N]
@@ -139,26 +149,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // D (+)= A * B: M = 128, N from idesc, K = 16; A in TMEM, B through a shared-memory descriptor.
+// Issued by the lanes whose `issue` is true (one lane), with the whole warp executing the
+// instruction so that no branch surrounds it.
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+                                       uint32_t accumulate, bool issue) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"((uint32_t)issue)
         : "memory");
 }
 
-// Arrive once on an mbarrier when all tcgen05 operations this thread issued so far are done.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+// Arrive once on an mbarrier when all tcgen05 operations the issuing lane issued so far are done
+// (predicated like tc_mma).
+__device__ __forceinline__ void tc_commit(uint32_t bar, bool issue) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"((uint32_t)issue)
+        : "memory");
 }
 
-// Shared-memory descriptor of a K-major operand without swizzle: core matrices of 8 rows x 16
-// bytes, lbo = bytes between K-adjacent cores, sbo = bytes between 8-row groups.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
-           (1ull << 46);
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzled layout: rows of 128
+// bytes (64 bf16 of K), 8-row atoms of 1024 bytes (the stride between 8-row groups), atoms
+// 1024-byte aligned. A K step of 16 starts 32 bytes further into the row.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = n.
@@ -175,6 +191,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint16_t bf16_bits_rn_tc(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
@@ -183,12 +208,15 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     return d;
 }
 
-// K step J of a lane's code word as four bf16x2 registers holding q - z exactly.
+// K step J of a lane's code word as four bf16x2 registers holding (q - z) 2^-12 exactly: the
+// offset code is placed under the bf16 exponent of 2^-5 (fraction unit 2^-12), so a register
+// holds 2^-5 + q 2^-12, and subtracting 2^-5 + z 2^-12 leaves (q - z) 2^-12, representable.
 template <int BITS, int J>
 __device__ __forceinline__ void tc_decode(const uint4& w, uint32_t hb, uint32_t a[4]) {
-    constexpr uint32_t kOff = BITS == 4 ? 0x43084308u : 0x43104310u;  // 128 + z in both halves
+    constexpr uint32_t kMagic = 0x3D003D00u;                          // 2^-5 in both halves
+    constexpr uint32_t kOff = BITS == 4 ? 0x3D083D08u : 0x3D103D10u;  // 2^-5 + z 2^-12
     uint32_t magic;
-    asm("mov.b32 %0, %1;" : "=r"(magic) : "n"(kBf16Magic));
+    asm("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
     const uint32_t word = J == 0 ? w.x : (J == 1 ? w.y : (J == 2 ? w.z : w.w));
     if constexpr (BITS == 4)
         decode_q4_bf16(word, a, magic);
@@ -198,6 +226,15 @@ __device__ __forceinline__ void tc_decode(const uint4& w, uint32_t hb, uint32_t 
     for (int i = 0; i < 4; ++i) a[i] = bf16x2_sub(a[i], kOff);
 }
 
+// One lane of a full warp returns true (the same lane every time the whole warp calls it).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\telect.sync rx|px, %1;\n\tselp.b32 %0, 1, 0, px;\n\t}"
+                 : "=r"(pred)
+                 : "r"(0xFFFFFFFFu));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <int BITS, int TP>
@@ -205,20 +242,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
     constexpr int BG = kTcStageGroups;
-    static_assert(BG % kTcPair == 0, "steps do not straddle stages");
+    static_assert(BG % kTcPair == 0 && BG / kTcPair == 2, "two P steps per stage");
+    static_assert((TB * kTcTiles * BG + kScaleTileBytes * kTcTiles * BG) % 1024 == 0 && (TP * 128) % 1024 == 0,
+                  "activation blocks on 1024-byte boundaries");
     constexpr int kWBytes = kTcTiles * BG * (TB + kScaleTileBytes);
     constexpr int kXBytes = TP * BG * kGroup * 2;
     constexpr int kStageBytes = kWBytes + kXBytes;
     constexpr uint32_t kCols = 512;                   // TMEM columns: A buffers, then P buffers
-    constexpr int kACols = kTcPair * 32, kPCols = kTcPair * TP;
-    static_assert(kTcA * kACols + kTcP * kPCols <= (int)kCols, "TMEM budget");
+    constexpr int kAStage = BG * 32, kPCols = kTcPair * TP;  // TMEM columns of an A buffer, a P buffer
+    constexpr int kP = kTcPCols / kPCols;             // P buffers: 8, 4, 2 for TP = 16, 32, 64
+    static_assert(kTcA * kAStage + kTcPCols <= (int)kCols && kP >= 2 && kP <= kTcMaxP, "TMEM budget");
     constexpr uint32_t kIdesc = tc_idesc_bf16(TP);
     constexpr int kDec = kTcDecoders, kEpi = kTcEpilogue;
     constexpr int kMmaWarp = 1 + kDec;
 
     const TcPlan& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nstages = p.stages;
+    constexpr int nstages = tc_stages(BITS, TP);      // compile time: no division in the loops
     const int rb = (int)blockIdx.x / p.KS, kp = (int)blockIdx.x % p.KS;
     const int g0 = (int)((long long)kp * p.G / p.KS), g1 = (int)((long long)(kp + 1) * p.G / p.KS);
     const int ngroups = g1 - g0;
@@ -226,29 +266,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     const int nsteps = (ngroups + kTcPair - 1) / kTcPair;
     const uint64_t wait_ns = a.wait_ns;
 
-    uint8_t* stage_mem = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + nstages * kStageBytes);
-    // bars: full[S], empty[S], xchk[S], a_full[A], a_empty[A], p_full[P], p_empty[P], done;
-    // then flags, then per stage the token exponents of the range check
-    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kTcMaxStages, xchk0 = empty0 + 8 * kTcMaxStages;
-    const uint32_t afull0 = xchk0 + 8 * kTcMaxStages, aempty0 = afull0 + 8 * kTcA;
-    const uint32_t pfull0 = aempty0 + 8 * kTcA, pempty0 = pfull0 + 8 * kTcP, done_bar = pempty0 + 8 * kTcP;
-    volatile int* flags = reinterpret_cast<volatile int*>(bars + 3 * kTcMaxStages + 2 * kTcA + 2 * kTcP + 1);
+    uint8_t* stage_mem = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_mem + nstages * kStageBytes);
+    // bars: full[S], empty[S], a_full[A], a_empty[A], p_full[P], p_empty[P], done; then flags
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kTcMaxStages;
+    const uint32_t afull0 = empty0 + 8 * kTcMaxStages, aempty0 = afull0 + 8 * kTcA;
+    const uint32_t pfull0 = aempty0 + 8 * kTcA, pempty0 = pfull0 + 8 * kTcMaxP, done_bar = pempty0 + 8 * kTcMaxP;
+    volatile int* flags = reinterpret_cast<volatile int*>(bars + 2 * kTcMaxStages + 2 * kTcA + 2 * kTcMaxP + 1);
     // flags: [0] abort, [1] stages issued, [2] producer done, [3] TMEM base, [4] last ticket
-    // xexp: per stage, TP token exponents e (the chunk holds x * 2^-e) and [TP] = any e > 0
-    int* xexp = const_cast<int*>(flags) + 16;
 
     if (tid == 0) {
         for (int i = 0; i < nstages; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, kDec + 1 + kEpi);
-            mbar_init(xchk0 + 8 * i, kDec);
         }
         for (int i = 0; i < kTcA; ++i) {
             mbar_init(afull0 + 8 * i, kDec);
             mbar_init(aempty0 + 8 * i, 1);
         }
-        for (int i = 0; i < kTcP; ++i) {
+        for (int i = 0; i < kP; ++i) {
             mbar_init(pfull0 + 8 * i, 1);
             mbar_init(pempty0 + 8 * i, kEpi);
         }
@@ -264,7 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = (uint32_t)flags[3];
-    const uint32_t a_col0 = 0, p_col0 = kTcA * kACols;
+    const uint32_t a_col0 = 0, p_col0 = kTcA * kAStage;
 
     // Step k covers groups 2k, 2k+1 of the block (the second may be past its end), both in
     // stage k / 2 at positions gs0 = 2 (k % 2), gs0 + 1.
@@ -280,24 +316,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                const int g = g0 + si * BG, ng = g1 - g < BG ? g1 - g : BG;
+                const int g = g0 + si * BG;
                 uint8_t* sb = stage_mem + st * kStageBytes;
-                uint32_t bytes = (uint32_t)kXBytes;
-                for (int m = 0; m < kTcTiles; ++m)
-                    if (rb * kTcTiles + m < p.RT) bytes += (uint32_t)ng * (TB + kScaleTileBytes);
                 const uint32_t fb = full0 + 8 * st;
-                mbar_arrive_expect_tx(fb, bytes);
-                for (int m = 0; m < kTcTiles; ++m) {
-                    const int rt = rb * kTcTiles + m;
-                    if (rt >= p.RT) continue;
-                    bulk_g2s(smem_u32(sb + m * BG * TB), a.W + packed_code_off(rt, g, p.G, TB), ng * TB, fb, pol);
-                    bulk_g2s(smem_u32(sb + kTcTiles * BG * TB + m * BG * kScaleTileBytes),
-                             a.S + packed_scale_off(rt, g, p.G, kScaleTileBytes), ng * kScaleTileBytes, fb, pol);
-                }
+                mbar_arrive_expect_tx(fb, (uint32_t)kStageBytes);  // whole boxes, zeros included
+                tma_load_3d_hint(smem_u32(sb), &a.wmap, 0, g, rb * kTcTiles, fb, pol);
+                tma_load_3d_hint(smem_u32(sb + kTcTiles * BG * TB), &a.smap, 0, g, rb * kTcTiles, fb, pol);
                 // the weights are never written by a kernel that lets its dependents start
                 // early; X may be the preceding kernel's output
                 if (si == 0) grid_dependency_wait();
-                tma_load_3d(smem_u32(sb + kWBytes), &a.xmap, 0, 0, g * (kGroup / 8), fb);
+                tma_load_3d(smem_u32(sb + kWBytes), &a.xmap, 0, 0, g, fb);
                 ++it;
             }
             if (!ok) {
@@ -313,124 +341,93 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         // ------------------------------------------------------------ decoders
         const int q = warp & 3, h = (warp - 1) >> 2;  // TMEM lane quarter, and which half of it
         const int m = 2 * q + h;                       // the warp's 16-row tile of the block
-        const int dt = tid - 32;                       // decoder thread 0 .. 32 kDec - 1
-        for (int k = 0; k < nsteps; ++k) {
-            const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
-            const int ab = k % kTcA;
-            const bool first = k % 2 == 0, last = k % 2 == 1 || k == nsteps - 1;
-            bool ok = true;
-            if (first) {
-                ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
-                // Range check of the stage's activation chunk (every decoder thread, every stage,
-                // so the named barriers below always match): the group partials sum (q - z) x
-                // in fp32, so a token with some |x| >= 2^100 (bits 0x7180) is scaled by 2^-e,
-                // e = exponent(max |x|) - 99, exact in bf16; the epilogue multiplies its
-                // partials back by 2^e. Chunk c of the [K/8][TP][8] layout belongs to token c % TP.
-                uint4* xc = reinterpret_cast<uint4*>(stage_mem + st * kStageBytes + kWBytes);
-                int* ex = xexp + st * (TP + 1);
-                constexpr int kChunks = kXBytes / 16;
-                uint32_t big = 0;
-                for (int c = dt; c < kChunks; c += kDec * 32) {
-                    const uint4 v = xc[c];
-                    big |= ((v.x & 0x7FFF7FFFu) + 0x0E800E80u) | ((v.y & 0x7FFF7FFFu) + 0x0E800E80u) |
-                           ((v.z & 0x7FFF7FFFu) + 0x0E800E80u) | ((v.w & 0x7FFF7FFFu) + 0x0E800E80u);
-                }
-                if (named_bar_or(2, kDec * 32, (big & 0x80008000u) != 0)) {
-                    for (int t = dt; t < TP; t += kDec * 32) ex[t] = 0;
-                    named_bar_sync(2, kDec * 32);
-                    for (int c = dt; c < kChunks; c += kDec * 32) {
-                        const uint4 v = xc[c];
-                        const uint32_t mx = max(max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                                max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-                        atomicMax(ex + c % TP, (int)max(mx & 0xFFFFu, mx >> 16));
-                    }
-                    named_bar_sync(2, kDec * 32);
-                    for (int c = dt; c < kChunks; c += kDec * 32) {
-                        const int e = ((ex[c % TP] >> 7) & 0xFF) - 127 - 99;
-                        if (e <= 0) continue;
-                        const float sc = __int_as_float((127 - e) << 23);
-                        uint4 v = xc[c];
-                        uint32_t* iv = reinterpret_cast<uint32_t*>(&v);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col0;
+        // Groups gl, gl + 1 of the block (those inside its range), at positions gl % BG of stage st.
+        auto decode_pair = [&](int st, int gl, uint32_t (&r)[kTcPair][16]) {
+            const uint8_t* sb = stage_mem + st * kStageBytes + m * BG * TB;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(iv[i] << 16) * sc,
-                                                                            __uint_as_float(iv[i] & 0xFFFF0000u) * sc);
-                            iv[i] = *reinterpret_cast<const uint32_t*>(&b2);
-                        }
-                        xc[c] = v;
-                    }
-                    named_bar_sync(2, kDec * 32);
-                    for (int t = dt; t < TP; t += kDec * 32) {
-                        const int e = ((ex[t] >> 7) & 0xFF) - 127 - 99;
-                        ex[t] = e > 0 ? e : 0;
-                    }
-                    if (dt == 0) ex[TP] = 1;
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tensor core reads it next
-                } else if (dt == 0) {
-                    ex[TP] = 0;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xchk0 + 8 * st);
+            for (int gp = 0; gp < kTcPair; ++gp) {
+                if (gl + gp >= ngroups) break;
+                const uint8_t* code = sb + ((gl + gp) % BG) * TB + lane * 16;
+                const uint4 w = *reinterpret_cast<const uint4*>(code);
+                const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
+                tc_decode<BITS, 0>(w, hb, r[gp] + 0);
+                tc_decode<BITS, 1>(w, hb, r[gp] + 4);
+                tc_decode<BITS, 2>(w, hb, r[gp] + 8);
+                tc_decode<BITS, 3>(w, hb, r[gp] + 12);
             }
-            if (k >= kTcA) ok = mbar_wait(aempty0 + 8 * ab, ((k / kTcA) - 1) & 1, flags, a.dev_err, wait_ns) && ok;
+        };
+        uint32_t ra[kTcPair][16], rb[kTcPair][16];
+        bool ok = true;
+        for (int si = 0; si < nst; ++si) {
+            // one stage per hand-off: its four groups go to A buffer si % kTcA (128 columns)
+            const int st = si % nstages, ab = si % kTcA, gl = si * BG;
+            ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns) && ok;
+            if (si >= kTcA) ok = mbar_wait(aempty0 + 8 * ab, ((si / kTcA) - 1) & 1, flags, a.dev_err, wait_ns) && ok;
+            ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
-                const uint8_t* sb = stage_mem + st * kStageBytes;
-                const uint32_t base = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col0 + kACols * ab;
+                const uint32_t base = lane_base + kAStage * ab;
+                decode_pair(st, gl, ra);
 #pragma unroll
-                for (int gp = 0; gp < kTcPair; ++gp) {
-                    if (2 * k + gp >= ngroups) break;
-                    const uint8_t* code = sb + m * BG * TB + (gs0 + gp) * TB + lane * 16;
-                    const uint4 w = *reinterpret_cast<const uint4*>(code);
-                    const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
-                    uint32_t r[16];
-                    tc_decode<BITS, 0>(w, hb, r + 0);
-                    tc_decode<BITS, 1>(w, hb, r + 4);
-                    tc_decode<BITS, 2>(w, hb, r + 8);
-                    tc_decode<BITS, 3>(w, hb, r + 12);
-                    tmem_st_group(base + 32 * gp, r);
-                }
-                tmem_wait_st();
+                for (int gp = 0; gp < kTcPair; ++gp)
+                    if (gl + gp < ngroups) tmem_st_group(base + 32 * gp, ra[gp]);
+                decode_pair(st, gl + kTcPair, rb);     // while the first pair's stores complete
+#pragma unroll
+                for (int gp = 0; gp < kTcPair; ++gp)
+                    if (gl + kTcPair + gp < ngroups) tmem_st_group(base + 32 * (kTcPair + gp), rb[gp]);
             }
+            __syncwarp();
+            mbar_arrive_if(empty0 + 8 * st, lane == 0);  // the stage's codes are all in registers
+            if (ok) tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(afull0 + 8 * ab);
-                if (last) mbar_arrive(empty0 + 8 * st);
-            }
+            mbar_arrive_if(afull0 + 8 * ab, lane == 0);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            for (int k = 0; k < nsteps; ++k) {
-                const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
-                const int ab = k % kTcA, pb = k % kTcP;
-                const bool last = k % 2 == 1 || k == nsteps - 1;
-                bool ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
-                ok = ok && mbar_wait(afull0 + 8 * ab, (k / kTcA) & 1, flags, a.dev_err, wait_ns);
-                if (k >= kTcP) ok = ok && mbar_wait(pempty0 + 8 * pb, ((k / kTcP) - 1) & 1, flags, a.dev_err, wait_ns);
+        bool ok = true;
+        for (int si = 0; si < nst && ok; ++si) {
+            const int st = si % nstages, ab = si % kTcA;
+            ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+            ok = ok && mbar_wait(afull0 + 8 * ab, (si / kTcA) & 1, flags, a.dev_err, wait_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t xbase = smem_u32(stage_mem + st * kStageBytes + kWBytes);
+            const uint32_t a0 = tmem + a_col0 + kAStage * ab;
+            const bool leader = elect_one();
+#pragma unroll
+            for (int hh = 0; hh < BG / kTcPair; ++hh) {
+                const int k = (BG / kTcPair) * si + hh;  // P step: groups 2k, 2k + 1 of the block
+                if (k >= nsteps) break;
+                const int pb = k % kP;
+                if (k >= kP) ok = mbar_wait(pempty0 + 8 * pb, ((k / kP) - 1) & 1, flags, a.dev_err, wait_ns);
+                ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t xbase = smem_u32(stage_mem + st * kStageBytes + kWBytes);
+                const uint32_t d0 = tmem + p_col0 + kPCols * pb;
+                const int ng = 2 * k + 1 < ngroups ? 2 : 1;
 #pragma unroll
                 for (int gp = 0; gp < kTcPair; ++gp) {
-                    if (2 * k + gp >= ngroups) break;
+                    if (gp >= ng) break;
+                    const int gs = kTcPair * hh + gp;    // position in the stage
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        // K step j of group gs0 + gp: core-matrix (8 K) columns 8 (gs0 + gp) + 2 j, + 1
-                        const uint64_t bd =
-                            smem_desc(xbase + (uint32_t)(8 * (gs0 + gp) + 2 * j) * (TP * 16), TP * 16, 128);
-                        tc_mma(tmem + p_col0 + kPCols * pb + TP * gp, tmem + a_col0 + kACols * ab + 32 * gp + 8 * j,
-                               bd, kIdesc, j > 0 ? 1u : 0u);
+                        // K step j of group gs: bytes 32 j .. 32 j + 31 of the group block's rows
+                        const uint64_t bd = smem_desc_sw128(xbase + (uint32_t)(gs * TP * 128 + 32 * j));
+                        tc_mma(d0 + TP * gp, a0 + 32 * gs + 8 * j, bd, kIdesc, j > 0 ? 1u : 0u, leader);
                     }
                 }
-                tc_commit(aempty0 + 8 * ab);
-                tc_commit(pfull0 + 8 * pb);
-                if (last) tc_commit(empty0 + 8 * st);
+                tc_commit(pfull0 + 8 * pb, leader);
             }
-            // every MMA this thread issued has completed before TMEM can be freed
-            tc_commit(done_bar);
-            mbar_wait_drain(done_bar, 0, kDrainNs);
+            if (!ok) break;
+            tc_commit(aempty0 + 8 * ab, leader);
+            tc_commit(empty0 + 8 * st, leader);
         }
+        // every MMA the elected lane issued has completed before TMEM can be freed
+        const bool leader = elect_one();
+        tc_commit(done_bar, leader);
+        mbar_wait_drain(done_bar, 0, kDrainNs);
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
@@ -441,47 +438,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         float acc[TP];
 #pragma unroll
         for (int t = 0; t < TP; ++t) acc[t] = 0.f;
+        constexpr int kChunk = TP < 32 ? TP : 32;      // columns loaded before one wait
         for (int k = 0; k < nsteps; ++k) {
             const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
-            const int pb = k % kTcP;
-            const bool first = k % 2 == 0, last = k % 2 == 1 || k == nsteps - 1;
+            const int pb = k % kP;
+            const bool last = k % 2 == 1 || k == nsteps - 1;
             bool ok = true;
-            if (first) ok = mbar_wait(xchk0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
-            ok = mbar_wait(pfull0 + 8 * pb, (k / kTcP) & 1, flags, a.dev_err, wait_ns) && ok;
+            if (k % 2 == 0) ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+            ok = mbar_wait(pfull0 + 8 * pb, (k / kP) & 1, flags, a.dev_err, wait_ns) && ok;
             tc_fence_after();
             if (ok) {
-                const uint8_t* sb = stage_mem + st * kStageBytes;
-                const int* ex = xexp + st * (TP + 1);
-                const bool scaled = ex[TP] != 0;
+                const uint8_t* sc = stage_mem + st * kStageBytes + kTcTiles * BG * TB + m * BG * kScaleTileBytes;
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb;
 #pragma unroll
                 for (int gp = 0; gp < kTcPair; ++gp) {
                     if (2 * k + gp >= ngroups) break;
                     const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
-                        sb + kTcTiles * BG * TB + m * BG * kScaleTileBytes + (gs0 + gp) * kScaleTileBytes + 2 * sidx)));
-                    const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb + TP * gp;
+                                        sc + (gs0 + gp) * kScaleTileBytes + 2 * sidx))) *
+                                    (float)(1 << kTcScaleExp);
 #pragma unroll
-                    for (int c = 0; c < TP; c += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(base + c, v);
+                    for (int c = 0; c < TP; c += kChunk) {
+                        uint32_t v[kChunk];
+#pragma unroll
+                        for (int c2 = 0; c2 < kChunk; c2 += 16) tmem_ld16(base + TP * gp + c + c2, v + c2);
                         tmem_wait_ld();
-                        if (!scaled) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                acc[c + i] = fmaf(s * __int_as_float((127 + ex[c + i]) << 23), __uint_as_float(v[i]),
-                                                  acc[c + i]);
-                        }
+                        for (int i = 0; i < kChunk; ++i) acc[c + i] = fmaf(s, __uint_as_float(v[i]), acc[c + i]);
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(pempty0 + 8 * pb);
-                if (last) mbar_arrive(empty0 + 8 * st);
-            }
+            mbar_arrive_if(pempty0 + 8 * pb, lane == 0);
+            mbar_arrive_if(empty0 + 8 * st, lane == 0 && last);
         }
         // outputs: rows past N and tokens past T are not stored. The four epilogue warps agree on
         // whether the block aborted before any of them enters the barriers below.
