@@ -52,3 +52,26 @@ def test_timeout_in_fused_swiglu(nq):
     nq.device_error()
     g, u, _ = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
     assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+
+
+# the tensor-core kernel (8 < T <= 64): one K piece per row block, and a K split in three
+# (tickets part-counted when a block aborts)
+@pytest.mark.parametrize("bits,T,K,N,seed", [(4, 16, 640, 17408, 21), (5, 20, 5120, 6144, 22)])
+def test_timeout_in_tensor_core_kernel(nq, bits, T, K, N, seed):
+    assert nq.tensor_core_batches(1) == 1
+    if bits == 4:
+        p = si.q4_problem(T, K, N, seed)
+        w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+        fn = nq.gemm_q4
+        ref = lambda: oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)
+    else:
+        p = si.q5_problem(T, K, N, seed)
+        w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+        fn = nq.gemm_q5
+        ref = lambda: oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)
+    x = gu.dev_bf16(p["x"])
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    gu.expect_timeout(nq, lambda: fn(x, *w, N, out=y))
+    y = gu.host_f64(fn(x, *w, N))
+    nq.device_error()
+    assert gu.rel_err(y, ref()) <= gu.TOL
