@@ -37,7 +37,8 @@ L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "µs/call and achieved HBM GB/s (% of roofline) for Q4/Q5 skinny GEMM, T=1..8"
 MAX_T = 64
-KERNEL_SOURCES = ["nq_common.cuh", "nq_proj.cuh", "nq_launch.h", "nq_api.cu"]
+KERNEL_SOURCES = sorted(f for f in os.listdir(os.path.join(ROOT, "weight_only_groupwise_gb300", "csrc"))
+                        if f.endswith((".cu", ".cuh", ".h")))
 
 
 # ---------------------------------------------------------------- ranks
@@ -132,14 +133,15 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
-    when the summary is absent or was taken on different kernel sources."""
+def ncu_traffic(workload: str, T: int):
+    """DRAM bytes per launch of the dominant kernel of `workload` at T tokens (key
+    "<workload>@T<T>") from the committed ncu summary, or None when the summary is absent or
+    was taken on different kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d[workload]
+        e = d[f"{workload}@T{T}"]
         if e.get("kernel_hash") != kernel_hash():
             return None
         return int(e["dram_bytes_per_launch"])
@@ -558,7 +560,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": ncu_traffic(args.workload)},
+                     "traffic": ncu_traffic(args.workload, w["T"])},
         "gpu_launches": launches * args.steps * args.reps,
         "spread": {"replays": args.reps, "statistic": "median",
                    "us_per_step_min": round(1e3 * min(reps) / args.steps, 3),
