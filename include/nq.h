@@ -36,10 +36,12 @@
  *     default stream). Calls are asynchronous on `stream`; none synchronises or prints.
  *   - Shapes: K % 64 == 0, N % 16 == 0, 0 <= T <= 64. T == 0 or N == 0 is an empty problem
  *     (NQ_OK, nothing launched). K == 0 makes Y an empty sum: zeros are written.
- *   - Token batches: one kernel launch handles up to 8 tokens (decode, and the T = 8 verify
- *     rounds the pages tune); a call with T > 8 (larger speculative-verify batches, e.g.
- *     4 requests x 8 draft tokens) runs one launch per slice of 8 tokens, each streaming the
- *     weights again, so its time grows with ceil(T / 8).
+ *   - Token batches: one launch of the 8-token kernel handles up to 8 tokens (decode, and the
+ *     T = 8 verify rounds the pages tune). A plain nq_gemm_q4/q5 call with 8 < T <= 64 (larger
+ *     speculative-verify batches, e.g. 4 requests x 8 draft tokens) runs one launch of the
+ *     tensor-core kernel, which streams the weights once whatever T (nq_tensor_core_batches).
+ *     Every other call with T > 8 (SwiGLU, NVFP4, grouped, no-allocation) runs one launch per
+ *     slice of 8 tokens, each streaming the weights again, so its time grows with ceil(T / 8).
  *   - Alignment: every pointer 16-byte aligned.
  *   - All argument checks run on the host before anything is launched; a call that returns
  *     an error has launched nothing and left every output untouched.
@@ -273,7 +275,9 @@ nq_status nq_dequant_q5_debug_bf16(const void* Wq, const void* S, float* out, in
 /*
  * nq_reserve: allocate the current device's workspace for projections of up to
  * (T_max, K_max, N_max) now, so that later calls of at most that size allocate nothing
- * (e.g. before capturing a CUDA graph). Synchronises the device.
+ * (e.g. before capturing a CUDA graph). With T_max > 8 this includes the tensor-core
+ * kernel's partial sums (at most max(SMs, N_max / 128) x 128 x 64 floats, about 5 MB).
+ * Synchronises the device.
  */
 nq_status nq_reserve(int T_max, int K_max, int N_max);
 
@@ -329,8 +333,8 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
  * cores' memory (TMEM) and multiplies them with all T tokens (tcgen05.mma, M = 128 rows,
  * N = 16, 32 or 64 padded tokens), so the weights stream from HBM once. Off (0): one launch of
  * the 8-token kernel per slice of 8 tokens. -1 only queries. Returns the previous setting.
- * Either way the results agree with the oracle within the same tolerance. The SwiGLU, NVFP4 and
- * no-allocation calls use slices at every T. Not synchronised with calls in flight.
+ * Either way the results agree with the oracle within the same tolerance. The SwiGLU, NVFP4,
+ * grouped and no-allocation calls use slices at every T. Not synchronised with calls in flight.
  */
 int nq_tensor_core_batches(int enable);
 

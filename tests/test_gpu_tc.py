@@ -120,3 +120,49 @@ def test_tc_activation_outliers(nq):
     for t in range(T):
         assert np.all(np.isfinite(y[t]))
         assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+
+
+_RESERVE_SCRIPT = r"""
+import sys
+import torch
+from weight_only_groupwise_gb300 import nq
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+# a small eager call at the same padded token count (64) prepares the kernel instantiation;
+# its plan needs no partial sums, so it leaves a small workspace behind
+small = si.q5_problem(40, 640, 256, 40)
+ws = gu.pack_q5(nq, small["wn"], small["wh"], small["s"], 640, 256)
+nq.gemm_q5(gu.dev_bf16(small["x"]), *ws, 256)
+torch.cuda.synchronize()
+T, K, N = 40, 5120, 6144                      # three K pieces per row block: fp32 partials
+p = si.q5_problem(T, K, N, 41)
+w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+x = gu.dev_bf16(p["x"])
+y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+assert nq.plan_tc_info(5, T, K, N, torch.cuda.get_device_properties(0).multi_processor_count)["k_pieces"] > 1
+nq.reserve(64, K, N)
+graph = torch.cuda.CUDAGraph()
+with torch.cuda.graph(graph):                 # an allocation here would fail the call
+    nq.gemm_q5(x, *w, N, out=y)
+graph.replay()
+torch.cuda.synchronize()
+nq.device_error()
+err = gu.rel_err(gu.host_f64(y), oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N))
+assert err <= gu.TOL, err
+print("reserve-ok")
+"""
+
+
+def test_reserve_covers_tensor_core_partials(nq):
+    """nq_reserve(64, K, N) allocates the tensor-core kernel's partial sums too: a later
+    split-K call of that size, in a fresh process, runs inside CUDA graph capture (where the
+    library could not allocate) and matches the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", _RESERVE_SCRIPT], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "reserve-ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]

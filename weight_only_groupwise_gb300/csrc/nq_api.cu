@@ -797,12 +797,21 @@ long long nq_wait_limit(long long ns) {
 
 nq_status nq_reserve(int T_max, int K_max, int N_max) {
     if (T_max < 1 || T_max > kMaxT) return NQ_ERR_SHAPE;
-    if (T_max > kSliceT) T_max = kSliceT;  // larger batches run as slices of kSliceT tokens
     nq_status st = check_shape(K_max, N_max);
     if (st != NQ_OK) return st;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
+    if (T_max > kSliceT) {
+        // The tensor-core kernel's partials and tickets, for every shape up to the bound: a
+        // plan has at most max(SMs, row blocks) blocks of kTcRows x TP partial floats and one
+        // ticket per row block (reserved whether or not tensor-core batches are on now).
+        const long long rb = ((N_max > 0 ? N_max : 16) + kTcRows - 1) / kTcRows;
+        const long long blocks = rb > d->sms ? rb : d->sms;
+        st = ensure_tc_workspace(*d, rb, blocks * kTcRows * tc_tpad(T_max));
+        if (st != NQ_OK) return st;
+        T_max = kSliceT;  // the 8-token kernel's plans: slices of at most kSliceT tokens
+    }
     long long slots = 0, tickets = 0;
     // The largest plan over T <= T_max and both modes bounds every smaller call; slab-cluster
     // plans (at most SMs / S clusters) are counted as well.
