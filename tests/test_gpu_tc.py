@@ -87,11 +87,12 @@ def test_tc_zero_point_codes_give_exact_zero(nq):
     assert torch.count_nonzero(nq.gemm_q5(x, *z5, N).float()) == 0
 
 
-@pytest.mark.parametrize("bits,K,N", [(4, 5120, 17408), (5, 5120, 6144)])
-def test_tc_full_size_sampled(nq, bits, K, N):
-    """T=64 on the decode (Q4) and verify (Q5) weight shapes, full-size launch, sampled rows."""
-    T = 64
-    p, pack, _ = _problem(bits, T, K, N, 890 + bits)
+@pytest.mark.parametrize("T", [16, 32, 64])
+@pytest.mark.parametrize("bits,K,N", [(4, 5120, 17408), (5, 5120, 6144), (4, 17408, 5120)])
+def test_tc_full_size_sampled(nq, T, bits, K, N):
+    """The decode (Q4), verify (Q5) and down-projection (Q4, K split across blocks) weight
+    shapes at every padded token count the bench times: full-size launch, sampled rows."""
+    p, pack, _ = _problem(bits, T, K, N, 890 + bits + T)
     w = pack(nq)
     fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
     y = gu.host_f64(fn(gu.dev_bf16(p["x"]), *w, N))
