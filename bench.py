@@ -103,8 +103,17 @@ def workload_bytes(w: dict) -> int:
 
 
 def launches_per_step(w: dict) -> int:
-    """Kernel launches per step (T <= 8: one per call; the stack's q-gate and kv share one)."""
-    return {"proj": 1, "swiglu": 2, "stack": 4 * w.get("layers", 1)}[w["kind"]]
+    """Kernel launches per step. T <= 8: one per call (the stack's q-gate and kv share one).
+    8 < T <= 64: one per projection on the tensor-core kernel, two for a fused SwiGLU call
+    (gate, then up), and one per 8-token slice for the stack's grouped q-gate/kv call."""
+    T = w.get("T", 1)
+    big = T > 8
+    swiglu = 2 if big else 1
+    if w["kind"] == "proj":
+        return 1
+    if w["kind"] == "swiglu":
+        return swiglu + 1
+    return (swiglu + 1 + -(-T // 8) + 1) * w.get("layers", 1)
 
 
 # ---------------------------------------------------------------- environment helpers
@@ -638,11 +647,11 @@ def sweep(nq, dev, stream, peak):
         record("decode_fp4", T, time_graph(step, 100, 5, stream), 100, fp4_bytes(T, K, N), 1)
     del copies
     torch.cuda.empty_cache()
-    for name in ("swiglu_block", "swiglu_block_q5"):
-        w = dict(WORKLOADS[name], T=8)
+    for name, T in (("swiglu_block", 8), ("swiglu_block_q5", 8), ("swiglu_block", 16), ("swiglu_block", 64)):
+        w = dict(WORKLOADS[name], T=T)
         step, b, R, note, keep = build_step(nq, w, dev)
         steps = 100
-        record(name, 8, time_graph(step, steps, 5, stream), steps, b, launches_per_step(w))
+        record(name, T, time_graph(step, steps, 5, stream), steps, b, launches_per_step(w))
         del step, keep
         torch.cuda.empty_cache()
     layers = build_layers(nq, WORKLOADS["layer_stack"]["layers"], dev)

@@ -37,11 +37,12 @@
  *   - Shapes: K % 64 == 0, N % 16 == 0, 0 <= T <= 64. T == 0 or N == 0 is an empty problem
  *     (NQ_OK, nothing launched). K == 0 makes Y an empty sum: zeros are written.
  *   - Token batches: one launch of the 8-token kernel handles up to 8 tokens (decode, and the
- *     T = 8 verify rounds the pages tune). A plain nq_gemm_q4/q5 call with 8 < T <= 64 (larger
- *     speculative-verify batches, e.g. 4 requests x 8 draft tokens) runs one launch of the
- *     tensor-core kernel, which streams the weights once whatever T (nq_tensor_core_batches).
- *     Every other call with T > 8 (SwiGLU, NVFP4, grouped, no-allocation) runs one launch per
- *     slice of 8 tokens, each streaming the weights again, so its time grows with ceil(T / 8).
+ *     T = 8 verify rounds the pages tune). An nq_gemm_q4/q5 or nq_swiglu_q4/q5 call with
+ *     8 < T <= 64 (larger speculative-verify batches, e.g. 4 requests x 8 draft tokens) runs on
+ *     the tensor-core kernel, which streams the weights once whatever T
+ *     (nq_tensor_core_batches). The NVFP4, grouped and no-allocation calls with T > 8 run one
+ *     launch per slice of 8 tokens, each streaming the weights again, so their time grows with
+ *     ceil(T / 8).
  *   - Alignment: every pointer 16-byte aligned.
  *   - All argument checks run on the host before anything is launched; a call that returns
  *     an error has launched nothing and left every output untouched.
@@ -197,6 +198,10 @@ nq_status nq_gemm_q5_grouped(const void* X, const nq_group* groups, int count, i
  *   H = bf16(silu(g) * u),    silu(g) = g / (1 + exp(-g)) in fp32
  *   X device bf16 [T][K]; (Wg, Sg) and (Wu, Su) packed by nq_pack_q4 (K x N each);
  *   H device bf16 [T][N], written. The down projection is nq_gemm_q4 on H.
+ * T <= 8: one launch that computes g and u together. 8 < T <= 64 (with tensor-core batches
+ * on): two launches of the tensor-core kernel on the same X, the gate projection writing g in
+ * fp32 to a library buffer (T x N floats, see nq_reserve) and the up projection finishing
+ * H = bf16(silu(g) * u) from it; the same fp32 arithmetic, each weight matrix streamed once.
  */
 nq_status nq_swiglu_q4(const void* X, const void* Wg, const void* Sg, const void* Wu, const void* Su,
                        void* H, int T, int K, int N, void* stream);
@@ -276,7 +281,8 @@ nq_status nq_dequant_q5_debug_bf16(const void* Wq, const void* S, float* out, in
  * nq_reserve: allocate the current device's workspace for projections of up to
  * (T_max, K_max, N_max) now, so that later calls of at most that size allocate nothing
  * (e.g. before capturing a CUDA graph). With T_max > 8 this includes the tensor-core
- * kernel's partial sums (at most max(SMs, N_max / 128) x 128 x 64 floats, about 5 MB).
+ * kernel's partial sums (at most max(SMs, N_max / 128) x 128 x 64 floats, about 5 MB) and
+ * the fp32 gate outputs of its SwiGLU calls (T_max x N_max floats).
  * Synchronises the device.
  */
 nq_status nq_reserve(int T_max, int K_max, int N_max);
@@ -327,14 +333,15 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
                          int64_t* seg, int64_t cap);
 
 /*
- * nq_tensor_core_batches: how plain Q4/Q5 projections with 8 < T <= 64 run. On (1, the
- * default; the environment variable NQ_TC=0 read at the first call turns it off): one launch of
- * the tensor-core kernel, which decodes the weights once into the fifth-generation tensor
- * cores' memory (TMEM) and multiplies them with all T tokens (tcgen05.mma, M = 128 rows,
- * N = 16, 32 or 64 padded tokens), so the weights stream from HBM once. Off (0): one launch of
- * the 8-token kernel per slice of 8 tokens. -1 only queries. Returns the previous setting.
- * Either way the results agree with the oracle within the same tolerance. The SwiGLU, NVFP4,
- * grouped and no-allocation calls use slices at every T. Not synchronised with calls in flight.
+ * nq_tensor_core_batches: how Q4/Q5 projections and SwiGLU blocks with 8 < T <= 64 run.
+ * On (1, the default; the environment variable NQ_TC=0 read at the first call turns it off):
+ * one launch of the tensor-core kernel per weight matrix (two for a SwiGLU block), which
+ * decodes the weights once into the fifth-generation tensor cores' memory (TMEM) and
+ * multiplies them with all T tokens (tcgen05.mma, M = 128 rows, N = 16, 32 or 64 padded
+ * tokens), so the weights stream from HBM once. Off (0): one launch of the 8-token kernel per
+ * slice of 8 tokens. -1 only queries. Returns the previous setting. Either way the results
+ * agree with the oracle within the same tolerance. The NVFP4, grouped and no-allocation calls
+ * use slices at every T. Not synchronised with calls in flight.
  */
 int nq_tensor_core_batches(int enable);
 

@@ -167,3 +167,89 @@ def test_reserve_covers_tensor_core_partials(nq):
     r = subprocess.run([sys.executable, "-c", _RESERVE_SCRIPT], cwd=root, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and "reserve-ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+# ---------------------------------------------------------------- SwiGLU blocks, 8 < T <= 64
+# Two tensor-core launches: the gate projection writes fp32 G, the up projection's epilogue
+# writes H = bf16(silu(G) * U).
+
+TC_SWIGLU_SHAPES = [(9, 640, 272, 0), (20, 1024, 1040, 1), (33, 5120, 384, 2), (64, 512, 144, 3),
+                    (48, 17408, 96, 4)]
+
+
+def _swiglu_problem(bits, T, K, N, seed):
+    return si.swiglu_problem(T, K, N, seed) if bits == 4 else si.swiglu_q5_problem(T, K, N, seed)
+
+
+def _swiglu_dev(nq, bits, p, K, N):
+    if bits == 4:
+        wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+        wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+        return nq.swiglu_q4(gu.dev_bf16(p["x"]), *wg, *wu, N)
+    wg = gu.pack_q5(nq, p["wgn"], p["wgh"], p["sg"], K, N)
+    wu = gu.pack_q5(nq, p["wun"], p["wuh"], p["su"], K, N)
+    return nq.swiglu_q5(gu.dev_bf16(p["x"]), *wg, *wu, N)
+
+
+def _swiglu_ref(bits, p, T, K, N):
+    if bits == 4:
+        g, u, _ = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
+    else:
+        g, u, _ = oracle.swiglu_q5(p["x"], p["wgn"], p["wgh"], p["sg"], p["wun"], p["wuh"], p["su"], T, K, N)
+    return g / (1.0 + np.exp(-g)) * u
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("T,K,N,seed", TC_SWIGLU_SHAPES)
+def test_tc_swiglu_parity(nq, bits, T, K, N, seed):
+    p = _swiglu_problem(bits, T, K, N, 950 + seed)
+    h = gu.host_f64(_swiglu_dev(nq, bits, p, K, N))
+    h_ref = _swiglu_ref(bits, p, T, K, N)
+    for t in range(T):
+        assert gu.rel_err(h[t], h_ref[t]) <= gu.TOL, t
+    nq.device_error()
+
+
+def test_tc_swiglu_matches_slices_and_is_deterministic(nq):
+    T, K, N = 40, 2048, 1152
+    p = _swiglu_problem(4, T, K, N, 960)
+    h1 = _swiglu_dev(nq, 4, p, K, N)
+    h2 = _swiglu_dev(nq, 4, p, K, N)
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    prev = nq.tensor_core_batches(0)
+    try:
+        hs = _swiglu_dev(nq, 4, p, K, N)
+    finally:
+        nq.tensor_core_batches(prev)
+    h_ref = _swiglu_ref(4, p, T, K, N)
+    for h in (h1, hs):
+        hh = gu.host_f64(h)
+        for t in range(T):
+            assert gu.rel_err(hh[t], h_ref[t]) <= gu.TOL
+    nq.device_error()
+
+
+def test_tc_swiglu_zero_point_gate_gives_exact_zero(nq):
+    """Gate codes equal to z make G exactly 0, so H = silu(0) * U is exactly 0 everywhere."""
+    T, K, N = 24, 1024, 272
+    p = _swiglu_problem(4, T, K, N, 961)
+    q = dict(p, wg=np.full_like(p["wg"], 0x88888888))
+    assert torch.count_nonzero(_swiglu_dev(nq, 4, q, K, N).float()) == 0
+
+
+@pytest.mark.parametrize("T", [16, 64])
+@pytest.mark.parametrize("bits", [4, 5])
+def test_tc_swiglu_full_size_sampled(nq, bits, T):
+    """The SwiGLU gate/up block of the bench (K=5120, N=17408), full-size launches, sampled rows."""
+    K, N = 5120, 17408
+    p = _swiglu_problem(bits, T, K, N, 970 + bits + T)
+    h = gu.host_f64(_swiglu_dev(nq, bits, p, K, N))
+    rows = gu.sample_rows(N, 128, 12)
+    if bits == 4:
+        g, u, _ = oracle.swiglu_q4_rows(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, rows)
+    else:
+        g, u, _ = oracle.swiglu_q5_rows(p["x"], p["wgn"], p["wgh"], p["sg"], p["wun"], p["wuh"], p["su"], T, K, rows)
+    h_ref = (g / (1.0 + np.exp(-g)) * u).T
+    for t in range(T):
+        assert gu.rel_err(h[t, rows], h_ref[t]) <= gu.TOL, t
+    nq.device_error()

@@ -75,3 +75,21 @@ def test_timeout_in_tensor_core_kernel(nq, bits, T, K, N, seed):
     y = gu.host_f64(fn(x, *w, N))
     nq.device_error()
     assert gu.rel_err(y, ref()) <= gu.TOL
+
+
+def test_timeout_in_tensor_core_swiglu(nq):
+    """A SwiGLU block with 8 < T <= 64 is two tensor-core launches (gate, then up); both abort
+    under the 1 ns bound, and the next call is correct."""
+    assert nq.tensor_core_batches(1) == 1
+    T, K, N = 24, 5120, 1024
+    p = si.swiglu_problem(T, K, N, 23)
+    wg = gu.pack_q4(nq, p["wg"], p["sg"], K, N)
+    wu = gu.pack_q4(nq, p["wu"], p["su"], K, N)
+    x = gu.dev_bf16(p["x"])
+    gu.expect_timeout(nq, lambda: nq.swiglu_q4(x, *wg, *wu, N))
+    h = gu.host_f64(nq.swiglu_q4(x, *wg, *wu, N))
+    nq.device_error()
+    g, u, _ = oracle.swiglu_q4(p["x"], p["wg"], p["sg"], p["wu"], p["su"], T, K, N)
+    ref = g / (1.0 + np.exp(-g)) * u
+    for t in range(T):
+        assert gu.rel_err(h[t], ref[t]) <= gu.TOL

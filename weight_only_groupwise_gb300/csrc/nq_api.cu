@@ -239,6 +239,8 @@ struct DevState {
     // large-batch tensor-core kernel: [tickets: 4 B per row block, 256-B rounded][partials]
     uint8_t* tc_ws = nullptr;
     long long tc_tickets = 0, tc_floats = 0;
+    float* tc_gate = nullptr;   // fp32 gate outputs of a tensor-core SwiGLU call, [T][N]
+    long long tc_gate_floats = 0;
 };
 
 constexpr int kMaxDevices = 64;
@@ -352,6 +354,23 @@ nq_status ensure_tc_workspace(DevState& d, long long tickets, long long floats) 
     return NQ_OK;
 }
 
+// The fp32 gate buffer of tensor-core SwiGLU calls, grown to at least `floats`.
+nq_status ensure_tc_gate(DevState& d, long long floats) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d.tc_gate && floats <= d.tc_gate_floats) return NQ_OK;
+    if (d.tc_gate) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return NQ_ERR_CUDA;
+        cudaFree(d.tc_gate);
+        d.tc_gate = nullptr;
+        d.tc_gate_floats = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, (size_t)floats * sizeof(float)) != cudaSuccess) return NQ_ERR_CUDA;
+    d.tc_gate = static_cast<float*>(p);
+    d.tc_gate_floats = floats;
+    return NQ_OK;
+}
+
 // ---------------------------------------------------------------- argument checks
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
@@ -443,23 +462,42 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     if (K == 0) {  // empty sum
         return cudaMemsetAsync(Y, 0, yb, as_stream(stream)) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
     }
-    // Larger batches of a plain projection: the tensor-core kernel, one weight pass.
-    if (g_tc && !swiglu && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
+    // Larger batches: the tensor-core kernel, one weight pass per matrix. A SwiGLU block is two
+    // launches on the same X: the gate projection writes fp32 G to a library buffer, the up
+    // projection's epilogue writes H = silu(G) * U in bf16.
+    if (g_tc && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
         alignas(64) TcArgs ta;
+        alignas(64) TcArgs tu;
         if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP) &&
-            encode_weight_maps(&ta.wmap, &ta.smap, W0, S0, bits, K, N)) {
+            encode_weight_maps(&ta.wmap, &ta.smap, W0, S0, bits, K, N) &&
+            (!swiglu || encode_weight_maps(&tu.wmap, &tu.smap, W1, S1, bits, K, N))) {
             st = ensure_workspace(*d, 1, 1);
             if (st != NQ_OK) return st;
             st = ensure_tc_workspace(*d, ta.p.RB, ta.p.KS > 1 ? (long long)ta.p.P * kTcRows * ta.p.TP : 1);
             if (st != NQ_OK) return st;
+            if (swiglu) {
+                st = ensure_tc_gate(*d, (long long)T * N);
+                if (st != NQ_OK) return st;
+            }
             ta.W = static_cast<const uint8_t*>(W0);
             ta.S = static_cast<const uint8_t*>(S0);
             ta.Y = static_cast<uint16_t*>(Y);
+            ta.G = d->tc_gate;
+            ta.mode = swiglu ? kTcOutGate : kTcOutY;
             ta.tickets = reinterpret_cast<int*>(d->tc_ws);
             ta.partials = reinterpret_cast<float*>(d->tc_ws + (((size_t)d->tc_tickets * 4 + 255) / 256) * 256);
             ta.dev_err = reinterpret_cast<int*>(d->ws);
             ta.wait_ns = g_wait_ns;
-            return launch_tc_proj(bits, ta, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+            if (launch_tc_proj(bits, ta, as_stream(stream), g_pdl) != cudaSuccess) return NQ_ERR_CUDA;
+            if (!swiglu) return NQ_OK;
+            const CUtensorMap wmap = tu.wmap, smap = tu.smap;
+            tu = ta;
+            tu.wmap = wmap;
+            tu.smap = smap;
+            tu.W = static_cast<const uint8_t*>(W1);
+            tu.S = static_cast<const uint8_t*>(S1);
+            tu.mode = kTcOutSwiglu;
+            return launch_tc_proj(bits, tu, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
         }
     }
     // At most two distinct slice sizes: full slices and the remainder.
@@ -810,6 +848,8 @@ nq_status nq_reserve(int T_max, int K_max, int N_max) {
         const long long blocks = rb > d->sms ? rb : d->sms;
         st = ensure_tc_workspace(*d, rb, blocks * kTcRows * tc_tpad(T_max));
         if (st != NQ_OK) return st;
+        st = ensure_tc_gate(*d, (long long)T_max * (N_max > 0 ? N_max : 16));  // SwiGLU gate outputs
+        if (st != NQ_OK) return st;
         T_max = kSliceT;  // the 8-token kernel's plans: slices of at most kSliceT tokens
     }
     long long slots = 0, tickets = 0;
@@ -856,7 +896,7 @@ void nq_shutdown(void) {
     int cur = 0;
     cudaGetDevice(&cur);
     for (int i = 0; i < kMaxDevices; ++i) {
-        if (!g_dev[i].ws && !g_dev[i].tc_ws) continue;
+        if (!g_dev[i].ws && !g_dev[i].tc_ws && !g_dev[i].tc_gate) continue;
         cudaSetDevice(i);
         cudaDeviceSynchronize();
         cudaFree(g_dev[i].ws);
@@ -865,6 +905,9 @@ void nq_shutdown(void) {
         cudaFree(g_dev[i].tc_ws);
         g_dev[i].tc_ws = nullptr;
         g_dev[i].tc_tickets = g_dev[i].tc_floats = 0;
+        cudaFree(g_dev[i].tc_gate);
+        g_dev[i].tc_gate = nullptr;
+        g_dev[i].tc_gate_floats = 0;
     }
     cudaSetDevice(cur);
 }

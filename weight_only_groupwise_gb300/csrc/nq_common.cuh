@@ -365,6 +365,8 @@ NQ_HD long long slot_of(const Plan& p, int s, int rp, int c) { return (long long
 }  // namespace nq
 
 #if defined(__CUDACC__)
+#include <cuda_bf16.h>
+
 namespace nq {
 
 // ---------------------------------------------------------------- PTX helpers
@@ -389,6 +391,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+
+// bf16 bits of v, round to nearest even.
+__device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// The SwiGLU epilogue in fp32: silu(g) * u = g / (1 + e^-g) * u.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // One arrive by the lanes whose pred is true, issued by the whole warp with the predicate inside
 // the instruction: no branch, so the warp does not reconverge behind the arrive (a branch around

@@ -208,12 +208,6 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * 
     }
 }
 
-__device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
-
 // Power-of-two range exponent of one token's X slab from the bits of its max |x| (bf16):
 // x * 2^-e has its maximum in [2^14, 2^15), clear of fp16 overflow and far above its
 // subnormals; clamped so that 2^e and 2^-e stay normal fp32 numbers.

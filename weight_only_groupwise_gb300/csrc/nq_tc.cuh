@@ -57,6 +57,10 @@ constexpr int kTcEpilogue = 4;                    // epilogue warps: one TMEM la
 constexpr int kTcWarps = 2 + kTcDecoders + kTcEpilogue;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcMinT = 9, kTcMaxT = 64;
+// What the epilogue writes for (token t, row n) from the finished fp32 value v: bf16 Y = v;
+// fp32 G = v (a SwiGLU gate projection); bf16 Y = silu(G) * v (the up projection of the same
+// SwiGLU block, G written by the preceding launch).
+constexpr int kTcOutY = 0, kTcOutGate = 1, kTcOutSwiglu = 2;
 
 // Shared-memory bytes of one stage: codes and scales of kTcTiles tiles x kTcStageGroups groups,
 // then the activation chunk (kTcStageGroups * 64 K x TP tokens, bf16).
@@ -102,7 +106,9 @@ struct alignas(64) TcArgs {
     CUtensorMap smap;        // packed scales viewed as [RT][G][4] (8-byte elements)
     const uint8_t* W;        // packed codes
     const uint8_t* S;        // packed scales
-    uint16_t* Y;             // bf16 [T][N]
+    uint16_t* Y;             // bf16 [T][N] (output modes kTcOutY and kTcOutSwiglu)
+    float* G;                // fp32 [T][N]: written (kTcOutGate) or read (kTcOutSwiglu)
+    int mode;                // kTcOutY, kTcOutGate or kTcOutSwiglu
     float* partials;         // RB * KS slots of kTcRows x TP floats (K split only)
     int* tickets;            // one per row block, zero between calls
     int* dev_err;
@@ -200,7 +206,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-__device__ __forceinline__ uint16_t bf16_bits_rn_tc(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         const int row = 32 * q + lane;                 // row of the block = TMEM lane
         const int m = row >> 4, rr = row & 15;
         const int sidx = 2 * (rr & 7) + (rr >> 3);     // the row's place in a packed scale tile
-        grid_dependency_wait();                        // Y, partials and tickets may be in use before
+        grid_dependency_wait();                        // Y, G, partials and tickets may be in use before
         float acc[TP];
 #pragma unroll
         for (int t = 0; t < TP; ++t) acc[t] = 0.f;
@@ -475,12 +480,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         // outputs: rows past N and tokens past T are not stored. The four epilogue warps agree on
         // whether the block aborted before any of them enters the barriers below.
         const int nrow = rb * kTcRows + row;
+        auto store = [&](int t, float v) {
+            const size_t i = (size_t)t * p.N + nrow;
+            if (a.mode == kTcOutGate)
+                a.G[i] = v;
+            else if (a.mode == kTcOutSwiglu)
+                a.Y[i] = bf16_bits_rn(silu_mul(__ldcg(a.G + i), v));
+            else
+                a.Y[i] = bf16_bits_rn(v);
+        };
         if (!named_bar_or(1, kEpi * 32, flags[0] != 0)) {
             if (p.KS == 1) {
                 if (nrow < p.N) {
 #pragma unroll
                     for (int t = 0; t < TP; ++t)
-                        if (t < p.T) a.Y[(size_t)t * p.N + nrow] = bf16_bits_rn_tc(acc[t]);
+                        if (t < p.T) store(t, acc[t]);
                 }
             } else {
                 float* part = a.partials + ((size_t)rb * p.KS + kp) * (kTcRows * TP);
@@ -506,7 +520,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                     if (nrow < p.N) {
 #pragma unroll
                         for (int t = 0; t < TP; ++t)
-                            if (t < p.T) a.Y[(size_t)t * p.N + nrow] = bf16_bits_rn_tc(sum[t]);
+                            if (t < p.T) store(t, sum[t]);
                     }
                     if (tid == leader) a.tickets[rb] = 0;
                 }
