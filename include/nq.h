@@ -40,9 +40,9 @@
  *     T = 8 verify rounds the pages tune). An nq_gemm_q4/q5 or nq_swiglu_q4/q5 call with
  *     8 < T <= 64 (larger speculative-verify batches, e.g. 4 requests x 8 draft tokens) runs on
  *     the tensor-core kernel, which streams the weights once whatever T
- *     (nq_tensor_core_batches). The NVFP4, grouped and no-allocation calls with T > 8 run one
- *     launch per slice of 8 tokens, each streaming the weights again, so their time grows with
- *     ceil(T / 8).
+ *     (nq_tensor_core_batches); a grouped call then runs one such launch per matrix. The NVFP4
+ *     and no-allocation calls with T > 8 run one launch per slice of 8 tokens, each streaming
+ *     the weights again, so their time grows with ceil(T / 8).
  *   - Alignment: every pointer 16-byte aligned.
  *   - All argument checks run on the host before anything is launched; a call that returns
  *     an error has launched nothing and left every output untouched.
@@ -185,8 +185,10 @@ typedef struct nq_group {
 /*
  * nq_gemm_q4_grouped / nq_gemm_q5_grouped: Y_g = X * dequant(Wq_g, S_g) for each of `count`
  * groups (1..4, host array), all with the same X (device bf16 [T][K]) and code width.
- * Results equal those of one nq_gemm_q4 / nq_gemm_q5 call per group. Outputs must not overlap
- * X, any group's weights or each other. Errors and launch behaviour as nq_gemm_q4.
+ * Results equal those of one nq_gemm_q4 / nq_gemm_q5 call per group. T <= 8: one launch for
+ * all groups; 8 < T <= 64 (tensor-core batches on): one tensor-core launch per group, each
+ * streaming its weights once. Outputs must not overlap X, any group's weights or each other;
+ * every argument is checked before the first launch. Errors as nq_gemm_q4.
  */
 nq_status nq_gemm_q4_grouped(const void* X, const nq_group* groups, int count, int T, int K, void* stream);
 nq_status nq_gemm_q5_grouped(const void* X, const nq_group* groups, int count, int T, int K, void* stream);
@@ -340,8 +342,9 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
  * multiplies them with all T tokens (tcgen05.mma, M = 128 rows, N = 16, 32 or 64 padded
  * tokens), so the weights stream from HBM once. Off (0): one launch of the 8-token kernel per
  * slice of 8 tokens. -1 only queries. Returns the previous setting. Either way the results
- * agree with the oracle within the same tolerance. The NVFP4, grouped and no-allocation calls
- * use slices at every T. Not synchronised with calls in flight.
+ * agree with the oracle within the same tolerance. A grouped call runs one such launch per
+ * matrix. The NVFP4 and no-allocation calls use slices at every T. Not synchronised with calls
+ * in flight.
  */
 int nq_tensor_core_batches(int enable);
 

@@ -507,6 +507,8 @@ GROUPED_CASES = [
     # four groups, K slabs at T=8, several 8-token slices
     (5, 8, 1024, [192, 32]), (4, 1, 640, [48, 16, 80]), (5, 3, 5120, [96, 48, 16, 272]),
     (4, 8, 17408, [64, 48]), (5, 12, 512, [32, 112]), (4, 2, 256, [16]),
+    # 8 < T <= 64: one tensor-core launch per matrix (K split across blocks for the small N)
+    (4, 40, 5120, [192, 48, 272]), (5, 64, 1024, [16, 144]),
 ]
 
 
@@ -525,6 +527,28 @@ def test_grouped_projections_parity(nq, bits, T, K, Ns):
             refs.append(oracle.gemm_q5(x, p["wn"], p["wh"], p["s"], T, K, N))
     fn = nq.gemm_q4_grouped if bits == 4 else nq.gemm_q5_grouped
     ys = fn(gu.dev_bf16(x), groups)
+    for y, r in zip(ys, refs):
+        y = gu.host_f64(y)
+        for t in range(T):
+            assert gu.rel_err(y[t], r[t]) <= gu.TOL, t
+    nq.device_error()
+
+
+def test_grouped_slices_when_tensor_cores_are_off(nq):
+    """With tensor-core batches off, a grouped call with T > 8 runs as 8-token slices of one
+    grouped launch: the same results within the tolerance."""
+    T, K, Ns = 20, 1024, [48, 112]
+    x = si.activations(si.rng(790), T, K)
+    groups, refs = [], []
+    for j, N in enumerate(Ns):
+        p = si.q4_problem(T, K, N, 791 + j)
+        groups.append((*gu.pack_q4(nq, p["wq"], p["s"], K, N), N))
+        refs.append(oracle.gemm_q4(x, p["wq"], p["s"], T, K, N))
+    prev = nq.tensor_core_batches(0)
+    try:
+        ys = nq.gemm_q4_grouped(gu.dev_bf16(x), groups)
+    finally:
+        nq.tensor_core_batches(prev)
     for y, r in zip(ys, refs):
         y = gu.host_f64(y)
         for t in range(T):

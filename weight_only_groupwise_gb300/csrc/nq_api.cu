@@ -579,6 +579,16 @@ nq_status project_grouped(int bits, const void* X, const nq_group* groups, int c
                 return NQ_ERR_CUDA;
         return NQ_OK;
     }
+    // 8 < T <= 64: one tensor-core launch per matrix (each streams its weights once) instead of
+    // 8-token slices of a grouped launch (each slice streams all of them again).
+    if (g_tc && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
+        for (int g = 0; g < count; ++g) {
+            st = project(bits, false, X, groups[g].Wq, groups[g].S, nullptr, nullptr, groups[g].Y, T, K, groups[g].N,
+                         stream);
+            if (st != NQ_OK) return st;
+        }
+        return NQ_OK;
+    }
     int gpair[kMaxGroups + 1];
     gpair[0] = 0;
     for (int g = 0; g < count; ++g) gpair[g + 1] = gpair[g] + (groups[g].N + 2 * kTileRows - 1) / (2 * kTileRows);
