@@ -638,7 +638,7 @@ def sweep(nq, dev, stream, peak):
     K, N = 5120, 17408
     R = max(2, -(-3 * L2_BYTES // fp4_bytes(8, K, N)))
     copies = make_fp4_copies(nq, K, N, R, 9, dev)
-    for T in (1, 2, 4, 8):
+    for T in (1, 2, 4, 8, 16, 64):
         x = si.device_activations(T, K, gen, dev)
         y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
 

@@ -40,9 +40,9 @@
  *     T = 8 verify rounds the pages tune). An nq_gemm_q4/q5 or nq_swiglu_q4/q5 call with
  *     8 < T <= 64 (larger speculative-verify batches, e.g. 4 requests x 8 draft tokens) runs on
  *     the tensor-core kernel, which streams the weights once whatever T
- *     (nq_tensor_core_batches); a grouped call then runs one such launch per matrix. The NVFP4
- *     and no-allocation calls with T > 8 run one launch per slice of 8 tokens, each streaming
- *     the weights again, so their time grows with ceil(T / 8).
+ *     (nq_tensor_core_batches); so does nq_gemm_fp4, and a grouped call runs one such launch
+ *     per matrix. The no-allocation call with T > 8 runs one launch per slice of 8 tokens, each
+ *     streaming the weights again, so its time grows with ceil(T / 8).
  *   - Alignment: every pointer 16-byte aligned.
  *   - All argument checks run on the host before anything is launched; a call that returns
  *     an error has launched nothing and left every output untouched.
@@ -245,8 +245,9 @@ nq_status nq_pack_fp4(const uint32_t* codes_canon, const uint8_t* sf_canon, int 
                       void* s_packed, void* stream);
 
 /* nq_gemm_fp4: Y = X * W for NVFP4 weights packed by nq_pack_fp4, global_scale = g,
- * 1 <= T <= 64 (slices of 8 tokens as the other projections). Arguments, alignment, errors
- * and launch behaviour as nq_gemm_q4. */
+ * 1 <= T <= 64 (8 < T <= 64 on the tensor-core kernel as the other projections: the decoded
+ * weights e2m1 x e4m3 are exact in bf16). Arguments, alignment, errors and launch behaviour as
+ * nq_gemm_q4. */
 nq_status nq_gemm_fp4(const void* X, const void* Wq, const void* S, float global_scale, void* Y, int T, int K,
                       int N, void* stream);
 
@@ -335,16 +336,16 @@ int64_t nq_plan_segments(int bits, int mode, int T, int K, int N, int num_sms, i
                          int64_t* seg, int64_t cap);
 
 /*
- * nq_tensor_core_batches: how Q4/Q5 projections and SwiGLU blocks with 8 < T <= 64 run.
- * On (1, the default; the environment variable NQ_TC=0 read at the first call turns it off):
- * one launch of the tensor-core kernel per weight matrix (two for a SwiGLU block), which
- * decodes the weights once into the fifth-generation tensor cores' memory (TMEM) and
- * multiplies them with all T tokens (tcgen05.mma, M = 128 rows, N = 16, 32 or 64 padded
+ * nq_tensor_core_batches: how projections (Q4, Q5, NVFP4) and SwiGLU blocks with
+ * 8 < T <= 64 run. On (1, the default; the environment variable NQ_TC=0 read at the first call
+ * turns it off): one launch of the tensor-core kernel per weight matrix (two for a SwiGLU
+ * block), which decodes the weights once into the fifth-generation tensor cores' memory (TMEM)
+ * and multiplies them with all T tokens (tcgen05.mma, M = 128 rows, N = 16, 32 or 64 padded
  * tokens), so the weights stream from HBM once. Off (0): one launch of the 8-token kernel per
  * slice of 8 tokens. -1 only queries. Returns the previous setting. Either way the results
  * agree with the oracle within the same tolerance. A grouped call runs one such launch per
- * matrix. The NVFP4 and no-allocation calls use slices at every T. Not synchronised with calls
- * in flight.
+ * matrix. The no-allocation call uses slices at every T. Not synchronised with calls in
+ * flight.
  */
 int nq_tensor_core_batches(int enable);
 
@@ -352,7 +353,8 @@ int nq_tensor_core_batches(int enable);
  * nq_plan_tc_info: the work split the tensor-core kernel would use (host only): out[0] blocks,
  * [1] row blocks of 128 rows, [2] K pieces per row block (their fp32 partials are added in
  * fixed order by the row block's last piece), [3] padded token count, [4] pipeline stages,
- * [5] shared-memory bytes, [6] 64-wide K groups, [7] groups per stage. bits 4 or 5, 8 < T <= 64.
+ * [5] shared-memory bytes, [6] 64-wide K groups, [7] groups per stage. bits 4, 5 or 14 (NVFP4
+ * weights), 8 < T <= 64.
  */
 nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t out[8]);
 

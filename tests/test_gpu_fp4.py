@@ -110,3 +110,75 @@ def test_fp4_deterministic(nq):
     y2 = nq.gemm_fp4(x, *w, p["g"], N)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     nq.device_error()
+
+
+# ---------------------------------------------------------------- 8 < T <= 64: tensor cores
+# The decoded weights e2m1 x e4m3 x 2^-20 are exact in bf16; the epilogue multiplies by
+# 2^20 g.
+
+FP4_TC_SHAPES = [(9, 640, 272, 0), (16, 5120, 384, 1), (33, 512, 144, 2), (64, 17408, 96, 3), (40, 6208, 1040, 4)]
+
+
+@pytest.mark.parametrize("T,K,N,seed", FP4_TC_SHAPES)
+def test_fp4_tc_parity(nq, T, K, N, seed):
+    assert nq.tensor_core_batches(-1) == 1
+    p = si.fp4_problem(T, K, N, 600 + seed)
+    w = pack(nq, p, K, N)
+    y = gu.host_f64(nq.gemm_fp4(gu.dev_bf16(p["x"]), *w, p["g"], N))
+    y_ref = oracle.gemm_fp4(p["x"], p["codes"], p["sf"], p["g"], T, K, N)
+    for t in range(T):
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+    nq.device_error()
+
+
+@pytest.mark.parametrize("T", [16, 64])
+def test_fp4_tc_full_size_sampled(nq, T):
+    K, N = 5120, 17408
+    p = si.fp4_problem(T, K, N, 610 + T)
+    w = pack(nq, p, K, N)
+    y = gu.host_f64(nq.gemm_fp4(gu.dev_bf16(p["x"]), *w, p["g"], N))
+    rows = gu.sample_rows(N, 128, 13)
+    y_ref = oracle.gemm_fp4_rows(p["x"], p["codes"], p["sf"], p["g"], T, K, rows).T
+    for t in range(T):
+        assert gu.rel_err(y[t, rows], y_ref[t]) <= gu.TOL, t
+
+
+def test_fp4_tc_matches_slices_and_is_deterministic(nq):
+    T, K, N = 24, 2048, 1152
+    p = si.fp4_problem(T, K, N, 620)
+    w = pack(nq, p, K, N)
+    x = gu.dev_bf16(p["x"])
+    y1 = nq.gemm_fp4(x, *w, p["g"], N)
+    y2 = nq.gemm_fp4(x, *w, p["g"], N)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    prev = nq.tensor_core_batches(0)
+    try:
+        ys = nq.gemm_fp4(x, *w, p["g"], N)
+    finally:
+        nq.tensor_core_batches(prev)
+    y_ref = oracle.gemm_fp4(p["x"], p["codes"], p["sf"], p["g"], T, K, N)
+    for y in (y1, ys):
+        yh = gu.host_f64(y)
+        for t in range(T):
+            assert gu.rel_err(yh[t], y_ref[t]) <= gu.TOL, t
+    nq.device_error()
+
+
+def test_fp4_tc_activation_outliers(nq):
+    """Activations up to the bf16 maximum times weights up to 2688: the 2^-20 in the decoded
+    weights keeps every group partial finite."""
+    T, K, N = 20, 1280, 160
+    p = si.fp4_problem(T, K, N, 630)
+    g = np.random.default_rng(631)
+    x = g.standard_normal((T, K)).astype(np.float32)
+    x[0, 5] = 3.0e38
+    x[1, :] *= 1.0e6
+    x[3, :] *= 1.0e-30
+    x[17, 700] = -2.0e37
+    xb = si.bf16_bits(x)
+    w = pack(nq, p, K, N)
+    y = gu.host_f64(nq.gemm_fp4(gu.dev_bf16(xb), *w, p["g"], N))
+    y_ref = oracle.gemm_fp4(xb, p["codes"], p["sf"], p["g"], T, K, N)
+    for t in range(T):
+        assert np.all(np.isfinite(y[t])), t
+        assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t

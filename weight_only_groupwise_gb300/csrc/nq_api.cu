@@ -465,7 +465,7 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     // Larger batches: the tensor-core kernel, one weight pass per matrix. A SwiGLU block is two
     // launches on the same X: the gate projection writes fp32 G to a library buffer, the up
     // projection's epilogue writes H = silu(G) * U in bf16.
-    if (g_tc && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
+    if (g_tc && (bits == 4 || bits == 5 || (bits == kFp4 && !swiglu)) && T > kSliceT && T <= kTcMaxT) {
         alignas(64) TcArgs ta;
         alignas(64) TcArgs tu;
         if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP) &&
@@ -484,6 +484,7 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
             ta.Y = static_cast<uint16_t*>(Y);
             ta.G = d->tc_gate;
             ta.mode = swiglu ? kTcOutGate : kTcOutY;
+            ta.gscale = gscale;
             ta.tickets = reinterpret_cast<int*>(d->tc_ws);
             ta.partials = reinterpret_cast<float*>(d->tc_ws + (((size_t)d->tc_tickets * 4 + 255) / 256) * 256);
             ta.dev_err = reinterpret_cast<int*>(d->ws);
@@ -979,7 +980,8 @@ int nq_tensor_core_batches(int enable) {
 
 nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t out[8]) {
     if (!out) return NQ_ERR_NULL;
-    if ((bits != 4 && bits != 5) || T <= kSliceT || T > kTcMaxT || num_sms < 1 || K < kGroup || N < kTileRows)
+    if ((bits != 4 && bits != 5 && bits != kFp4) || T <= kSliceT || T > kTcMaxT || num_sms < 1 || K < kGroup ||
+        N < kTileRows)
         return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;

@@ -1,5 +1,5 @@
-// Instantiations and host launch of the large-batch tensor-core projection kernel (nq_tc.cuh):
-// the activation tensor map and the launch.
+// Instantiations (4- and 5-bit codes) and host side of the large-batch tensor-core projection
+// kernel (nq_tc.cuh): the tensor maps and the launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -27,30 +27,6 @@ EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
-}
-
-template <int BITS, int TP>
-cudaError_t launch_t(const TcArgs& a, cudaStream_t stream, bool pdl) {
-    auto kern = tc_proj_kernel<BITS, TP>;
-    static thread_local int set_for_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (set_for_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-        if (e != cudaSuccess) return e;
-        set_for_device = dev;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.p.P);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = a.p.smem_bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
@@ -85,9 +61,10 @@ bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, con
     const cuuint64_t wdims[3] = {(cuuint64_t)(tb / 8), (cuuint64_t)G, (cuuint64_t)RT};
     const cuuint64_t wstr[2] = {(cuuint64_t)tb, (cuuint64_t)G * tb};
     const cuuint32_t wbox[3] = {(cuuint32_t)(tb / 8), (cuuint32_t)kTcStageGroups, (cuuint32_t)kTcTiles};
-    const cuuint64_t sdims[3] = {(cuuint64_t)(kScaleTileBytes / 8), (cuuint64_t)G, (cuuint64_t)RT};
-    const cuuint64_t sstr[2] = {(cuuint64_t)kScaleTileBytes, (cuuint64_t)G * kScaleTileBytes};
-    const cuuint32_t sbox[3] = {(cuuint32_t)(kScaleTileBytes / 8), (cuuint32_t)kTcStageGroups, (cuuint32_t)kTcTiles};
+    const int stb = scale_tile_bytes(bits);
+    const cuuint64_t sdims[3] = {(cuuint64_t)(stb / 8), (cuuint64_t)G, (cuuint64_t)RT};
+    const cuuint64_t sstr[2] = {(cuuint64_t)stb, (cuuint64_t)G * stb};
+    const cuuint32_t sbox[3] = {(cuuint32_t)(stb / 8), (cuuint32_t)kTcStageGroups, (cuuint32_t)kTcTiles};
     return fn(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(W), wdims, wstr, wbox, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
@@ -97,10 +74,11 @@ bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, con
 }
 
 cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl) {
+    if (bits == kFp4) return launch_tc_proj_fp4(a, stream, pdl);
     switch (a.p.TP) {
-        case 16: return bits == 4 ? launch_t<4, 16>(a, stream, pdl) : launch_t<5, 16>(a, stream, pdl);
-        case 32: return bits == 4 ? launch_t<4, 32>(a, stream, pdl) : launch_t<5, 32>(a, stream, pdl);
-        default: return bits == 4 ? launch_t<4, 64>(a, stream, pdl) : launch_t<5, 64>(a, stream, pdl);
+        case 16: return bits == 4 ? tc_launch<4, 16>(a, stream, pdl) : tc_launch<5, 16>(a, stream, pdl);
+        case 32: return bits == 4 ? tc_launch<4, 32>(a, stream, pdl) : tc_launch<5, 32>(a, stream, pdl);
+        default: return bits == 4 ? tc_launch<4, 64>(a, stream, pdl) : tc_launch<5, 64>(a, stream, pdl);
     }
 }
 

@@ -51,7 +51,8 @@ constexpr int kTcPair = 2;                        // groups per P buffer (one MM
 constexpr int kTcA = 2;                           // A buffers in TMEM (a stage: 128 columns each)
 constexpr int kTcPCols = 256;                     // TMEM columns of the P buffers (2 TP each)
 constexpr int kTcMaxP = kTcPCols / (kTcPair * 16);
-constexpr int kTcScaleExp = 12;                   // decoded weights carry 2^-12
+constexpr int kTcScaleExp = 12;                   // decoded 4/5-bit weights carry 2^-12
+constexpr int kTcFp4ScaleExp = 20;                // decoded NVFP4 weights carry 2^-20
 constexpr int kTcDecoders = 8;                    // decoder warps: one 16-row tile each
 constexpr int kTcEpilogue = 4;                    // epilogue warps: one TMEM lane quarter each
 constexpr int kTcWarps = 2 + kTcDecoders + kTcEpilogue;
@@ -64,7 +65,9 @@ constexpr int kTcOutY = 0, kTcOutGate = 1, kTcOutSwiglu = 2;
 
 // Shared-memory bytes of one stage: codes and scales of kTcTiles tiles x kTcStageGroups groups,
 // then the activation chunk (kTcStageGroups * 64 K x TP tokens, bf16).
-NQ_HD constexpr int tc_weight_bytes(int bits) { return kTcTiles * kTcStageGroups * (code_tile_bytes(bits) + kScaleTileBytes); }
+NQ_HD constexpr int tc_weight_bytes(int bits) {
+    return kTcTiles * kTcStageGroups * (code_tile_bytes(bits) + scale_tile_bytes(bits));
+}
 NQ_HD constexpr int tc_x_bytes(int TP) { return TP * kTcStageGroups * kGroup * 2; }
 NQ_HD constexpr int tc_stage_bytes(int bits, int TP) { return tc_weight_bytes(bits) + tc_x_bytes(TP); }
 // Alignment of the stages to 1024 bytes (the swizzle atom), then barriers and flags after them.
@@ -109,6 +112,7 @@ struct alignas(64) TcArgs {
     uint16_t* Y;             // bf16 [T][N] (output modes kTcOutY and kTcOutSwiglu)
     float* G;                // fp32 [T][N]: written (kTcOutGate) or read (kTcOutSwiglu)
     int mode;                // kTcOutY, kTcOutGate or kTcOutSwiglu
+    float gscale;            // NVFP4 tensor scale (applied with each group partial), else 1
     float* partials;         // RB * KS slots of kTcRows x TP floats (K split only)
     int* tickets;            // one per row block, zero between calls
     int* dev_err;
@@ -231,6 +235,22 @@ __device__ __forceinline__ void tc_decode(const uint4& w, uint32_t hb, uint32_t 
     for (int i = 0; i < 4; ++i) a[i] = bf16x2_sub(a[i], kOff);
 }
 
+// K step of a lane's NVFP4 code word (w: registers 0..3 of the mma.sync A fragment, rows r,
+// r + 8; sc: the e4m3 block scales of rows r (low byte) and r + 8) as four bf16x2 registers
+// holding e2m1 x e4m3 x 2^-20, exactly: the fp16 product has at most 6 significant bits and is
+// exact in bf16, and |e2m1 x e4m3| <= 2688 keeps 64 products with any finite bf16 activation
+// below 2^126 once scaled by 2^-20.
+__device__ __forceinline__ void tc_decode_fp4(uint32_t w, uint32_t sc, uint32_t a[4]) {
+    decode_fp4(w, sc, a);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = *reinterpret_cast<const __half2*>(&a[i]);
+        const float2 f = __half22float2(h);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * 0x1p-20f, f.y * 0x1p-20f);
+        a[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+}
+
 // One lane of a full warp returns true (the same lane every time the whole warp calls it).
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred = 0;
@@ -248,9 +268,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
     constexpr int BG = kTcStageGroups;
     static_assert(BG % kTcPair == 0 && BG / kTcPair == 2, "two P steps per stage");
-    static_assert((TB * kTcTiles * BG + kScaleTileBytes * kTcTiles * BG) % 1024 == 0 && (TP * 128) % 1024 == 0,
+    constexpr int STB = scale_tile_bytes(BITS);
+    constexpr bool FP4 = BITS == kFp4;
+    static_assert((TB * kTcTiles * BG + STB * kTcTiles * BG) % 1024 == 0 && (TP * 128) % 1024 == 0,
                   "activation blocks on 1024-byte boundaries");
-    constexpr int kWBytes = kTcTiles * BG * (TB + kScaleTileBytes);
+    constexpr int kWBytes = kTcTiles * BG * (TB + STB);
     constexpr int kXBytes = TP * BG * kGroup * 2;
     constexpr int kStageBytes = kWBytes + kXBytes;
     constexpr uint32_t kCols = 512;                   // TMEM columns: A buffers, then P buffers
@@ -355,11 +377,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 if (gl + gp >= ngroups) break;
                 const uint8_t* code = sb + ((gl + gp) % BG) * TB + lane * 16;
                 const uint4 w = *reinterpret_cast<const uint4*>(code);
-                const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
-                tc_decode<BITS, 0>(w, hb, r[gp] + 0);
-                tc_decode<BITS, 1>(w, hb, r[gp] + 4);
-                tc_decode<BITS, 2>(w, hb, r[gp] + 8);
-                tc_decode<BITS, 3>(w, hb, r[gp] + 12);
+                if constexpr (FP4) {
+                    // the lane's 8 block-scale bytes: rows r, r + 8 for each K step
+                    const uint2 sc = *reinterpret_cast<const uint2*>(stage_mem + st * kStageBytes + kTcTiles * BG * TB +
+                                                                     m * BG * STB + ((gl + gp) % BG) * STB + (lane >> 2) * 8);
+                    tc_decode_fp4(w.x, sc.x, r[gp] + 0);
+                    tc_decode_fp4(w.y, sc.x >> 16, r[gp] + 4);
+                    tc_decode_fp4(w.z, sc.y, r[gp] + 8);
+                    tc_decode_fp4(w.w, sc.y >> 16, r[gp] + 12);
+                } else {
+                    const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
+                    tc_decode<BITS, 0>(w, hb, r[gp] + 0);
+                    tc_decode<BITS, 1>(w, hb, r[gp] + 4);
+                    tc_decode<BITS, 2>(w, hb, r[gp] + 8);
+                    tc_decode<BITS, 3>(w, hb, r[gp] + 12);
+                }
             }
         };
         uint32_t ra[kTcPair][16], rb[kTcPair][16];
@@ -453,14 +485,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
             ok = mbar_wait(pfull0 + 8 * pb, (k / kP) & 1, flags, a.dev_err, wait_ns) && ok;
             tc_fence_after();
             if (ok) {
-                const uint8_t* sc = stage_mem + st * kStageBytes + kTcTiles * BG * TB + m * BG * kScaleTileBytes;
+                const uint8_t* sc = stage_mem + st * kStageBytes + kTcTiles * BG * TB + m * BG * STB;
                 const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb;
 #pragma unroll
                 for (int gp = 0; gp < kTcPair; ++gp) {
                     if (2 * k + gp >= ngroups) break;
-                    const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
-                                        sc + (gs0 + gp) * kScaleTileBytes + 2 * sidx))) *
-                                    (float)(1 << kTcScaleExp);
+                    // NVFP4: the block scales are in the decoded weights, which carry 2^-20; the
+                    // tensor scale g joins 2^20 here (exact), so that a partial is never
+                    // scaled up past what g brings back down
+                    const float s = FP4 ? (float)(1 << kTcFp4ScaleExp) * a.gscale
+                                        : __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(
+                                              sc + (gs0 + gp) * kScaleTileBytes + 2 * sidx))) *
+                                              (float)(1 << kTcScaleExp);
 #pragma unroll
                     for (int c = 0; c < TP; c += kChunk) {
                         uint32_t v[kChunk];
@@ -544,5 +580,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         tmem_dealloc(tmem, kCols);
     }
 }
+
+// ---------------------------------------------------------------- host launch
+
+// One launch of tc_proj_kernel<BITS, TP>: a block per plan block, programmatic dependent launch
+// when `pdl`. The shared-memory opt-in is set once per device and thread.
+template <int BITS, int TP>
+inline cudaError_t tc_launch(const TcArgs& a, cudaStream_t stream, bool pdl) {
+    auto kern = tc_proj_kernel<BITS, TP>;
+    static thread_local int set_for_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (set_for_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        set_for_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.p.P);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = a.p.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 
 }  // namespace nq
