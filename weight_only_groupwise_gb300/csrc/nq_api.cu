@@ -483,22 +483,22 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
             ta.S = static_cast<const uint8_t*>(S0);
             ta.Y = static_cast<uint16_t*>(Y);
             ta.G = d->tc_gate;
-            ta.mode = swiglu ? kTcOutGate : kTcOutY;
             ta.gscale = gscale;
             ta.tickets = reinterpret_cast<int*>(d->tc_ws);
             ta.partials = reinterpret_cast<float*>(d->tc_ws + (((size_t)d->tc_tickets * 4 + 255) / 256) * 256);
             ta.dev_err = reinterpret_cast<int*>(d->ws);
             ta.wait_ns = g_wait_ns;
-            if (launch_tc_proj(bits, ta, as_stream(stream), g_pdl) != cudaSuccess) return NQ_ERR_CUDA;
-            if (!swiglu) return NQ_OK;
+            if (!swiglu) return launch_tc_proj(bits, ta, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+            if (launch_tc_proj_swiglu(bits, kTcOutGate, ta, as_stream(stream), g_pdl) != cudaSuccess)
+                return NQ_ERR_CUDA;
             const CUtensorMap wmap = tu.wmap, smap = tu.smap;
             tu = ta;
             tu.wmap = wmap;
             tu.smap = smap;
             tu.W = static_cast<const uint8_t*>(W1);
             tu.S = static_cast<const uint8_t*>(S1);
-            tu.mode = kTcOutSwiglu;
-            return launch_tc_proj(bits, tu, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+            return launch_tc_proj_swiglu(bits, kTcOutSwiglu, tu, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK
+                                                                                                : NQ_ERR_CUDA;
         }
     }
     // At most two distinct slice sizes: full slices and the remainder.

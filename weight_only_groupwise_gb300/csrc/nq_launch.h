@@ -14,6 +14,8 @@ bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP);
 bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N);
 cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc_proj_fp4(const TcArgs& a, cudaStream_t stream, bool pdl);
+// The two launches of a SwiGLU block (mode kTcOutGate, then kTcOutSwiglu), 4- or 5-bit codes.
+cudaError_t launch_tc_proj_swiglu(int bits, int mode, const TcArgs& a, cudaStream_t stream, bool pdl);
 
 // Bound of every device-side wait for later launches (nq_wait_limit; NQ_WAIT_NS).
 unsigned long long wait_limit_ns();
