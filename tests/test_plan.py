@@ -174,7 +174,8 @@ def test_one_slab_k_limits_stated_in_header(nq, T, k_max):
 
 
 @pytest.mark.parametrize("bits,T,K,N", [(4, 64, 5120, 17408), (5, 16, 5120, 6144), (4, 33, 17408, 5120),
-                                        (5, 9, 64, 16), (4, 64, 192, 4096), (5, 48, 6208, 1040)])
+                                        (5, 9, 64, 16), (4, 64, 192, 4096), (5, 48, 6208, 1040),
+                                        (14, 40, 5120, 17408), (14, 64, 512, 144)])
 @pytest.mark.parametrize("sms", [152, 148, 7])
 def test_tc_plan(nq, bits, T, K, N, sms):
     """The tensor-core kernel's split: every (row block, K piece) is one block, the pieces of a

@@ -1,8 +1,10 @@
 // nq_tc.cuh -- the large-batch projection kernel: Y[T,N] = X[T,K] * dequant(W) for
 // 8 < T <= 64 tokens (several concurrent requests' speculative-verify rows: "ninfer-ext"
 // README, section "与原版 NInfer 的对比", C = 1..8 requests; "NInfer-4090" post, section
-// "实测数据", C2/C4/C8), 4- or 5-bit codes with one fp16 scale per 64-wide K group, on the
-// fifth-generation tensor cores (tcgen05) so that the weights stream from HBM once whatever T.
+// "实测数据", C2/C4/C8), 4- or 5-bit codes with one fp16 scale per 64-wide K group or NVFP4
+// weights, on the fifth-generation tensor cores (tcgen05) so that the weights stream from HBM
+// once whatever T. A SwiGLU block is two launches (the output-mode template argument): the
+// gate projection writes fp32 G, the up projection writes bf16 silu(G) * U.
 //
 // One block per (128-row block, K piece), 14 warps, in steps of two 64-wide groups:
 //   * warp 0, one lane -- producer: per stage (kTcStageGroups groups) three 3-D TMA copies:
