@@ -469,8 +469,8 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
         alignas(64) TcArgs ta;
         alignas(64) TcArgs tu;
         if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP) &&
-            encode_weight_maps(&ta.wmap, &ta.smap, W0, S0, bits, K, N) &&
-            (!swiglu || encode_weight_maps(&tu.wmap, &tu.smap, W1, S1, bits, K, N))) {
+            encode_weight_maps(&ta.wmap, &ta.smap, W0, S0, bits, K, N, ta.p.TP) &&
+            (!swiglu || encode_weight_maps(&tu.wmap, &tu.smap, W1, S1, bits, K, N, ta.p.TP))) {
             st = ensure_workspace(*d, 1, 1);
             if (st != NQ_OK) return st;
             st = ensure_tc_workspace(*d, ta.p.RB, ta.p.KS > 1 ? (long long)ta.p.P * kTcRows * ta.p.TP : 1);
@@ -994,7 +994,7 @@ nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t ou
     out[4] = p.stages;
     out[5] = p.smem_bytes;
     out[6] = p.G;
-    out[7] = kTcStageGroups;
+    out[7] = tc_stage_groups(p.TP);
     return NQ_OK;
 }
 

@@ -11,7 +11,8 @@ namespace nq {
 // Large-batch tensor-core kernel (nq_tc.cuh): the activation tensor map (false if the driver
 // entry point is missing or rejects the view) and the launch.
 bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP);
-bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N);
+bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N,
+                        int TP);
 cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc_proj_fp4(const TcArgs& a, cudaStream_t stream, bool pdl);
 // The two launches of a SwiGLU block (mode kTcOutGate, then kTcOutSwiglu), 4- or 5-bit codes.

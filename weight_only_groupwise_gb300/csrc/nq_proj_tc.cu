@@ -31,7 +31,8 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// X (bf16 [T][K], row-major) as a 3-D tensor [K/64][T][64]: a box {64, TP, kTcStageGroups} lands
+// X (bf16 [T][K], row-major) as a 3-D tensor [K/64][T][64]: a box {64, TP, BG} (BG = the
+// stage's groups) lands
 // in shared memory as one [TP][64] block per group, 128-byte rows with the 128-byte swizzle
 // (16-byte chunk c of token t at chunk c ^ (t % 8)), which is the tensor core's K-major
 // swizzled layout; tokens T..TP-1 are outside the tensor and read as zeros. 128-byte rows keep
@@ -41,7 +42,7 @@ bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP) {
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)kGroup, (cuuint64_t)T, (cuuint64_t)(K / kGroup)};
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kGroup * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kGroup, (cuuint32_t)TP, (cuuint32_t)kTcStageGroups};
+    const cuuint32_t box[3] = {(cuuint32_t)kGroup, (cuuint32_t)TP, (cuuint32_t)tc_stage_groups(TP)};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(X), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -49,10 +50,12 @@ bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP) {
 }
 
 // The packed codes and scales of a matrix as 3-D tensors of 8-byte elements [RT][G][bytes / 8]
-// (16-row tiles, 64-wide K groups, one tile-group block): a box {bytes / 8, kTcStageGroups,
-// kTcTiles} is one stage's codes (or scales) of a 128-row block, laid out tile-major as the
-// kernel reads them; tiles past RT and groups past G read as zeros.
-bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N) {
+// (16-row tiles, 64-wide K groups, one tile-group block): a box {bytes / 8, BG, kTcTiles} (BG =
+// the stage's groups for TP padded tokens) is one stage's codes (or scales) of a 128-row
+// block, laid out tile-major as the kernel reads them; tiles past RT and groups past G read as
+// zeros.
+bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N,
+                        int TP) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int G = K / kGroup, RT = N / kTileRows;
@@ -60,11 +63,12 @@ bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, con
     const int tb = code_tile_bytes(bits);
     const cuuint64_t wdims[3] = {(cuuint64_t)(tb / 8), (cuuint64_t)G, (cuuint64_t)RT};
     const cuuint64_t wstr[2] = {(cuuint64_t)tb, (cuuint64_t)G * tb};
-    const cuuint32_t wbox[3] = {(cuuint32_t)(tb / 8), (cuuint32_t)kTcStageGroups, (cuuint32_t)kTcTiles};
+    const cuuint32_t bg = (cuuint32_t)tc_stage_groups(TP);
+    const cuuint32_t wbox[3] = {(cuuint32_t)(tb / 8), bg, (cuuint32_t)kTcTiles};
     const int stb = scale_tile_bytes(bits);
     const cuuint64_t sdims[3] = {(cuuint64_t)(stb / 8), (cuuint64_t)G, (cuuint64_t)RT};
     const cuuint64_t sstr[2] = {(cuuint64_t)stb, (cuuint64_t)G * stb};
-    const cuuint32_t sbox[3] = {(cuuint32_t)(stb / 8), (cuuint32_t)kTcStageGroups, (cuuint32_t)kTcTiles};
+    const cuuint32_t sbox[3] = {(cuuint32_t)(stb / 8), bg, (cuuint32_t)kTcTiles};
     return fn(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(W), wdims, wstr, wbox, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&

@@ -6,24 +6,27 @@
 // once whatever T. A SwiGLU block is two launches (the output-mode template argument): the
 // gate projection writes fp32 G, the up projection writes bf16 silu(G) * U.
 //
-// One block per (128-row block, K piece), 14 warps, in steps of two 64-wide groups:
-//   * warp 0, one lane -- producer: per stage (kTcStageGroups groups) three 3-D TMA copies:
-//     the codes and the scales of the eight 16-row tiles (tiles and groups past the matrix
-//     read as zeros), and the stage's activation chunk, one [TP][64] block per group in the tensor core's K-major 128-byte-swizzled
-//     layout, tokens past T filled with zeros by the copy. A ring of shared-memory stages
-//     (1024-byte aligned), mbarriers.
+// One block per (128-row block, K piece), 14 warps. Work moves between the warp roles in
+// stages of BG 64-wide K groups (six for TP <= 32 padded tokens, four for TP = 64: the TMEM
+// budget), one hand-off per stage:
+//   * warp 0, one lane -- producer: per stage three 3-D TMA copies: the codes and the scales of
+//     the eight 16-row tiles (tiles and groups past the matrix read as zeros), and the stage's
+//     activation chunk, one [TP][64] block per group in the tensor core's K-major
+//     128-byte-swizzled layout, tokens past T filled with zeros by the copy. A ring of
+//     shared-memory stages (1024-byte aligned), mbarriers.
 //   * warps 1..8 -- decoders: warp w owns one 16-row tile, TMEM lanes 32 (w % 4) + 16 h .. + 15
 //     (h = 0 for warps 1..4, 1 for 5..8). A lane decodes its fragment words of a group into
 //     bf16 (q - z) 2^-12, exact, and stores all four K steps with one tcgen05.st.16x128b.x8,
 //     which places the mma.sync A-fragment registers of lane t at TMEM lanes t/4, t/4 + 8 and
-//     columns 8 j + t%4, 8 j + 4 + t%4: K in natural order, one row per TMEM lane. A buffer
-//     holds a step (2 groups, 64 columns). Software-pipelined: the next step is loaded and
-//     decoded while the current step's stores complete.
+//     columns 8 j + t%4, 8 j + 4 + t%4: K in natural order, one row per TMEM lane. An A buffer
+//     holds a stage (32 columns a group); two alternate. Groups are decoded in pairs, each pair
+//     into registers of its own, so that a pair decodes while the stores of the pairs before it
+//     complete.
 //   * warp 9 -- MMA issuer (the whole warp runs the loop, one elected lane issues): per group,
 //     four tcgen05.mma.kind::f16 (M = 128, N = TP, K = 16; A from TMEM, B = the activation
 //     chunk through a shared-memory descriptor; D in TMEM, fp32, a fresh accumulator per group:
-//     P = 2^-12 sum over the group of (q - z) x), then per step tcgen05.commit to the barriers
-//     that free the A buffer and publish the step's two P.
+//     P = 2^-12 sum over the group of (q - z) x); per pair of groups a tcgen05.commit publishes
+//     their two P (a P buffer), per stage one frees the A buffer and the shared-memory stage.
 //   * warps 10..13 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
 //     adds 2^12 s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y,
 //     or, when K is split across blocks, an fp32 partial; the last block of a row block
@@ -47,12 +50,11 @@ namespace nq {
 
 constexpr int kTcRows = 128;                      // rows per block = MMA M
 constexpr int kTcTiles = kTcRows / kTileRows;     // 16-row tiles per block
-constexpr int kTcStageGroups = 4;                 // 64-wide K groups per pipeline stage
 constexpr int kTcMaxStages = 8;
-constexpr int kTcPair = 2;                        // groups per P buffer (one MMA-to-epilogue hand-off)
-constexpr int kTcA = 2;                           // A buffers in TMEM (a stage: 128 columns each)
-constexpr int kTcPCols = 256;                     // TMEM columns of the P buffers (2 TP each)
-constexpr int kTcMaxP = kTcPCols / (kTcPair * 16);
+constexpr int kTcPair = 2;                        // groups per decode step and per P buffer
+constexpr int kTcA = 2;                           // A buffers in TMEM (a stage: 32 columns a group)
+constexpr int kTcCols = 512;                      // TMEM columns: A buffers, then P buffers
+constexpr int kTcMaxP = 8;
 constexpr int kTcScaleExp = 12;                   // decoded 4/5-bit weights carry 2^-12
 constexpr int kTcFp4ScaleExp = 20;                // decoded NVFP4 weights carry 2^-20
 constexpr int kTcDecoders = 8;                    // decoder warps: one 16-row tile each
@@ -67,13 +69,20 @@ constexpr int kTcMinT = 9, kTcMaxT = 64;
 // code (measured +5 % at TP = 16 and +16 % at TP = 64 on plain projections).
 constexpr int kTcOutY = 0, kTcOutGate = 1, kTcOutSwiglu = 2;
 
-// Shared-memory bytes of one stage: codes and scales of kTcTiles tiles x kTcStageGroups groups,
-// then the activation chunk (kTcStageGroups * 64 K x TP tokens, bf16).
-NQ_HD constexpr int tc_weight_bytes(int bits) {
-    return kTcTiles * kTcStageGroups * (code_tile_bytes(bits) + scale_tile_bytes(bits));
+// 64-wide K groups per pipeline stage (one hand-off between the warp roles). Six while the P
+// buffers of two groups fit beside two six-group A buffers (2 x 192 + 2 x 2 TP <= 512 TMEM
+// columns: TP <= 32), else four, which leaves the 64-token kernel its four stages.
+NQ_HD constexpr int tc_stage_groups(int TP) { return TP <= 32 ? 6 : 4; }
+// Shared-memory bytes of one stage: codes and scales of kTcTiles tiles x BG groups, then the
+// activation chunk (BG * 64 K x TP tokens, bf16).
+NQ_HD constexpr int tc_weight_bytes(int bits, int TP) {
+    return kTcTiles * tc_stage_groups(TP) * (code_tile_bytes(bits) + scale_tile_bytes(bits));
 }
-NQ_HD constexpr int tc_x_bytes(int TP) { return TP * kTcStageGroups * kGroup * 2; }
-NQ_HD constexpr int tc_stage_bytes(int bits, int TP) { return tc_weight_bytes(bits) + tc_x_bytes(TP); }
+NQ_HD constexpr int tc_x_bytes(int TP) { return TP * tc_stage_groups(TP) * kGroup * 2; }
+// The weights of a stage padded to 1024 bytes: the activation chunk after them starts on a
+// 1024-byte boundary (the swizzle atom).
+NQ_HD constexpr int tc_weight_region(int bits, int TP) { return (tc_weight_bytes(bits, TP) + 1023) / 1024 * 1024; }
+NQ_HD constexpr int tc_stage_bytes(int bits, int TP) { return tc_weight_region(bits, TP) + tc_x_bytes(TP); }
 // Alignment of the stages to 1024 bytes (the swizzle atom), then barriers and flags after them.
 NQ_HD constexpr int tc_extra_bytes(int) { return 2048; }
 NQ_HD constexpr int tc_stages(int bits, int TP) {
@@ -97,7 +106,8 @@ NQ_HD bool make_tc_plan(int bits, int T, int K, int N, int num_sms, TcPlan& p) {
     p.RT = N / kTileRows;
     p.RB = (N + kTcRows - 1) / kTcRows;
     int ks = num_sms / (p.RB > 0 ? p.RB : 1);
-    const int max_ks = p.G / (2 * kTcStageGroups) > 0 ? p.G / (2 * kTcStageGroups) : 1;  // >= 8 groups a piece
+    const int sg = tc_stage_groups(p.TP);
+    const int max_ks = p.G / (2 * sg) > 0 ? p.G / (2 * sg) : 1;  // >= 2 stages a piece
     if (ks > max_ks) ks = max_ks;
     if (ks < 1) ks = 1;
     p.KS = ks;
@@ -269,19 +279,24 @@ template <int BITS, int TP, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_constant__ TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
-    constexpr int BG = kTcStageGroups;
-    static_assert(BG % kTcPair == 0 && BG / kTcPair == 2, "two P steps per stage");
+    constexpr int BG = tc_stage_groups(TP);
+    static_assert(BG % kTcPair == 0, "decoder pairs tile a stage");
     constexpr int STB = scale_tile_bytes(BITS);
     constexpr bool FP4 = BITS == kFp4;
-    static_assert((TB * kTcTiles * BG + STB * kTcTiles * BG) % 1024 == 0 && (TP * 128) % 1024 == 0,
-                  "activation blocks on 1024-byte boundaries");
-    constexpr int kWBytes = kTcTiles * BG * (TB + STB);
+    constexpr int kWBytes = kTcTiles * BG * (TB + STB);     // codes, then scales
+    constexpr int kWRegion = tc_weight_region(BITS, TP);    // padded: X starts 1024-aligned
     constexpr int kXBytes = TP * BG * kGroup * 2;
-    constexpr int kStageBytes = kWBytes + kXBytes;
-    constexpr uint32_t kCols = 512;                   // TMEM columns: A buffers, then P buffers
-    constexpr int kAStage = BG * 32, kPCols = kTcPair * TP;  // TMEM columns of an A buffer, a P buffer
-    constexpr int kP = kTcPCols / kPCols;             // P buffers: 8, 4, 2 for TP = 16, 32, 64
-    static_assert(kTcA * kAStage + kTcPCols <= (int)kCols && kP >= 2 && kP <= kTcMaxP, "TMEM budget");
+    constexpr int kStageBytes = kWRegion + kXBytes;
+    static_assert(kWRegion % 1024 == 0 && kWRegion >= kWBytes && (TP * 128) % 1024 == 0,
+                  "activation blocks on 1024-byte boundaries");
+    constexpr uint32_t kCols = kTcCols;
+    // TMEM columns of an A buffer (a stage) and of a P buffer (kPG groups: one MMA-to-epilogue
+    // hand-off); P buffers: 4, 2, 2 for TP = 16, 32, 64
+    constexpr int kPG = kTcPair, kPSteps = BG / kPG;
+    static_assert(BG % kPG == 0, "P steps tile a stage");
+    constexpr int kAStage = BG * 32, kPCols = kPG * TP;
+    constexpr int kP = (kTcCols - kTcA * kAStage) / kPCols;
+    static_assert(kP >= 2 && kP <= kTcMaxP, "TMEM budget");
     constexpr uint32_t kIdesc = tc_idesc_bf16(TP);
     constexpr int kDec = kTcDecoders, kEpi = kTcEpilogue;
     constexpr int kMmaWarp = 1 + kDec;
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     const int g0 = (int)((long long)kp * p.G / p.KS), g1 = (int)((long long)(kp + 1) * p.G / p.KS);
     const int ngroups = g1 - g0;
     const int nst = (ngroups + BG - 1) / BG;          // stages this block streams
-    const int nsteps = (ngroups + kTcPair - 1) / kTcPair;
+    const int nsteps = (ngroups + kPG - 1) / kPG;    // P steps
     const uint64_t wait_ns = a.wait_ns;
 
     uint8_t* stage_mem = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
@@ -332,8 +347,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     const uint32_t tmem = (uint32_t)flags[3];
     const uint32_t a_col0 = 0, p_col0 = kTcA * kAStage;
 
-    // Step k covers groups 2k, 2k+1 of the block (the second may be past its end), both in
-    // stage k / 2 at positions gs0 = 2 (k % 2), gs0 + 1.
+    // P step k covers groups kPG k .. kPG k + kPG - 1 of the block (the last may be past its
+    // end), all in stage k / kPSteps from position gs0 = kPG (k % kPSteps).
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -349,13 +364,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 const int g = g0 + si * BG;
                 uint8_t* sb = stage_mem + st * kStageBytes;
                 const uint32_t fb = full0 + 8 * st;
-                mbar_arrive_expect_tx(fb, (uint32_t)kStageBytes);  // whole boxes, zeros included
+                mbar_arrive_expect_tx(fb, (uint32_t)(kWBytes + kXBytes));  // whole boxes, zeros included
                 tma_load_3d_hint(smem_u32(sb), &a.wmap, 0, g, rb * kTcTiles, fb, pol);
                 tma_load_3d_hint(smem_u32(sb + kTcTiles * BG * TB), &a.smap, 0, g, rb * kTcTiles, fb, pol);
                 // the weights are never written by a kernel that lets its dependents start
                 // early; X may be the preceding kernel's output
                 if (si == 0) grid_dependency_wait();
-                tma_load_3d(smem_u32(sb + kWBytes), &a.xmap, 0, 0, g, fb);
+                tma_load_3d(smem_u32(sb + kWRegion), &a.xmap, 0, 0, g, fb);
                 ++it;
             }
             if (!ok) {
@@ -397,24 +412,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 }
             }
         };
-        uint32_t ra[kTcPair][16], rb[kTcPair][16];
-        bool ok = true;
+        uint32_t r[BG / kTcPair][kTcPair][16];           // one register set per pair: none is
+        bool ok = true;                                  // rewritten while its stores may be in flight
         for (int si = 0; si < nst; ++si) {
-            // one stage per hand-off: its four groups go to A buffer si % kTcA (128 columns)
+            // one stage per hand-off: its BG groups go to A buffer si % kTcA (32 columns a group)
             const int st = si % nstages, ab = si % kTcA, gl = si * BG;
             ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns) && ok;
             if (si >= kTcA) ok = mbar_wait(aempty0 + 8 * ab, ((si / kTcA) - 1) & 1, flags, a.dev_err, wait_ns) && ok;
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
                 const uint32_t base = lane_base + kAStage * ab;
-                decode_pair(st, gl, ra);
 #pragma unroll
-                for (int gp = 0; gp < kTcPair; ++gp)
-                    if (gl + gp < ngroups) tmem_st_group(base + 32 * gp, ra[gp]);
-                decode_pair(st, gl + kTcPair, rb);     // while the first pair's stores complete
+                for (int pr = 0; pr < BG / kTcPair; ++pr) {
+                    // a pair decodes while the stores of the pairs before it complete
+                    const int g = gl + kTcPair * pr;
+                    decode_pair(st, g, r[pr]);
 #pragma unroll
-                for (int gp = 0; gp < kTcPair; ++gp)
-                    if (gl + kTcPair + gp < ngroups) tmem_st_group(base + 32 * (kTcPair + gp), rb[gp]);
+                    for (int gp = 0; gp < kTcPair; ++gp)
+                        if (g + gp < ngroups) tmem_st_group(base + 32 * (kTcPair * pr + gp), r[pr][gp]);
+                }
             }
             __syncwarp();
             mbar_arrive_if(empty0 + 8 * st, lane == 0);  // the stage's codes are all in registers
@@ -433,12 +449,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t xbase = smem_u32(stage_mem + st * kStageBytes + kWBytes);
+            const uint32_t xbase = smem_u32(stage_mem + st * kStageBytes + kWRegion);
             const uint32_t a0 = tmem + a_col0 + kAStage * ab;
             const bool leader = elect_one();
 #pragma unroll
-            for (int hh = 0; hh < BG / kTcPair; ++hh) {
-                const int k = (BG / kTcPair) * si + hh;  // P step: groups 2k, 2k + 1 of the block
+            for (int hh = 0; hh < kPSteps; ++hh) {
+                const int k = kPSteps * si + hh;         // P step: groups kPG k .. kPG k + kPG - 1
                 if (k >= nsteps) break;
                 const int pb = k % kP;
                 if (k >= kP) ok = mbar_wait(pempty0 + 8 * pb, ((k / kP) - 1) & 1, flags, a.dev_err, wait_ns);
@@ -446,11 +462,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem + p_col0 + kPCols * pb;
-                const int ng = 2 * k + 1 < ngroups ? 2 : 1;
 #pragma unroll
-                for (int gp = 0; gp < kTcPair; ++gp) {
-                    if (gp >= ng) break;
-                    const int gs = kTcPair * hh + gp;    // position in the stage
+                for (int gp = 0; gp < kPG; ++gp) {
+                    if (kPG * k + gp >= ngroups) break;
+                    const int gs = kPG * hh + gp;        // position in the stage
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         // K step j of group gs: bytes 32 j .. 32 j + 31 of the group block's rows
@@ -480,19 +495,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         for (int t = 0; t < TP; ++t) acc[t] = 0.f;
         constexpr int kChunk = TP < 32 ? TP : 32;      // columns loaded before one wait
         for (int k = 0; k < nsteps; ++k) {
-            const int si = k / 2, gs0 = kTcPair * (k % 2), st = si % nstages;
+            const int si = k / kPSteps, hh = k % kPSteps, gs0 = kPG * hh, st = si % nstages;
             const int pb = k % kP;
-            const bool last = k % 2 == 1 || k == nsteps - 1;
+            const bool last = hh == kPSteps - 1 || k == nsteps - 1;
             bool ok = true;
-            if (k % 2 == 0) ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
+            if (hh == 0) ok = mbar_wait(full0 + 8 * st, (si / nstages) & 1, flags, a.dev_err, wait_ns);
             ok = mbar_wait(pfull0 + 8 * pb, (k / kP) & 1, flags, a.dev_err, wait_ns) && ok;
             tc_fence_after();
             if (ok) {
                 const uint8_t* sc = stage_mem + st * kStageBytes + kTcTiles * BG * TB + m * BG * STB;
                 const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb;
 #pragma unroll
-                for (int gp = 0; gp < kTcPair; ++gp) {
-                    if (2 * k + gp >= ngroups) break;
+                for (int gp = 0; gp < kPG; ++gp) {
+                    if (kPG * k + gp >= ngroups) break;
                     // NVFP4: the block scales are in the decoded weights, which carry 2^-20; the
                     // tensor scale g joins 2^20 here (exact), so that a partial is never
                     // scaled up past what g brings back down
