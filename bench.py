@@ -334,6 +334,51 @@ def stack_step(nq, layers, T: int, dev, grouped: bool):
     return step, (x, x6, h, yd, yq, ykv, yo)
 
 
+def stack_program(nq, layers, T: int, dev):
+    """The calls of stack_step (grouped) recorded once into a library program (nq_program_*),
+    replayed by one graph launch per pass."""
+    import torch
+    import seeded_inputs as si
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(12345)
+    x = si.device_activations(T, 5120, gen, dev)
+    x6 = si.device_activations(T, 6144, gen, dev)
+    h = torch.empty((T, 17408), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty((T, 5120), dtype=torch.bfloat16, device=dev)
+    yq = torch.empty((T, 6144), dtype=torch.bfloat16, device=dev)
+    ykv = torch.empty((T, 1024), dtype=torch.bfloat16, device=dev)
+    yo = torch.empty((T, 5120), dtype=torch.bfloat16, device=dev)
+    prog = nq.Program()
+    for ly in layers:
+        prog.swiglu_q4(x, *ly["gate"], *ly["up"], 17408, out=h)
+        prog.gemm_q4(h, *ly["down"], 5120, out=yd)
+        prog.grouped_q5(x, [(*ly["qg"], 6144), (*ly["kv"], 1024)], outs=[yq, ykv])
+        prog.gemm_q5(x6, *ly["out"], 5120, out=yo)
+    prog.build()
+    return prog
+
+
+def time_launches(launch, steps: int, warmup: int, stream, reps: int = 5):
+    """`warmup` untimed calls of launch(), then `reps` timed runs of `steps` calls, each
+    bracketed by CUDA events on `stream`. Returns the run times in milliseconds."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            launch()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                launch()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
 def time_graph(step, steps: int, warmup: int, stream, soak_s: float = 0.0, reps: int = 5):
     """Eager warm-up, capture `steps` steps into one CUDA graph, replay it untimed (and for
     `soak_s` seconds), then time `reps` replays, each bracketed by CUDA events on the
@@ -600,11 +645,11 @@ def main():
 
 def sweep(nq, dev, stream, peak):
     """µs/call and GB/s of the other shapes (context, not the headline): the decode Q4 and
-    verify Q5 projections at every T = 1..8 and at T = 16, 32, 64 (larger verify batches, one
-    launch per 8-token slice; GB/s counts the weights once) with one weight set per shape,
-    reused across T; the
-    Q4 and Q5 SwiGLU blocks at T=8 and the 64-layer stack at T = 1 and 8. Each entry is the
-    median of 5 timed graph replays."""
+    verify Q5 projections at every T = 1..8 and at T = 16, 32, 64 (larger verify batches, on
+    the tensor-core kernel) with one weight set per shape, reused across T; NVFP4 on the
+    decode shape; the Q4 and Q5 SwiGLU blocks at T=8 and the Q4 block at T = 16 and 64; the
+    64-layer stack at T = 1 and 8, grouped, ungrouped and as one recorded library program.
+    Each entry is the median of 5 timed runs (graph replays, or program launches)."""
     import torch
     out = []
 
@@ -662,6 +707,13 @@ def sweep(nq, dev, stream, peak):
             record("layer_stack" if grouped else "layer_stack_ungrouped", T, time_graph(step, 2, 1, stream), 2,
                    workload_bytes(w), launches_per_step(w) + (0 if grouped else w["layers"]))
             del step, keep
+        # the same pass recorded once as a library program (one graph launch per pass)
+        prog = stack_program(nq, layers, T, dev)
+        kernels = prog.info()["kernels"]
+        record("layer_stack_program", T, time_launches(lambda: prog.launch(stream), 2, 1, stream), 2,
+               workload_bytes(w), kernels)
+        prog.close()
+        del prog
     del layers
     torch.cuda.empty_cache()
     return out

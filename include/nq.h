@@ -278,6 +278,95 @@ nq_status nq_dequant_q5_debug(const void* Wq, const void* S, float* out, int K, 
 nq_status nq_dequant_q4_debug_bf16(const void* Wq, const void* S, float* out, int K, int N, void* stream);
 nq_status nq_dequant_q5_debug_bf16(const void* Wq, const void* S, float* out, int K, int N, void* stream);
 
+/* ---------------------------------------------------------------- recorded programs */
+
+/*
+ * A program: a sequence of projection calls (a decoder layer, or a stack of layers) recorded
+ * once and replayed as one CUDA graph. The pages run decode through CUDA graphs ("ninfer-ext"
+ * README, section "推荐设置": keep CUDA graphs on; NInfer digest, section "项目定位": the
+ * engine uses CUDA graphs in the decode phase; "NInfer-4090" post, section "快速启动": the
+ * graphs are built once at start-up, outside the steady-state decode time). A program is that
+ * step for this library's calls: every launch of every recorded call is captured in the
+ * recorded order, with the work split, tensor maps and workspace addresses fixed at build
+ * time, and nq_program_launch then costs one graph launch instead of one host call per kernel.
+ *
+ * What a program fixes and what it does not:
+ *   - It records the DEVICE ADDRESSES of X, the packed weights and the outputs, not their
+ *     contents: a launch reads whatever X holds at that point (write the next token's
+ *     activations into the same buffer, then launch again). The buffers must stay allocated
+ *     while the program can be launched; the library never frees them.
+ *   - Shapes (T, K, N) are fixed; a different token count needs another program.
+ *   - The library settings in force at build time are baked in: tensor-core batches
+ *     (nq_tensor_core_batches), slab clusters, the wait bound (nq_wait_limit) and the
+ *     dependent-launch mode.
+ *   - The per-device workspace addresses are baked in as well. nq_program_build reserves the
+ *     workspace for every recorded call first (as nq_reserve), so that capture allocates
+ *     nothing. If the workspace is later reallocated (a larger call or nq_reserve grew it,
+ *     or nq_shutdown freed it), the next nq_program_launch builds the program again before
+ *     launching it (nq_program_info counts the builds).
+ *   - A program belongs to the device that was current when it was built; launching it with
+ *     another current device returns NQ_ERR_DEVICE.
+ *   - One program must not be used by several host threads at once. Programs, like the
+ *     projection calls themselves, share the device workspace: launches that overlap in time
+ *     (different streams, no ordering) race. Order them on one stream.
+ *
+ * Results are those of making the recorded calls, in order, on one stream: the kernels are
+ * deterministic, so a replay writes the same bits as the eager calls.
+ */
+typedef struct nq_program nq_program;
+
+/* nq_program_create: a new, empty program in *out (host memory only; no CUDA call).
+ * NQ_ERR_NULL if out is NULL; NQ_ERR_CUDA if the host allocation fails. */
+nq_status nq_program_create(nq_program** out);
+
+/*
+ * Recording calls: append one projection call to the program. Arguments, layouts and
+ * ownership are those of the call named (nq_gemm_q4 / nq_gemm_q5 for bits 4 / 5,
+ * nq_gemm_fp4, nq_swiglu_q4 / nq_swiglu_q5, nq_gemm_q4_grouped / nq_gemm_q5_grouped), without
+ * the stream. Every host-side check of that call runs here, on the host and without a GPU
+ * (shape, NULL, alignment, aliasing: the same status codes); a call that fails them is not
+ * recorded. An empty call (T == 0 or N == 0) is accepted and records nothing. Recording into
+ * a program that was built marks it for building again. The grouped call copies `groups`.
+ */
+nq_status nq_program_gemm(nq_program* prog, int bits, const void* X, const void* Wq, const void* S, void* Y, int T,
+                          int K, int N);
+nq_status nq_program_gemm_fp4(nq_program* prog, const void* X, const void* Wq, const void* S, float global_scale,
+                              void* Y, int T, int K, int N);
+nq_status nq_program_swiglu(nq_program* prog, int bits, const void* X, const void* Wg, const void* Sg,
+                            const void* Wu, const void* Su, void* H, int T, int K, int N);
+nq_status nq_program_grouped(nq_program* prog, int bits, const void* X, const nq_group* groups, int count, int T,
+                             int K);
+
+/*
+ * nq_program_build: reserve the current device's workspace for every recorded call, capture
+ * the calls in order into a CUDA graph (on a stream the program owns) and instantiate it.
+ * Synchronises the device when the workspace has to grow. On an error from a recorded call
+ * the capture is abandoned, nothing has run, and that status is returned (nq_program_info
+ * names the call). A program with no recorded calls builds to an empty graph.
+ */
+nq_status nq_program_build(nq_program* prog);
+
+/*
+ * nq_program_launch: launch the program's graph on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream), asynchronously, building it first if it has not been built or the
+ * workspace has moved since. Errors: NQ_ERR_NULL, NQ_ERR_DEVICE (another device is current),
+ * a build error, NQ_ERR_CUDA. A bounded device-side wait that runs out is reported by
+ * nq_device_error, as for the eager calls.
+ */
+nq_status nq_program_launch(nq_program* prog, void* stream);
+
+/*
+ * nq_program_info: out[0] recorded calls, out[1] kernel launches in the built graph (0 if not
+ * built), out[2] builds so far, out[3] index of the recorded call whose error ended the last
+ * build, or -1. No GPU needed.
+ */
+nq_status nq_program_info(const nq_program* prog, int64_t out[4]);
+
+/* nq_program_destroy: free the program's graph, its stream and its records. Does not
+ * synchronise: a launch still in flight completes, and its graph is freed after it. NULL is
+ * ignored. The recorded buffers are untouched. */
+void nq_program_destroy(nq_program* prog);
+
 /* ---------------------------------------------------------------- runtime */
 
 /*

@@ -1,0 +1,183 @@
+"""Recorded programs on the GPU: a decoder layer's projection calls (fused gate/up SwiGLU, the
+down projection, the grouped q-gate/kv projections, the out projection, an NVFP4 projection)
+recorded once and replayed as one CUDA graph write the same bits as the same calls made
+eagerly on one stream, and the H of the replay matches the fp64 oracle. A replay reads X as
+it is at launch time; a moved workspace makes the next launch build again."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+K, NH, NQ, NKV, KO = 640, 1088, 384, 64, 384   # a small layer: hidden 640, MLP 1088
+
+
+@pytest.fixture(scope="module")
+def nq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from weight_only_groupwise_gb300 import build
+    build.build()
+    from weight_only_groupwise_gb300 import nq
+    return nq
+
+
+def weights(nq, bits, K_, N_, seed):
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    wn = si.device_code_words(N_, K_ // 8, gen, dev)
+    if bits == 5:
+        wh = si.device_code_words(N_, K_ // 32, gen, dev)
+    s = si.device_scales(N_, K_, gen, dev)
+    return nq.pack_q4(wn, s, K_, N_) if bits == 4 else nq.pack_q5(wn, wh, s, K_, N_)
+
+
+def fp4_weights(nq, K_, N_, seed):
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    return nq.pack_fp4(si.device_code_words(N_, K_ // 8, gen, dev), si.device_fp4_scales(N_, K_, gen, dev), K_, N_)
+
+
+class Layer:
+    def __init__(self, nq, T, seed):
+        dev = torch.device("cuda", 0)
+        self.gate, self.up = weights(nq, 4, K, NH, seed), weights(nq, 4, K, NH, seed + 1)
+        self.down = weights(nq, 4, NH, K, seed + 2)
+        self.qg, self.kv = weights(nq, 5, K, NQ, seed + 3), weights(nq, 5, K, NKV, seed + 4)
+        self.out = weights(nq, 5, KO, K, seed + 5)
+        self.f4 = fp4_weights(nq, K, 272, seed + 6)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed + 7)
+        self.x = si.device_activations(T, K, gen, dev)
+        self.x6 = si.device_activations(T, KO, gen, dev)
+        self.outs = [torch.empty((T, n), dtype=torch.bfloat16, device=dev) for n in (NH, K, NQ, NKV, K, 272)]
+
+    def eager(self, nq):
+        h = nq.swiglu_q4(self.x, *self.gate, *self.up, NH)
+        yd = nq.gemm_q4(h, *self.down, K)
+        yq, ykv = nq.gemm_q5_grouped(self.x, [(*self.qg, NQ), (*self.kv, NKV)])
+        yo = nq.gemm_q5(self.x6, *self.out, K)
+        yf = nq.gemm_fp4(self.x, *self.f4, si.FP4_GLOBAL_SCALE, 272)
+        return [h, yd, yq, ykv, yo, yf]
+
+    def record(self, nq):
+        p = nq.Program()
+        h, yd, yq, ykv, yo, yf = self.outs
+        p.swiglu_q4(self.x, *self.gate, *self.up, NH, out=h)
+        p.gemm_q4(h, *self.down, K, out=yd)
+        p.grouped_q5(self.x, [(*self.qg, NQ), (*self.kv, NKV)], outs=[yq, ykv])
+        p.gemm_q5(self.x6, *self.out, K, out=yo)
+        p.gemm_fp4(self.x, *self.f4, si.FP4_GLOBAL_SCALE, 272, out=yf)
+        return p
+
+
+def same_bits(a, b):
+    return all(torch.equal(u.view(torch.int16), v.view(torch.int16)) for u, v in zip(a, b))
+
+
+@pytest.mark.parametrize("T", [1, 8, 40])
+def test_program_replays_a_layer_bit_for_bit(nq, T):
+    ly = Layer(nq, T, 900 + T)
+    ref = ly.eager(nq)
+    p = ly.record(nq)
+    for o in ly.outs:
+        o.fill_(0)
+    p.launch()
+    torch.cuda.synchronize()
+    nq.device_error()
+    assert same_bits(ly.outs, ref)
+    i = p.info()
+    # T <= 8: one launch per call; T = 40: the SwiGLU block and the grouped call are two
+    # tensor-core launches each
+    assert i["calls"] == 5 and i["builds"] == 1 and i["failed_call"] == -1
+    assert i["kernels"] == (5 if T <= 8 else 7)
+    # a replay reads X as it is at launch time
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(77)
+    ly.x.copy_(si.device_activations(T, K, gen, ly.x.device))
+    ly.x6.copy_(si.device_activations(T, KO, gen, ly.x.device))
+    p.launch()
+    ref2 = ly.eager(nq)
+    torch.cuda.synchronize()
+    assert same_bits(ly.outs, ref2) and not same_bits(ref, ref2)
+    p.close()
+
+
+def test_program_swiglu_matches_the_oracle(nq):
+    """The replay's H against the fp64 oracle on host-drawn inputs, at the parity bar of the
+    eager call."""
+    T, K_, N_ = 8, 640, 272
+    pr = si.swiglu_problem(T, K_, N_, 91)
+    wg = gu.pack_q4(nq, pr["wg"], pr["sg"], K_, N_)
+    wu = gu.pack_q4(nq, pr["wu"], pr["su"], K_, N_)
+    x = gu.dev_bf16(pr["x"])
+    h = torch.empty((T, N_), dtype=torch.bfloat16, device="cuda")
+    p = nq.Program()
+    p.swiglu_q4(x, *wg, *wu, N_, out=h)
+    p.launch()
+    torch.cuda.synchronize()
+    g, u, _ = oracle.swiglu_q4(pr["x"], pr["wg"], pr["sg"], pr["wu"], pr["su"], T, K_, N_)
+    h_exact = g / (1.0 + np.exp(-g)) * u
+    assert gu.rel_err(gu.host_f64(h), h_exact) <= gu.TOL
+    p.close()
+
+
+def test_program_rebuilds_after_the_workspace_moves(nq):
+    ly = Layer(nq, 8, 950)
+    ref = ly.eager(nq)
+    p = ly.record(nq)
+    p.build()
+    p.launch()
+    torch.cuda.synchronize()
+    assert same_bits(ly.outs, ref) and p.info()["builds"] == 1
+    p.launch()
+    assert p.info()["builds"] == 1          # nothing moved: the same graph
+    torch.cuda.synchronize()
+    nq.shutdown()                           # frees the workspace the graph points at
+    for o in ly.outs:
+        o.fill_(0)
+    p.launch()                              # builds again on the new workspace
+    torch.cuda.synchronize()
+    nq.device_error()
+    assert same_bits(ly.outs, ref) and p.info()["builds"] == 2
+    p.close()
+
+
+def test_program_on_another_stream_and_empty_program(nq):
+    ly = Layer(nq, 3, 960)
+    ref = ly.eager(nq)
+    p = ly.record(nq)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    p.launch(stream=s)
+    s.synchronize()
+    assert same_bits(ly.outs, ref)
+    p.close()
+    e = nq.Program()
+    e.build()
+    e.launch()
+    torch.cuda.synchronize()
+    assert e.info() == {"calls": 0, "kernels": 0, "builds": 1, "failed_call": -1}
+    e.close()
+
+
+def test_program_recording_after_build_builds_again(nq):
+    ly = Layer(nq, 8, 970)
+    ref = ly.eager(nq)
+    p = nq.Program()
+    h, yd = ly.outs[0], ly.outs[1]
+    p.swiglu_q4(ly.x, *ly.gate, *ly.up, NH, out=h)
+    p.launch()
+    assert p.info()["kernels"] == 1
+    p.gemm_q4(h, *ly.down, K, out=yd)         # marks the program for building again
+    p.launch()
+    torch.cuda.synchronize()
+    i = p.info()
+    assert i["calls"] == 2 and i["kernels"] == 2 and i["builds"] == 2
+    assert same_bits([h, yd], ref[:2])
+    p.close()

@@ -2,6 +2,7 @@
 // offline repack kernels, the debug dequantisation kernels and the projection launches.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -251,6 +252,9 @@ bool g_cluster = false;
 bool g_env_read = false;
 bool g_tc = true;
 unsigned long long g_wait_ns = (unsigned long long)kWaitTimeoutNs;
+// Bumped whenever a device workspace buffer is allocated, moved or freed: a recorded program
+// built under another value holds stale workspace addresses and is built again.
+std::atomic<unsigned long long> g_ws_epoch{0};
 
 // Reads NQ_PDL, NQ_CLUSTER and NQ_WAIT_NS once (the first call that needs them). g_mu held.
 void read_env_locked() {
@@ -323,6 +327,7 @@ nq_status ensure_workspace(DevState& d, long long slots, long long tickets) {
     d.ws = static_cast<uint8_t*>(p);
     d.slots_cap = sc;
     d.tickets_cap = tc;
+    ++g_ws_epoch;
     return NQ_OK;
 }
 
@@ -351,6 +356,7 @@ nq_status ensure_tc_workspace(DevState& d, long long tickets, long long floats) 
     d.tc_ws = static_cast<uint8_t*>(p);
     d.tc_tickets = tc;
     d.tc_floats = fc;
+    ++g_ws_epoch;
     return NQ_OK;
 }
 
@@ -368,6 +374,7 @@ nq_status ensure_tc_gate(DevState& d, long long floats) {
     if (cudaMalloc(&p, (size_t)floats * sizeof(float)) != cudaSuccess) return NQ_ERR_CUDA;
     d.tc_gate = static_cast<float*>(p);
     d.tc_gate_floats = floats;
+    ++g_ws_epoch;
     return NQ_OK;
 }
 
@@ -441,8 +448,10 @@ bool choose_plans(int bits, bool swiglu, int T, int K, int N, DevState& d, Plan&
 // as one launch; larger batches (up to kMaxT) as one launch per slice of kSliceT tokens, each
 // streaming the weights again. Every slice's plan and the workspace are settled before the
 // first launch, so an error still launches nothing.
-nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
-                  const void* S1, void* Y, int T, int K, int N, void* stream, float gscale = 1.f) {
+// The host-side argument checks of a projection call, in order: shape, then (for a non-empty
+// problem) NULL, alignment, aliasing. NQ_OK for an empty problem.
+nq_status projection_args(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
+                          const void* S1, const void* Y, int T, int K, int N) {
     if (T < 0 || T > kMaxT) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;
@@ -456,11 +465,19 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     if (overlap(Y, yb, X, xb) || overlap(Y, yb, W0, wb) || overlap(Y, yb, S0, sb) ||
         (swiglu && (overlap(Y, yb, W1, wb) || overlap(Y, yb, S1, sb))))
         return NQ_ERR_ALIAS;
+    return NQ_OK;
+}
+
+nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
+                  const void* S1, void* Y, int T, int K, int N, void* stream, float gscale = 1.f) {
+    nq_status st = projection_args(bits, swiglu, X, W0, S0, W1, S1, Y, T, K, N);
+    if (st != NQ_OK) return st;
+    if (T == 0 || N == 0) return NQ_OK;  // empty output
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
     if (K == 0) {  // empty sum
-        return cudaMemsetAsync(Y, 0, yb, as_stream(stream)) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
+        return cudaMemsetAsync(Y, 0, (size_t)T * N * 2, as_stream(stream)) == cudaSuccess ? NQ_OK : NQ_ERR_CUDA;
     }
     // Larger batches: the tensor-core kernel, one weight pass per matrix. A SwiGLU block is two
     // launches on the same X: the gate projection writes fp32 G to a library buffer, the up
@@ -542,7 +559,8 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
 
 // Several projections of the same X in one launch per slice (gemm only, no slab clusters):
 // group g owns ceil(N_g / 32) consecutive row pairs of the work split.
-nq_status project_grouped(int bits, const void* X, const nq_group* groups, int count, int T, int K, void* stream) {
+// The host-side argument checks of a grouped call, in order (NQ_OK for T == 0).
+nq_status grouped_args(int bits, const void* X, const nq_group* groups, int count, int T, int K) {
     if (!groups) return NQ_ERR_NULL;
     if (count < 1 || count > kMaxGroups || T < 0 || T > kMaxT) return NQ_ERR_SHAPE;
     for (int g = 0; g < count; ++g) {
@@ -571,6 +589,13 @@ nq_status project_grouped(int bits, const void* X, const nq_group* groups, int c
             if (h != g && overlap(groups[g].Y, yb, groups[h].Y, (size_t)T * groups[h].N * 2)) return NQ_ERR_ALIAS;
         }
     }
+    return NQ_OK;
+}
+
+nq_status project_grouped(int bits, const void* X, const nq_group* groups, int count, int T, int K, void* stream) {
+    nq_status st = grouped_args(bits, X, groups, count, T, K);
+    if (st != NQ_OK) return st;
+    if (T == 0) return NQ_OK;
     DevState* d = nullptr;
     st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
@@ -630,6 +655,64 @@ nq_status project_grouped(int bits, const void* X, const nq_group* groups, int c
         if (e != cudaSuccess) return NQ_ERR_CUDA;
     }
     return NQ_OK;
+}
+
+// The workspace a projection call of this shape will use, allocated now; nothing is launched.
+// It draws the same plans as project(): the tensor-core plan where that branch applies, and
+// the 8-token slice plans (the fallback of that branch, and the path of every other call).
+nq_status reserve_projection(int bits, bool swiglu, int T, int K, int N) {
+    if (T <= 0 || K <= 0 || N <= 0) return NQ_OK;  // empty problems use no workspace
+    DevState* d = nullptr;
+    nq_status st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    if (g_tc && (bits == 4 || bits == 5 || (bits == kFp4 && !swiglu)) && T > kSliceT && T <= kTcMaxT) {
+        TcPlan p;
+        if (make_tc_plan(bits, T, K, N, d->sms, p)) {
+            st = ensure_workspace(*d, 1, 1);
+            if (st == NQ_OK) st = ensure_tc_workspace(*d, p.RB, p.KS > 1 ? (long long)p.P * kTcRows * p.TP : 1);
+            if (st == NQ_OK && swiglu) st = ensure_tc_gate(*d, (long long)T * N);
+            if (st != NQ_OK) return st;
+        }
+    }
+    const int full = T < kSliceT ? T : kSliceT, rest = T > kSliceT ? T % kSliceT : 0;
+    Plan p, q;
+    if (!choose_plans(bits, swiglu, full, K, N, *d, p, q)) return NQ_ERR_SHAPE;
+    long long slots = q.slots;
+    const long long tickets = q.RP;
+    if (rest > 0) {
+        if (!choose_plans(bits, swiglu, rest, K, N, *d, p, q)) return NQ_ERR_SHAPE;
+        if (q.slots > slots) slots = q.slots;
+    }
+    return ensure_workspace(*d, slots, tickets);
+}
+
+// As reserve_projection for a grouped call (its arguments already checked).
+nq_status reserve_grouped(int bits, const nq_group* groups, int count, int T, int K) {
+    if (T <= 0 || K <= 0) return NQ_OK;
+    DevState* d = nullptr;
+    nq_status st = current_device(&d, nullptr);
+    if (st != NQ_OK) return st;
+    if (g_tc && (bits == 4 || bits == 5) && T > kSliceT && T <= kTcMaxT) {
+        for (int g = 0; g < count; ++g) {
+            st = reserve_projection(bits, false, T, K, groups[g].N);
+            if (st != NQ_OK) return st;
+        }
+        return NQ_OK;
+    }
+    int n_pairs = 0;
+    for (int g = 0; g < count; ++g) n_pairs += (groups[g].N + 2 * kTileRows - 1) / (2 * kTileRows);
+    if ((long long)n_pairs * 2 * kTileRows > kMaxDim) return NQ_ERR_SHAPE;
+    const int full = T < kSliceT ? T : kSliceT, rest = T > kSliceT ? T % kSliceT : 0;
+    long long slots = 0;
+    for (int i = 0; i < 2; ++i) {
+        const int tn = i == 0 ? full : rest;
+        Plan p;
+        if (tn > 0) {
+            if (!make_plan(bits, 0, tn, K, n_pairs * 2 * kTileRows, d->sms, p)) return NQ_ERR_SHAPE;
+            if (p.slots > slots) slots = p.slots;
+        }
+    }
+    return ensure_workspace(*d, slots, n_pairs);
 }
 
 nq_status pack(int bits, const uint32_t* wn, const uint32_t* wh, const uint16_t* s, int K, int N, void* wq_packed,
@@ -739,6 +822,25 @@ unsigned long long wait_limit_ns() {
     read_env_locked();
     return g_wait_ns;
 }
+
+int check_projection_args(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
+                          const void* S1, const void* Y, int T, int K, int N) {
+    return projection_args(bits, swiglu, X, W0, S0, W1, S1, Y, T, K, N);
+}
+
+int check_grouped_args(int bits, const void* X, const nq_group* groups, int count, int T, int K) {
+    return grouped_args(bits, X, groups, count, T, K);
+}
+
+int reserve_projection_workspace(int bits, bool swiglu, int T, int K, int N) {
+    return reserve_projection(bits, swiglu, T, K, N);
+}
+
+int reserve_grouped_workspace(int bits, const nq_group* groups, int count, int T, int K) {
+    return reserve_grouped(bits, groups, count, T, K);
+}
+
+unsigned long long workspace_epoch() { return g_ws_epoch.load(); }
 }  // namespace nq
 
 // ---------------------------------------------------------------- C ABI
@@ -919,6 +1021,7 @@ void nq_shutdown(void) {
         cudaFree(g_dev[i].tc_gate);
         g_dev[i].tc_gate = nullptr;
         g_dev[i].tc_gate_floats = 0;
+        ++g_ws_epoch;
     }
     cudaSetDevice(cur);
 }

@@ -6,6 +6,8 @@
 #include "nq_proj.cuh"
 #include "nq_tc.cuh"
 
+struct nq_group;
+
 namespace nq {
 
 // Large-batch tensor-core kernel (nq_tc.cuh): the activation tensor map (false if the driver
@@ -20,6 +22,17 @@ cudaError_t launch_tc_proj_swiglu(int bits, int mode, const TcArgs& a, cudaStrea
 
 // Bound of every device-side wait for later launches (nq_wait_limit; NQ_WAIT_NS).
 unsigned long long wait_limit_ns();
+
+// Host-side argument checks of the projection and grouped calls (an nq_status; NQ_OK for an
+// empty problem), the reservation of the workspace a call of that shape will use (nothing is
+// launched), and the workspace epoch, bumped whenever a device workspace buffer is allocated,
+// moved or freed. Recorded programs (nq_program.cu) are built on these.
+int check_projection_args(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
+                          const void* S1, const void* Y, int T, int K, int N);
+int check_grouped_args(int bits, const void* X, const nq_group* groups, int count, int T, int K);
+int reserve_projection_workspace(int bits, bool swiglu, int T, int K, int N);
+int reserve_grouped_workspace(int bits, const nq_group* groups, int count, int T, int K);
+unsigned long long workspace_epoch();
 
 // Reports and clears the error word of nq_gemm_q4_noalloc's fixed scratch on device `dev`
 // (NQ_OK if that device never ran it). The caller has synchronised the device.

@@ -88,6 +88,19 @@ def lib() -> ctypes.CDLL:
         L.nq_plan_cluster_info.argtypes = [I, I, I, I, I, I, P]
         L.nq_plan_cluster_segments.argtypes = [I, I, I, I, I, I, I, P, ctypes.c_int64]
         L.nq_plan_cluster_segments.restype = ctypes.c_int64
+        L.nq_program_create.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        L.nq_program_gemm.argtypes = [P, I, P, P, P, P, I, I, I]
+        L.nq_program_gemm_fp4.argtypes = [P, P, P, P, ctypes.c_float, P, I, I, I]
+        L.nq_program_swiglu.argtypes = [P, I, P, P, P, P, P, P, I, I, I]
+        L.nq_program_grouped.argtypes = [P, I, P, P, I, I, I]
+        L.nq_program_build.argtypes = [P]
+        L.nq_program_launch.argtypes = [P, P]
+        L.nq_program_info.argtypes = [P, P]
+        for f in ("nq_program_create", "nq_program_gemm", "nq_program_gemm_fp4", "nq_program_swiglu",
+                  "nq_program_grouped", "nq_program_build", "nq_program_launch", "nq_program_info"):
+            getattr(L, f).restype = I
+        L.nq_program_destroy.argtypes = [P]
+        L.nq_program_destroy.restype = None
         for f in ("nq_pack_q4", "nq_pack_q5", "nq_gemm_q4", "nq_gemm_q5", "nq_gemm_q4_noalloc", "nq_swiglu_q4",
                   "nq_swiglu_q5", "nq_reserve", "nq_device_error", "nq_plan_info", "nq_plan_cluster_info"):
             getattr(L, f).restype = I
@@ -298,6 +311,106 @@ def dequant_fp4_debug(wq, s, global_scale: float, K: int, N: int, stream=None) -
     _check(lib().nq_dequant_fp4_debug(_ptr(wq), _ptr(s), ctypes.c_float(global_scale), _ptr(out), K, N,
                                       _stream(stream)))
     return out
+
+
+# ---------------------------------------------------------------- recorded programs
+
+PROGRAM_KEYS = ("calls", "kernels", "builds", "failed_call")
+
+
+class Program:
+    """A sequence of projection calls recorded once and replayed as one CUDA graph
+    (nq_program_* of include/nq.h). The library records the tensors' device addresses, not
+    their contents: write new activations into the same X tensor and launch again. The
+    program keeps a reference to every tensor it records, so they stay allocated while it can
+    be launched. Outputs not given are allocated here (torch) and returned."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(lib().nq_program_create(ctypes.byref(h)))
+        self._h = h
+        self._keep = []
+
+    def _rec(self, status, *tensors):
+        _check(status)
+        self._keep.extend(t for t in tensors if t is not None)
+
+    def _gemm(self, bits, x, wq, s, N, out):
+        _cuda(x, "x")
+        T, K = x.shape
+        y = _out(x, N, out)
+        self._rec(lib().nq_program_gemm(self._h, bits, _ptr(x), _ptr(wq), _ptr(s), _ptr(y), T, K, N), x, wq, s, y)
+        return y
+
+    def gemm_q4(self, x, wq, s, N: int, out=None):
+        return self._gemm(4, x, wq, s, N, out)
+
+    def gemm_q5(self, x, wq, s, N: int, out=None):
+        return self._gemm(5, x, wq, s, N, out)
+
+    def gemm_fp4(self, x, wq, s, global_scale: float, N: int, out=None):
+        _cuda(x, "x")
+        T, K = x.shape
+        y = _out(x, N, out)
+        self._rec(lib().nq_program_gemm_fp4(self._h, _ptr(x), _ptr(wq), _ptr(s), ctypes.c_float(global_scale),
+                                            _ptr(y), T, K, N), x, wq, s, y)
+        return y
+
+    def _swiglu(self, bits, x, wg, sg, wu, su, N, out):
+        _cuda(x, "x")
+        T, K = x.shape
+        h = _out(x, N, out)
+        self._rec(lib().nq_program_swiglu(self._h, bits, _ptr(x), _ptr(wg), _ptr(sg), _ptr(wu), _ptr(su), _ptr(h),
+                                          T, K, N), x, wg, sg, wu, su, h)
+        return h
+
+    def swiglu_q4(self, x, wg, sg, wu, su, N: int, out=None):
+        return self._swiglu(4, x, wg, sg, wu, su, N, out)
+
+    def swiglu_q5(self, x, wg, sg, wu, su, N: int, out=None):
+        return self._swiglu(5, x, wg, sg, wu, su, N, out)
+
+    def _grouped(self, bits, x, groups, outs):
+        _cuda(x, "x")
+        T, K = x.shape
+        if outs is None:
+            outs = [torch.empty((T, N), dtype=torch.bfloat16, device=x.device) for (_, _, N) in groups]
+        arr = (NqGroup * len(groups))()
+        for i, ((wq, s, N), y) in enumerate(zip(groups, outs)):
+            _cuda(y, "out")
+            arr[i] = NqGroup(wq.data_ptr(), s.data_ptr(), y.data_ptr(), N)
+        self._rec(lib().nq_program_grouped(self._h, bits, _ptr(x), ctypes.cast(arr, ctypes.c_void_p), len(groups),
+                                           T, K), x, *[t for (wq, s, _) in groups for t in (wq, s)], *outs)
+        return outs
+
+    def grouped_q4(self, x, groups, outs=None):
+        return self._grouped(4, x, groups, outs)
+
+    def grouped_q5(self, x, groups, outs=None):
+        return self._grouped(5, x, groups, outs)
+
+    def build(self) -> None:
+        _check(lib().nq_program_build(self._h))
+
+    def launch(self, stream=None) -> None:
+        _check(lib().nq_program_launch(self._h, _stream(stream)))
+
+    def info(self) -> dict:
+        out = (ctypes.c_int64 * 4)()
+        _check(lib().nq_program_info(self._h, ctypes.cast(out, ctypes.c_void_p)))
+        return dict(zip(PROGRAM_KEYS, list(out)))
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            lib().nq_program_destroy(self._h)
+        self._h = None
+        self._keep = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ---------------------------------------------------------------- runtime / plan
