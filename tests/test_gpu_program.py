@@ -44,35 +44,41 @@ def fp4_weights(nq, K_, N_, seed):
 
 
 class Layer:
-    def __init__(self, nq, T, seed):
+    """The projections of one decoder layer (dims: hidden K, MLP NH, q-gate NQ, kv NKV, out
+    input KO, NVFP4 output NF), with its activations and output buffers."""
+
+    def __init__(self, nq, T, seed, dims=(K, NH, NQ, NKV, KO, 272)):
         dev = torch.device("cuda", 0)
-        self.gate, self.up = weights(nq, 4, K, NH, seed), weights(nq, 4, K, NH, seed + 1)
-        self.down = weights(nq, 4, NH, K, seed + 2)
-        self.qg, self.kv = weights(nq, 5, K, NQ, seed + 3), weights(nq, 5, K, NKV, seed + 4)
-        self.out = weights(nq, 5, KO, K, seed + 5)
-        self.f4 = fp4_weights(nq, K, 272, seed + 6)
+        self.d = k, nh, nqg, nkv, ko, nf = dims
+        self.gate, self.up = weights(nq, 4, k, nh, seed), weights(nq, 4, k, nh, seed + 1)
+        self.down = weights(nq, 4, nh, k, seed + 2)
+        self.qg, self.kv = weights(nq, 5, k, nqg, seed + 3), weights(nq, 5, k, nkv, seed + 4)
+        self.out = weights(nq, 5, ko, k, seed + 5)
+        self.f4 = fp4_weights(nq, k, nf, seed + 6)
         gen = torch.Generator(device=dev)
         gen.manual_seed(seed + 7)
-        self.x = si.device_activations(T, K, gen, dev)
-        self.x6 = si.device_activations(T, KO, gen, dev)
-        self.outs = [torch.empty((T, n), dtype=torch.bfloat16, device=dev) for n in (NH, K, NQ, NKV, K, 272)]
+        self.x = si.device_activations(T, k, gen, dev)
+        self.x6 = si.device_activations(T, ko, gen, dev)
+        self.outs = [torch.empty((T, n), dtype=torch.bfloat16, device=dev) for n in (nh, k, nqg, nkv, k, nf)]
 
     def eager(self, nq):
-        h = nq.swiglu_q4(self.x, *self.gate, *self.up, NH)
-        yd = nq.gemm_q4(h, *self.down, K)
-        yq, ykv = nq.gemm_q5_grouped(self.x, [(*self.qg, NQ), (*self.kv, NKV)])
-        yo = nq.gemm_q5(self.x6, *self.out, K)
-        yf = nq.gemm_fp4(self.x, *self.f4, si.FP4_GLOBAL_SCALE, 272)
+        k, nh, nqg, nkv, ko, nf = self.d
+        h = nq.swiglu_q4(self.x, *self.gate, *self.up, nh)
+        yd = nq.gemm_q4(h, *self.down, k)
+        yq, ykv = nq.gemm_q5_grouped(self.x, [(*self.qg, nqg), (*self.kv, nkv)])
+        yo = nq.gemm_q5(self.x6, *self.out, k)
+        yf = nq.gemm_fp4(self.x, *self.f4, si.FP4_GLOBAL_SCALE, nf)
         return [h, yd, yq, ykv, yo, yf]
 
     def record(self, nq):
+        k, nh, nqg, nkv, ko, nf = self.d
         p = nq.Program()
         h, yd, yq, ykv, yo, yf = self.outs
-        p.swiglu_q4(self.x, *self.gate, *self.up, NH, out=h)
-        p.gemm_q4(h, *self.down, K, out=yd)
-        p.grouped_q5(self.x, [(*self.qg, NQ), (*self.kv, NKV)], outs=[yq, ykv])
-        p.gemm_q5(self.x6, *self.out, K, out=yo)
-        p.gemm_fp4(self.x, *self.f4, si.FP4_GLOBAL_SCALE, 272, out=yf)
+        p.swiglu_q4(self.x, *self.gate, *self.up, nh, out=h)
+        p.gemm_q4(h, *self.down, k, out=yd)
+        p.grouped_q5(self.x, [(*self.qg, nqg), (*self.kv, nkv)], outs=[yq, ykv])
+        p.gemm_q5(self.x6, *self.out, k, out=yo)
+        p.gemm_fp4(self.x, *self.f4, si.FP4_GLOBAL_SCALE, nf, out=yf)
         return p
 
 
@@ -105,6 +111,24 @@ def test_program_replays_a_layer_bit_for_bit(nq, T):
     ref2 = ly.eager(nq)
     torch.cuda.synchronize()
     assert same_bits(ly.outs, ref2) and not same_bits(ref, ref2)
+    p.close()
+
+
+@pytest.mark.parametrize("T", [8, 40])
+def test_program_full_size_layer(nq, T):
+    """One 27B-class layer at full size (the layer-stack shapes: gate/up 5120 x 17408, down
+    17408 x 5120, q-gate 5120 x 6144, kv 5120 x 1024, out 6144 x 5120; NVFP4 5120 x 17408), in
+    the launch configuration a replay of the stack uses: bit for bit the eager calls."""
+    ly = Layer(nq, T, 990 + T, dims=(5120, 17408, 6144, 1024, 6144, 17408))
+    ref = ly.eager(nq)
+    p = ly.record(nq)
+    for o in ly.outs:
+        o.fill_(0)
+    p.launch()
+    torch.cuda.synchronize()
+    nq.device_error()
+    assert same_bits(ly.outs, ref)
+    assert all(torch.isfinite(o.float()).all() for o in ly.outs)
     p.close()
 
 
