@@ -90,6 +90,18 @@ WORKLOADS = {
 }
 
 
+# The pages' own single-op numbers for this path ("NInfer-4090" release post, section "实测数据"):
+# another GPU (an RTX 4090 fork) and shapes the pages do not state, so context for the line,
+# not a baseline (vs_baseline stays null).
+PAGES_CONTEXT = {
+    "source": "\"NInfer-4090\" release post, section 实测数据",
+    "hardware": "RTX 4090 (sm_89 fork)",
+    "t8_attention_q5_gate_value_us": {"before": 57.344, "after": 39.936},
+    "t8_gdn_qk_q4_us": {"before": 35.840, "after": 31.744},
+    "note": "shapes not stated on the pages; this GPU's calls are judged against its HBM roofline",
+}
+
+
 def workload_bytes(w: dict) -> int:
     if w["kind"] == "proj":
         return proj_bytes(w["bits"], w["T"], w["K"], w["N"])
@@ -105,15 +117,16 @@ def workload_bytes(w: dict) -> int:
 def launches_per_step(w: dict) -> int:
     """Kernel launches per step. T <= 8: one per call (the stack's q-gate and kv share one).
     8 < T <= 64: one per projection on the tensor-core kernel, two for a fused SwiGLU call
-    (gate, then up), and one per 8-token slice for the stack's grouped q-gate/kv call."""
+    (gate, then up) and two for the stack's grouped q-gate/kv call (one per matrix)."""
     T = w.get("T", 1)
     big = T > 8
     swiglu = 2 if big else 1
+    grouped = 2 if big else 1
     if w["kind"] == "proj":
         return 1
     if w["kind"] == "swiglu":
         return swiglu + 1
-    return (swiglu + 1 + -(-T // 8) + 1) * w.get("layers", 1)
+    return (swiglu + 1 + grouped + 1) * w.get("layers", 1)
 
 
 # ---------------------------------------------------------------- environment helpers
@@ -621,6 +634,7 @@ def main():
                    "us_per_step_median": round(1e3 * statistics.median(reps) / args.steps, 3),
                    "us_per_step_max": round(1e3 * max(reps) / args.steps, 3)},
         "clocks": clk.summary(),
+        "pages_context": PAGES_CONTEXT,
     }
     if not args.no_e2e and w["kind"] == "proj":
         e_ms, b, h2d, d2h = time_e2e(nq, w, args.steps, warmup, stream, dev)
