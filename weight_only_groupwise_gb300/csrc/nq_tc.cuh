@@ -6,7 +6,8 @@
 // once whatever T. A SwiGLU block is two launches (the output-mode template argument): the
 // gate projection writes fp32 G, the up projection writes bf16 silu(G) * U.
 //
-// One block per (128-row block, K piece), 14 warps. Work moves between the warp roles in
+// One block per (128-row block, K piece), D + 6 warps (D decoders: 8, or 16 for NVFP4 with
+// TP <= 32). Work moves between the warp roles in
 // stages of BG 64-wide K groups (six for TP <= 32 padded tokens, four for TP = 64: the TMEM
 // budget), one hand-off per stage:
 //   * warp 0, one lane -- producer: per stage three 3-D TMA copies: the codes and the scales of
@@ -14,20 +15,21 @@
 //     activation chunk, one [TP][64] block per group in the tensor core's K-major
 //     128-byte-swizzled layout, tokens past T filled with zeros by the copy. A ring of
 //     shared-memory stages (1024-byte aligned), mbarriers.
-//   * warps 1..8 -- decoders: warp w owns one 16-row tile, TMEM lanes 32 (w % 4) + 16 h .. + 15
-//     (h = 0 for warps 1..4, 1 for 5..8). A lane decodes its fragment words of a group into
+//   * warps 1..D -- decoders: warp w owns one 16-row tile, TMEM lanes 32 (w % 4) + 16 h .. + 15
+//     (h = 0 for warps 1..4, 1 for 5..8, and again for 9..16, which take the odd groups of
+//     each stage when D = 16). A lane decodes its fragment words of a group into
 //     bf16 (q - z) 2^-12, exact, and stores all four K steps with one tcgen05.st.16x128b.x8,
 //     which places the mma.sync A-fragment registers of lane t at TMEM lanes t/4, t/4 + 8 and
 //     columns 8 j + t%4, 8 j + 4 + t%4: K in natural order, one row per TMEM lane. An A buffer
-//     holds a stage (32 columns a group); two alternate. Groups are decoded in pairs, each pair
-//     into registers of its own, so that a pair decodes while the stores of the pairs before it
-//     complete.
-//   * warp 9 -- MMA issuer (the whole warp runs the loop, one elected lane issues): per group,
+//     holds a stage (32 columns a group); two alternate. Groups are decoded in pairs (D = 8)
+//     or one by one (D = 16), each into registers of its own, so that they decode while the
+//     stores of the groups before them complete.
+//   * warp D + 1 -- MMA issuer (the whole warp runs the loop, one elected lane issues): per group,
 //     four tcgen05.mma.kind::f16 (M = 128, N = TP, K = 16; A from TMEM, B = the activation
 //     chunk through a shared-memory descriptor; D in TMEM, fp32, a fresh accumulator per group:
 //     P = 2^-12 sum over the group of (q - z) x); per pair of groups a tcgen05.commit publishes
 //     their two P (a P buffer), per stage one frees the A buffer and the shared-memory stage.
-//   * warps 10..13 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
+//   * warps D + 2 .. D + 5 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
 //     adds 2^12 s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y,
 //     or, when K is split across blocks, an fp32 partial; the last block of a row block
 //     (ticket) adds the partials in fixed order and stores Y.
@@ -57,10 +59,13 @@ constexpr int kTcCols = 512;                      // TMEM columns: A buffers, th
 constexpr int kTcMaxP = 8;
 constexpr int kTcScaleExp = 12;                   // decoded 4/5-bit weights carry 2^-12
 constexpr int kTcFp4ScaleExp = 20;                // decoded NVFP4 weights carry 2^-20
-constexpr int kTcDecoders = 8;                    // decoder warps: one 16-row tile each
 constexpr int kTcEpilogue = 4;                    // epilogue warps: one TMEM lane quarter each
-constexpr int kTcWarps = 2 + kTcDecoders + kTcEpilogue;
-constexpr int kTcThreads = kTcWarps * 32;
+// Decoder warps: one per 16-row tile; two (each every other group of a stage) for NVFP4 with
+// TP <= 32, whose decode (e2m1 x e4m3 to fp16, then bf16) is the longest. Measured at T = 16
+// on the decode shape: NVFP4 26.7 -> 24.5 us, Q4 18.0 -> 18.6 us (so Q4/Q5 keep one); at
+// TP = 64 the epilogue accumulators need the registers of the smaller block.
+NQ_HD constexpr int tc_decoders(int bits, int TP) { return bits == kFp4 && TP <= 32 ? 16 : 8; }
+NQ_HD constexpr int tc_threads(int bits, int TP) { return (2 + tc_decoders(bits, TP) + kTcEpilogue) * 32; }
 constexpr int kTcMinT = 9, kTcMaxT = 64;
 // What the epilogue writes for (token t, row n) from the finished fp32 value v: bf16 Y = v;
 // fp32 G = v (a SwiGLU gate projection); bf16 Y = silu(G) * v (the up projection of the same
@@ -276,7 +281,7 @@ __device__ __forceinline__ bool elect_one() {
 // ---------------------------------------------------------------- the kernel
 
 template <int BITS, int TP, int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const __grid_constant__ TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
     constexpr int BG = tc_stage_groups(TP);
@@ -298,7 +303,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
     constexpr int kP = (kTcCols - kTcA * kAStage) / kPCols;
     static_assert(kP >= 2 && kP <= kTcMaxP, "TMEM budget");
     constexpr uint32_t kIdesc = tc_idesc_bf16(TP);
-    constexpr int kDec = kTcDecoders, kEpi = kTcEpilogue;
+    constexpr int kDec = tc_decoders(BITS, TP), kEpi = kTcEpilogue;
+    constexpr int kDecPerTile = kDec / kTcTiles;     // warps sharing a tile's groups
     constexpr int kMmaWarp = 1 + kDec;
 
     const TcPlan& p = a.p;
@@ -384,36 +390,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
         }
     } else if (warp <= kDec) {
         // ------------------------------------------------------------ decoders
-        const int q = warp & 3, h = (warp - 1) >> 2;  // TMEM lane quarter, and which half of it
+        const int q = warp & 3;                        // TMEM lane quarter
+        const int h = ((warp - 1) >> 2) & 1;           // which half of it
+        const int e = (warp - 1) >> 3;                 // which of the tile's decoders
         const int m = 2 * q + h;                       // the warp's 16-row tile of the block
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col0;
+        // Group gs of stage st (position gs of the stage) into the lane's 16 A-fragment registers.
+        auto decode_group = [&](int st, int gs, uint32_t (&r)[16]) {
+            const uint8_t* code = stage_mem + st * kStageBytes + m * BG * TB + gs * TB + lane * 16;
+            const uint4 w = *reinterpret_cast<const uint4*>(code);
+            if constexpr (FP4) {
+                // the lane's 8 block-scale bytes: rows r, r + 8 for each K step
+                const uint2 sc = *reinterpret_cast<const uint2*>(stage_mem + st * kStageBytes + kTcTiles * BG * TB +
+                                                                 m * BG * STB + gs * STB + (lane >> 2) * 8);
+                tc_decode_fp4(w.x, sc.x, r + 0);
+                tc_decode_fp4(w.y, sc.x >> 16, r + 4);
+                tc_decode_fp4(w.z, sc.y, r + 8);
+                tc_decode_fp4(w.w, sc.y >> 16, r + 12);
+            } else {
+                const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
+                tc_decode<BITS, 0>(w, hb, r + 0);
+                tc_decode<BITS, 1>(w, hb, r + 4);
+                tc_decode<BITS, 2>(w, hb, r + 8);
+                tc_decode<BITS, 3>(w, hb, r + 12);
+            }
+        };
         // Groups gl, gl + 1 of the block (those inside its range), at positions gl % BG of stage st.
         auto decode_pair = [&](int st, int gl, uint32_t (&r)[kTcPair][16]) {
-            const uint8_t* sb = stage_mem + st * kStageBytes + m * BG * TB;
 #pragma unroll
             for (int gp = 0; gp < kTcPair; ++gp) {
                 if (gl + gp >= ngroups) break;
-                const uint8_t* code = sb + ((gl + gp) % BG) * TB + lane * 16;
-                const uint4 w = *reinterpret_cast<const uint4*>(code);
-                if constexpr (FP4) {
-                    // the lane's 8 block-scale bytes: rows r, r + 8 for each K step
-                    const uint2 sc = *reinterpret_cast<const uint2*>(stage_mem + st * kStageBytes + kTcTiles * BG * TB +
-                                                                     m * BG * STB + ((gl + gp) % BG) * STB + (lane >> 2) * 8);
-                    tc_decode_fp4(w.x, sc.x, r[gp] + 0);
-                    tc_decode_fp4(w.y, sc.x >> 16, r[gp] + 4);
-                    tc_decode_fp4(w.z, sc.y, r[gp] + 8);
-                    tc_decode_fp4(w.w, sc.y >> 16, r[gp] + 12);
-                } else {
-                    const uint32_t hb = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code + 512 - lane * 12) : 0u;
-                    tc_decode<BITS, 0>(w, hb, r[gp] + 0);
-                    tc_decode<BITS, 1>(w, hb, r[gp] + 4);
-                    tc_decode<BITS, 2>(w, hb, r[gp] + 8);
-                    tc_decode<BITS, 3>(w, hb, r[gp] + 12);
-                }
+                decode_group(st, (gl + gp) % BG, r[gp]);
             }
         };
-        uint32_t r[BG / kTcPair][kTcPair][16];           // one register set per pair: none is
-        bool ok = true;                                  // rewritten while its stores may be in flight
+        // One register set per group of the stage that the warp decodes: none is rewritten while
+        // its store may be in flight. One decoder per tile: pairs of groups (both decoded, then
+        // both stored); two: every other group, each stored once decoded.
+        constexpr int kMine = BG / kDecPerTile;
+        static_assert(BG % kDecPerTile == 0 && (kDecPerTile == 1 || kDecPerTile == 2), "decoders split a stage");
+        uint32_t r[kDecPerTile == 1 ? BG / kTcPair : 1][kTcPair][16];   // one decoder per tile
+        uint32_t r1[kDecPerTile == 1 ? 1 : kMine][16];                   // two decoders per tile
+        bool ok = true;
         for (int si = 0; si < nst; ++si) {
             // one stage per hand-off: its BG groups go to A buffer si % kTcA (32 columns a group)
             const int st = si % nstages, ab = si % kTcA, gl = si * BG;
@@ -422,14 +439,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_proj_kernel(const __grid_con
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (ok) {
                 const uint32_t base = lane_base + kAStage * ab;
+                if constexpr (kDecPerTile == 1) {
 #pragma unroll
-                for (int pr = 0; pr < BG / kTcPair; ++pr) {
-                    // a pair decodes while the stores of the pairs before it complete
-                    const int g = gl + kTcPair * pr;
-                    decode_pair(st, g, r[pr]);
+                    for (int pr = 0; pr < BG / kTcPair; ++pr) {
+                        // a pair decodes while the stores of the pairs before it complete
+                        const int g = gl + kTcPair * pr;
+                        decode_pair(st, g, r[pr]);
 #pragma unroll
-                    for (int gp = 0; gp < kTcPair; ++gp)
-                        if (g + gp < ngroups) tmem_st_group(base + 32 * (kTcPair * pr + gp), r[pr][gp]);
+                        for (int gp = 0; gp < kTcPair; ++gp)
+                            if (g + gp < ngroups) tmem_st_group(base + 32 * (kTcPair * pr + gp), r[pr][gp]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kMine; ++j) {
+                        // a group decodes while the stores of the groups before it complete
+                        const int gs = kDecPerTile * j + e;
+                        if (gl + gs < ngroups) {
+                            decode_group(st, gs, r1[j]);
+                            tmem_st_group(base + 32 * gs, r1[j]);
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -616,7 +645,7 @@ inline cudaError_t tc_launch(const TcArgs& a, cudaStream_t stream, bool pdl) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.p.P);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(tc_threads(BITS, TP));
     cfg.dynamicSmemBytes = a.p.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
