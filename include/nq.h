@@ -448,6 +448,26 @@ int nq_tensor_core_batches(int enable);
 nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t out[8]);
 
 /*
+ * nq_route_info: which kernel and variant a projection call of this shape takes with the
+ * current settings (nq_tensor_core_batches, nq_slab_clusters), for a GPU of num_sms SMs; host
+ * only, no GPU needed. The pages route their small-batch projections by shape ("NInfer-4090"
+ * release post, section "V3 做了什么": T=8 routing); this is the library's routing, each
+ * choice measured on GB300. bits 4, 5 or 14 (NVFP4); mode 0 = gemm, 1 = SwiGLU block (4 or 5
+ * bits); 1 <= T <= 64.
+ *   out[0] kernel: 0 = the 8-token kernel (mma.sync), 1 = the tensor-core kernel (tcgen05)
+ *   out[1] launches per call (slices of 8 tokens, or the SwiGLU block's two tensor-core launches)
+ *   out[2] MMA operand type: 0 = fp16 (T <= 2, and NVFP4 on the 8-token kernel), 1 = bf16
+ *   out[3] work split: 0 = stream-K over the SMs, 1 = whole row pairs per block, 2 = slab
+ *          clusters, 3 = 128-row blocks times K pieces (tensor-core kernel)
+ *   out[4] blocks of the (first) launch
+ *   out[5] K slabs (8-token kernel) or K pieces per row block (tensor-core kernel)
+ *   out[6] pipeline stages
+ *   out[7] padded token count of the (first) launch
+ * With slab clusters on, their plan assumes that all num_sms / S clusters can be resident.
+ */
+nq_status nq_route_info(int bits, int mode, int T, int K, int N, int num_sms, int64_t out[8]);
+
+/*
  * nq_slab_clusters: turn slab clusters on (1) or off (0) for later projection calls of this
  * process, or only query (-1); returns the previous setting. Off unless the environment
  * variable NQ_CLUSTER is "1" at the first call. On GB300 a slab-cluster call is 8-23 %

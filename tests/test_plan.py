@@ -190,3 +190,63 @@ def test_tc_plan(nq, bits, T, K, N, sms):
     assert bounds[0] == 0 and bounds[-1] == G and all(b1 > b0 for b0, b1 in zip(bounds, bounds[1:]))
     assert p["tokens_padded"] in (16, 32, 64) and p["tokens_padded"] >= T > p["tokens_padded"] // 2 - (8 if T <= 16 else 0)
     assert 2 <= p["stages"] and p["smem_bytes"] <= 227 * 1024
+
+
+# The routing of the pages' shapes on a 152-SM GB300, each choice the measured winner (the
+# design notes give the times): (bits, mode, T, K, N) -> (kernel, launches, operands, split,
+# blocks, K slabs or pieces). kernel 0 = mma.sync 8-token, 1 = tcgen05; operands 0 = fp16,
+# 1 = bf16; split 0 = stream-K, 1 = whole row pairs, 3 = row blocks x K pieces.
+ROUTES = [
+    ((4, 0, 1, 5120, 17408), (0, 1, 0, 1, 136, 1)),    # decode Q4: fp16, four whole pairs per block
+    ((4, 0, 2, 5120, 17408), (0, 1, 0, 1, 136, 1)),
+    ((4, 0, 3, 5120, 17408), (0, 1, 1, 1, 136, 1)),    # T >= 3: bf16 operands
+    ((4, 0, 8, 5120, 17408), (0, 1, 1, 1, 136, 1)),
+    ((5, 0, 1, 5120, 6144), (0, 1, 0, 1, 96, 1)),      # spec-verify Q5: two whole pairs per block
+    ((5, 0, 8, 5120, 6144), (0, 1, 1, 1, 96, 1)),
+    ((5, 0, 8, 5120, 1024), (0, 1, 1, 1, 32, 1)),      # kv: one pair per block
+    ((5, 0, 1, 6144, 5120), (0, 1, 0, 1, 80, 1)),      # out projection T=1: whole pairs
+    ((5, 0, 8, 6144, 5120), (0, 1, 1, 0, 152, 1)),     # ... T=8: two stages only, stream-K
+    ((4, 0, 8, 17408, 5120), (0, 1, 1, 0, 152, 3)),    # down projection T=8: three K slabs
+    ((4, 1, 8, 5120, 17408), (0, 1, 1, 0, 152, 1)),    # fused gate/up: eight pairs per block, stream-K
+    ((5, 1, 8, 5120, 17408), (0, 1, 1, 0, 152, 1)),
+    ((14, 0, 1, 5120, 17408), (0, 1, 0, 1, 136, 1)),   # NVFP4: fp16 at every T
+    ((14, 0, 8, 5120, 17408), (0, 1, 0, 1, 136, 1)),
+    ((4, 0, 9, 5120, 17408), (1, 1, 1, 3, 136, 1)),    # T > 8: one tensor-core launch
+    ((4, 0, 64, 5120, 17408), (1, 1, 1, 3, 136, 1)),
+    ((5, 0, 16, 5120, 6144), (1, 1, 1, 3, 144, 3)),    # 48 row blocks x 3 K pieces
+    ((4, 0, 16, 17408, 5120), (1, 1, 1, 3, 120, 3)),
+    ((4, 1, 16, 5120, 17408), (1, 2, 1, 3, 136, 1)),   # SwiGLU: gate launch, then up launch
+    ((14, 0, 40, 5120, 17408), (1, 1, 1, 3, 136, 1)),
+]
+
+
+@pytest.mark.parametrize("shape,route", ROUTES)
+def test_routing_table(nq, shape, route):
+    r = nq.route_info(*shape, 152)
+    assert (r["kernel"], r["launches"], r["operands"], r["split"], r["ctas"], r["k_split"]) == route
+    if r["kernel"] == 0:
+        info = nq.plan_info(shape[0], shape[1], min(shape[2], 8), shape[3], shape[4], 152) if shape[0] != 14 else None
+        if info:
+            assert info["ctas"] == r["ctas"] and info["slabs"] == r["k_split"]
+    else:
+        tc = nq.plan_tc_info(shape[0], shape[2], shape[3], shape[4], 152)
+        assert tc["ctas"] == r["ctas"] and tc["k_pieces"] == r["k_split"] and tc["tokens_padded"] == r["tokens_padded"]
+
+
+def test_routing_without_tensor_core_batches(nq):
+    prev = nq.tensor_core_batches(0)
+    try:
+        r = nq.route_info(4, 0, 20, 5120, 17408, 152)
+        assert r["kernel"] == 0 and r["launches"] == 3 and r["operands"] == 1 and r["tokens_padded"] == 8
+        assert nq.route_info(4, 1, 64, 5120, 17408, 152)["launches"] == 8
+    finally:
+        nq.tensor_core_batches(prev)
+    assert nq.route_info(4, 0, 20, 5120, 17408, 152)["kernel"] == 1
+
+
+def test_routing_rejects_bad_arguments(nq):
+    from weight_only_groupwise_gb300.nq import NqError
+    for args in [(3, 0, 1, 64, 16), (14, 1, 1, 64, 16), (4, 2, 1, 64, 16), (4, 0, 0, 64, 16), (4, 0, 65, 64, 16),
+                 (4, 0, 1, 96, 16), (4, 0, 1, 64, 24)]:
+        with pytest.raises(NqError):
+            nq.route_info(*args, 152)

@@ -1101,6 +1101,60 @@ nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t ou
     return NQ_OK;
 }
 
+nq_status nq_route_info(int bits, int mode, int T, int K, int N, int num_sms, int64_t out[8]) {
+    if (!out) return NQ_ERR_NULL;
+    if ((bits != 4 && bits != 5 && bits != kFp4) || (mode != 0 && mode != 1) || (bits == kFp4 && mode == 1))
+        return NQ_ERR_SHAPE;
+    if (T < 1 || T > kMaxT || K < kGroup || N < kTileRows || num_sms < 1) return NQ_ERR_SHAPE;
+    nq_status st = check_shape(K, N);
+    if (st != NQ_OK) return st;
+    bool tc = true, cluster = false;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        read_env_locked();
+        tc = g_tc;
+        cluster = g_cluster;
+    }
+    // the branch project() takes: the tensor-core kernel for 8 < T <= 64 ...
+    if (tc && T > kSliceT && T <= kTcMaxT) {
+        TcPlan p;
+        if (make_tc_plan(bits, T, K, N, num_sms, p)) {
+            out[0] = 1;
+            out[1] = mode == 1 ? 2 : 1;
+            out[2] = 1;
+            out[3] = 3;
+            out[4] = p.P;
+            out[5] = p.KS;
+            out[6] = p.stages;
+            out[7] = p.TP;
+            return NQ_OK;
+        }
+    }
+    // ... else one launch of the 8-token kernel per slice of up to 8 tokens (the first slice's
+    // plan), slab clusters when switched on and K needs 2..4 bf16 slabs (assuming every
+    // cluster the SMs hold is resident)
+    const int full = T < kSliceT ? T : kSliceT;
+    Plan p;
+    if (!make_plan(bits, mode, full, K, N, num_sms, p)) return NQ_ERR_SHAPE;
+    int split = p.S == 1 && p.U % p.P == 0 && (p.U / p.P) % p.G == 0 ? 1 : 0;
+    if (cluster && p.S >= 2 && p.S <= kMaxCluster && !p.f16) {
+        Plan pc, qc;
+        if (make_cluster_plans(bits, mode, full, K, N, num_sms / p.S, pc, qc)) {
+            p = pc;
+            split = 2;
+        }
+    }
+    out[0] = 0;
+    out[1] = (T + kSliceT - 1) / kSliceT;
+    out[2] = p.f16 ? 0 : 1;
+    out[3] = split;
+    out[4] = p.P;
+    out[5] = p.S;
+    out[6] = p.stages;
+    out[7] = p.TP;
+    return NQ_OK;
+}
+
 int nq_slab_clusters(int enable) {
     DevState* d = nullptr;
     current_device(&d, nullptr);  // reads the environment once, like every call

@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.nq_tensor_core_batches.restype = I
         L.nq_plan_tc_info.argtypes = [I, I, I, I, I, P]
         L.nq_plan_tc_info.restype = I
+        L.nq_route_info.argtypes = [I, I, I, I, I, I, P]
+        L.nq_route_info.restype = I
         L.nq_slab_clusters.argtypes = [I]
         L.nq_slab_clusters.restype = I
         L.nq_plan_cluster_info.argtypes = [I, I, I, I, I, I, P]
@@ -463,6 +465,22 @@ def plan_tc_info(bits: int, T: int, K: int, N: int, num_sms: int) -> dict:
     out = (ctypes.c_int64 * 8)()
     _check(lib().nq_plan_tc_info(bits, T, K, N, num_sms, ctypes.cast(out, ctypes.c_void_p)))
     return dict(zip(TC_KEYS, list(out)))
+
+
+ROUTE_KEYS = ("kernel", "launches", "operands", "split", "ctas", "k_split", "stages", "tokens_padded")
+ROUTE_NAMES = {"kernel": ("mma.sync 8-token", "tcgen05"), "operands": ("fp16", "bf16"),
+               "split": ("stream-K", "whole row pairs", "slab clusters", "row blocks x K pieces")}
+
+
+def route_info(bits: int, mode: int, T: int, K: int, N: int, num_sms: int) -> dict:
+    """The kernel and variant a call of this shape takes with the current settings (host
+    only): ROUTE_KEYS, with the kernel, operand type and split also given by name."""
+    out = (ctypes.c_int64 * 8)()
+    _check(lib().nq_route_info(bits, mode, T, K, N, num_sms, ctypes.cast(out, ctypes.c_void_p)))
+    d = dict(zip(ROUTE_KEYS, list(out)))
+    for k, names in ROUTE_NAMES.items():
+        d[k + "_name"] = names[d[k]]
+    return d
 
 
 def slab_clusters(enable: int = -1) -> int:
