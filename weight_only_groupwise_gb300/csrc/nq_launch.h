@@ -54,9 +54,9 @@ int cluster_capacity_q5(int S, int smem);
 int cluster_capacity_swiglu_q4(int S, int smem);
 int cluster_capacity_swiglu_q5(int S, int smem);
 
-template <int BITS, bool SWIGLU, bool F16, bool ONE, bool CLU>
+template <int BITS, bool SWIGLU, bool F16, int EVEN, bool CLU>
 cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    auto kern = proj_kernel<BITS, SWIGLU, F16, ONE, CLU>;
+    auto kern = proj_kernel<BITS, SWIGLU, F16, EVEN, CLU>;
     // The shared-memory opt-in is per device; set it on every launch of a new size class
     // (cheap: the driver caches it) rather than tracking devices here.
     static thread_local int set_for_device = -1;
@@ -91,7 +91,7 @@ cudaError_t launch_proj_t(const ProjArgs& a, cudaStream_t stream, bool pdl) {
 
 template <int BITS, bool SWIGLU>
 int cluster_capacity_t(int S, int smem) {
-    auto kern = proj_kernel<BITS, SWIGLU, false, false, true>;
+    auto kern = proj_kernel<BITS, SWIGLU, false, 0, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -113,22 +113,28 @@ int cluster_capacity_t(int S, int smem) {
     return n;
 }
 
-// The operand type is part of the plan (a.p.f16): fp16 operands for small T, bf16 otherwise;
-// a single token has its own fp16 instantiation; slab clusters (a.p.cl > 1, bf16 only) theirs.
+// The operand type is part of the plan (a.p.f16): fp16 operands for small T, bf16 otherwise.
+// Up to four tokens sit in the even MMA columns (EVEN = 1, 2 for fp16; 4 for bf16 with
+// T = 3, 4): the tile epilogue then scales half the accumulators. Slab clusters (a.p.cl > 1,
+// bf16 only) have their own instantiation.
+static_assert(NQ_F16_MAX_T <= 2, "fp16-operand batches fit the two-token even layout");
+
 template <int BITS, bool SWIGLU>
 cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    if (a.p.cl > 1) return launch_proj_t<BITS, SWIGLU, false, false, true>(a, stream, pdl);
-    if (!a.p.f16) return launch_proj_t<BITS, SWIGLU, false, false, false>(a, stream, pdl);
-    return a.p.T == 1 ? launch_proj_t<BITS, SWIGLU, true, true, false>(a, stream, pdl)
-                      : launch_proj_t<BITS, SWIGLU, true, false, false>(a, stream, pdl);
+    if (a.p.cl > 1) return launch_proj_t<BITS, SWIGLU, false, 0, true>(a, stream, pdl);
+    if (!a.p.f16)
+        return a.p.T <= 4 ? launch_proj_t<BITS, SWIGLU, false, 4, false>(a, stream, pdl)
+                          : launch_proj_t<BITS, SWIGLU, false, 0, false>(a, stream, pdl);
+    return a.p.T == 1 ? launch_proj_t<BITS, SWIGLU, true, 1, false>(a, stream, pdl)
+                      : launch_proj_t<BITS, SWIGLU, true, 2, false>(a, stream, pdl);
 }
 
 // NVFP4 weights decode to fp16 at every T: only the fp16-operand instantiations exist (one
-// token, or up to eight).
+// token in column 0, or up to eight in columns 0..7).
 template <int BITS>
 cudaError_t launch_proj_f16_only(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    return a.p.T == 1 ? launch_proj_t<BITS, false, true, true, false>(a, stream, pdl)
-                      : launch_proj_t<BITS, false, true, false, false>(a, stream, pdl);
+    return a.p.T == 1 ? launch_proj_t<BITS, false, true, 1, false>(a, stream, pdl)
+                      : launch_proj_t<BITS, false, true, 0, false>(a, stream, pdl);
 }
 
 }  // namespace nq

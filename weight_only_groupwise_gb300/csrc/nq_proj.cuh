@@ -141,7 +141,7 @@ __device__ __forceinline__ constexpr int mtile_of(int t) { return t / GROUPS; }
 // partial P, minus the zero-point chain O of its group, times the group scale, is added to
 // the accumulator. NVFP4: the A registers already carry their block scales (exact fp16), so
 // the tile's partial is added as is.
-template <int BITS, bool F16, int GROUPS, int TILES, bool ONE = false>
+template <int BITS, bool F16, int GROUPS, int TILES, bool HALF = false>
 __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * TILES],
                                           const uint8_t* const (&scale)[GROUPS * TILES],
                                           const uint32_t (&xb)[GROUPS][8], const float2 (&o)[GROUPS],
@@ -189,7 +189,7 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * 
         if constexpr (FP4) {
             acc[m][0] += d[t][0];
             acc[m][2] += d[t][2];
-            if constexpr (!ONE) {
+            if constexpr (!HALF) {
                 acc[m][1] += d[t][1];
                 acc[m][3] += d[t][3];
             }
@@ -200,7 +200,7 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * 
             const int h = group_of<GROUPS>(t);
             acc[m][0] = fmaf(s.x, d[t][0] - o[h].x, acc[m][0]);
             acc[m][2] = fmaf(s.y, d[t][2] - o[h].x, acc[m][2]);
-            if constexpr (!ONE) {  // token columns 2(l%4) + 1: none when there is one token
+            if constexpr (!HALF) {  // token columns 2(l%4) + 1: none when tokens sit in even columns
                 acc[m][1] = fmaf(s.x, d[t][1] - o[h].y, acc[m][1]);
                 acc[m][3] = fmaf(s.y, d[t][3] - o[h].y, acc[m][3]);
             }
@@ -231,8 +231,10 @@ __device__ __forceinline__ int red_index(int w, int m, int tok, int row) {
     return ((w * 2 + m) * 32 + l) * 4 + j;
 }
 
-// ONE: a single token (T = 1), whose odd token columns need no scaling.
-template <int BITS, bool SWIGLU, bool F16, bool ONE, bool CLU>
+// EVEN = 0: token t in MMA column t (T <= 8). EVEN = n (1, 2 or 4): at most n tokens, token t
+// in column 2t, so that the odd columns of every lane hold no token and need no scaling, and
+// the epilogue loops are bounded by n tokens.
+template <int BITS, bool SWIGLU, bool F16, int EVEN, bool CLU>
 __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool FP4 = BITS == kFp4;
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         // Outputs per lane at most: one token (16 or 32 outputs), fp16 path (T <= 2: up to
         // 64), else 8 tokens (256). A compile-time bound keeps the epilogue code small.
         constexpr int kF16TP = NQ_F16_MAX_T <= 1 ? 1 : (NQ_F16_MAX_T <= 2 ? 2 : (NQ_F16_MAX_T <= 4 ? 4 : 8));
-        constexpr int kMaxTP = ONE ? 1 : ((F16 && !FP4) ? kF16TP : 8);
+        constexpr int kMaxTP = EVEN > 0 ? EVEN : ((F16 && !FP4) ? kF16TP : 8);
         constexpr int JN8 = (SWIGLU ? 16 : 32) * kMaxTP / 32 > 0 ? (SWIGLU ? 16 : 32) * kMaxTP / 32 : 1;
         grid_dependency_wait();  // Y, partial sums and tickets may still be in the preceding kernel's use
         Segment nat;
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 float s0 = 0.f, s1 = 0.f;
                 if (o < nout) {
                     const int m = SWIGLU ? 0 : o >> (4 + tp_log), tok = (o >> 4) & (TP - 1), row = o & 15;
-                    const float* r0 = rb + red_index(0, m, tok, row);
+                    const float* r0 = rb + red_index(0, m, EVEN > 0 ? 2 * tok : tok, row);
 #pragma unroll
                     for (int w = 0; w < NW; ++w) {
                         s0 += r0[w * 256];
@@ -589,11 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     uint32_t magic;
     asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(F16 ? kF16Magic : kBf16Magic));
 
-    // ldmatrix row addresses: lane l serves row (l & 7) of matrix (l >> 3); matrix mi covers
-    // K step (mi >> 1) and its half (mi & 1). Absent tokens read the zero row.
+    // ldmatrix row addresses: lane l serves row (l & 7) of matrix (l >> 3), i.e. MMA column
+    // l & 7; matrix mi covers K step (mi >> 1) and its half (mi & 1). Columns without a token
+    // (past T; with EVEN, the odd ones) read the zero row.
     const int lt = lane & 7, mi = lane >> 3;
-    const bool lt_valid = lt < T;
-    const uint32_t ld_base = lt_valid ? smem_u32(xs + lt * pitch + ((mi >> 1) * 16 + (mi & 1) * 8) * 2)
+    const int ltok = EVEN > 0 ? lt >> 1 : lt;
+    const bool lt_valid = (EVEN == 0 || (lt & 1) == 0) && ltok < T;
+    const uint32_t ld_base = lt_valid ? smem_u32(xs + ltok * pitch + ((mi >> 1) * 16 + (mi & 1) * 8) * 2)
                                       : smem_u32(zero_row);
     const uint32_t ld_group_step = lt_valid ? 128u : 0u;
     const uint32_t ld_half_step = lt_valid ? 64u : 0u;  // K steps 2,3 are 32 elements further
@@ -756,7 +760,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             __syncwarp();
             // 2^e of the lane's two token columns (from the max bits), applied at the hand-over
             {
-                const int m0 = xmax[2 * (lane & 3)], m1 = xmax[2 * (lane & 3) + 1];
+                const int m0 = xmax[EVEN > 0 ? (lane & 3) : 2 * (lane & 3)];
+                const int m1 = EVEN > 0 ? m0 : xmax[2 * (lane & 3) + 1];
                 const int e0 = F16 ? token_exponent(m0) : token_exponent_bf16(m0);
                 const int e1 = F16 ? token_exponent(m1) : token_exponent_bf16(m1);
                 tok_scale0 = __int_as_float((127 + e0) << 23);
@@ -803,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         code[t] = c0 + m * kTileArea + NW * h * TB;
                         scale[t] = s0 + m * kTileArea + NW * h * STB;
                     }
-                    tiles_mma<BITS, F16, GPW, 2, ONE>(code, scale, xb, o, magic, acc);
+                    tiles_mma<BITS, F16, GPW, 2, (EVEN > 0)>(code, scale, xb, o, magic, acc);
                 } else if (i0 == 0 && i1 == BG / 2) {
                     // the first half of a block (the 16-group tail of a row whose group count
                     // is 16 mod 32, e.g. K = 5120): groups warp and warp + NW, unrolled
@@ -827,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                         code[t] = c0 + m * kTileArea + NW * h * TB;
                         scale[t] = s0 + m * kTileArea + NW * h * STB;
                     }
-                    tiles_mma<BITS, F16, H, 2, ONE>(code, scale, xb, o, magic, acc);
+                    tiles_mma<BITS, F16, H, 2, (EVEN > 0)>(code, scale, xb, o, magic, acc);
                 } else {
                     // part of a block (first or last block of a run): group by group, in a
                     // loop that is not unrolled (rare, and it keeps the code small)
@@ -844,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                             const uint8_t* s0 = t0 + scale_lane + i * STB;
                             const uint8_t* const code[2] = {c0, c0 + kTileArea};
                             const uint8_t* const scale[2] = {s0, s0 + kTileArea};
-                            tiles_mma<BITS, F16, 1, 2, ONE>(code, scale, xb, o, magic, acc);
+                            tiles_mma<BITS, F16, 1, 2, (EVEN > 0)>(code, scale, xb, o, magic, acc);
                         }
                     }
                 }
