@@ -129,11 +129,13 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
                       : launch_proj_t<BITS, SWIGLU, true, 2, false>(a, stream, pdl);
 }
 
-// NVFP4 weights decode to fp16 at every T: only the fp16-operand instantiations exist (one
-// token in column 0, or up to eight in columns 0..7).
+// NVFP4 weights decode to fp16 at every T: only the fp16-operand instantiations exist, with
+// up to 1, 2 or 4 tokens in the even columns, or up to eight in columns 0..7.
 template <int BITS>
 cudaError_t launch_proj_f16_only(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    return a.p.T == 1 ? launch_proj_t<BITS, false, true, 1, false>(a, stream, pdl)
+    if (a.p.T == 1) return launch_proj_t<BITS, false, true, 1, false>(a, stream, pdl);
+    if (a.p.T == 2) return launch_proj_t<BITS, false, true, 2, false>(a, stream, pdl);
+    return a.p.T <= 4 ? launch_proj_t<BITS, false, true, 4, false>(a, stream, pdl)
                       : launch_proj_t<BITS, false, true, 0, false>(a, stream, pdl);
 }
 
