@@ -62,6 +62,9 @@ def lib():
         L.orc_dequant_fp4.argtypes = [P, P, ctypes.c_float, I, I, P]
         L.orc_gemm_fp4.argtypes = [P, P, P, ctypes.c_float, I, I, I, P]
         L.orc_gemm_fp4_rows.argtypes = [P, P, P, ctypes.c_float, I, I, P, I, P]
+        F = ctypes.c_float
+        L.orc_swiglu_fp4.argtypes = [P, P, P, F, P, P, F, I, I, I, P, P, P]
+        L.orc_swiglu_fp4_rows.argtypes = [P, P, P, F, P, P, F, I, I, P, I, P, P, P]
         L.orc_num_threads.restype = I
         L.orc_set_num_threads.argtypes = [I]
         _lib = L
@@ -221,6 +224,32 @@ def gemm_fp4_rows(x, codes, sf, g: float, T: int, K: int, rows) -> np.ndarray:
     y = np.empty((len(r), T), np.float64)
     lib().orc_gemm_fp4_rows(_p(x), _p(codes), _p(sf), float(g), T, K, _p(r), len(r), _p(y))
     return y
+
+
+def swiglu_fp4(x, cg, sfg, gg: float, cu, sfu, gu: float, T: int, K: int, N: int):
+    """NVFP4 gate/up block: (G fp64 [T][N], U fp64 [T][N], H bf16 bits [T][N])."""
+    x = _c(x, np.uint16)
+    cg, cu = _c(cg, np.uint32), _c(cu, np.uint32)
+    sfg, sfu = _c(sfg, np.uint8), _c(sfu, np.uint8)
+    g = np.empty((T, N), np.float64)
+    u = np.empty((T, N), np.float64)
+    h = np.empty((T, N), np.uint16)
+    lib().orc_swiglu_fp4(_p(x), _p(cg), _p(sfg), float(gg), _p(cu), _p(sfu), float(gu), T, K, N, _p(g), _p(u), _p(h))
+    return g, u, h
+
+
+def swiglu_fp4_rows(x, cg, sfg, gg: float, cu, sfu, gu: float, T: int, K: int, rows):
+    """(G, U, H) of the NVFP4 block on selected rows, each [len(rows)][T]."""
+    x = _c(x, np.uint16)
+    cg, cu = _c(cg, np.uint32), _c(cu, np.uint32)
+    sfg, sfu = _c(sfg, np.uint8), _c(sfu, np.uint8)
+    r = _c(rows, np.int32)
+    g = np.empty((len(r), T), np.float64)
+    u = np.empty((len(r), T), np.float64)
+    h = np.empty((len(r), T), np.uint16)
+    lib().orc_swiglu_fp4_rows(_p(x), _p(cg), _p(sfg), float(gg), _p(cu), _p(sfu), float(gu), T, K, _p(r), len(r),
+                              _p(g), _p(u), _p(h))
+    return g, u, h
 
 
 def num_threads() -> int:

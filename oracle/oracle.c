@@ -328,6 +328,23 @@ void orc_gemm_fp4_rows(const uint16_t* x, const uint32_t* codes, const uint8_t* 
     }
 }
 
+/* The SwiGLU block of an NVFP4 MLP: gate and up matrices, each with its own tensor scale;
+ * G, U in fp64 ([T][N] each) and H = bf16(silu(G) * U). */
+void orc_swiglu_fp4(const uint16_t* x, const uint32_t* cg, const uint8_t* sfg, float gg, const uint32_t* cu,
+                    const uint8_t* sfu, float gu, int T, int K, int N, double* g, double* u, uint16_t* h) {
+    orc_gemm_fp4(x, cg, sfg, gg, T, K, N, g);
+    orc_gemm_fp4(x, cu, sfu, gu, T, K, N, u);
+    for (size_t i = 0; i < (size_t)T * N; ++i) h[i] = orc_round_bf16(orc_silu_mul(g[i], u[i]));
+}
+
+void orc_swiglu_fp4_rows(const uint16_t* x, const uint32_t* cg, const uint8_t* sfg, float gg, const uint32_t* cu,
+                         const uint8_t* sfu, float gu, int T, int K, const int* rows, int count, double* g,
+                         double* u, uint16_t* h) {
+    orc_gemm_fp4_rows(x, cg, sfg, gg, T, K, rows, count, g);
+    orc_gemm_fp4_rows(x, cu, sfu, gu, T, K, rows, count, u);
+    for (size_t i = 0; i < (size_t)count * T; ++i) h[i] = orc_round_bf16(orc_silu_mul(g[i], u[i]));
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -124,6 +124,23 @@ def fp4_problem(T: int, K: int, N: int, seed: int, g: float = FP4_GLOBAL_SCALE) 
     return {"T": T, "K": K, "N": N, "x": x, "codes": codes, "sf": sf, "g": float(g)}
 
 
+FP4_UP_SCALE = 0.005859375  # 3 * 2^-9: a tensor scale for the up matrix that differs from the gate's
+
+
+def swiglu_fp4_problem(T: int, K: int, N: int, seed: int, gg: float = FP4_GLOBAL_SCALE,
+                       gu: float = FP4_UP_SCALE) -> dict:
+    """The NVFP4 gate/up block: gate codes, up codes, gate block scales, up block scales (the
+    draws of fp4_problem, twice), then X; gg, gu are the two tensor scales."""
+    rg = rng(seed)
+    cg = code_words(rg, N, K // 8)
+    cu = code_words(rg, N, K // 8)
+    sfg = e4m3_bits(np.exp(SCALE_SIGMA * rg.standard_normal((N, K // FP4_BLOCK))).astype(np.float32))
+    sfu = e4m3_bits(np.exp(SCALE_SIGMA * rg.standard_normal((N, K // FP4_BLOCK))).astype(np.float32))
+    x = activations(rg, T, K)
+    return {"T": T, "K": K, "N": N, "x": x, "cg": cg, "sfg": sfg, "gg": float(gg), "cu": cu, "sfu": sfu,
+            "gu": float(gu)}
+
+
 # The five workloads. Shapes are those of a 27B-class dense decoder layer.
 TINY_Q4 = dict(T=1, K=256, N=128, seed=0)                  # tiny Q4 correctness case
 DECODE_Q4 = dict(T=1, K=5120, N=17408, seed=1)             # decode GEMV, FFN up-projection

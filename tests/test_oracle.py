@@ -371,6 +371,40 @@ def test_fp4_block_structure():
     assert np.array_equal(w, exact)
 
 
+def test_swiglu_fp4_vs_twin():
+    """The NVFP4 gate/up block against the NumPy twin, with different gate and up tensor scales
+    (a swapped or shared scale would fail), and its row variant against the full block."""
+    T, K, N = 6, 256, 32
+    p = si.swiglu_fp4_problem(T, K, N, 43)
+    assert p["gg"] != p["gu"]
+    g, u, h = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, N)
+    g_t = twin.gemm_fp4(p["x"], p["cg"], p["sfg"], p["gg"], K)
+    u_t = twin.gemm_fp4(p["x"], p["cu"], p["sfu"], p["gu"], K)
+    assert np.max(np.abs(g - g_t)) <= 1e-12 * np.max(np.abs(g_t))
+    assert np.max(np.abs(u - u_t)) <= 1e-12 * np.max(np.abs(u_t))
+    h_t = twin.silu(g_t) * u_t
+    h_ours = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.all(np.abs(h_ours - h_t) <= 2.0**-7 * np.abs(h_t) + 1e-30)
+    rows = [31, 0, 7]
+    gr, ur, hr = oracle.swiglu_fp4_rows(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, rows)
+    assert np.array_equal(hr, h[:, rows].T) and np.array_equal(gr, g[:, rows].T) and np.array_equal(ur, u[:, rows].T)
+
+
+def test_swiglu_fp4_closed_forms():
+    """Code 0 is +0: an all-zero gate gives g = 0 and h a zero carrying u's sign; an all-zero up
+    gives u = 0 and h a zero carrying g's sign. Doubling the up tensor scale doubles u exactly."""
+    T, K, N = 2, 128, 16
+    p = si.swiglu_fp4_problem(T, K, N, 47)
+    z = np.zeros_like(p["cg"])
+    g, u, h = oracle.swiglu_fp4(p["x"], z, p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, N)
+    assert np.all(g == 0.0) and np.array_equal(h, np.where(u < 0, 0x8000, 0).astype(np.uint16))
+    g, u, h = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], z, p["sfu"], p["gu"], T, K, N)
+    assert np.all(u == 0.0) and np.array_equal(h, np.where(g < 0, 0x8000, 0).astype(np.uint16))
+    _, u1, _ = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, N)
+    _, u2, _ = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], 2 * p["gu"], T, K, N)
+    assert np.array_equal(u2, 2.0 * u1)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 MUTATIONS = [
