@@ -12,7 +12,7 @@ steps are replayed as one CUDA graph of K back-to-back launches (how a decode en
 them), bracketed by CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode_q4|verify_q5|swiglu_block|swiglu_block_q5|layer_stack] [--T T]
+                  [--workload decode_q4|verify_q5|swiglu_block|swiglu_block_q5|swiglu_block_fp4|layer_stack] [--T T]
                   [--no-sweep] [--no-cpu-baseline]
 
 --impl reference times the CPU oracle (the deliberately slow fp64 definition) on the host
@@ -62,17 +62,28 @@ def job_rate_gbs(bytes_per_step_per_rank: int, ms_per_step: float, world: int) -
 
 # ---------------------------------------------------------------- workloads
 
+FP4 = 14  # format tag of NVFP4 weights in the library's calls
+
+
+def weight_bytes(bits: int, K: int, N: int) -> int:
+    """Packed codes + packed scales of one K x N matrix: Q4 / Q5 codes with an fp16 scale per
+    64 along K; NVFP4 e2m1 codes (K*N/2) with an e4m3 scale per 16 (N*K/16)."""
+    if bits == FP4:
+        return K * N // 2 + N * K // 16
+    return K * N * bits // 8 + N * (K // 64) * 2
+
+
 def proj_bytes(bits: int, T: int, K: int, N: int) -> int:
-    return K * N * bits // 8 + N * (K // 64) * 2 + T * K * 2 + T * N * 2
+    return weight_bytes(bits, K, N) + T * K * 2 + T * N * 2
 
 
 def fp4_bytes(T: int, K: int, N: int) -> int:
     """NVFP4: e2m1 codes (K*N/2) + e4m3 block scales (N*K/16) + X + Y."""
-    return K * N // 2 + N * K // 16 + T * K * 2 + T * N * 2
+    return proj_bytes(FP4, T, K, N)
 
 
 def swiglu_bytes(T: int, K: int, N: int, bits: int = 4) -> int:
-    return 2 * (K * N * bits // 8 + N * (K // 64) * 2) + T * K * 2 + T * N * 2
+    return 2 * weight_bytes(bits, K, N) + T * K * 2 + T * N * 2
 
 
 WORKLOADS = {
@@ -84,6 +95,8 @@ WORKLOADS = {
                          desc="SwiGLU block Q4, T=8: fused gate+up K=5120 N=17408, then down K=17408 N=5120"),
     "swiglu_block_q5": dict(kind="swiglu", bits=5, T=8, K=5120, N=17408, Kd=17408, Nd=5120,
                             desc="SwiGLU block Q5, T=8: fused gate+up K=5120 N=17408, then down K=17408 N=5120"),
+    "swiglu_block_fp4": dict(kind="swiglu", bits=FP4, T=8, K=5120, N=17408, Kd=17408, Nd=5120,
+                             desc="SwiGLU block NVFP4, T=8: fused gate+up K=5120 N=17408, then down K=17408 N=5120"),
     "layer_stack": dict(kind="stack", T=8, layers=64,
                         desc="64 independent 27B-class layers: fused gate+up and down (Q4), "
                              "q-gate 5120x6144, kv 5120x1024, out 6144x5120 (Q5)"),
@@ -283,11 +296,23 @@ def build_step(nq, w: dict, dev, T_override=None):
         bits, T, K, N, Kd, Nd = w["bits"], T_override or w["T"], w["K"], w["N"], w["Kd"], w["Nd"]
         b = swiglu_bytes(T, K, N, bits) + proj_bytes(bits, T, Kd, Nd)
         R = max(2, -(-3 * L2_BYTES // b))
-        gate = make_proj_copies(nq, bits, K, N, R, 3 + 10 * (bits - 4), dev)
-        up = make_proj_copies(nq, bits, K, N, R, 4 + 10 * (bits - 4), dev)
-        down = make_proj_copies(nq, bits, Kd, Nd, R, 5 + 10 * (bits - 4), dev)
-        fused = nq.swiglu_q4 if bits == 4 else nq.swiglu_q5
-        fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
+        if bits == FP4:
+            gate = make_fp4_copies(nq, K, N, R, 33, dev)
+            up = make_fp4_copies(nq, K, N, R, 34, dev)
+            down = make_fp4_copies(nq, Kd, Nd, R, 35, dev)
+            gsc = si.FP4_GLOBAL_SCALE
+
+            def fused(x, wg, sg, wu, su, n, out):
+                nq.swiglu_fp4(x, wg, sg, gsc, wu, su, gsc, n, out=out)
+
+            def fn(x, wd, sd, n, out):
+                nq.gemm_fp4(x, wd, sd, gsc, n, out=out)
+        else:
+            gate = make_proj_copies(nq, bits, K, N, R, 3 + 10 * (bits - 4), dev)
+            up = make_proj_copies(nq, bits, K, N, R, 4 + 10 * (bits - 4), dev)
+            down = make_proj_copies(nq, bits, Kd, Nd, R, 5 + 10 * (bits - 4), dev)
+            fused = nq.swiglu_q4 if bits == 4 else nq.swiglu_q5
+            fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
         x = si.device_activations(T, K, gen, dev)
         h = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         y = torch.empty((T, Nd), dtype=torch.bfloat16, device=dev)
@@ -520,31 +545,40 @@ def oracle_sample(w: dict, budget_s: float):
     if w["kind"] != "proj":
         w = dict(kind="proj", bits=w.get("bits", 4), T=w.get("T", 8), K=5120, N=17408)
     bits, T, K, N = w["bits"], w["T"], w["K"], w["N"]
-    p = si.q4_problem(T, K, N, 1) if bits == 4 else si.q5_problem(T, K, N, 2)
+    if bits == FP4:
+        p = si.fp4_problem(T, K, N, 3)
+
+        def run(rows):
+            oracle.gemm_fp4_rows(p["x"], p["codes"], p["sf"], p["g"], T, K, rows)
+    elif bits == 4:
+        p = si.q4_problem(T, K, N, 1)
+
+        def run(rows):
+            oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows)
+    else:
+        p = si.q5_problem(T, K, N, 2)
+
+        def run(rows):
+            oracle.gemm_q5_rows(p["x"], p["wn"], p["wh"], p["s"], T, K, rows)
     rows_all = np.arange(N, dtype=np.int32)
     # first: one pass over a 1/16 row sample to size the run
     n0 = max(16, N // 16)
     t0 = time.perf_counter()
-    if bits == 4:
-        oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows_all[:n0])
-    else:
-        oracle.gemm_q5_rows(p["x"], p["wn"], p["wh"], p["s"], T, K, rows_all[:n0])
+    run(rows_all[:n0])
     t_row = (time.perf_counter() - t0) / n0
     rows = int(min(N, max(n0, budget_s / max(t_row, 1e-12))))
     # the whole problem fits the budget: repeat full passes until the budget is used
     reps = max(1, int(budget_s / max(t_row * N, 1e-9))) if rows == N else 1
     t0 = time.perf_counter()
     for _ in range(reps):
-        if bits == 4:
-            oracle.gemm_q4_rows(p["x"], p["wq"], p["s"], T, K, rows_all[:rows])
-        else:
-            oracle.gemm_q5_rows(p["x"], p["wn"], p["wh"], p["s"], T, K, rows_all[:rows])
+        run(rows_all[:rows])
     dt = (time.perf_counter() - t0) / reps
     frac = rows / N
     sample_bytes = proj_bytes(bits, T, K, N) * frac
     gbs = sample_bytes / dt / 1e9
     us_full = dt / frac * 1e6
-    desc = (f"CPU fp64 oracle on {rows}/{N} output rows of the {bits}-bit T={T} K={K} N={N} "
+    fmt = "NVFP4" if bits == FP4 else f"{bits}-bit"
+    desc = (f"CPU fp64 oracle on {rows}/{N} output rows of the {fmt} T={T} K={K} N={N} "
             f"projection, {reps} pass(es) of {dt:.2f} s, bytes scaled by the row fraction")
     return gbs, us_full, oracle.num_threads(), desc, (rows, dt)
 
@@ -718,7 +752,8 @@ def sweep(nq, dev, stream, peak):
         record("decode_fp4", T, time_graph(step, 100, 5, stream), 100, fp4_bytes(T, K, N), 1)
     del copies
     torch.cuda.empty_cache()
-    for name, T in (("swiglu_block", 8), ("swiglu_block_q5", 8), ("swiglu_block", 16), ("swiglu_block", 64)):
+    for name, T in (("swiglu_block", 8), ("swiglu_block_q5", 8), ("swiglu_block", 16), ("swiglu_block", 64),
+                    ("swiglu_block_fp4", 8), ("swiglu_block_fp4", 16)):
         w = dict(WORKLOADS[name], T=T)
         step, b, R, note, keep = build_step(nq, w, dev)
         steps = 100

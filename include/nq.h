@@ -251,6 +251,19 @@ nq_status nq_pack_fp4(const uint32_t* codes_canon, const uint8_t* sf_canon, int 
 nq_status nq_gemm_fp4(const void* X, const void* Wq, const void* S, float global_scale, void* Y, int T, int K,
                       int N, void* stream);
 
+/*
+ * nq_swiglu_fp4: the SwiGLU block of an NVFP4 MLP (the pages' NVFP4 MLP projections, "ninfer-ext"
+ * README, section "与原版 NInfer 的对比"): as nq_swiglu_q4 with gate and up weights packed by
+ * nq_pack_fp4, each with its own tensor scale:
+ *   g = X * W(Wg, Sg, gate_scale),  u = X * W(Wu, Su, up_scale),  H = bf16(silu(g) * u).
+ * T <= 8: one launch computing g and u together (fp16 operands, tensor scales applied to the
+ * fp32 partials); 8 < T <= 64: the two tensor-core launches of nq_swiglu_q4. Arguments,
+ * alignment, errors and launch behaviour as nq_swiglu_q4; the down projection is nq_gemm_fp4
+ * on H.
+ */
+nq_status nq_swiglu_fp4(const void* X, const void* Wg, const void* Sg, float gate_scale, const void* Wu,
+                        const void* Su, float up_scale, void* H, int T, int K, int N, void* stream);
+
 /* nq_dequant_fp4_debug: out[n][k] = g * (scale * element) in fp32 through the kernels' own
  * decoder; exact, so it must equal the CPU definition bit for bit. */
 nq_status nq_dequant_fp4_debug(const void* Wq, const void* S, float global_scale, float* out, int K, int N,
@@ -322,7 +335,8 @@ nq_status nq_program_create(nq_program** out);
 /*
  * Recording calls: append one projection call to the program. Arguments, layouts and
  * ownership are those of the call named (nq_gemm_q4 / nq_gemm_q5 for bits 4 / 5,
- * nq_gemm_fp4, nq_swiglu_q4 / nq_swiglu_q5, nq_gemm_q4_grouped / nq_gemm_q5_grouped), without
+ * nq_gemm_fp4, nq_swiglu_q4 / nq_swiglu_q5, nq_swiglu_fp4, nq_gemm_q4_grouped /
+ * nq_gemm_q5_grouped), without
  * the stream. Every host-side check of that call runs here, on the host and without a GPU
  * (shape, NULL, alignment, aliasing: the same status codes); a call that fails them is not
  * recorded. An empty call (T == 0 or N == 0) is accepted and records nothing. Recording into
@@ -334,6 +348,8 @@ nq_status nq_program_gemm_fp4(nq_program* prog, const void* X, const void* Wq, c
                               void* Y, int T, int K, int N);
 nq_status nq_program_swiglu(nq_program* prog, int bits, const void* X, const void* Wg, const void* Sg,
                             const void* Wu, const void* Su, void* H, int T, int K, int N);
+nq_status nq_program_swiglu_fp4(nq_program* prog, const void* X, const void* Wg, const void* Sg, float gate_scale,
+                                const void* Wu, const void* Su, float up_scale, void* H, int T, int K, int N);
 nq_status nq_program_grouped(nq_program* prog, int bits, const void* X, const nq_group* groups, int count, int T,
                              int K);
 
@@ -452,8 +468,8 @@ nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t ou
  * current settings (nq_tensor_core_batches, nq_slab_clusters), for a GPU of num_sms SMs; host
  * only, no GPU needed. The pages route their small-batch projections by shape ("NInfer-4090"
  * release post, section "V3 做了什么": T=8 routing); this is the library's routing, each
- * choice measured on GB300. bits 4, 5 or 14 (NVFP4); mode 0 = gemm, 1 = SwiGLU block (4 or 5
- * bits); 1 <= T <= 64.
+ * choice measured on GB300. bits 4, 5 or 14 (NVFP4); mode 0 = gemm, 1 = SwiGLU block;
+ * 1 <= T <= 64.
  *   out[0] kernel: 0 = the 8-token kernel (mma.sync), 1 = the tensor-core kernel (tcgen05)
  *   out[1] launches per call (slices of 8 tokens, or the SwiGLU block's two tensor-core launches)
  *   out[2] MMA operand type: 0 = fp16 (T <= 2, and NVFP4 on the 8-token kernel), 1 = bf16

@@ -17,6 +17,10 @@ def test_algorithmic_bytes():
     assert bench.proj_bytes(5, 8, 5120, 6144) == 19660800 + 983040 + 81920 + 98304 == 20824064
     # NVFP4: codes K*N/2 + e4m3 scales N*K/16
     assert bench.fp4_bytes(1, 5120, 17408) == 44564480 + 5570560 + 10240 + 34816
+    assert bench.weight_bytes(bench.FP4, 5120, 17408) == 44564480 + 5570560
+    w4 = bench.WORKLOADS["swiglu_block_fp4"]
+    assert bench.workload_bytes(w4) == (2 * (44564480 + 5570560) + 8 * 5120 * 2 + 8 * 17408 * 2
+                                        + bench.fp4_bytes(8, 17408, 5120))
     # SwiGLU block: two weight sets on one X, one H
     w = bench.WORKLOADS["swiglu_block"]
     assert bench.workload_bytes(w) == (2 * (44564480 + 2785280) + 8 * 5120 * 2 + 8 * 17408 * 2

@@ -182,3 +182,71 @@ def test_fp4_tc_activation_outliers(nq):
     for t in range(T):
         assert np.all(np.isfinite(y[t])), t
         assert gu.rel_err(y[t], y_ref[t]) <= gu.TOL, t
+
+
+# ---------------------------------------------------------------- NVFP4 SwiGLU blocks
+# The gate/up block of an NVFP4 MLP, gate and up with different tensor scales: one launch for
+# T <= 8, two tensor-core launches (gate -> fp32 G, up -> bf16 silu(G) * U) for 8 < T <= 64.
+# H against silu(g) * u from the oracle's fp64 g and u, at the parity bar of the other blocks.
+
+def _swiglu_fp4(nq, p, T, K, N):
+    wg = nq.pack_fp4(gu.dev_u32(p["cg"]), torch.from_numpy(np.ascontiguousarray(p["sfg"])).cuda(), K, N)
+    wu = nq.pack_fp4(gu.dev_u32(p["cu"]), torch.from_numpy(np.ascontiguousarray(p["sfu"])).cuda(), K, N)
+    return wg, wu
+
+
+SWIGLU_FP4_SHAPES = [(1, 256, 48, 0), (2, 640, 16, 1), (3, 1024, 272, 2), (4, 320, 112, 3), (8, 6208, 32, 4),
+                     (6, 17408, 64, 5), (9, 640, 272, 6), (16, 1024, 1040, 7), (33, 5120, 384, 8),
+                     (64, 512, 144, 9), (48, 17408, 96, 10)]
+
+
+@pytest.mark.parametrize("T,K,N,seed", SWIGLU_FP4_SHAPES)
+def test_swiglu_fp4_parity(nq, T, K, N, seed):
+    p = si.swiglu_fp4_problem(T, K, N, 700 + seed)
+    wg, wu = _swiglu_fp4(nq, p, T, K, N)
+    h = gu.host_f64(nq.swiglu_fp4(gu.dev_bf16(p["x"]), *wg, p["gg"], *wu, p["gu"], N))
+    g, u, _ = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, N)
+    assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+    nq.device_error()
+
+
+@pytest.mark.parametrize("T", [8, 16])
+def test_swiglu_fp4_full_size_sampled(nq, T):
+    """The NVFP4 SwiGLU block at the 27B-class MLP shape (K=5120, N=17408), sampled rows."""
+    K, N = 5120, 17408
+    p = si.swiglu_fp4_problem(T, K, N, 720 + T)
+    wg, wu = _swiglu_fp4(nq, p, T, K, N)
+    h = gu.host_f64(nq.swiglu_fp4(gu.dev_bf16(p["x"]), *wg, p["gg"], *wu, p["gu"], N))
+    rows = gu.sample_rows(N, 256, 17)
+    g, u, _ = oracle.swiglu_fp4_rows(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, rows)
+    assert gu.rel_err(h[:, rows], (g / (1.0 + np.exp(-g)) * u).T) <= gu.TOL
+
+
+def test_swiglu_fp4_scales_are_per_matrix_and_deterministic(nq):
+    """Swapping the two tensor scales changes H (each scale belongs to its matrix); equal calls
+    give equal bits; tensor-core batches agree with 8-token slices within the bar."""
+    T, K, N = 20, 1024, 272
+    p = si.swiglu_fp4_problem(T, K, N, 740)
+    wg, wu = _swiglu_fp4(nq, p, T, K, N)
+    x = gu.dev_bf16(p["x"])
+    h1 = nq.swiglu_fp4(x, *wg, p["gg"], *wu, p["gu"], N)
+    h2 = nq.swiglu_fp4(x, *wg, p["gg"], *wu, p["gu"], N)
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    hs = nq.swiglu_fp4(x, *wg, p["gu"], *wu, p["gg"], N)
+    assert not torch.equal(h1.view(torch.int16), hs.view(torch.int16))
+    prev = nq.tensor_core_batches(0)
+    try:
+        h_sl = nq.swiglu_fp4(x, *wg, p["gg"], *wu, p["gu"], N)
+    finally:
+        nq.tensor_core_batches(prev)
+    g, u, _ = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, N)
+    ref = g / (1.0 + np.exp(-g)) * u
+    for h in (h1, h_sl):
+        assert gu.rel_err(gu.host_f64(h), ref) <= gu.TOL
+    for T8 in (3, 8):                       # the 8-token kernel with the swapped scales as well
+        q = si.swiglu_fp4_problem(T8, K, N, 741 + T8)
+        qg, qu = _swiglu_fp4(nq, q, T8, K, N)
+        hq = gu.host_f64(nq.swiglu_fp4(gu.dev_bf16(q["x"]), *qg, q["gu"], *qu, q["gg"], N))
+        g, u, _ = oracle.swiglu_fp4(q["x"], q["cg"], q["sfg"], q["gu"], q["cu"], q["sfu"], q["gg"], T8, K, N)
+        assert gu.rel_err(hq, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+    nq.device_error()

@@ -217,6 +217,8 @@ ROUTES = [
     ((4, 0, 16, 17408, 5120), (1, 1, 1, 3, 120, 3)),
     ((4, 1, 16, 5120, 17408), (1, 2, 1, 3, 136, 1)),   # SwiGLU: gate launch, then up launch
     ((14, 0, 40, 5120, 17408), (1, 1, 1, 3, 136, 1)),
+    ((14, 1, 8, 5120, 17408), (0, 1, 0, 0, 152, 1)),   # NVFP4 SwiGLU: fp16, stream-K like Q4
+    ((14, 1, 16, 5120, 17408), (1, 2, 1, 3, 136, 1)),  # ... and two tensor-core launches
 ]
 
 
@@ -246,7 +248,7 @@ def test_routing_without_tensor_core_batches(nq):
 
 def test_routing_rejects_bad_arguments(nq):
     from weight_only_groupwise_gb300.nq import NqError
-    for args in [(3, 0, 1, 64, 16), (14, 1, 1, 64, 16), (4, 2, 1, 64, 16), (4, 0, 0, 64, 16), (4, 0, 65, 64, 16),
+    for args in [(3, 0, 1, 64, 16), (6, 1, 1, 64, 16), (4, 2, 1, 64, 16), (4, 0, 0, 64, 16), (4, 0, 65, 64, 16),
                  (4, 0, 1, 96, 16), (4, 0, 1, 64, 24)]:
         with pytest.raises(NqError):
             nq.route_info(*args, 152)

@@ -469,7 +469,8 @@ nq_status projection_args(int bits, bool swiglu, const void* X, const void* W0, 
 }
 
 nq_status project(int bits, bool swiglu, const void* X, const void* W0, const void* S0, const void* W1,
-                  const void* S1, void* Y, int T, int K, int N, void* stream, float gscale = 1.f) {
+                  const void* S1, void* Y, int T, int K, int N, void* stream, float gscale = 1.f,
+                  float gscale1 = 1.f) {
     nq_status st = projection_args(bits, swiglu, X, W0, S0, W1, S1, Y, T, K, N);
     if (st != NQ_OK) return st;
     if (T == 0 || N == 0) return NQ_OK;  // empty output
@@ -482,7 +483,7 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
     // Larger batches: the tensor-core kernel, one weight pass per matrix. A SwiGLU block is two
     // launches on the same X: the gate projection writes fp32 G to a library buffer, the up
     // projection's epilogue writes H = silu(G) * U in bf16.
-    if (g_tc && (bits == 4 || bits == 5 || (bits == kFp4 && !swiglu)) && T > kSliceT && T <= kTcMaxT) {
+    if (g_tc && (bits == 4 || bits == 5 || bits == kFp4) && T > kSliceT && T <= kTcMaxT) {
         alignas(64) TcArgs ta;
         alignas(64) TcArgs tu;
         if (make_tc_plan(bits, T, K, N, d->sms, ta.p) && encode_x_map(&ta.xmap, X, T, K, ta.p.TP) &&
@@ -514,6 +515,7 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
             tu.smap = smap;
             tu.W = static_cast<const uint8_t*>(W1);
             tu.S = static_cast<const uint8_t*>(S1);
+            tu.gscale = gscale1;
             return launch_tc_proj_swiglu(bits, kTcOutSwiglu, tu, as_stream(stream), g_pdl) == cudaSuccess ? NQ_OK
                                                                                                 : NQ_ERR_CUDA;
         }
@@ -542,9 +544,10 @@ nq_status project(int bits, bool swiglu, const void* X, const void* W0, const vo
         a.partials = reinterpret_cast<float*>(d->ws + ws_partials_off(d->tickets_cap));
         a.wait_ns = g_wait_ns;
         a.gscale = gscale;
+        a.gscale1 = swiglu ? gscale1 : gscale;
         cudaError_t e;
         if (bits == kFp4)
-            e = launch_proj_fp4(a, as_stream(stream), g_pdl);
+            e = swiglu ? launch_proj_swiglu_fp4(a, as_stream(stream), g_pdl) : launch_proj_fp4(a, as_stream(stream), g_pdl);
         else if (swiglu)
             e = bits == 4 ? launch_proj_swiglu_q4(a, as_stream(stream), g_pdl)
                           : launch_proj_swiglu_q5(a, as_stream(stream), g_pdl);
@@ -665,7 +668,7 @@ nq_status reserve_projection(int bits, bool swiglu, int T, int K, int N) {
     DevState* d = nullptr;
     nq_status st = current_device(&d, nullptr);
     if (st != NQ_OK) return st;
-    if (g_tc && (bits == 4 || bits == 5 || (bits == kFp4 && !swiglu)) && T > kSliceT && T <= kTcMaxT) {
+    if (g_tc && (bits == 4 || bits == 5 || bits == kFp4) && T > kSliceT && T <= kTcMaxT) {
         TcPlan p;
         if (make_tc_plan(bits, T, K, N, d->sms, p)) {
             st = ensure_workspace(*d, 1, 1);
@@ -922,6 +925,11 @@ nq_status nq_swiglu_q5(const void* X, const void* Wg, const void* Sg, const void
     return project(5, true, X, Wg, Sg, Wu, Su, H, T, K, N, stream);
 }
 
+nq_status nq_swiglu_fp4(const void* X, const void* Wg, const void* Sg, float gate_scale, const void* Wu,
+                        const void* Su, float up_scale, void* H, int T, int K, int N, void* stream) {
+    return project(kFp4, true, X, Wg, Sg, Wu, Su, H, T, K, N, stream, gate_scale, up_scale);
+}
+
 nq_status nq_dequant_q4_debug(const void* Wq, const void* S, float* W, int K, int N, void* stream) {
     return dequant(4, true, Wq, S, W, K, N, stream);
 }
@@ -1103,8 +1111,7 @@ nq_status nq_plan_tc_info(int bits, int T, int K, int N, int num_sms, int64_t ou
 
 nq_status nq_route_info(int bits, int mode, int T, int K, int N, int num_sms, int64_t out[8]) {
     if (!out) return NQ_ERR_NULL;
-    if ((bits != 4 && bits != 5 && bits != kFp4) || (mode != 0 && mode != 1) || (bits == kFp4 && mode == 1))
-        return NQ_ERR_SHAPE;
+    if ((bits != 4 && bits != 5 && bits != kFp4) || (mode != 0 && mode != 1)) return NQ_ERR_SHAPE;
     if (T < 1 || T > kMaxT || K < kGroup || N < kTileRows || num_sms < 1) return NQ_ERR_SHAPE;
     nq_status st = check_shape(K, N);
     if (st != NQ_OK) return st;

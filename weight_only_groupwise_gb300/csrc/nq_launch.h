@@ -17,7 +17,8 @@ bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, con
                         int TP);
 cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc_proj_fp4(const TcArgs& a, cudaStream_t stream, bool pdl);
-// The two launches of a SwiGLU block (mode kTcOutGate, then kTcOutSwiglu), 4- or 5-bit codes.
+// The two launches of a SwiGLU block (mode kTcOutGate, then kTcOutSwiglu), 4- or 5-bit codes
+// or NVFP4 weights (bits 14).
 cudaError_t launch_tc_proj_swiglu(int bits, int mode, const TcArgs& a, cudaStream_t stream, bool pdl);
 
 // Bound of every device-side wait for later launches (nq_wait_limit; NQ_WAIT_NS).
@@ -45,6 +46,7 @@ cudaError_t launch_proj_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_swiglu_q5(const ProjArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_proj_fp4(const ProjArgs& a, cudaStream_t stream, bool pdl);
+cudaError_t launch_proj_swiglu_fp4(const ProjArgs& a, cudaStream_t stream, bool pdl);
 
 // Slab clusters of S blocks that can be resident at once for the slab-cluster
 // instantiation with `smem` bytes of shared memory per block (cudaOccupancyMaxActiveClusters);
@@ -131,12 +133,12 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream, bool pdl) {
 
 // NVFP4 weights decode to fp16 at every T: only the fp16-operand instantiations exist, with
 // up to 1, 2 or 4 tokens in the even columns, or up to eight in columns 0..7.
-template <int BITS>
+template <int BITS, bool SWIGLU = false>
 cudaError_t launch_proj_f16_only(const ProjArgs& a, cudaStream_t stream, bool pdl) {
-    if (a.p.T == 1) return launch_proj_t<BITS, false, true, 1, false>(a, stream, pdl);
-    if (a.p.T == 2) return launch_proj_t<BITS, false, true, 2, false>(a, stream, pdl);
-    return a.p.T <= 4 ? launch_proj_t<BITS, false, true, 4, false>(a, stream, pdl)
-                      : launch_proj_t<BITS, false, true, 0, false>(a, stream, pdl);
+    if (a.p.T == 1) return launch_proj_t<BITS, SWIGLU, true, 1, false>(a, stream, pdl);
+    if (a.p.T == 2) return launch_proj_t<BITS, SWIGLU, true, 2, false>(a, stream, pdl);
+    return a.p.T <= 4 ? launch_proj_t<BITS, SWIGLU, true, 4, false>(a, stream, pdl)
+                      : launch_proj_t<BITS, SWIGLU, true, 0, false>(a, stream, pdl);
 }
 
 }  // namespace nq

@@ -21,7 +21,7 @@
 
 namespace {
 
-enum class CallKind { kGemm, kGemmFp4, kSwiglu, kGrouped };
+enum class CallKind { kGemm, kGemmFp4, kSwiglu, kSwigluFp4, kGrouped };
 
 struct RecordedCall {
     CallKind kind;
@@ -32,7 +32,7 @@ struct RecordedCall {
     const void* W1 = nullptr;
     const void* S1 = nullptr;
     void* Y = nullptr;
-    float gscale = 1.f;
+    float gscale = 1.f, gscale1 = 1.f;  // NVFP4 tensor scales (SwiGLU: gate, up)
     std::vector<nq_group> groups;
 };
 
@@ -72,6 +72,7 @@ nq_status reserve_call(const RecordedCall& c) {
         case CallKind::kGemm: return nq::reserve_projection_workspace(c.bits, false, c.T, c.K, c.N);
         case CallKind::kGemmFp4: return nq::reserve_projection_workspace(nq::kFp4, false, c.T, c.K, c.N);
         case CallKind::kSwiglu: return nq::reserve_projection_workspace(c.bits, true, c.T, c.K, c.N);
+        case CallKind::kSwigluFp4: return nq::reserve_projection_workspace(nq::kFp4, true, c.T, c.K, c.N);
         case CallKind::kGrouped:
             return nq::reserve_grouped_workspace(c.bits, c.groups.data(), (int)c.groups.size(), c.T, c.K);
     }
@@ -88,6 +89,8 @@ nq_status make_call(const RecordedCall& c, cudaStream_t s) {
         case CallKind::kSwiglu:
             return c.bits == 4 ? nq_swiglu_q4(c.X, c.W0, c.S0, c.W1, c.S1, c.Y, c.T, c.K, c.N, st)
                                : nq_swiglu_q5(c.X, c.W0, c.S0, c.W1, c.S1, c.Y, c.T, c.K, c.N, st);
+        case CallKind::kSwigluFp4:
+            return nq_swiglu_fp4(c.X, c.W0, c.S0, c.gscale, c.W1, c.S1, c.gscale1, c.Y, c.T, c.K, c.N, st);
         case CallKind::kGrouped:
             return c.bits == 4 ? nq_gemm_q4_grouped(c.X, c.groups.data(), (int)c.groups.size(), c.T, c.K, st)
                                : nq_gemm_q5_grouped(c.X, c.groups.data(), (int)c.groups.size(), c.T, c.K, st);
@@ -240,6 +243,28 @@ nq_status nq_program_swiglu(nq_program* prog, int bits, const void* X, const voi
     c.W1 = Wu;
     c.S1 = Su;
     c.Y = H;
+    return append(prog, std::move(c));
+}
+
+nq_status nq_program_swiglu_fp4(nq_program* prog, const void* X, const void* Wg, const void* Sg, float gate_scale,
+                                const void* Wu, const void* Su, float up_scale, void* H, int T, int K, int N) {
+    if (!prog) return NQ_ERR_NULL;
+    const nq_status st = nq::check_projection_args(nq::kFp4, true, X, Wg, Sg, Wu, Su, H, T, K, N);
+    if (st != NQ_OK || T == 0 || N == 0) return st;
+    RecordedCall c;
+    c.kind = CallKind::kSwigluFp4;
+    c.bits = nq::kFp4;
+    c.T = T;
+    c.K = K;
+    c.N = N;
+    c.X = X;
+    c.W0 = Wg;
+    c.S0 = Sg;
+    c.W1 = Wu;
+    c.S1 = Su;
+    c.Y = H;
+    c.gscale = gate_scale;
+    c.gscale1 = up_scale;
     return append(prog, std::move(c));
 }
 

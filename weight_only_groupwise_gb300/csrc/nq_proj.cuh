@@ -54,6 +54,7 @@ struct ProjArgs {
     int* dev_err;        // workspace: device error word
     unsigned long long wait_ns;  // bound of every device-side wait
     float gscale = 1.f;  // tensor scale of NVFP4 weights (1 for the integer formats)
+    float gscale1 = 1.f; // NVFP4 SwiGLU: tensor scale of the up matrix (M tile 1); gemm: gscale
     // Grouped launch (gemm only): ngroups > 0 projections of the same X, group g owning the
     // global row pairs [gpair[g], gpair[g+1]) with its own packed weight, scales and output
     // (N = gN[g]); W0/W1/S0/S1/Y are then unused. ngroups == 0: one matrix.
@@ -766,10 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                 const int e1 = F16 ? token_exponent(m1) : token_exponent_bf16(m1);
                 tok_scale0 = __int_as_float((127 + e0) << 23);
                 tok_scale1 = __int_as_float((127 + e1) << 23);
-                if constexpr (FP4) {
-                    tok_scale0 *= a.gscale;
-                    tok_scale1 *= a.gscale;
-                }
             }
         }
 
@@ -863,10 +860,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         const int b = si % p.nred;
         if (si >= p.nred) named_bar_sync(kBarRedFree + b, kHandoffThreads);
         float4* r4 = reinterpret_cast<float4*>(red + b * kRedFloats);
-        r4[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0] * tok_scale0, acc[0][1] * tok_scale1,
-                                                     acc[0][2] * tok_scale0, acc[0][3] * tok_scale1);
-        r4[(warp * 2 + 1) * 32 + lane] = make_float4(acc[1][0] * tok_scale0, acc[1][1] * tok_scale1,
-                                                     acc[1][2] * tok_scale0, acc[1][3] * tok_scale1);
+        {
+            // NVFP4: the tensor scale of M tile m's matrix (for SwiGLU, gate or up) joins the
+            // token scales (a power of two: exact)
+            const float g0 = FP4 ? a.gscale : 1.f, g1 = FP4 ? a.gscale1 : 1.f;
+            const float a0 = tok_scale0 * g0, a1 = tok_scale1 * g0, b0 = tok_scale0 * g1, b1 = tok_scale1 * g1;
+            r4[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0] * a0, acc[0][1] * a1, acc[0][2] * a0, acc[0][3] * a1);
+            r4[(warp * 2 + 1) * 32 + lane] = make_float4(acc[1][0] * b0, acc[1][1] * b1, acc[1][2] * b0, acc[1][3] * b1);
+        }
         named_bar_arrive(kBarRedFull + b, kHandoffThreads);
 #pragma unroll
         for (int m = 0; m < 2; ++m)

@@ -5,13 +5,20 @@
 
 namespace nq {
 namespace {
+template <int BITS, int MODE>
+cudaError_t launch_tp(const TcArgs& a, cudaStream_t stream, bool pdl) {
+    switch (a.p.TP) {
+        case 16: return tc_launch<BITS, 16, MODE>(a, stream, pdl);
+        case 32: return tc_launch<BITS, 32, MODE>(a, stream, pdl);
+        default: return tc_launch<BITS, 64, MODE>(a, stream, pdl);
+    }
+}
+
 template <int MODE>
 cudaError_t launch_mode(int bits, const TcArgs& a, cudaStream_t stream, bool pdl) {
-    switch (a.p.TP) {
-        case 16: return bits == 4 ? tc_launch<4, 16, MODE>(a, stream, pdl) : tc_launch<5, 16, MODE>(a, stream, pdl);
-        case 32: return bits == 4 ? tc_launch<4, 32, MODE>(a, stream, pdl) : tc_launch<5, 32, MODE>(a, stream, pdl);
-        default: return bits == 4 ? tc_launch<4, 64, MODE>(a, stream, pdl) : tc_launch<5, 64, MODE>(a, stream, pdl);
-    }
+    if (bits == 4) return launch_tp<4, MODE>(a, stream, pdl);
+    if (bits == 5) return launch_tp<5, MODE>(a, stream, pdl);
+    return launch_tp<kFp4, MODE>(a, stream, pdl);
 }
 }  // namespace
 

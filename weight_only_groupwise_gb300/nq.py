@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.nq_pack_fp4.restype = I
         L.nq_gemm_fp4.argtypes = [P, P, P, ctypes.c_float, P, I, I, I, P]
         L.nq_gemm_fp4.restype = I
+        L.nq_swiglu_fp4.argtypes = [P, P, P, ctypes.c_float, P, P, ctypes.c_float, P, I, I, I, P]
+        L.nq_swiglu_fp4.restype = I
         L.nq_dequant_fp4_debug.argtypes = [P, P, ctypes.c_float, P, I, I, P]
         L.nq_dequant_fp4_debug.restype = I
         for f in ("nq_gemm_q4_grouped", "nq_gemm_q5_grouped"):
@@ -95,10 +97,11 @@ def lib() -> ctypes.CDLL:
         L.nq_program_gemm_fp4.argtypes = [P, P, P, P, ctypes.c_float, P, I, I, I]
         L.nq_program_swiglu.argtypes = [P, I, P, P, P, P, P, P, I, I, I]
         L.nq_program_grouped.argtypes = [P, I, P, P, I, I, I]
+        L.nq_program_swiglu_fp4.argtypes = [P, P, P, P, ctypes.c_float, P, P, ctypes.c_float, P, I, I, I]
         L.nq_program_build.argtypes = [P]
         L.nq_program_launch.argtypes = [P, P]
         L.nq_program_info.argtypes = [P, P]
-        for f in ("nq_program_create", "nq_program_gemm", "nq_program_gemm_fp4", "nq_program_swiglu",
+        for f in ("nq_program_create", "nq_program_gemm", "nq_program_gemm_fp4", "nq_program_swiglu", "nq_program_swiglu_fp4",
                   "nq_program_grouped", "nq_program_build", "nq_program_launch", "nq_program_info"):
             getattr(L, f).restype = I
         L.nq_program_destroy.argtypes = [P]
@@ -308,6 +311,17 @@ def gemm_fp4(x: torch.Tensor, wq: torch.Tensor, s: torch.Tensor, global_scale: f
     return y
 
 
+def swiglu_fp4(x, wg, sg, gate_scale: float, wu, su, up_scale: float, N: int, out=None, stream=None):
+    """H[T,N] = bf16(silu(X*Wg) * (X*Wu)) with NVFP4 gate and up weights (packed codes, packed
+    scales, tensor scale each)."""
+    _cuda(x, "x")
+    T, K = x.shape
+    h = _out(x, N, out)
+    _check(lib().nq_swiglu_fp4(_ptr(x), _ptr(wg), _ptr(sg), ctypes.c_float(gate_scale), _ptr(wu), _ptr(su),
+                               ctypes.c_float(up_scale), _ptr(h), T, K, N, _stream(stream)))
+    return h
+
+
 def dequant_fp4_debug(wq, s, global_scale: float, K: int, N: int, stream=None) -> torch.Tensor:
     out = torch.empty((N, K), dtype=torch.float32, device=wq.device)
     _check(lib().nq_dequant_fp4_debug(_ptr(wq), _ptr(s), ctypes.c_float(global_scale), _ptr(out), K, N,
@@ -371,6 +385,15 @@ class Program:
 
     def swiglu_q5(self, x, wg, sg, wu, su, N: int, out=None):
         return self._swiglu(5, x, wg, sg, wu, su, N, out)
+
+    def swiglu_fp4(self, x, wg, sg, gate_scale: float, wu, su, up_scale: float, N: int, out=None):
+        _cuda(x, "x")
+        T, K = x.shape
+        h = _out(x, N, out)
+        self._rec(lib().nq_program_swiglu_fp4(self._h, _ptr(x), _ptr(wg), _ptr(sg), ctypes.c_float(gate_scale),
+                                              _ptr(wu), _ptr(su), ctypes.c_float(up_scale), _ptr(h), T, K, N),
+                  x, wg, sg, wu, su, h)
+        return h
 
     def _grouped(self, bits, x, groups, outs):
         _cuda(x, "x")
@@ -516,5 +539,6 @@ nq_swiglu_q4, nq_swiglu_q5 = swiglu_q4, swiglu_q5
 nq_gemm_q4_grouped, nq_gemm_q5_grouped = gemm_q4_grouped, gemm_q5_grouped
 nq_dequant_q4_debug, nq_dequant_q5_debug = dequant_q4_debug, dequant_q5_debug
 nq_pack_fp4, nq_gemm_fp4, nq_dequant_fp4_debug = pack_fp4, gemm_fp4, dequant_fp4_debug
+nq_swiglu_fp4 = swiglu_fp4
 nq_reserve, nq_device_error, nq_shutdown, nq_wait_limit = reserve, device_error, shutdown, wait_limit
 nq_plan_info, nq_plan_segments = plan_info, plan_segments
