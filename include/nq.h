@@ -40,8 +40,8 @@
  *     T = 8 verify rounds the pages tune). An nq_gemm_q4/q5 or nq_swiglu_q4/q5 call with
  *     8 < T <= 64 (larger speculative-verify batches, e.g. 4 requests x 8 draft tokens) runs on
  *     the tensor-core kernel, which streams the weights once whatever T
- *     (nq_tensor_core_batches); so does nq_gemm_fp4, and a grouped call runs one such launch
- *     per matrix. The no-allocation call with T > 8 runs one launch per slice of 8 tokens, each
+ *     (nq_tensor_core_batches); so do nq_gemm_fp4 and nq_swiglu_fp4, and a grouped call runs
+ *     one such launch per matrix. The no-allocation call with T > 8 runs one launch per slice of 8 tokens, each
  *     streaming the weights again, so its time grows with ceil(T / 8).
  *   - Alignment: every pointer 16-byte aligned.
  *   - All argument checks run on the host before anything is launched; a call that returns
@@ -54,7 +54,8 @@
  *     (different streams, no ordering) share it and race: order them on one stream.
  *   - Device-side waits are bounded (2 s by default, see nq_wait_limit); a wait that runs
  *     out sets a device error flag that nq_device_error reads.
- *   - nq_gemm_q4, nq_gemm_q5, nq_swiglu_q4 and nq_swiglu_q5 launch with programmatic dependent launch:
+ *   - The projection calls (nq_gemm_*, nq_swiglu_*, the grouped calls) launch with programmatic
+ *     dependent launch:
  *     their kernel may start while the previous kernel on `stream` is finishing. It reads
  *     X and writes Y, H and its workspace only after that kernel has completed, but starts
  *     streaming the packed weights at once: the weights must not be written by a kernel

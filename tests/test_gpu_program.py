@@ -205,3 +205,26 @@ def test_program_recording_after_build_builds_again(nq):
     assert i["calls"] == 2 and i["kernels"] == 2 and i["builds"] == 2
     assert same_bits([h, yd], ref[:2])
     p.close()
+
+
+@pytest.mark.parametrize("T", [8, 24])
+def test_program_nvfp4_mlp_bit_for_bit(nq, T):
+    """An NVFP4 MLP (SwiGLU block with its own gate and up tensor scales, then the down
+    projection) replayed as a program writes the bits of the eager calls."""
+    dev = torch.device("cuda", 0)
+    wg, wu, wd = fp4_weights(nq, K, NH, 980), fp4_weights(nq, K, NH, 981), fp4_weights(nq, NH, K, 982)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(983)
+    x = si.device_activations(T, K, gen, dev)
+    gg, gu_, gd = 0.0078125, 0.005859375, 0.001953125
+    h_ref = nq.swiglu_fp4(x, *wg, gg, *wu, gu_, NH)
+    y_ref = nq.gemm_fp4(h_ref, *wd, gd, K)
+    p = nq.Program()
+    h = p.swiglu_fp4(x, *wg, gg, *wu, gu_, NH)
+    y = p.gemm_fp4(h, *wd, gd, K)
+    p.launch()
+    torch.cuda.synchronize()
+    nq.device_error()
+    assert same_bits([h, y], [h_ref, y_ref])
+    assert p.info()["kernels"] == (2 if T <= 8 else 3)
+    p.close()

@@ -68,6 +68,11 @@ def test_recording_checks_match_the_calls(L, prog):
     assert s(prog, 4, P(A), P(2 * A), P(3 * A), P(4 * A), P(5 * A), P(4 * A + 32), 1, 64, 16) == ALIAS
     f = L.nq_program_gemm_fp4
     assert f(prog, P(A), P(2 * A), P(3 * A), ctypes.c_float(1.0), P(4 * A + 4), 1, 64, 16) == ALIGN
+    sf = L.nq_program_swiglu_fp4
+    one = ctypes.c_float(1.0)
+    assert sf(prog, P(A), P(2 * A), P(3 * A), one, P(4 * A), P(5 * A), one, P(6 * A), 1, 96, 16) == SHAPE
+    assert sf(prog, P(A), P(2 * A), None, one, P(4 * A), P(5 * A), one, P(6 * A), 1, 64, 16) == NULL
+    assert sf(prog, P(A), P(2 * A), P(3 * A), one, P(4 * A), P(5 * A), one, P(5 * A + 16), 1, 64, 16) == ALIAS
     assert info(L, prog)["calls"] == 0
 
 
@@ -87,8 +92,10 @@ def test_valid_calls_are_recorded_in_order(L, prog):
     assert L.nq_program_grouped(prog, 5, P(A), ctypes.cast(groups, ctypes.c_void_p), 2, 8, 640) == 0
     # K == 0 with outputs present is a call (it writes zeros), not an empty problem
     assert L.nq_program_gemm(prog, 5, P(A), P(2 * A), P(3 * A), P(19 * A), 4, 0, 32) == 0
+    assert L.nq_program_swiglu_fp4(prog, P(A), P(20 * A), P(21 * A), ctypes.c_float(0.5), P(22 * A), P(23 * A),
+                                   ctypes.c_float(0.25), P(24 * A), 8, 640, 1088) == 0
     i = info(L, prog)
-    assert i["calls"] == 5 and i["kernels"] == 0 and i["builds"] == 0
+    assert i["calls"] == 6 and i["kernels"] == 0 and i["builds"] == 0
 
 
 def test_grouped_recording_checks(L, prog):
