@@ -670,7 +670,7 @@ nq_status reserve_projection(int bits, bool swiglu, int T, int K, int N) {
     if (st != NQ_OK) return st;
     if (g_tc && (bits == 4 || bits == 5 || bits == kFp4) && T > kSliceT && T <= kTcMaxT) {
         TcPlan p;
-        if (make_tc_plan(bits, T, K, N, d->sms, p)) {
+        if (make_tc_plan(bits, T, K, N, d->sms, p) && tensor_maps_available()) {
             st = ensure_workspace(*d, 1, 1);
             if (st == NQ_OK) st = ensure_tc_workspace(*d, p.RB, p.KS > 1 ? (long long)p.P * kTcRows * p.TP : 1);
             if (st == NQ_OK && swiglu) st = ensure_tc_gate(*d, (long long)T * N);

@@ -13,6 +13,9 @@ namespace nq {
 // Large-batch tensor-core kernel (nq_tc.cuh): the activation tensor map (false if the driver
 // entry point is missing or rejects the view) and the launch.
 bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP);
+// Looks up the driver's tensor-map encoder once (later calls reuse it); false if it is
+// missing. Recorded programs call it before a stream capture, where the lookup may not run.
+bool tensor_maps_available();
 bool encode_weight_maps(CUtensorMap* wmap, CUtensorMap* smap, const void* W, const void* S, int bits, int K, int N,
                         int TP);
 cudaError_t launch_tc_proj(int bits, const TcArgs& a, cudaStream_t stream, bool pdl);

@@ -31,12 +31,13 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+bool tensor_maps_available() { return encode_fn() != nullptr; }
+
 // X (bf16 [T][K], row-major) as a 3-D tensor [K/64][T][64]: a box {64, TP, BG} (BG = the
-// stage's groups) lands
-// in shared memory as one [TP][64] block per group, 128-byte rows with the 128-byte swizzle
-// (16-byte chunk c of token t at chunk c ^ (t % 8)), which is the tensor core's K-major
-// swizzled layout; tokens T..TP-1 are outside the tensor and read as zeros. 128-byte rows keep
-// the copy engine's request count at TP per group.
+// stage's groups) lands in shared memory as one [TP][64] block per group, 128-byte rows with
+// the 128-byte swizzle (16-byte chunk c of token t at chunk c ^ (t % 8)), which is the tensor
+// core's K-major swizzled layout; tokens T..TP-1 are outside the tensor and read as zeros.
+// 128-byte rows keep the copy engine's request count at TP per group.
 bool encode_x_map(CUtensorMap* map, const void* X, int T, int K, int TP) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
