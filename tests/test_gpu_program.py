@@ -228,3 +228,47 @@ def test_program_nvfp4_mlp_bit_for_bit(nq, T):
     assert same_bits([h, y], [h_ref, y_ref])
     assert p.info()["kernels"] == (2 if T <= 8 else 3)
     p.close()
+
+
+_FRESH_SCRIPT = r"""
+import torch
+import numpy as np
+import oracle, seeded_inputs as si
+from tests import gpu_util as gu
+from weight_only_groupwise_gb300 import nq
+# a fresh process whose first tensor-core and NVFP4 calls are made inside a program's capture
+T, K, N = 24, 640, 272
+p = si.q4_problem(T, K, N, 991)
+w = gu.pack_q4(nq, p["wq"], p["s"], K, N)
+x = gu.dev_bf16(p["x"])
+q = si.swiglu_fp4_problem(T, K, N, 992)
+wg = nq.pack_fp4(gu.dev_u32(q["cg"]), torch.from_numpy(np.ascontiguousarray(q["sfg"])).cuda(), K, N)
+wu = nq.pack_fp4(gu.dev_u32(q["cu"]), torch.from_numpy(np.ascontiguousarray(q["sfu"])).cuda(), K, N)
+xq = gu.dev_bf16(q["x"])
+torch.cuda.synchronize()
+prog = nq.Program()
+y = prog.gemm_q4(x, *w, N)
+h = prog.swiglu_fp4(xq, *wg, q["gg"], *wu, q["gu"], N)
+prog.launch()
+torch.cuda.synchronize()
+nq.device_error()
+assert prog.info()["kernels"] == 3, prog.info()
+assert gu.rel_err(gu.host_f64(y), oracle.gemm_q4(p["x"], p["wq"], p["s"], T, K, N)) <= gu.TOL
+g, u, _ = oracle.swiglu_fp4(q["x"], q["cg"], q["sfg"], q["gg"], q["cu"], q["sfu"], q["gu"], T, K, N)
+assert gu.rel_err(gu.host_f64(h), g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+print("fresh-ok")
+"""
+
+
+def test_program_builds_in_a_fresh_process(nq):
+    """A process whose first tensor-core calls are recorded: building the program reserves the
+    workspace and looks up the tensor-map encoder before the capture, so the capture allocates
+    nothing and queries nothing, and the replay matches the oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", _FRESH_SCRIPT], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "fresh-ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
