@@ -111,3 +111,16 @@ def test_grouped_recording_checks(L, prog):
     assert gr(prog, 4, P(A), ctypes.cast(overlapping, ctypes.c_void_p), 2, 8, 640) == ALIAS
     assert gr(prog, 4, P(A), arr, 1, 0, 640) == 0             # empty: nothing recorded
     assert info(L, prog)["calls"] == 0
+
+
+def test_build_without_a_gpu_reports_an_error(L, prog):
+    """Without a CUDA device, building or launching a recorded program returns an error status
+    (the runtime's device query fails) instead of crashing; the records stay."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    assert L.nq_program_gemm(prog, 4, P(A), P(2 * A), P(3 * A), P(4 * A), 1, 64, 16) == 0
+    assert L.nq_program_build(prog) < 0
+    assert L.nq_program_launch(prog, None) < 0
+    i = info(L, prog)
+    assert i["calls"] == 1 and i["builds"] == 0 and i["kernels"] == 0
