@@ -93,3 +93,54 @@ def test_timeout_in_tensor_core_swiglu(nq):
     ref = g / (1.0 + np.exp(-g)) * u
     for t in range(T):
         assert gu.rel_err(h[t], ref[t]) <= gu.TOL
+
+
+@pytest.mark.parametrize("T", [4, 24])
+def test_timeout_in_nvfp4_swiglu(nq, T):
+    """The NVFP4 SwiGLU block on the 8-token kernel (T = 4) and as two tensor-core launches
+    (T = 24): both abort under the 1 ns bound, and the next call is correct."""
+    K, N = 2048, 1040
+    p = si.swiglu_fp4_problem(T, K, N, 27)
+    wg = nq.pack_fp4(gu.dev_u32(p["cg"]), torch.from_numpy(np.ascontiguousarray(p["sfg"])).cuda(), K, N)
+    wu = nq.pack_fp4(gu.dev_u32(p["cu"]), torch.from_numpy(np.ascontiguousarray(p["sfu"])).cuda(), K, N)
+    x = gu.dev_bf16(p["x"])
+    gu.expect_timeout(nq, lambda: nq.swiglu_fp4(x, *wg, p["gg"], *wu, p["gu"], N))
+    h = gu.host_f64(nq.swiglu_fp4(x, *wg, p["gg"], *wu, p["gu"], N))
+    nq.device_error()
+    g, u, _ = oracle.swiglu_fp4(p["x"], p["cg"], p["sfg"], p["gg"], p["cu"], p["sfu"], p["gu"], T, K, N)
+    assert gu.rel_err(h, g / (1.0 + np.exp(-g)) * u) <= gu.TOL
+
+
+def test_timeout_in_a_recorded_program(nq):
+    """A program built while the wait bound is 1 ns keeps that bound (settings are baked in at
+    build time): its replay aborts and nq_device_error reports it; built again under the
+    default bound, the replay is correct."""
+    from weight_only_groupwise_gb300.nq import NqError
+    T, K, N = 8, 5120, 6144
+    p = si.q5_problem(T, K, N, 29)
+    w = gu.pack_q5(nq, p["wn"], p["wh"], p["s"], K, N)
+    x = gu.dev_bf16(p["x"])
+    prog = nq.Program()
+    y = prog.gemm_q5(x, *w, N)
+    timed_out = False
+    for _ in range(5):
+        prev = nq.wait_limit(1)
+        try:
+            prog.build()
+        finally:
+            nq.wait_limit(prev)
+        prog.launch()
+        try:
+            nq.device_error()
+        except NqError as e:
+            assert e.status == -7, e
+            nq.device_error()
+            timed_out = True
+            break
+    assert timed_out, "no bounded wait ran out in the replay with a 1 ns bound"
+    prog.build()
+    prog.launch()
+    torch.cuda.synchronize()
+    nq.device_error()
+    assert gu.rel_err(gu.host_f64(y), oracle.gemm_q5(p["x"], p["wn"], p["wh"], p["s"], T, K, N)) <= gu.TOL
+    prog.close()
