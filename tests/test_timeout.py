@@ -99,7 +99,7 @@ def test_timeout_in_tensor_core_swiglu(nq):
 def test_timeout_in_nvfp4_swiglu(nq, T):
     """The NVFP4 SwiGLU block on the 8-token kernel (T = 4) and as two tensor-core launches
     (T = 24): both abort under the 1 ns bound, and the next call is correct."""
-    K, N = 2048, 1040
+    K, N = 5120, 4096
     p = si.swiglu_fp4_problem(T, K, N, 27)
     wg = nq.pack_fp4(gu.dev_u32(p["cg"]), torch.from_numpy(np.ascontiguousarray(p["sfg"])).cuda(), K, N)
     wu = nq.pack_fp4(gu.dev_u32(p["cu"]), torch.from_numpy(np.ascontiguousarray(p["sfu"])).cuda(), K, N)
