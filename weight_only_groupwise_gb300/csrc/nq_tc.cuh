@@ -296,8 +296,9 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
                   "activation blocks on 1024-byte boundaries");
     constexpr uint32_t kCols = kTcCols;
     // TMEM columns of an A buffer (a stage) and of a P buffer (kPG groups: one MMA-to-epilogue
-    // hand-off); P buffers: 4, 2, 2 for TP = 16, 32, 64
-    constexpr int kPG = kTcPair, kPSteps = BG / kPG;
+    // hand-off; three groups where two such buffers still fit, TP = 16: fewer hand-offs, 18.1
+    // -> 17.7 us at T = 16 on the decode shape); two P buffers at every TP
+    constexpr int kPG = (TP == 16 && BG % 3 == 0) ? 3 : kTcPair, kPSteps = BG / kPG;
     static_assert(BG % kPG == 0, "P steps tile a stage");
     constexpr int kAStage = BG * 32, kPCols = kPG * TP;
     constexpr int kP = (kTcCols - kTcA * kAStage) / kPCols;
