@@ -1,5 +1,5 @@
 // nq_proj.cuh -- the projection kernel: Y[T,N] = X[T,K] * dequant(W) for T <= 8, 4- or 5-bit
-// codes with one fp16 scale per 64-wide K group, optionally fused into the SwiGLU gate/up
+// codes with one fp16 scale per 64-wide K group (or NVFP4 weights), optionally fused into the SwiGLU gate/up
 // pair ("NInfer-4090" release post, section "V3 做了什么": small-batch Q4/Q5 projections
 // tuned at T=8 for GDN, attention and SwiGLU; "ninfer-ext" README, section
 // "与原版 NInfer 的对比": the Q5 K-split MMA path for verify rounds).
@@ -20,6 +20,8 @@
 //     16-row tiles of the row pair: a lane decodes its 16 code bytes into A fragments
 //     (fp16: 1024 + q, or 1024 + 16 q against X / 16; bf16: 128 + q; exact), loads the B
 //     fragment of X with ldmatrix and runs four m16n8k16 MMAs from a zero accumulator: P.
+//     The MMA's eight columns are the tokens: token t in column t, or, for up to four tokens
+//     (the EVEN instantiations), in column 2t, so that no lane's odd columns hold a token.
 //     The warp's eight tiles are issued K-step by K-step so their chains overlap.
 //     P - O = sum((q - z) * x) up to fp32 rounding, and exactly 0 where every code equals z
 //     (identical MMA inputs). The fp16 scale is applied with one FMA per group.
