@@ -1,6 +1,6 @@
 // nq_proj.cuh -- the projection kernel: Y[T,N] = X[T,K] * dequant(W) for T <= 8, 4- or 5-bit
-// codes with one fp16 scale per 64-wide K group (or NVFP4 weights), optionally fused into the SwiGLU gate/up
-// pair ("NInfer-4090" release post, section "V3 做了什么": small-batch Q4/Q5 projections
+// codes with one fp16 scale per 64-wide K group (or NVFP4 weights), optionally fused into the
+// SwiGLU gate/up pair ("NInfer-4090" release post, section "V3 做了什么": small-batch Q4/Q5 projections
 // tuned at T=8 for GDN, attention and SwiGLU; "ninfer-ext" README, section
 // "与原版 NInfer 的对比": the Q5 K-split MMA path for verify rounds).
 //
