@@ -28,6 +28,9 @@ TC_SHAPES = [
     # T, K, N, seed
     (9, 64, 16, 0), (16, 256, 128, 1), (17, 640, 272, 2), (32, 1024, 48, 3), (33, 5120, 384, 4),
     (48, 1536, 1040, 5), (64, 512, 144, 6), (64, 17408, 96, 7), (24, 6208, 2064, 8), (12, 192, 4096, 9),
+    # 16 padded tokens with K split in five pieces of 14 and 15 groups: stages of 6, 6 and 2 or 3
+    # groups, so full pairs, a pair and a lone group at a stage's end
+    (16, 4544, 2064, 10),
 ]
 
 
