@@ -6,10 +6,10 @@
 // once whatever T. A SwiGLU block is two launches (the output-mode template argument): the
 // gate projection writes fp32 G, the up projection writes bf16 silu(G) * U.
 //
-// One block per (128-row block, K piece), D + 6 warps (D decoders: 8, or 16 for NVFP4 with
-// TP <= 32). Work moves between the warp roles in
-// stages of BG 64-wide K groups (six for TP <= 32 padded tokens, four for TP = 64: the TMEM
-// budget), one hand-off per stage:
+// One block per (128-row block, K piece), D + E + 3 warps (D decoders: 8, or 16 for NVFP4 with
+// TP <= 32; E epilogue warps: 4, or 8 for 4/5-bit codes at TP = 64). Work moves between the
+// warp roles in stages of BG 64-wide K groups (six for TP <= 32 padded tokens, four for
+// TP = 64: the TMEM budget), one hand-off per stage:
 //   * warp 0, one lane -- producer: per stage three 3-D TMA copies: the codes and the scales of
 //     the eight 16-row tiles (tiles and groups past the matrix read as zeros), and the stage's
 //     activation chunk, one [TP][64] block per group in the tensor core's K-major
@@ -24,13 +24,15 @@
 //     holds a stage (32 columns a group); two alternate. Groups are decoded in pairs (D = 8)
 //     or one by one (D = 16), each into registers of its own, so that they decode while the
 //     stores of the groups before them complete.
-//   * warp D + 1 -- MMA issuer (the whole warp runs the loop, one elected lane issues): per group,
-//     four tcgen05.mma.kind::f16 (M = 128, N = TP, K = 16; A from TMEM, B = the activation
-//     chunk through a shared-memory descriptor; D in TMEM, fp32, a fresh accumulator per group:
-//     P = 2^-12 sum over the group of (q - z) x); per pair of groups a tcgen05.commit publishes
-//     their two P (a P buffer), per stage one frees the A buffer and the shared-memory stage.
-//   * warps D + 2 .. D + 5 -- epilogue: thread = row (TMEM lane); per group it loads P (tcgen05.ld) and
-//     adds 2^12 s[row, g] * P[t] to its fp32 accumulators acc[t]. At the end it stores bf16 Y,
+//   * warps D + 1, D + 2 -- MMA issuers, alternate P buffers (the whole warp runs the loop, one
+//     elected lane issues): per group, four tcgen05.mma.kind::f16 (M = 128, N = TP, K = 16;
+//     A from TMEM, B = the activation chunk through a shared-memory descriptor; D in TMEM,
+//     fp32, a fresh accumulator per group: P = 2^-12 sum over the group of (q - z) x); per P
+//     buffer (two or three groups) a tcgen05.commit publishes their P, per stage each issuer's
+//     commits free the A buffer and the shared-memory stage.
+//   * warps D + 3 .. D + E + 2 -- epilogue: thread = row (TMEM lane) and E / 4 token ranges;
+//     per group it loads P (tcgen05.ld) and adds 2^12 s[row, g] * P[t] to its fp32
+//     accumulators acc[t] of its tokens. At the end it stores bf16 Y,
 //     or, when K is split across blocks, an fp32 partial; the last block of a row block
 //     (ticket) adds the partials in fixed order and stores Y.
 // The 2^-12 in the decoded weights keeps every group partial finite for any finite bf16
@@ -38,7 +40,7 @@
 // overflows at 2^128); 2^12 s is exact in fp32, so the result is the unscaled one. No range
 // pass over the activations is needed.
 // Every wait is bounded (the abort protocol of the small-batch kernel); TMEM is allocated and
-// freed by warp 0, after the issuer has waited for its last MMAs. With one block per SM the
+// freed by warp 0, after the issuers have waited for their last MMAs. With one block per SM the
 // kernel takes all 512 TMEM columns.
 #pragma once
 
@@ -59,13 +61,27 @@ constexpr int kTcCols = 512;                      // TMEM columns: A buffers, th
 constexpr int kTcMaxP = 8;
 constexpr int kTcScaleExp = 12;                   // decoded 4/5-bit weights carry 2^-12
 constexpr int kTcFp4ScaleExp = 20;                // decoded NVFP4 weights carry 2^-20
-constexpr int kTcEpilogue = 4;                    // epilogue warps: one TMEM lane quarter each
 // Decoder warps: one per 16-row tile; two (each every other group of a stage) for NVFP4 with
 // TP <= 32, whose decode (e2m1 x e4m3 to fp16, then bf16) is the longest. Measured at T = 16
 // on the decode shape: NVFP4 26.7 -> 24.5 us, Q4 18.0 -> 18.6 us (so Q4/Q5 keep one); at
 // TP = 64 the epilogue accumulators need the registers of the smaller block.
 NQ_HD constexpr int tc_decoders(int bits, int TP) { return bits == kFp4 && TP <= 32 ? 16 : 8; }
-NQ_HD constexpr int tc_threads(int bits, int TP) { return (2 + tc_decoders(bits, TP) + kTcEpilogue) * 32; }
+// Epilogue warps: one per TMEM lane quarter (all the tokens of its 32 rows), or two per quarter
+// (each half the tokens) for 4/5-bit codes at TP = 64, where one warp's 64 accumulators and
+// loads set the pace. Measured at T = 64 (with two issuers): decode shape 22.3 -> 21.7 us,
+// 5120 x 6144 Q5 15.9 -> 15.1, down projection 28.6 -> 27.6; NVFP4 gains nothing and keeps four.
+NQ_HD constexpr int tc_epilogues(int bits, int TP) { return TP == 64 && bits != kFp4 ? 8 : 4; }
+// MMA issuers: two warps on different SM sub-partitions take alternate P steps. A single
+// issuer slowed the other warps of its sub-partition (traced: its decoder and epilogue warps
+// finished each hand-off about 0.35 us after the others), and every hand-off waits for the
+// slowest TMEM lane quarter. Measured, one issuer -> two, T = 16 / 32: decode shape Q4 16.6 /
+// 18.9 -> 16.0 / 18.6 us, down projection 20.2 / 23.1 -> 19.6 / 22.6, NVFP4 23.7 / 26.0 ->
+// 23.3 / 25.5 (T = 64: 30.4 -> 29.8); 5120 x 6144 Q5 unchanged. Three issuers won on some
+// shapes and lost on others.
+constexpr int kTcIssuers = 2;
+NQ_HD constexpr int tc_threads(int bits, int TP) {
+    return (1 + tc_decoders(bits, TP) + kTcIssuers + tc_epilogues(bits, TP)) * 32;
+}
 constexpr int kTcMinT = 9, kTcMaxT = 64;
 // What the epilogue writes for (token t, row n) from the finished fp32 value v: bf16 Y = v;
 // fp32 G = v (a SwiGLU gate projection); bf16 Y = silu(G) * v (the up projection of the same
@@ -316,9 +332,9 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
     constexpr int kP = (kTcCols - kTcA * kAStage) / kPCols;
     static_assert(kP >= 2 && kP <= kTcMaxP, "TMEM budget");
     constexpr uint32_t kIdesc = tc_idesc_bf16(TP);
-    constexpr int kDec = tc_decoders(BITS, TP), kEpi = kTcEpilogue;
+    constexpr int kDec = tc_decoders(BITS, TP), kEpi = tc_epilogues(BITS, TP);
     constexpr int kDecPerTile = kDec / kTcTiles;     // warps sharing a tile's groups
-    constexpr int kMmaWarp = 1 + kDec;
+    constexpr int kMmaWarp = 1 + kDec, kEpi0 = kMmaWarp + kTcIssuers;  // first issuer, first epilogue warp
 
     const TcPlan& p = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -342,17 +358,17 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
     if (tid == 0) {
         for (int i = 0; i < nstages; ++i) {
             mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, kDec + 1 + kEpi);
+            mbar_init(empty0 + 8 * i, kDec + kTcIssuers + kEpi);
         }
         for (int i = 0; i < kTcA; ++i) {
             mbar_init(afull0 + 8 * i, kDec);
-            mbar_init(aempty0 + 8 * i, 1);
+            mbar_init(aempty0 + 8 * i, kTcIssuers);
         }
         for (int i = 0; i < kP; ++i) {
             mbar_init(pfull0 + 8 * i, 1);
             mbar_init(pempty0 + 8 * i, kEpi);
         }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, kTcIssuers);
         flags[0] = 0;
         flags[1] = 0;
         flags[2] = 0;
@@ -488,8 +504,12 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
             __syncwarp();
             mbar_arrive_if(afull0 + 8 * ab, lane == 0);
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp < kEpi0) {
+        // ------------------------------------------------------------ MMA issuers
+        // Issuer i takes the P steps k with k % kTcIssuers == i. Every issuer waits for every
+        // stage and, after its P steps of the stage, commits the stage's A buffer and shared
+        // memory (those barriers count one arrival per issuer).
+        const int iss = warp - kMmaWarp;
         bool ok = true;
         for (int si = 0; si < nst && ok; ++si) {
             const int st = si % nstages, ab = si % kTcA;
@@ -505,6 +525,7 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
             for (int hh = 0; hh < kPSteps; ++hh) {
                 const int k = kPSteps * si + hh;         // P step: groups kPG k .. kPG k + kPG - 1
                 if (k >= nsteps) break;
+                if (k % kTcIssuers != iss) continue;
                 const int pb = k % kP;
                 if (k >= kP) ok = mbar_wait(pempty0 + 8 * pb, ((k / kP) - 1) & 1, flags, a.dev_err, wait_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok);
@@ -528,7 +549,7 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
             tc_commit(aempty0 + 8 * ab, leader);
             tc_commit(empty0 + 8 * st, leader);
         }
-        // every MMA the elected lane issued has completed before TMEM can be freed
+        // every MMA of both issuers has completed before TMEM can be freed
         const bool leader = elect_one();
         tc_commit(done_bar, leader);
         mbar_wait_drain(done_bar, 0, kDrainNs);
@@ -538,11 +559,13 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
         const int row = 32 * q + lane;                 // row of the block = TMEM lane
         const int m = row >> 4, rr = row & 15;
         const int sidx = 2 * (rr & 7) + (rr >> 3);     // the row's place in a packed scale tile
+        constexpr int kTok = TP / (kEpi / 4);          // tokens of one epilogue warp: t0 .. t0 + kTok - 1
+        const int t0 = kEpi == 4 ? 0 : kTok * ((warp - kEpi0) >> 2);
         grid_dependency_wait();                        // Y, G, partials and tickets may be in use before
-        float acc[TP];
+        float acc[kTok];
 #pragma unroll
-        for (int t = 0; t < TP; ++t) acc[t] = 0.f;
-        constexpr int kChunk = TP < 32 ? TP : 32;      // columns loaded before one wait
+        for (int i = 0; i < kTok; ++i) acc[i] = 0.f;
+        constexpr int kChunk = kTok < 32 ? kTok : 32;  // columns loaded before one wait
         for (int k = 0; k < nsteps; ++k) {
             const int si = k / kPSteps, hh = k % kPSteps, gs0 = kPG * hh, st = si % nstages;
             const int pb = k % kP;
@@ -553,7 +576,7 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
             tc_fence_after();
             if (ok) {
                 const uint8_t* sc = stage_mem + st * kStageBytes + kTcTiles * BG * TB + m * BG * STB;
-                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb;
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + p_col0 + kPCols * pb + t0;
 #pragma unroll
                 for (int gp = 0; gp < kPG; ++gp) {
                     if (kPG * k + gp >= ngroups) break;
@@ -565,7 +588,7 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
                                               sc + (gs0 + gp) * kScaleTileBytes + 2 * sidx))) *
                                               (float)(1 << kTcScaleExp);
 #pragma unroll
-                    for (int c = 0; c < TP; c += kChunk) {
+                    for (int c = 0; c < kTok; c += kChunk) {
                         uint32_t v[kChunk];
 #pragma unroll
                         for (int c2 = 0; c2 < kChunk; c2 += 16) tmem_ld16(base + TP * gp + c + c2, v + c2);
@@ -596,15 +619,15 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
             if (p.KS == 1) {
                 if (nrow < p.N) {
 #pragma unroll
-                    for (int t = 0; t < TP; ++t)
-                        if (t < p.T) store(t, acc[t]);
+                    for (int i = 0; i < kTok; ++i)
+                        if (t0 + i < p.T) store(t0 + i, acc[i]);
                 }
             } else {
                 float* part = a.partials + ((size_t)rb * p.KS + kp) * (kTcRows * TP);
 #pragma unroll
-                for (int t = 0; t < TP; ++t) part[t * kTcRows + row] = acc[t];
+                for (int i = 0; i < kTok; ++i) part[(t0 + i) * kTcRows + row] = acc[i];
                 named_bar_sync(1, kEpi * 32);          // the block's partial is complete
-                const int leader = (kMmaWarp + 1) * 32;
+                const int leader = kEpi0 * 32;
                 if (tid == leader) {
                     fence_acq_rel_gpu();
                     flags[4] = ticket_add(a.tickets + rb) == p.KS - 1;
@@ -612,18 +635,18 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
                 named_bar_sync(1, kEpi * 32);
                 if (flags[4]) {
                     fence_acq_rel_gpu();
-                    float sum[TP];
+                    float sum[kTok];
 #pragma unroll
-                    for (int t = 0; t < TP; ++t) sum[t] = 0.f;
+                    for (int i = 0; i < kTok; ++i) sum[i] = 0.f;
                     for (int k2 = 0; k2 < p.KS; ++k2) {   // fixed order: deterministic
                         const float* src = a.partials + ((size_t)rb * p.KS + k2) * (kTcRows * TP);
 #pragma unroll
-                        for (int t = 0; t < TP; ++t) sum[t] += __ldcg(src + t * kTcRows + row);
+                        for (int i = 0; i < kTok; ++i) sum[i] += __ldcg(src + (t0 + i) * kTcRows + row);
                     }
                     if (nrow < p.N) {
 #pragma unroll
-                        for (int t = 0; t < TP; ++t)
-                            if (t < p.T) store(t, sum[t]);
+                        for (int i = 0; i < kTok; ++i)
+                            if (t0 + i < p.T) store(t0 + i, sum[i]);
                     }
                     if (tid == leader) a.tickets[rb] = 0;
                 }
