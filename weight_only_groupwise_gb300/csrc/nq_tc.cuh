@@ -474,10 +474,11 @@ __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const 
                         // a pair decodes while the stores of the pairs before it complete
                         const int g = gl + kTcPair * pr;
                         decode_pair(st, g, r[pr]);
-                        // 4-bit codes at TP = 16: one store per pair (measured 17.7 -> 16.5 us on
-                        // the decode shape at T = 16; slower for 5-bit codes and larger TP)
+                        // one store per pair for 4-bit codes and NVFP4 at TP = 16 and 64 (decode
+                        // shape: T = 16 17.7 -> 16.5 us, T = 64 21.7 -> 20.7, NVFP4 T = 64 29.8 ->
+                        // 29.3); at TP = 32 (18.6 -> 18.7) and for 5-bit codes (+1-2 %) slower
                         static_assert(kTcPair == 2, "one store per pair of groups");
-                        if (BITS == 4 && TP == 16 && g + 1 < ngroups) {
+                        if (BITS != 5 && TP != 32 && g + 1 < ngroups) {
                             tmem_st_pair(base + 32 * (kTcPair * pr), r[pr][0], r[pr][1]);
                         } else {
 #pragma unroll
