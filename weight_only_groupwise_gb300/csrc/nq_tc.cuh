@@ -62,10 +62,14 @@ constexpr int kTcMaxP = 8;
 constexpr int kTcScaleExp = 12;                   // decoded 4/5-bit weights carry 2^-12
 constexpr int kTcFp4ScaleExp = 20;                // decoded NVFP4 weights carry 2^-20
 // Decoder warps: one per 16-row tile; two (each every other group of a stage) for NVFP4 with
-// TP <= 32, whose decode (e2m1 x e4m3 to fp16, then bf16) is the longest. Measured at T = 16
-// on the decode shape: NVFP4 26.7 -> 24.5 us, Q4 18.0 -> 18.6 us (so Q4/Q5 keep one); at
-// TP = 64 the epilogue accumulators need the registers of the smaller block.
-NQ_HD constexpr int tc_decoders(int bits, int TP) { return bits == kFp4 && TP <= 32 ? 16 : 8; }
+// TP <= 32, whose decode (e2m1 x e4m3 to fp16, then bf16) is the longest, and for 5-bit codes
+// at TP = 16. Measured at T = 16: NVFP4 on the decode shape 26.7 -> 24.5 us, Q5 on the verify
+// shape 11.7 -> 11.4 us; slower for Q4 (16.0 -> 16.5: it loses the one-store pairs) and for
+// Q5 at TP = 32 (13.0 -> 13.2); at TP = 64 the epilogue accumulators need the registers of the
+// smaller block.
+NQ_HD constexpr int tc_decoders(int bits, int TP) {
+    return (bits == kFp4 && TP <= 32) || (bits == 5 && TP == 16) ? 16 : 8;
+}
 // Epilogue warps: one per TMEM lane quarter (all the tokens of its 32 rows), or two per quarter
 // (each half the tokens) for 4/5-bit codes at TP = 64, where one warp's 64 accumulators and
 // loads set the pace. Measured at T = 64 (with two issuers): decode shape 22.3 -> 21.7 us,
