@@ -91,6 +91,9 @@ WORKLOADS = {
                       desc="decode GEMV Q4, T=1, K=5120, N=17408 (27B-class FFN up-projection)"),
     "verify_q5": dict(kind="proj", bits=5, T=8, K=5120, N=6144,
                       desc="spec-verify Q5, T=8, K=5120, N=6144 (attention gate/value projection)"),
+    "decode_fp4": dict(kind="proj", bits=FP4, T=1, K=5120, N=17408,
+                       desc="decode GEMV NVFP4, T=1, K=5120, N=17408 (e2m1 codes, an e4m3 scale per 16, "
+                            "an fp32 tensor scale)"),
     "swiglu_block": dict(kind="swiglu", bits=4, T=8, K=5120, N=17408, Kd=17408, Nd=5120,
                          desc="SwiGLU block Q4, T=8: fused gate+up K=5120 N=17408, then down K=17408 N=5120"),
     "swiglu_block_q5": dict(kind="swiglu", bits=5, T=8, K=5120, N=17408, Kd=17408, Nd=5120,
@@ -274,6 +277,20 @@ def make_fp4_copies(nq, K, N, copies, seed, dev):
     return out
 
 
+def proj_copies_and_call(nq, bits: int, K: int, N: int, R: int, dev, seed=None):
+    """R packed weight copies of one K x N matrix and the library call fn(x, w, s, N, out=y)
+    that projects through one of them (NVFP4: with the seeded inputs' tensor scale)."""
+    import seeded_inputs as si
+    if bits == FP4:
+        copies = make_fp4_copies(nq, K, N, R, 9 if seed is None else seed, dev)
+
+        def fn(x, wq, s, n, out, stream=None):
+            nq.gemm_fp4(x, wq, s, si.FP4_GLOBAL_SCALE, n, out=out, stream=stream)
+        return copies, fn
+    copies = make_proj_copies(nq, bits, K, N, R, (1 if bits == 4 else 2) if seed is None else seed, dev)
+    return copies, (nq.gemm_q4 if bits == 4 else nq.gemm_q5)
+
+
 def build_step(nq, w: dict, dev, T_override=None):
     """Returns (step(i) -> None launching one step, bytes_per_step, copies, note)."""
     import torch
@@ -284,10 +301,9 @@ def build_step(nq, w: dict, dev, T_override=None):
         bits, T, K, N = w["bits"], T_override or w["T"], w["K"], w["N"]
         b = proj_bytes(bits, T, K, N)
         R = max(2, -(-3 * L2_BYTES // b))
-        copies = make_proj_copies(nq, bits, K, N, R, 1 if bits == 4 else 2, dev)
+        copies, fn = proj_copies_and_call(nq, bits, K, N, R, dev)
         x = si.device_activations(T, K, gen, dev)
         y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
-        fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
 
         def step(i):
             fn(x, *copies[i % R], N, out=y)
@@ -466,7 +482,7 @@ def time_e2e(nq, w: dict, steps: int, warmup: int, stream, dev):
     bits, T, K, N = w["bits"], w["T"], w["K"], w["N"]
     b = proj_bytes(bits, T, K, N)
     R = max(2, -(-3 * L2_BYTES // b))
-    copies = make_proj_copies(nq, bits, K, N, R, 7, dev)
+    copies, fn = proj_copies_and_call(nq, bits, K, N, R, dev, seed=7)
     gen = torch.Generator(device="cpu")
     gen.manual_seed(99)
     B, NR = 4, 12                                     # steps per wait, device ring buffers
@@ -475,7 +491,6 @@ def time_e2e(nq, w: dict, steps: int, warmup: int, stream, dev):
     xd = [torch.empty((T, K), dtype=torch.bfloat16, device=dev) for _ in range(NR)]
     yd = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(NR)]
     h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    fn = nq.gemm_q4 if bits == 4 else nq.gemm_q5
 
     def steps_on_streams(n):
         """n steps; events order every reuse of the ring buffers."""

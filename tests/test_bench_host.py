@@ -18,6 +18,7 @@ def test_algorithmic_bytes():
     # NVFP4: codes K*N/2 + e4m3 scales N*K/16
     assert bench.fp4_bytes(1, 5120, 17408) == 44564480 + 5570560 + 10240 + 34816
     assert bench.weight_bytes(bench.FP4, 5120, 17408) == 44564480 + 5570560
+    assert bench.workload_bytes(bench.WORKLOADS["decode_fp4"]) == bench.fp4_bytes(1, 5120, 17408)
     w4 = bench.WORKLOADS["swiglu_block_fp4"]
     assert bench.workload_bytes(w4) == (2 * (44564480 + 5570560) + 8 * 5120 * 2 + 8 * 17408 * 2
                                         + bench.fp4_bytes(8, 17408, 5120))
