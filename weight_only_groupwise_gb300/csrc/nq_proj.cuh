@@ -172,38 +172,13 @@ __device__ __forceinline__ void fp4_kstep(const uint4 (&w)[GROUPS * TILES], cons
     }
 }
 
-// GROUPS x TILES tiles in one pass, K-step-major so their accumulator chains overlap. Each
-// tile's chain is "K step 0 from a zero accumulator, then K steps 1..3", exactly as for O.
-// code[t] / scale[t]: this lane's code bytes / scales of tile t. Integer codes: the tile's
-// partial P, minus the zero-point chain O of its group, times the group scale, is added to
-// the accumulator. NVFP4: per K step (fp4_kstep).
-template <int BITS, bool F16, int GROUPS, int TILES, bool HALF = false>
-__device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * TILES],
-                                          const uint8_t* const (&scale)[GROUPS * TILES],
-                                          const uint32_t (&xb)[GROUPS][8], const float2 (&o)[GROUPS],
-                                          uint32_t magic, float (&acc)[2][4]) {
+// Integer codes, the tiles of a pass: the four K steps of each tile as one MMA chain, then the
+// tile's partial P minus its group's zero-point chain O, times the group scale, into acc.
+template <int BITS, bool F16, int GROUPS, int TILES, bool HALF>
+__device__ __forceinline__ void int_tiles(const uint4 (&w)[GROUPS * TILES], const uint32_t (&hb)[GROUPS * TILES],
+                                          const uint2 (&sw)[GROUPS * TILES], const uint32_t (&xb)[GROUPS][8],
+                                          const float2 (&o)[GROUPS], uint32_t magic, float (&acc)[2][4]) {
     constexpr int NT = GROUPS * TILES;
-    constexpr bool FP4 = BITS == kFp4;
-    uint4 w[NT];
-    uint32_t hb[NT];
-    uint2 sw[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        w[t] = *reinterpret_cast<const uint4*>(code[t]);
-        // high-bit word of the lane: after the tile's 512 nibble bytes, 4 bytes per lane
-        hb[t] = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code[t] + 512 - (threadIdx.x & 31) * 12) : 0u;
-        if constexpr (FP4)
-            sw[t] = *reinterpret_cast<const uint2*>(scale[t]);
-        else
-            sw[t] = make_uint2(*reinterpret_cast<const uint32_t*>(scale[t]), 0u);
-    }
-    if constexpr (FP4) {
-        fp4_kstep<0, GROUPS, TILES, HALF>(w, sw, xb, acc);
-        fp4_kstep<1, GROUPS, TILES, HALF>(w, sw, xb, acc);
-        fp4_kstep<2, GROUPS, TILES, HALF>(w, sw, xb, acc);
-        fp4_kstep<3, GROUPS, TILES, HALF>(w, sw, xb, acc);
-        return;
-    }
     float d[NT][4];
     uint32_t a[NT][4];
 #pragma unroll
@@ -239,6 +214,41 @@ __device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * 
             acc[m][1] = fmaf(s.x, d[t][1] - o[h].y, acc[m][1]);
             acc[m][3] = fmaf(s.y, d[t][3] - o[h].y, acc[m][3]);
         }
+    }
+}
+
+// GROUPS x TILES tiles in one pass, K-step-major so their accumulator chains overlap. Each
+// tile's chain is "K step 0 from a zero accumulator, then K steps 1..3", exactly as for O.
+// code[t] / scale[t]: this lane's code bytes / scales of tile t. Integer codes: the tile's
+// partial P, minus the zero-point chain O of its group, times the group scale, is added to
+// the accumulator. NVFP4: per K step (fp4_kstep).
+template <int BITS, bool F16, int GROUPS, int TILES, bool HALF = false>
+__device__ __forceinline__ void tiles_mma(const uint8_t* const (&code)[GROUPS * TILES],
+                                          const uint8_t* const (&scale)[GROUPS * TILES],
+                                          const uint32_t (&xb)[GROUPS][8], const float2 (&o)[GROUPS],
+                                          uint32_t magic, float (&acc)[2][4]) {
+    constexpr int NT = GROUPS * TILES;
+    constexpr bool FP4 = BITS == kFp4;
+    uint4 w[NT];
+    uint32_t hb[NT];
+    uint2 sw[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        w[t] = *reinterpret_cast<const uint4*>(code[t]);
+        // high-bit word of the lane: after the tile's 512 nibble bytes, 4 bytes per lane
+        hb[t] = BITS == 5 ? *reinterpret_cast<const uint32_t*>(code[t] + 512 - (threadIdx.x & 31) * 12) : 0u;
+        if constexpr (FP4)
+            sw[t] = *reinterpret_cast<const uint2*>(scale[t]);
+        else
+            sw[t] = make_uint2(*reinterpret_cast<const uint32_t*>(scale[t]), 0u);
+    }
+    if constexpr (FP4) {
+        fp4_kstep<0, GROUPS, TILES, HALF>(w, sw, xb, acc);
+        fp4_kstep<1, GROUPS, TILES, HALF>(w, sw, xb, acc);
+        fp4_kstep<2, GROUPS, TILES, HALF>(w, sw, xb, acc);
+        fp4_kstep<3, GROUPS, TILES, HALF>(w, sw, xb, acc);
+    } else {
+        int_tiles<BITS, F16, GROUPS, TILES, HALF>(w, hb, sw, xb, o, magic, acc);
     }
 }
 

@@ -142,7 +142,7 @@ NQ_HD bool make_tc_plan(int bits, int T, int K, int N, int num_sms, TcPlan& p) {
     return p.stages >= 2 && p.G > 0;
 }
 
-struct alignas(64) TcArgs {
+struct TcArgs {                // aligned as CUtensorMap requires
     CUtensorMap xmap;        // X viewed as [K/64][T][64] bf16 (tokens past T read as zeros)
     CUtensorMap wmap;        // packed codes viewed as [RT][G][tile bytes / 8] (8-byte elements)
     CUtensorMap smap;        // packed scales viewed as [RT][G][4] (8-byte elements)
@@ -314,7 +314,8 @@ __device__ __forceinline__ bool elect_one() {
 
 template <int BITS, int TP, int MODE>
 __global__ void __launch_bounds__(tc_threads(BITS, TP), 1) tc_proj_kernel(const __grid_constant__ TcArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t tc_smem[];
+    uint8_t* const smem = tc_smem;
     constexpr int TB = BITS == 5 ? kQ5TileBytes : kQ4TileBytes;
     constexpr int BG = tc_stage_groups(TP);
     static_assert(BG % kTcPair == 0, "decoder pairs tile a stage");
