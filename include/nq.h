@@ -154,7 +154,7 @@ nq_status nq_gemm_q4(const void* X, const void* Wq, const void* S, void* Y, int 
  *   divides the room: e.g. T = 8, K = 17408 (three slabs) allows N <= 20224. Larger
  *   problems return NQ_ERR_SCRATCH before anything is launched.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *   with that device current; make that first call before any stream capture.
+ *   with that device current; later calls on that device reuse it.
  *   Every call clears the tickets it uses on its own stream, then launches. All calls share
  *   the one array: calls that overlap on the GPU (unordered streams) race and give wrong
  *   results; order them on one stream.
