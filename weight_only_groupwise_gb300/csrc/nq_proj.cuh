@@ -300,6 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     // plan fields used in loops, in registers
     const Plan& p = a.p;
     const int T = p.T, G = p.G, GS = p.GS, nstages = p.stages;
+    // How the X slab is staged: by every consumer thread (cp.async) for the single-token fp16
+    // instantiation, else by one bulk copy per token row, with the weight stream held after its
+    // first stage until the rows land. Measured (bulk against cp.async, decode shape): Q4 T = 2
+    // 12.7 -> 12.0 us, Q5 verify shape T = 2 10.0 -> 9.25, NVFP4 T = 2 / 4 / 8 14.2 / 15.7 / 19.2
+    // -> 13.6 / 14.5 / 17.8; bulk at T = 1 was slower (11.2 -> 11.5). A compile-time choice:
+    // the bulk path compiled into the single-token instantiation cost it 0.5-1.7 % (code size).
+    constexpr bool kBulkX = !(F16 && EVEN == 1);
     const long long row_tile_codes = (long long)G * TB, row_tile_scales = (long long)G * STB;
     const uint64_t wait_ns = a.wait_ns;
 
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
                     // After the first stage, hold the weight stream until a bulk-copied first
                     // activation slab has landed: its copies share this block's copy engine,
                     // and behind a full ring of weight stages they would start the consumers late.
-                    if (!F16 && it == 1 && !mbar_wait(x_bar, 0, flags, a.dev_err, wait_ns)) {
+                    if (kBulkX && it == 1 && !mbar_wait(x_bar, 0, flags, a.dev_err, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -664,13 +671,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
             cur_slab = sg.s;
             const int gs = slab_groups(p, sg.s);
             const int chunks = gs * 8;  // 16-byte chunks per token row
-            // The X slab into shared memory. fp16 operands (one or two token rows): 16-byte
-            // copies by every consumer thread (LSU path, off the weight stream's copy engine).
-            // bf16 operands (more rows): one bulk copy per row, since the LSU path stages
-            // through the L1 left beside this block's shared memory and would take several
-            // round trips.
+            // The X slab into shared memory. One token row (the single-token instantiation):
+            // 16-byte copies by every consumer thread (LSU path, off the weight stream's copy
+            // engine). More rows: one bulk copy per row, since the LSU path stages through the
+            // L1 left beside this block's shared memory and would take several round trips.
             const uint16_t* xg = a.X + (size_t)sg.s * GS * kGroup;
-            if constexpr (F16) {
+            if constexpr (!kBulkX) {
                 for (int t = 0; t < T; ++t)
                     for (int c = tid; c < chunks; c += kConsumerThreads)
                         cp_async16(smem_u32(xs + t * pitch + c * 16), xg + (size_t)t * p.K + c * 8);
